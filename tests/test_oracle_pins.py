@@ -1,0 +1,416 @@
+"""Pins for the CPU oracle: checks against things other than the oracle itself.
+
+Each test ties one oracle function to an independent fact: hand-derived
+landmarks (tests/golden), library casts (torch's and ml_dtypes' float8/bf16
+conversions, used only in the range where they agree with the spec),
+closed forms, brute force and invariants.
+
+Sources: "User Guide on Native XLA-FP8" (NVIDIA JAX-Toolbox), sections
+"JAX" (Q, DQ, delayed scaling) and "Gradient accumulation of FP8 params";
+"Fusion of Fp8 quantization and amax reduction kernels" (openxla/xla issue);
+"Implement fused kernel for FP8 scale update" (TransformerEngine PR).
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from conftest import GOLDEN
+
+E4M3FN, E5M2 = 0, 1
+FMT_NAME = {"e4m3fn": E4M3FN, "e5m2": E5M2}
+TORCH_FP8 = {E4M3FN: torch.float8_e4m3fn, E5M2: torch.float8_e5m2}
+FP8_MAX = {E4M3FN: 448.0, E5M2: 57344.0}
+MAX_CODE = {E4M3FN: 0x7E, E5M2: 0x7B}
+
+
+def _val(expr: str) -> float:
+    expr = expr.strip()
+    if expr == "nan":
+        return math.nan
+    if expr in ("inf", "-inf"):
+        return math.inf if expr == "inf" else -math.inf
+    if expr == "-0":
+        return -0.0
+    total = 0.0
+    for term in expr.split("+"):
+        if "*2^" in term:
+            p, e = term.split("*2^")
+            total += float(p) * 2.0 ** int(e)
+        else:
+            total += float(term)
+    return total
+
+
+def _golden(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                rows.append(line.split())
+    return rows
+
+
+def _is_nan_code(c, fmt):
+    c &= 0x7F
+    return c == 0x7F if fmt == E4M3FN else c > 0x7C
+
+
+def _torch_decode(fmt):
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    return codes.view(TORCH_FP8[fmt]).to(torch.float32).numpy()
+
+
+def _torch_cast_codes(y, fmt):
+    """Library cast float32 -> fp8 codes (non-saturating; valid for |y| <= max only)."""
+    return torch.from_numpy(np.ascontiguousarray(y, np.float32)).to(TORCH_FP8[fmt]).view(torch.uint8).numpy()
+
+
+ALL_BF16 = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+ALL_BF16_F32 = (ALL_BF16.astype(np.uint32) << 16).view(np.float32)
+
+SCALES = [1.0, 0.5, 2.0 ** -6, 2.0 ** 20, 1.0 / 3.0, 0.012345678, 7.5, 448.0 / 3.9,
+          3.0e-5, 1.7e4, 2.0 ** -70, 2.0 ** 70, 1.0e-38, 5.0e-45]
+
+
+# --------------------------------------------------------------------------- decode
+
+def test_decode_landmarks(orc):
+    for fmt_s, code_s, val_s in _golden("fp8_landmarks.txt"):
+        fmt, code, want = FMT_NAME[fmt_s], int(code_s, 16), _val(val_s)
+        got = orc.fp8_decode(code, fmt)
+        if math.isnan(want):
+            assert math.isnan(got), (fmt_s, code_s)
+        else:
+            assert got == want and math.copysign(1, got) == math.copysign(1, want), (fmt_s, code_s, got)
+
+
+@pytest.mark.parametrize("fmt", [E4M3FN, E5M2])
+def test_decode_all_codes_match_torch(orc, fmt):
+    lib_vals = _torch_decode(fmt)
+    for c in range(256):
+        got = orc.fp8_decode(c, fmt)
+        want = float(lib_vals[c])
+        if math.isnan(want):
+            assert math.isnan(got), c
+        else:
+            assert got == want and math.copysign(1, got) == math.copysign(1, want), (c, got, want)
+    assert orc.fp8_max(fmt) == FP8_MAX[fmt]
+    assert orc.fp8_max_code(fmt) == MAX_CODE[fmt]
+
+
+@pytest.mark.parametrize("fmt", [E4M3FN, E5M2])
+def test_decode_all_codes_match_ml_dtypes(orc, fmt):
+    ml = pytest.importorskip("ml_dtypes")
+    t = ml.float8_e4m3fn if fmt == E4M3FN else ml.float8_e5m2
+    vals = np.arange(256, dtype=np.uint32).astype(np.uint8).view(t).astype(np.float64)
+    for c in range(256):
+        got = orc.fp8_decode(c, fmt)
+        assert (math.isnan(got) and math.isnan(vals[c])) or got == vals[c], c
+
+
+def test_format_resolution_and_range(orc):
+    # E4M3 has twice the resolution of E5M2 (one more mantissa bit) and about half
+    # the dynamic range in binades ("User Guide on Native XLA-FP8", opening section).
+    def binades(fmt):
+        return math.log2(orc.fp8_max(fmt) / orc.fp8_decode(1, fmt))
+    assert orc.fp8_decode(0x39, E4M3FN) - 1.0 == 0.125      # ulp at 1: 2^-3
+    assert orc.fp8_decode(0x3D, E5M2) - 1.0 == 0.25          # ulp at 1: 2^-2
+    assert 0.45 < binades(E4M3FN) / binades(E5M2) < 0.65
+
+
+# --------------------------------------------------------------------------- encode
+
+def test_encode_landmarks(orc):
+    for fmt_s, y_s, code_s in _golden("fp8_rounding_cases.txt"):
+        fmt, y, want = FMT_NAME[fmt_s], _val(y_s), int(code_s, 16)
+        assert float(np.float32(y)) == y or math.isnan(y) or abs(y) > 3e38, "fixture must be exact in fp32"
+        got = orc.fp8_encode(y, fmt)
+        if math.isnan(y):
+            assert _is_nan_code(got, fmt), (fmt_s, y_s, hex(got))
+        else:
+            assert got == want, (fmt_s, y_s, hex(got), hex(want))
+
+
+@pytest.mark.parametrize("fmt", [E4M3FN, E5M2])
+def test_quantize_exhaustive_bf16_vs_library_cast(orc, fmt):
+    """All 65536 bf16 inputs x many scales: in range the oracle equals the library cast
+    of the IEEE fp32 quotient; above range it saturates; NaN gives a NaN code."""
+    x = ALL_BF16_F32
+    for s in SCALES:
+        s32 = np.float32(s)
+        with np.errstate(all="ignore"):
+            y = (x / s32).astype(np.float32)          # IEEE binary32 division, RN
+        q, _ = orc.quantize_amax(ALL_BF16, fmt, s32)
+        nan = np.isnan(y)
+        inr = ~nan & (np.abs(y) <= FP8_MAX[fmt])
+        lib_codes = _torch_cast_codes(np.where(inr, y, 0).astype(np.float32), fmt)
+        assert np.array_equal(q[inr], lib_codes[inr]), f"scale {s}"
+        over = ~nan & ~inr
+        sat = np.where(np.signbit(y[over]), 0x80 | MAX_CODE[fmt], MAX_CODE[fmt]).astype(np.uint8)
+        assert np.array_equal(q[over], sat), f"scale {s}"
+        assert all(_is_nan_code(int(c), fmt) for c in q[nan])
+
+
+@pytest.mark.parametrize("fmt", [E4M3FN, E5M2])
+def test_quantize_in_range_vs_ml_dtypes(orc, fmt):
+    ml = pytest.importorskip("ml_dtypes")
+    t = ml.float8_e4m3fn if fmt == E4M3FN else ml.float8_e5m2
+    rng = np.random.default_rng(7)
+    bits = rng.integers(0, 2 ** 32, 200000, dtype=np.uint64).astype(np.uint32)
+    y = bits.view(np.float32)
+    y = y[np.isfinite(y) & (np.abs(y) <= FP8_MAX[fmt])]
+    want = y.astype(t).view(np.uint8)
+    got = np.array([orc.fp8_encode(v, fmt) for v in y[:20000]], np.uint8)
+    assert np.array_equal(got, want[:20000])
+
+
+@pytest.mark.parametrize("fmt", [E4M3FN, E5M2])
+def test_exactly_representable_values_round_trip(orc, fmt):
+    """Every finite code's value, quantized with scale 1, returns the same code."""
+    for c in range(256):
+        v = orc.fp8_decode(c, fmt)
+        if math.isnan(v) or math.isinf(v):
+            continue
+        h = torch.tensor([v], dtype=torch.float32).to(torch.bfloat16)
+        assert float(h) == v or (v == 0 and float(h) == 0)
+        hb = h.view(torch.int16).numpy().view(np.uint16)
+        q, _ = orc.quantize_amax(hb, fmt, 1.0)
+        assert int(q[0]) == c, (c, v, hex(int(q[0])))
+
+
+# --------------------------------------------------------------------------- amax
+
+def _brute_amax(vals):
+    m = 0.0
+    for v in vals:
+        if math.isnan(v):
+            return math.nan
+        m = max(m, abs(v))
+    return m
+
+
+def test_amax_brute_force(orc):
+    rng = np.random.default_rng(11)
+    for trial in range(20):
+        n = int(rng.integers(1, 3000))
+        bits = rng.integers(0, 65536, n, dtype=np.uint32).astype(np.uint16)
+        f = (bits.astype(np.uint32) << 16).view(np.float32)
+        if trial % 3 == 0:  # mostly without NaN so the finite max is exercised
+            bits = np.where(np.isnan(f), np.uint16(0x8000), bits).astype(np.uint16)
+            f = (bits.astype(np.uint32) << 16).view(np.float32)
+        want = _brute_amax([float(v) for v in f])
+        got = float(orc.amax(bits))
+        _, got2 = orc.quantize_amax(bits, E4M3FN, 1.0)
+        for g in (got, float(got2)):
+            assert (math.isnan(want) and math.isnan(g)) or g == want
+        perm = rng.permutation(n)
+        g3 = float(orc.amax(bits[perm]))
+        assert (math.isnan(want) and math.isnan(g3)) or g3 == want
+
+
+def test_amax_signs_infs_and_accumulation(orc):
+    vals = torch.tensor([-3.0, 2.0, -0.0, 1e-40, -5.5], dtype=torch.float32).to(torch.bfloat16)
+    bits = vals.view(torch.int16).numpy().view(np.uint16)
+    _, a = orc.quantize_amax(bits, E4M3FN, 1.0)
+    assert float(a) == 5.5
+    _, a = orc.quantize_amax(bits, E4M3FN, 1.0, amax=7.25)   # max-accumulate, not overwrite
+    assert float(a) == 7.25
+    _, a = orc.quantize_amax(bits[:0], E4M3FN, 1.0, amax=3.5)  # empty: unchanged
+    assert float(a) == 3.5
+    neg_inf = torch.tensor([1.0, -math.inf], dtype=torch.float32).to(torch.bfloat16)
+    _, a = orc.quantize_amax(neg_inf.view(torch.int16).numpy().view(np.uint16), E5M2, 1.0)
+    assert math.isinf(float(a)) and float(a) > 0                # inf propagates, sign dropped
+    zeros = torch.tensor([-0.0, -0.0], dtype=torch.float32).to(torch.bfloat16)
+    _, a = orc.quantize_amax(zeros.view(torch.int16).numpy().view(np.uint16), E4M3FN, 1.0)
+    assert float(a) == 0.0 and not math.copysign(1, float(a)) < 0
+
+
+# --------------------------------------------------------------------------- dequantize / bf16
+
+def test_bf16_rounding_landmarks(orc):
+    for fb, hb in _golden("bf16_rounding_cases.txt"):
+        f = np.array([int(fb, 16)], np.uint32).view(np.float32)[0]
+        got = orc.f32_to_bf16(f)
+        if hb == "nan":
+            assert (got & 0x7F80) == 0x7F80 and (got & 0x7F) != 0, hex(got)
+        else:
+            assert got == int(hb, 16), (fb, hex(got), hb)
+
+
+def test_bf16_rounding_vs_torch(orc):
+    rng = np.random.default_rng(3)
+    bits = rng.integers(0, 2 ** 32, 50000, dtype=np.uint64).astype(np.uint32)
+    bits[:2000] &= 0x007FFFFF                       # subnormals
+    bits[2000:4000] = (bits[2000:4000] & 0x0000FFFF) | 0x7F7F0000   # near overflow
+    bits[4000:6000] = (bits[4000:6000] & 0xFFFF0000) | 0x8000      # exact ties
+    f = bits.view(np.float32)
+    want = torch.from_numpy(f.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    for i in range(len(f)):
+        if np.isnan(f[i]):
+            continue
+        assert orc.f32_to_bf16(f[i]) == want[i], hex(bits[i])
+
+
+@pytest.mark.parametrize("fmt", [E4M3FN, E5M2])
+def test_dequantize_all_codes_vs_library(orc, fmt):
+    codes = np.arange(256, dtype=np.uint32).astype(np.uint8)
+    dec = torch.from_numpy(codes.copy()).view(TORCH_FP8[fmt]).to(torch.float32)
+    for s in SCALES + [-2.5, 0.0]:
+        want = (dec * torch.tensor(np.float32(s))).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        got = orc.dequantize(codes, fmt, s)
+        for c in range(256):
+            wf = (int(want[c]) << 16)
+            if (wf & 0x7F800000) == 0x7F800000 and (wf & 0x007FFFFF):
+                assert (got[c] & 0x7F80) == 0x7F80 and (got[c] & 0x7F), (c, s)
+            else:
+                assert got[c] == want[c], (fmt, c, s, hex(got[c]), hex(want[c]))
+
+
+@pytest.mark.parametrize("fmt", [E4M3FN, E5M2])
+def test_dq_of_q_is_identity_on_representable_values(orc, fmt):
+    """DQ(Q(x)) == x when scale = 2^k and x / scale is an FP8 value."""
+    for k in (-8, -1, 0, 3, 12):
+        vals, codes = [], []
+        for c in range(256):
+            v = orc.fp8_decode(c, fmt)
+            if math.isnan(v) or math.isinf(v):
+                continue
+            vals.append(math.ldexp(v, k))
+            codes.append(c)
+        x = torch.tensor(vals, dtype=torch.float32)
+        xb = x.to(torch.bfloat16)
+        assert torch.equal(xb.float(), x)
+        bits = xb.view(torch.int16).numpy().view(np.uint16)
+        q, _ = orc.quantize_amax(bits, fmt, 2.0 ** k)
+        assert list(q) == codes
+        y = orc.dequantize(q, fmt, 2.0 ** k)
+        assert np.array_equal(y, bits)
+
+
+# --------------------------------------------------------------------------- multi-tensor
+
+def test_multi_tensor_equals_per_tensor(orc):
+    rng = np.random.default_rng(5)
+    xs = [rng.integers(0, 65536, n, dtype=np.uint32).astype(np.uint16) for n in (0, 1, 17, 4096, 333)]
+    scales = [1.0, 0.25, 3.3, 1e-3, 77.0]
+    qs, am = orc.multi_quantize_amax(xs, E5M2, scales)
+    for x, s, q, a in zip(xs, scales, qs, am):
+        q1, a1 = orc.quantize_amax(x, E5M2, s)
+        assert np.array_equal(q, q1)
+        assert (math.isnan(a) and math.isnan(a1)) or a == a1
+
+
+# --------------------------------------------------------------------------- scale update
+
+def _run_update(orc, H, S, seq, algo=0, margin=0, fmt=E4M3FN, slot_format=None, scale0=1.0):
+    hist = np.zeros((H, S), np.float32)
+    scale = np.full(S, scale0, np.float32)
+    scale_inv = np.full(S, 1.0 / scale0, np.float32)
+    for amax_new in seq:
+        orc.amax_scale_update(hist, np.asarray(amax_new, np.float32), scale, scale_inv, fmt, algo,
+                              margin, slot_format)
+    return hist, scale, scale_inv
+
+
+def test_history_roll_window_newest_first(orc):
+    rng = np.random.default_rng(1)
+    for H in (1, 2, 3, 4):
+        for S in (1, 2, 3):
+            seq = [rng.uniform(0.1, 10, S).astype(np.float32) for _ in range(6)]
+            for k in range(1, 7):
+                hist, _, _ = _run_update(orc, H, S, seq[:k])
+                for h in range(H):
+                    want = seq[k - 1 - h] if h < k else np.zeros(S, np.float32)
+                    assert np.array_equal(hist[h], want), (H, S, k, h)
+
+
+def test_scale_closed_form_powers_of_two(orc):
+    # amax = FP8_MAX * 2^j gives scale exactly 2^j and scale_inv 2^-j
+    for fmt in (E4M3FN, E5M2):
+        for j in (-20, -3, 0, 5, 30):
+            a = FP8_MAX[fmt] * 2.0 ** j
+            _, sc, si = _run_update(orc, 4, 1, [[a]], fmt=fmt)
+            assert sc[0] == 2.0 ** j and si[0] == 2.0 ** -j
+
+
+def test_scale_matches_page_example(orc):
+    """Delayed scaling example: A_scale = max|A| / E4M3_MAX ("User Guide on Native
+    XLA-FP8", section "JAX"), starting from a zero history and unit scale."""
+    from quantize_amax_scaling_gb300 import workloads as W
+    A, B = W.tiny_pair()
+    amax_A = torch.max(torch.abs(A.float()))
+    amax_B = torch.max(torch.abs(B.float()))
+    hist = np.zeros((16, 2), np.float32)
+    scale = np.ones(2, np.float32)
+    scale_inv = np.ones(2, np.float32)
+    qa, ra = orc.quantize_amax(W.bf16_bits(A), E4M3FN, 1.0)
+    qb, rb = orc.quantize_amax(W.bf16_bits(B), E4M3FN, 1.0)
+    assert float(ra) == float(amax_A) and float(rb) == float(amax_B)
+    orc.amax_scale_update(hist, np.array([ra, rb], np.float32), scale, scale_inv)
+    e4m3_max = torch.tensor(torch.finfo(torch.float8_e4m3fn).max, dtype=torch.float32)
+    assert scale[0] == float(amax_A / e4m3_max) and scale[1] == float(amax_B / e4m3_max)
+    assert scale_inv[0] == float(1.0 / (amax_A / e4m3_max))
+    # scale 1.0 is a plain cast: U[0,1) values are all in range
+    assert np.array_equal(qa, _torch_cast_codes(A.float().numpy().reshape(-1), E4M3FN))
+
+
+def test_scale_error_bound(orc):
+    rng = np.random.default_rng(9)
+    a = np.exp(rng.normal(0, 4, 64)).astype(np.float32)
+    _, sc, si = _run_update(orc, 3, 64, [a])
+    rel = np.abs(sc.astype(np.float64) * 448.0 / a.astype(np.float64) - 1.0)
+    assert rel.max() <= 2.0 ** -24
+    assert np.abs(sc.astype(np.float64) * si.astype(np.float64) - 1.0).max() <= 2.0 ** -23
+
+
+def test_select_max_equals_single_entry_run_of_window_max(orc):
+    rng = np.random.default_rng(4)
+    H, S = 4, 3
+    seq = [np.exp(rng.normal(0, 2, S)).astype(np.float32) for _ in range(7)]
+    _, sc_max, _ = _run_update(orc, H, S, seq, algo=0)
+    window_max = np.max(np.stack(seq[-H:]), axis=0)
+    _, sc_ref, _ = _run_update(orc, 1, S, [window_max], algo=0)
+    assert np.array_equal(sc_max, sc_ref)
+    _, sc_mr, _ = _run_update(orc, H, S, seq, algo=1)
+    _, sc_last, _ = _run_update(orc, 1, S, [seq[-1]], algo=0)
+    assert np.array_equal(sc_mr, sc_last)
+    assert not np.array_equal(sc_mr, sc_max)
+
+
+def test_margin_is_exact_power_of_two(orc):
+    rng = np.random.default_rng(6)
+    a = np.exp(rng.normal(0, 3, 5)).astype(np.float32)
+    _, s0, _ = _run_update(orc, 2, 5, [a], margin=0)
+    for m in (-3, 1, 2, 7):
+        _, sm, _ = _run_update(orc, 2, 5, [a], margin=m)
+        assert np.array_equal(sm, (s0.astype(np.float64) * 2.0 ** m).astype(np.float32))
+
+
+def test_pass_through_of_zero_and_non_finite(orc):
+    for bad in (0.0, math.inf, math.nan, -1.0):
+        hist, sc, si = _run_update(orc, 3, 2, [[bad, 448.0]], algo=1, scale0=4.0)
+        assert sc[0] == 4.0 and si[0] == 0.25                 # untouched
+        assert sc[1] == 1.0 and si[1] == 1.0                   # updated
+        assert (math.isnan(bad) and math.isnan(hist[0, 0])) or hist[0, 0] == bad  # still recorded
+    # a NaN anywhere in the window makes max-selection non-finite: pass-through
+    _, sc, _ = _run_update(orc, 3, 1, [[math.nan], [2.0]], algo=0, scale0=4.0)
+    assert sc[0] == 4.0
+    # ... and once it leaves the window the slot updates again
+    _, sc, _ = _run_update(orc, 2, 1, [[math.nan], [2.0], [448.0]], algo=0, scale0=4.0)
+    assert sc[0] == 1.0
+    # a scale that would underflow below the normal range passes through
+    _, sc, _ = _run_update(orc, 1, 1, [[1e-37]], margin=-20, scale0=4.0)
+    assert sc[0] == 4.0
+
+
+def test_per_slot_formats(orc):
+    sf = np.array([0, 1, 7], np.uint8)
+    _, sc, _ = _run_update(orc, 2, 3, [[448.0, 57344.0, 448.0]], slot_format=sf)
+    assert sc[0] == 1.0 and sc[1] == 1.0
+    assert sc[2] == 1.0   # unknown format code: slot left unchanged (started at 1.0)
+    _, sc, _ = _run_update(orc, 2, 3, [[57344.0, 57344.0, 448.0]], slot_format=sf, scale0=2.0)
+    assert sc[0] == 128.0 and sc[1] == 1.0 and sc[2] == 2.0
