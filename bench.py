@@ -1,0 +1,471 @@
+"""Benchmark of the FP8 delayed-scaling path on GB300.
+
+One step is the FP8 bookkeeping of one MLP training step on the FFN workload
+(sequence 2048 x batch 4, hidden 4096, FFN 16384, bf16):
+
+  1. fp8q_quantize_amax        activation 8192x16384 bf16 -> e4m3fn + amax
+  2. fp8q_multi_quantize_amax  W1 4096x16384 and W2 16384x4096 -> e4m3fn, one launch
+  3. fp8q_dequantize           e5m2 gradient 8192x16384 -> bf16
+  4. fp8q_amax_scale_update    96 layers x 6 slots, history 1024 -> next step's scales
+
+Step 4 reads the amaxes steps 1-2 wrote and writes the scales steps 1-3 read
+on the next step (delayed scaling entirely on the device).  Inputs are
+seeded synthetic tensors resident in HBM; each step streams ~1.2 GB, far more
+than the 129 MB L2, so no input is L2-resident when it is read again.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle
+instead, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import math
+import os
+import statistics
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "quantize+amax HBM GB/s (% of GB300 peak); scale-update µs per 576-slot call"
+WORKLOAD = ("fp8 delayed-scaling step, FFN config: quantize+amax act 8192x16384 (e4m3fn) + "
+            "multi-tensor quantize W1 4096x16384, W2 16384x4096 (e4m3fn, 1 launch) + dequantize "
+            "grad 8192x16384 (e5m2) + amax_scale_update 576 slots x history 1024")
+
+ACT = (8192, 16384)
+W1 = (4096, 16384)
+W2 = (16384, 4096)
+GRAD = (8192, 16384)
+H, S = 1024, 576
+
+N_ACT = ACT[0] * ACT[1]
+N_W = W1[0] * W1[1] + W2[0] * W2[1]
+N_GRAD = GRAD[0] * GRAD[1]
+BYTES_PER_ELEM = 3                      # 2 B bf16 read + 1 B fp8 written (or the reverse)
+UPDATE_BYTES = 2 * H * S * 4 + S * 4 + 4 * S * 4   # history read+write, amax_new, scale & scale_inv r+w
+BYTES_QUANT = BYTES_PER_ELEM * N_ACT
+BYTES_MULTI = BYTES_PER_ELEM * N_W
+BYTES_DEQ = BYTES_PER_ELEM * N_GRAD
+STEP_BYTES = BYTES_QUANT + BYTES_MULTI + BYTES_DEQ + UPDATE_BYTES
+KERNELS_PER_STEP = 4
+
+
+# --------------------------------------------------------------------------- peaks and clocks
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """Reads SM clock, max clock, power and clock-event reasons through NVML.
+
+    Only reads device state; never changes a setting.
+    """
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x100: "display_clock_setting"}
+
+    def __init__(self, torch_device_index: int):
+        self.ok = False
+        self.samples = []
+        try:
+            self.nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nv.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            import torch
+            uuid = getattr(torch.cuda.get_device_properties(torch_device_index), "uuid", None)
+            rc = 1
+            if uuid is not None:
+                rc = self.nv.nvmlDeviceGetHandleByUUID(("GPU-" + str(uuid)).encode(), ctypes.byref(self.h))
+            if rc != 0:
+                vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+                idx = int(vis.split(",")[torch_device_index]) if vis and vis.split(",")[0].isdigit() \
+                    else torch_device_index
+                rc = self.nv.nvmlDeviceGetHandleByIndex_v2(idx, ctypes.byref(self.h))
+            if rc != 0:
+                return
+            self._reasons = getattr(self.nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                self.nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            mx = ctypes.c_uint()
+            rc = self.nv.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))
+            self.max_mhz = mx.value if rc == 0 else None
+            self.ok = True
+        except OSError:
+            self.ok = False
+
+    def sample(self):
+        if not self.ok:
+            return
+        c = ctypes.c_uint()
+        r = ctypes.c_ulonglong()
+        p = ctypes.c_uint()
+        if self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(c)) != 0:
+            return
+        self._reasons(self.h, ctypes.byref(r))
+        self.nv.nvmlDeviceGetPowerUsage(self.h, ctypes.byref(p))
+        self.samples.append((c.value, r.value, p.value / 1000.0))
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": getattr(self, "max_mhz", None), "reasons": [],
+                    "samples": 0, "source": "nvml" if self.ok else "unavailable"}
+        mhz = [s[0] for s in self.samples]
+        bits = 0
+        for s in self.samples:
+            bits |= s[1]
+        reasons = [name for b, name in self.REASONS.items() if bits & b and name != "gpu_idle"]
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(self.samples), "power_w_max": max(s[2] for s in self.samples),
+                "source": "nvml, sampled on the host while the timed steps ran"}
+
+
+# --------------------------------------------------------------------------- multi-rank helpers
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(value: float, group=None) -> float:
+    """Max of a per-rank float over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend(group) == "nccl" \
+        else torch.device("cpu")
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def aggregate_throughput(bytes_per_rank: float, seconds_per_rank: float, world_size: int, group=None):
+    """Whole-job GB/s: bytes all ranks processed over the slowest rank's time."""
+    t = max_over_ranks(seconds_per_rank, group)
+    return bytes_per_rank * world_size / t / 1e9, t
+
+
+# --------------------------------------------------------------------------- workload
+
+class Step:
+    """Device-resident state of one benchmark step."""
+
+    def __init__(self, dev):
+        import torch
+        from quantize_amax_scaling_gb300 import fp8q
+        from quantize_amax_scaling_gb300 import workloads as W
+        self.fp8q = fp8q
+        self.dev = dev
+        self.act = W.gelu_activation(W.SEED_FFN, dev).reshape(-1)
+        ffn = W.ffn_tensors(dev)
+        self.w = [ffn[1].reshape(-1), ffn[2].reshape(-1)]
+        del ffn
+        grad = W.gradient(GRAD, W.SEED_GRAD, dev).reshape(-1)
+        hist, new, scale, scale_inv, slot_format = W.scale_update_inputs(dev)
+        self.hist, self.amax_new, self.slot_format = hist, new, slot_format
+        self.scale, self.scale_inv = scale, scale_inv
+        # realistic starting scales: one update from the synthetic amaxes
+        fp8q.fp8q_amax_scale_update(self.hist, self.amax_new, self.scale, self.scale_inv,
+                                    fp8q.E4M3FN, fp8q.ALGO_MAX, 0, self.slot_format)
+        # the gradient arrives already in e5m2 (quantized once with its own slot)
+        self.grad_q = torch.empty(grad.numel(), dtype=torch.uint8, device=dev)
+        gam = torch.zeros(1, device=dev)
+        fp8q.fp8q_quantize_amax(grad, self.grad_q, fp8q.E5M2, self.scale[4:5], gam)
+        del grad
+        self.q_act = torch.empty(self.act.numel(), dtype=torch.uint8, device=dev)
+        self.q_w = [torch.empty(w.numel(), dtype=torch.uint8, device=dev) for w in self.w]
+        self.y_grad = torch.empty(self.grad_q.numel(), dtype=torch.bfloat16, device=dev)
+        torch.cuda.synchronize(dev)
+
+    def run(self, stream, events=None):
+        """Enqueue one step on `stream`; `events` (5 CUDA events) bracket the four kernels."""
+        f = self.fp8q
+        st = stream.cuda_stream
+        self.amax_new[:3].zero_()  # this step's amax slots start from 0 (max-accumulated)
+        if events:
+            events[0].record(stream)
+        f.fp8q_quantize_amax(self.act, self.q_act, f.E4M3FN, self.scale[0:1], self.amax_new[0:1], st)
+        if events:
+            events[1].record(stream)
+        f.fp8q_multi_quantize_amax(self.w, self.q_w, f.E4M3FN, [self.scale[1:2], self.scale[2:3]],
+                                   [self.amax_new[1:2], self.amax_new[2:3]], st)
+        if events:
+            events[2].record(stream)
+        f.fp8q_dequantize(self.grad_q, self.y_grad, f.E5M2, self.scale[4:5], st)
+        if events:
+            events[3].record(stream)
+        f.fp8q_amax_scale_update(self.hist, self.amax_new, self.scale, self.scale_inv, f.E4M3FN,
+                                 f.ALGO_MAX, 0, self.slot_format, st)
+        if events:
+            events[4].record(stream)
+
+
+def run_gpu(args, ws, rank, local):
+    import torch
+    import torch.distributed as dist
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    step = Step(dev)
+    stream = torch.cuda.Stream(dev)
+    peak, peak_src = measured_peaks()
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step.run(stream)
+    torch.cuda.synchronize(dev)
+
+    # ---- timed region: K steps back to back, per-kernel events inside
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for k in range(args.steps):
+            step.run(stream, ev[k])
+        end.record(stream)
+    while not end.query():          # sample clocks while the GPU runs the timed steps
+        clocks.sample()
+        time.sleep(0.002)
+    torch.cuda.synchronize(dev)
+    barrier()
+    t_rank = start.elapsed_time(end) / 1e3
+    value, t_max = aggregate_throughput(STEP_BYTES, t_rank, ws)
+
+    per = {"quantize_amax": [], "multi_quantize_amax": [], "dequantize": [], "amax_scale_update": []}
+    for k in range(args.steps):
+        e = ev[k]
+        for j, name in enumerate(per):
+            per[name].append(e[j].elapsed_time(e[j + 1]) * 1e3)  # us
+    avg = {n: sum(v) / len(v) for n, v in per.items()}
+    kbytes = {"quantize_amax": BYTES_QUANT, "multi_quantize_amax": BYTES_MULTI,
+              "dequantize": BYTES_DEQ, "amax_scale_update": UPDATE_BYTES}
+    kernels = {n: {"us": round(avg[n], 3), "GB/s": round(kbytes[n] / (avg[n] * 1e-6) / 1e9, 1),
+                   "frac_of_peak": round(kbytes[n] / (avg[n] * 1e-6) / 1e9 / peak, 4)}
+               for n in per}
+    q_gbs = kbytes["quantize_amax"] / (avg["quantize_amax"] * 1e-6) / 1e9
+
+    # ---- end to end through the public API with host buffers
+    e2e = run_e2e(args, step, stream, dev) if not args.no_e2e else None
+
+    if rank != 0:
+        return None
+    traffic = read_traffic()
+    out = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(t_max / args.steps * 1e3, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded; shapes of the FFN/MLP and 96-layer workloads)",
+        "config": {"workload": WORKLOAD, "step_bytes": STEP_BYTES,
+                   "l2": "inputs larger than L2 (each step streams 1.21 GB; the 129 MB L2 holds none of "
+                         "a step's inputs when it is read again)",
+                   "parallelism": f"replicas x{ws} (no collective)"},
+        "headline": {"quantize_amax_gbs": round(q_gbs, 1), "quantize_amax_frac_of_peak": round(q_gbs / peak, 4),
+                     "scale_update_us": round(avg["amax_scale_update"], 3)},
+        "kernels": kernels,
+        "roofline": {"kernel": "quantize_amax_kernel (8192x16384 bf16 -> e4m3fn + amax)",
+                     "bound": "hbm", "achieved": round(q_gbs, 1), "peak": peak,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+                     else "fallback 6.8 TB/s",
+                     "unit": "GB/s", "frac": round(q_gbs / peak, 4), "traffic": traffic},
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "other_launches": {"torch fill (zero the step's 3 amax slots)": args.steps},
+        "clocks": clocks.summary(),
+        "e2e": e2e,
+    }
+    if not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(args.cpu_sample_frac)
+    return out
+
+
+def run_e2e(args, step, stream, dev):
+    """Same step through the public API, starting and ending in pinned host memory."""
+    import torch
+    steps = max(1, min(args.steps, args.e2e_steps))
+    host_in = {
+        "act": step.act.cpu().pin_memory(),
+        "w1": step.w[0].cpu().pin_memory(),
+        "w2": step.w[1].cpu().pin_memory(),
+        "grad_q": step.grad_q.cpu().pin_memory(),
+        "amax_new": step.amax_new.cpu().pin_memory(),
+    }
+    host_out = {
+        "q_act": torch.empty_like(step.q_act, device="cpu").pin_memory(),
+        "q_w1": torch.empty_like(step.q_w[0], device="cpu").pin_memory(),
+        "q_w2": torch.empty_like(step.q_w[1], device="cpu").pin_memory(),
+        "y_grad": torch.empty_like(step.y_grad, device="cpu").pin_memory(),
+        "scale": torch.empty_like(step.scale, device="cpu").pin_memory(),
+        "scale_inv": torch.empty_like(step.scale_inv, device="cpu").pin_memory(),
+    }
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+    def one():
+        step.act.copy_(host_in["act"], non_blocking=True)
+        step.w[0].copy_(host_in["w1"], non_blocking=True)
+        step.w[1].copy_(host_in["w2"], non_blocking=True)
+        step.grad_q.copy_(host_in["grad_q"], non_blocking=True)
+        step.amax_new.copy_(host_in["amax_new"], non_blocking=True)
+        step.run(stream)
+        host_out["q_act"].copy_(step.q_act, non_blocking=True)
+        host_out["q_w1"].copy_(step.q_w[0], non_blocking=True)
+        host_out["q_w2"].copy_(step.q_w[1], non_blocking=True)
+        host_out["y_grad"].copy_(step.y_grad, non_blocking=True)
+        host_out["scale"].copy_(step.scale, non_blocking=True)
+        host_out["scale_inv"].copy_(step.scale_inv, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        one()
+        torch.cuda.synchronize(dev)
+        barrier()
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for _ in range(steps):
+            one()
+        e.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    ws = dist_env()[0]
+    v, t = aggregate_throughput(STEP_BYTES, s.elapsed_time(e) / 1e3 / steps, ws)
+    return {"value": round(v, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": steps, "ms_per_step": round(t * 1e3, 3)}
+
+
+def read_traffic():
+    """DRAM bytes per launch of the quantize kernel from the committed ncu summary, if current."""
+    p = os.path.join(ROOT, "profiles", "quantize_amax_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    return d.get("dram_bytes_per_launch")
+
+
+# --------------------------------------------------------------------------- CPU oracle legs
+
+def _oracle_sample(frac: float):
+    """A bounded sample of the step for the CPU oracle: the first `frac` of each
+    tensor, plus one full 576-slot update.  Returns (inputs, algorithmic bytes)."""
+    import numpy as np
+    import torch
+    from quantize_amax_scaling_gb300 import workloads as W
+    n_act = max(8, int(N_ACT * frac))
+    n_w = max(8, int(N_W * frac))
+    n_g = max(8, int(N_GRAD * frac))
+    act = W.gelu_activation(W.SEED_FFN, "cpu", (max(1, n_act // ACT[1]) + 1, ACT[1])).reshape(-1)[:n_act]
+    w = W.truncated_normal_weight((max(1, n_w // W1[1]) + 1, W1[1]), 4096, W.SEED_FFN + 10, "cpu").reshape(-1)[:n_w]
+    rng = np.random.default_rng(W.SEED_GRAD)
+    gq = rng.integers(0, 256, n_g, dtype=np.uint8)
+    hist, new, scale, scale_inv, sf = W.scale_update_inputs("cpu")
+    inputs = {"act": W.bf16_bits(act), "w": W.bf16_bits(w), "gq": gq, "hist": hist.numpy(),
+              "new": new.numpy(), "scale": scale.numpy(), "scale_inv": scale_inv.numpy(), "sf": sf.numpy()}
+    nbytes = BYTES_PER_ELEM * (n_act + n_w + n_g) + UPDATE_BYTES
+    desc = (f"first {frac:g} of each tensor ({n_act} act + {n_w} weight elements quantized, {n_g} grad "
+            f"codes dequantized) + one full 576x1024 update")
+    del torch
+    return inputs, nbytes, desc
+
+
+def _oracle_step(inp):
+    import numpy as np
+    import oracle
+    s = np.float32(0.0091)
+    oracle.quantize_amax(inp["act"], oracle.E4M3FN, s)
+    oracle.quantize_amax(inp["w"], oracle.E4M3FN, s)
+    oracle.dequantize(inp["gq"], oracle.E5M2, s)
+    oracle.amax_scale_update(inp["hist"], inp["new"], inp["scale"], inp["scale_inv"], oracle.E4M3FN,
+                             oracle.ALGO_MAX, 0, inp["sf"])
+
+
+def cpu_baseline(frac: float):
+    inp, nbytes, desc = _oracle_sample(frac)
+    t0 = time.perf_counter()
+    _oracle_step(inp)
+    dt = time.perf_counter() - t0
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": desc, "seconds": round(dt, 3),
+            "host": f"{os.uname().machine}, {os.cpu_count()} cores present"}
+
+
+def run_reference(args):
+    """The CPU oracle, as it stands, timed on the host on a bounded sample per step."""
+    inp, nbytes, desc = _oracle_sample(args.ref_sample_frac)
+    for _ in range(args.warmup):
+        _oracle_step(inp)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_step(inp)
+    dt = (time.perf_counter() - t0) / args.steps
+    v = nbytes / dt / 1e9
+    return {"metric": METRIC, "impl": "reference", "value": round(v, 4), "unit": "GB/s", "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded)", "config": {"workload": WORKLOAD, "step_bytes_sampled": nbytes},
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["fp8q", "reference"], default="fp8q")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-frac", type=float, default=1.0 / 16)
+    ap.add_argument("--ref-sample-frac", type=float, default=1.0 / 128)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args)), flush=True)
+        return 0
+    out = run_gpu(args, ws, rank, local)
+    if rank == 0 and out is not None:
+        print(json.dumps(out), flush=True)
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,171 @@
+/*
+ * fp8q.h -- C ABI of libfp8q: FP8 delayed-scaling quantization on one GPU.
+ *
+ * Four operations, each one kernel launch on the caller's stream:
+ *   fp8q_quantize_amax        bf16 -> FP8 bytes, fused with amax = max|x|
+ *   fp8q_multi_quantize_amax  the same over a ragged list of tensors
+ *   fp8q_dequantize           FP8 bytes -> bf16
+ *   fp8q_amax_scale_update    amax-history roll + amax selection + scale and
+ *                             scale_inv, for many FP8 metadata slots at once
+ *
+ * Sources (web pages, by title and section):
+ *   "User Guide on Native XLA-FP8" (NVIDIA JAX-Toolbox): opening section
+ *     (E4M3 / E5M2 formats, quantization Q and de-quantization DQ); section
+ *     "JAX" (Q = cast(A / A_scale), DQ = cast(a_fp8) * a_scale, delayed
+ *     scaling A_scale = max|A| / E4M3_MAX); section "Gradient accumulation of
+ *     FP8 params" (FP8 meta accumulates with max, not add).
+ *   "Fusion of Fp8 quantization and amax reduction kernels" (openxla/xla
+ *     issue): quantization and the amax reduction are memory bound and
+ *     belong in one pass over the tensor.
+ *   "Implement fused kernel for FP8 scale update" (NVIDIA/TransformerEngine
+ *     PR): amax_and_scale_update (history roll, amax selection, scale,
+ *     scale_inv) as one in-place kernel in a framework-agnostic library,
+ *     batched over all layers.
+ *
+ * Conventions shared by every call:
+ *   - Data pointers are DEVICE memory of the calling thread's current CUDA
+ *     device, owned by the caller.  The library allocates nothing, frees
+ *     nothing and keeps no per-call state.  Inputs and outputs must not
+ *     overlap unless a call says it works in place.
+ *   - bf16 tensors are contiguous arrays of 16-bit patterns (any 2-byte
+ *     aligned address); FP8 tensors are contiguous byte arrays.  Any
+ *     alignment works; 16-byte-aligned bf16 with a matching FP8 offset take
+ *     the vectorised path.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *     return once the kernel is enqueued; results are ready when the stream
+ *     reaches that point.
+ *   - Errors are returned as fp8q_status, never raised or aborted.  Argument
+ *     errors are detected before anything is launched.  FP8Q_ERR_CUDA means
+ *     the launch itself failed; fp8q_last_cuda_error() (per thread) then
+ *     describes it.  A zero-sized call succeeds and launches nothing.
+ */
+#ifndef FP8Q_H
+#define FP8Q_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FP8Q_E4M3FN = 0, /* 1-4-3, bias 7, no inf, max 448 (forward pass) */
+    FP8Q_E5M2 = 1    /* 1-5-2, bias 15, IEEE inf/NaN, max 57344 (gradients) */
+} fp8q_format;
+
+typedef enum {
+    FP8Q_ALGO_MAX = 0,        /* amax = max over the (rolled) history window */
+    FP8Q_ALGO_MOST_RECENT = 1 /* amax = the newest entry */
+} fp8q_amax_algo;
+
+typedef enum {
+    FP8Q_OK = 0,
+    FP8Q_ERR_INVALID_ARG = 1,
+    FP8Q_ERR_UNSUPPORTED = 2,
+    FP8Q_ERR_CUDA = 3,
+    FP8Q_ERR_TOO_MANY_TENSORS = 4
+} fp8q_status;
+
+/* Largest tensor count of one fp8q_multi_quantize_amax call (descriptors
+ * travel inside the kernel's parameter block). */
+#define FP8Q_MAX_TENSORS 512
+
+/*
+ * Fused quantize + amax of one bf16 tensor ("User Guide on Native XLA-FP8",
+ * section "JAX", the quantization step; "Fusion of Fp8 quantization and amax
+ * reduction kernels": amax fused into the same pass).
+ *
+ *   q[i]  = FP8(x[i] / *scale)   quotient in binary32, rounded to nearest even;
+ *                                then rounded to the FP8 grid (nearest, ties
+ *                                to even), saturating to +-448 / +-57344;
+ *                                +-inf saturates; NaN gives a NaN code.
+ *   *amax = max(*amax, max_i |x[i]|)   max-accumulated (not overwritten); a
+ *                                NaN input makes it NaN; +-inf gives +inf.
+ *
+ * x_bf16: n bf16 values (device).  q: n bytes (device, written).
+ * scale:  one float (device, read); any value, positive normal scales in
+ *         [2^-60, 2^60] take the fast exact path.
+ * amax:   one float (device, read-modify-write).  Start it at +0 (or any
+ *         non-negative value) before the first tensor of a step.
+ * Errors: INVALID_ARG for n < 0, an unknown fmt, a NULL pointer with n > 0
+ *         or an odd x_bf16 address.
+ */
+fp8q_status fp8q_quantize_amax(const void* x_bf16, uint8_t* q, int64_t n, fp8q_format fmt,
+                               const float* scale, float* amax, void* stream);
+
+/* One tensor of a ragged list: its own size, scale and amax. */
+typedef struct {
+    const void* x_bf16; /* n bf16 values (device) */
+    uint8_t* q;         /* n bytes (device, written) */
+    int64_t n;          /* elements; 0 is allowed (pointers then unused) */
+    const float* scale; /* one float (device) */
+    float* amax;        /* one float (device), max-accumulated */
+} fp8q_tensor;
+
+/*
+ * fp8q_quantize_amax over `count` tensors in ONE launch ("Fusion of Fp8
+ * quantization and amax reduction kernels": weights and activations all need
+ * Q + amax; "Implement fused kernel for FP8 scale update": batch the per-layer
+ * work).  Each tensor gets exactly the result fp8q_quantize_amax would give.
+ *
+ * list:   `count` descriptors in HOST memory, read during the call only.
+ * Errors: TOO_MANY_TENSORS for count > FP8Q_MAX_TENSORS; INVALID_ARG for
+ *         count < 0, list == NULL with count > 0, or any descriptor that
+ *         fp8q_quantize_amax would reject.  Two tensors may share an amax or
+ *         a scale; outputs must not overlap.
+ */
+fp8q_status fp8q_multi_quantize_amax(const fp8q_tensor* list, int32_t count, fp8q_format fmt,
+                                     void* stream);
+
+/*
+ * Dequantize ("User Guide on Native XLA-FP8", section "JAX": up-cast the FP8
+ * value and multiply by the scale):
+ *   y[i] = bf16_rne( float(q[i]) * *scale )   product in binary32 (RN), then
+ *                                             rounded to nearest-even bf16;
+ *                                             NaN codes give a NaN.
+ * q: n bytes (device).  y_bf16: n bf16 (device, written).  scale: one float
+ * (device).  Errors: INVALID_ARG for n < 0, unknown fmt, NULL with n > 0, odd
+ * y_bf16 address.
+ */
+fp8q_status fp8q_dequantize(const uint8_t* q, void* y_bf16, int64_t n, fp8q_format fmt,
+                            const float* scale, void* stream);
+
+/*
+ * amax_and_scale_update for `num_slots` FP8 metadata slots in ONE launch,
+ * in place ("Implement fused kernel for FP8 scale update"; scale formula from
+ * "User Guide on Native XLA-FP8", section "JAX", delayed scaling).  Per slot s:
+ *   1. roll:   hist[h][s] <- hist[h-1][s] for h = H-1 .. 1 (oldest dropped);
+ *              hist[0][s] <- amax_new[s]
+ *   2. select: a = max_h hist[h][s] (ALGO_MAX; NaN wins) or hist[0][s]
+ *              (ALGO_MOST_RECENT)
+ *   3. scale:  if a is finite and > 0 and sc = RN(a / FP8_MAX) * 2^margin is
+ *              a normal float: scale[s] = sc, scale_inv[s] = RN(1 / sc);
+ *              otherwise scale[s] and scale_inv[s] are left unchanged.
+ * FP8_MAX = 448 (e4m3fn) or 57344 (e5m2): from slot_format[s] when it is not
+ * NULL (0 = e4m3fn, 1 = e5m2, any other code leaves that slot's scale alone),
+ * else from fmt for every slot.
+ *
+ * amax_history: float[history_len][num_slots], row-major, row 0 newest
+ * (device, updated in place).  amax_new: float[num_slots] (device, read).
+ * scale, scale_inv: float[num_slots] (device, updated in place).
+ * slot_format: uint8[num_slots] (device) or NULL.
+ * Errors: INVALID_ARG for history_len < 1, num_slots < 1, a NULL or
+ *         misaligned float pointer, unknown fmt or algo, margin outside
+ *         [-64, 64].  amax_new must not overlap the history.
+ */
+fp8q_status fp8q_amax_scale_update(float* amax_history, int32_t history_len, int32_t num_slots,
+                                   const float* amax_new, float* scale, float* scale_inv,
+                                   const uint8_t* slot_format, fp8q_format fmt,
+                                   fp8q_amax_algo algo, int32_t margin, void* stream);
+
+/* Static, human-readable name of a status. */
+const char* fp8q_status_string(fp8q_status status);
+
+/* Text of the calling thread's last FP8Q_ERR_CUDA ("" if none). */
+const char* fp8q_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8Q_H */

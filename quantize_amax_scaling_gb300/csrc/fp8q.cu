@@ -1,0 +1,786 @@
+// fp8q.cu -- sm_103a kernels and the C ABI of libfp8q (see include/fp8q.h).
+//
+// Sources (web pages, by title and section):
+//   "User Guide on Native XLA-FP8" (NVIDIA JAX-Toolbox), section "JAX":
+//     Q = cast(A / A_scale), DQ = cast(a_fp8) * a_scale, delayed scaling
+//     A_scale = max|A| / E4M3_MAX.
+//   "Fusion of Fp8 quantization and amax reduction kernels" (openxla/xla
+//     issue): Q and the amax reduction are memory bound; fuse them.
+//   "Implement fused kernel for FP8 scale update" (TransformerEngine PR):
+//     the whole amax_and_scale_update in one in-place kernel, all layers.
+//
+// Every kernel here streams HBM; none is a contraction, so there are no
+// tensor-core instructions.  Design points:
+//   * quantize+amax reads each bf16 once (16-byte vector loads), writes each
+//     FP8 byte once, and reduces |x| with packed NaN-propagating bf16x2 max,
+//     then one warp redux and one atomic per CTA and tensor.
+//   * the division x / scale is exact IEEE binary32 (round to nearest even)
+//     without a per-element divide: with r = RN(1/s) computed once per CTA,
+//     y0 = RN(x*r), e = fma(y0, s, -x), y = fma(-e, r, y0) is the correctly
+//     rounded quotient (Markstein's correction step, P. Markstein, "Computation
+//     of elementary functions on the IBM RISC System/6000 processor", IBM J.
+//     Res. Dev. 34(1), 1990).  This was checked for every bf16 significand
+//     against every binary32 scale significand; it is used for positive scales
+//     in [2^-60, 2^60], where no intermediate leaves the normal range while the
+//     quotient lies in [2^-18, 2^17] (outside that band the FP8 result is a
+//     signed zero or saturated, and the error there cannot change it).  Inputs
+//     are clamped to |x| <= RU_bf16(s * 2^17) first (NaN kept), so x*r cannot
+//     overflow and +-inf saturates.  Other scales use __fdiv_rn per element.
+//   * the ragged multi-tensor launch is a persistent grid-stride loop over a
+//     global tile numbering; descriptors travel by value in the kernel
+//     parameters, so the launch needs no host-to-device copy.
+//   * the scale update gives each CTA four slot columns and every history row
+//     of them, reads all rows into registers, synchronises, then writes the
+//     rows shifted by one; no other CTA touches those columns, so the in-place
+//     roll needs no grid-wide synchronisation.
+
+#include "fp8q.h"
+
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <climits>
+#include <cstdint>
+#include <cstdio>
+
+namespace {
+
+// ----------------------------------------------------------------------------
+// Error reporting
+
+thread_local char g_last_error[256] = "";
+
+fp8q_status cuda_fail(cudaError_t e, const char* where) {
+    std::snprintf(g_last_error, sizeof g_last_error, "%s: %s (%s)", where, cudaGetErrorName(e),
+                  cudaGetErrorString(e));
+    return FP8Q_ERR_CUDA;
+}
+
+fp8q_status after_launch(const char* where) {
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? FP8Q_OK : cuda_fail(e, where);
+}
+
+// ----------------------------------------------------------------------------
+// Launch geometry
+
+constexpr int kThreads = 256;                       // threads per CTA (streaming kernels)
+constexpr int kUnroll = 4;                          // 16-byte vectors in flight per thread
+constexpr int kVecElems = 8;                        // bf16 per 16-byte vector
+constexpr int kVecPerTile = kThreads * kUnroll;     // 1024 vectors
+constexpr int kTileElems = kVecPerTile * kVecElems; // 8192 elements per tile
+constexpr int kMaxDevices = 64;
+
+enum : int { kModeVec = 0, kModeScalar = 1 };
+
+// How a tensor is split: `head` scalar elements until the bf16 pointer is
+// 16-byte aligned, then `nvec` 8-element vectors, then a scalar tail of
+// fewer than 8.  If the byte pointer is not 8-byte aligned at the same
+// element the whole tensor is processed element by element.  Host and device
+// both call this, so they agree on the tile count.
+struct Split {
+    int64_t head, nvec, tiles;
+    int mode;
+};
+
+__host__ __device__ inline Split split_tensor(uintptr_t wide, uintptr_t narrow, int64_t n,
+                                              int narrow_vec_bytes) {
+    Split s;
+    if (n <= 0) {
+        s.head = 0; s.nvec = 0; s.tiles = 0; s.mode = kModeVec;
+        return s;
+    }
+    int64_t h = (int64_t)(((16u - (unsigned)(wide & 15u)) & 15u) >> 1);
+    if (h > n) h = n;
+    if (((narrow + (uintptr_t)h) & (uintptr_t)(narrow_vec_bytes - 1)) == 0) {
+        s.mode = kModeVec;
+        s.head = h;
+        s.nvec = (n - h) / kVecElems;
+        int64_t t = (s.nvec + kVecPerTile - 1) / kVecPerTile;
+        s.tiles = t > 0 ? t : 1;  // tile 0 also carries the scalar head and tail
+    } else {
+        s.mode = kModeScalar;
+        s.head = n;
+        s.nvec = 0;
+        s.tiles = (n + kTileElems - 1) / kTileElems;
+    }
+    return s;
+}
+
+// ----------------------------------------------------------------------------
+// Device helpers (inline PTX: documented instructions only)
+
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint2 ld_stream_v2(const void* p) {
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
+                 : "=r"(v.x), "=r"(v.y)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_v2(void* p, uint2 v) {
+    asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+
+__device__ __forceinline__ void st_v4(void* p, uint4 v) {
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+// max(|a|, |b|) per bf16 lane; NaN in either gives the canonical NaN.  The
+// result's sign is sign(a) ^ sign(b) and is ignored by every caller.
+__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// sign(a) * min(|a|, t) per bf16 lane for t >= 0; NaN stays NaN.
+__device__ __forceinline__ uint32_t bf16x2_clamp(uint32_t a, uint32_t t2) {
+    uint32_t d;
+    asm("min.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(t2));
+    return d;
+}
+
+// Two binary32 values -> two saturated, RNE FP8 codes; `lo` lands in the low byte.
+template <int FMT>
+__device__ __forceinline__ uint32_t cvt_fp8x2(float lo, float hi) {
+    uint16_t d;
+    if (FMT == FP8Q_E4M3FN)
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+    else
+        asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+// Two FP8 codes (low byte first) -> two half values, exact.
+template <int FMT>
+__device__ __forceinline__ uint32_t fp8x2_to_f16x2(uint32_t pair) {
+    uint32_t d;
+    if (FMT == FP8Q_E4M3FN) {
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"((uint16_t)pair));
+    } else {
+        // an e5m2 code is the upper byte of the half with the same value
+        d = __byte_perm(pair, 0u, 0x1404);  // bytes: [0]=0, [1]=b0, [2]=0, [3]=b1
+    }
+    return d;
+}
+
+__device__ __forceinline__ float f16_lo(uint32_t h2) {
+    float f;
+    asm("{ .reg .b16 l, h; mov.b32 {l, h}, %1; cvt.f32.f16 %0, l; }" : "=f"(f) : "r"(h2));
+    return f;
+}
+
+__device__ __forceinline__ float f16_hi(uint32_t h2) {
+    float f;
+    asm("{ .reg .b16 l, h; mov.b32 {l, h}, %1; cvt.f32.f16 %0, h; }" : "=f"(f) : "r"(h2));
+    return f;
+}
+
+// Two binary32 -> packed bf16x2, round to nearest even; `lo` in the low half.
+__device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+// ----------------------------------------------------------------------------
+// Quantize + amax
+
+// Per-tensor constants a CTA derives from the scale.
+struct QScale {
+    float s;      // the scale
+    float r;      // RN(1 / s)
+    uint32_t t2;  // clamp bound RU_bf16(s * 2^17), in both bf16 lanes
+    bool fast;    // s in [2^-60, 2^60]
+};
+
+__device__ __forceinline__ QScale make_qscale(const float* scale) {
+    QScale q;
+    q.s = __ldg(scale);
+    q.fast = (q.s >= 0x1p-60f) && (q.s <= 0x1p60f);  // false for NaN, <= 0, inf, tiny
+    q.r = q.fast ? __frcp_rn(q.s) : 1.0f;
+    uint32_t tb = q.fast ? __float_as_uint(q.s * 131072.0f) : 0u;  // exact: s * 2^17
+    tb = (tb + 0xFFFFu) & 0xFFFF0000u;                                 // round up to bf16
+    q.t2 = (tb >> 16) | tb;
+    return q;
+}
+
+template <bool FAST>
+__device__ __forceinline__ float divide(float x, const QScale& c) {
+    if (FAST) {
+        float y0 = __fmul_rn(x, c.r);
+        float e = __fmaf_rn(y0, c.s, -x);
+        return __fmaf_rn(-e, c.r, y0);
+    }
+    return __fdiv_rn(x, c.s);
+}
+
+// Two bf16 (one 32-bit word, element 0 in the low half) -> two FP8 codes.
+template <int FMT, bool FAST>
+__device__ __forceinline__ uint32_t quant_pair(uint32_t w, const QScale& c) {
+    if (FAST) w = bf16x2_clamp(w, c.t2);
+    const float f0 = __uint_as_float(w << 16);
+    const float f1 = __uint_as_float(w & 0xFFFF0000u);
+    return cvt_fp8x2<FMT>(divide<FAST>(f0, c), divide<FAST>(f1, c));
+}
+
+// |x| bits of one bf16 (low half of w), as a binary32 bit pattern.
+__device__ __forceinline__ uint32_t abs_bits_lo(uint32_t w) { return (w & 0x7FFFu) << 16; }
+
+struct QTensor {
+    const uint16_t* x;
+    uint8_t* q;
+    const float* scale;
+    float* amax;
+    int64_t n;
+    int64_t tile_end;  // exclusive end of this tensor's tiles in the global numbering
+};
+
+template <int MAXT>
+struct QList {
+    int64_t total_tiles;
+    int32_t count;
+    int32_t pad;
+    QTensor t[MAXT];
+};
+
+struct QCursor {
+    const uint16_t* x;
+    uint8_t* q;
+    float* amax;
+    int64_t n, head, nvec, tile_begin;
+    int mode;
+    QScale c;
+};
+
+__device__ __forceinline__ QCursor make_cursor(const QTensor& t, int64_t tile_begin) {
+    QCursor k;
+    Split sp = split_tensor((uintptr_t)t.x, (uintptr_t)t.q, t.n, 8);
+    k.x = t.x;
+    k.q = t.q;
+    k.amax = t.amax;
+    k.n = t.n;
+    k.head = sp.head;
+    k.nvec = sp.nvec;
+    k.mode = sp.mode;
+    k.tile_begin = tile_begin;
+    k.c = make_qscale(t.scale);
+    return k;
+}
+
+// CTA-wide max of the per-thread |x| bits, then one atomic into *amax.
+// Every thread of the CTA must call it (it synchronises).
+__device__ __forceinline__ void flush_amax(uint32_t m2, uint32_t ms, float* amax, uint32_t* red) {
+    uint32_t m = max(max(abs_bits_lo(m2), m2 & 0x7FFF0000u), ms);
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t b = red[0];
+#pragma unroll
+        for (int w = 1; w < kThreads / 32; ++w) b = max(b, red[w]);
+        // |x| bit patterns order like the values (NaN above +inf); a signed
+        // compare also lets any non-negative result beat a negative seed.
+        atomicMax(reinterpret_cast<int*>(amax), (int)b);
+    }
+    __syncthreads();  // `red` is reused by the next flush
+}
+
+template <int FMT, bool FAST>
+__device__ __forceinline__ void quant_vec_tile(const QCursor& k, int64_t local, uint32_t& m2) {
+    const uint16_t* xb = k.x + k.head;
+    uint8_t* qb = k.q + k.head;
+    const int64_t v0 = local * kVecPerTile + threadIdx.x;
+    uint4 w[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+        const int64_t v = v0 + (int64_t)u * kThreads;
+        if (v < k.nvec) w[u] = ld_stream_v4(xb + v * kVecElems);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+        const int64_t v = v0 + (int64_t)u * kThreads;
+        if (v < k.nvec) {
+            m2 = bf16x2_absmax(m2, bf16x2_absmax(bf16x2_absmax(w[u].x, w[u].y),
+                                                 bf16x2_absmax(w[u].z, w[u].w)));
+            uint2 o;
+            o.x = quant_pair<FMT, FAST>(w[u].x, k.c) | (quant_pair<FMT, FAST>(w[u].y, k.c) << 16);
+            o.y = quant_pair<FMT, FAST>(w[u].z, k.c) | (quant_pair<FMT, FAST>(w[u].w, k.c) << 16);
+            st_v2(qb + v * kVecElems, o);
+        }
+    }
+}
+
+template <int FMT, bool FAST>
+__device__ __forceinline__ void quant_scalar(const QCursor& k, int64_t i, uint32_t& ms) {
+    const uint32_t w = k.x[i];
+    ms = max(ms, abs_bits_lo(w));
+    k.q[i] = (uint8_t)(quant_pair<FMT, FAST>(w, k.c) & 0xFFu);
+}
+
+template <int FMT, bool FAST>
+__device__ __forceinline__ void quant_tile(const QCursor& k, int64_t local, uint32_t& m2,
+                                           uint32_t& ms) {
+    if (k.mode == kModeVec) {
+        quant_vec_tile<FMT, FAST>(k, local, m2);
+        if (local == 0) {  // scalar head (< 8) and tail (< 8) elements
+            const int64_t tail0 = k.head + k.nvec * kVecElems;
+            const int64_t nscalar = k.head + (k.n - tail0);
+            for (int64_t j = threadIdx.x; j < nscalar; j += kThreads)
+                quant_scalar<FMT, FAST>(k, j < k.head ? j : tail0 + (j - k.head), ms);
+        }
+    } else {
+        const int64_t base = local * kTileElems;
+        const int64_t end = min(base + (int64_t)kTileElems, k.n);
+        for (int64_t i = base + threadIdx.x; i < end; i += kThreads) quant_scalar<FMT, FAST>(k, i, ms);
+    }
+}
+
+template <int FMT, int MAXT>
+__global__ void __launch_bounds__(kThreads) quantize_amax_kernel(const __grid_constant__ QList<MAXT> L) {
+    __shared__ uint32_t red[kThreads / 32];
+    int64_t tile = blockIdx.x;
+    if (tile >= L.total_tiles) return;
+    int ti = 0;
+    while (tile >= L.t[ti].tile_end) ++ti;
+    QCursor k = make_cursor(L.t[ti], ti ? L.t[ti - 1].tile_end : 0);
+    uint32_t m2 = 0, ms = 0;
+    for (; tile < L.total_tiles; tile += gridDim.x) {
+        if (tile >= L.t[ti].tile_end) {  // uniform across the CTA
+            flush_amax(m2, ms, k.amax, red);
+            m2 = 0;
+            ms = 0;
+            do { ++ti; } while (tile >= L.t[ti].tile_end);
+            k = make_cursor(L.t[ti], L.t[ti - 1].tile_end);
+        }
+        const int64_t local = tile - k.tile_begin;
+        if (k.c.fast) quant_tile<FMT, true>(k, local, m2, ms);
+        else          quant_tile<FMT, false>(k, local, m2, ms);
+    }
+    flush_amax(m2, ms, k.amax, red);
+}
+
+// ----------------------------------------------------------------------------
+// Dequantize
+
+template <int FMT>
+__device__ __forceinline__ uint32_t dequant_pair(uint32_t pair, float s) {
+    const uint32_t h2 = fp8x2_to_f16x2<FMT>(pair);
+    return cvt_bf16x2(__fmul_rn(f16_lo(h2), s), __fmul_rn(f16_hi(h2), s));
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kThreads)
+    dequantize_kernel(const uint8_t* __restrict__ q, uint16_t* __restrict__ y, int64_t n,
+                      const float* __restrict__ scale, int64_t tiles) {
+    const float s = __ldg(scale);
+    const Split sp = split_tensor((uintptr_t)y, (uintptr_t)q, n, 8);
+    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+        if (sp.mode == kModeVec) {
+            const uint8_t* qb = q + sp.head;
+            uint16_t* yb = y + sp.head;
+            const int64_t v0 = tile * kVecPerTile + threadIdx.x;
+            uint2 w[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int64_t v = v0 + (int64_t)u * kThreads;
+                if (v < sp.nvec) w[u] = ld_stream_v2(qb + v * kVecElems);
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int64_t v = v0 + (int64_t)u * kThreads;
+                if (v < sp.nvec) {
+                    uint4 o;
+                    o.x = dequant_pair<FMT>(w[u].x & 0xFFFFu, s);
+                    o.y = dequant_pair<FMT>(w[u].x >> 16, s);
+                    o.z = dequant_pair<FMT>(w[u].y & 0xFFFFu, s);
+                    o.w = dequant_pair<FMT>(w[u].y >> 16, s);
+                    st_v4(yb + v * kVecElems, o);
+                }
+            }
+            if (tile == 0) {
+                const int64_t tail0 = sp.head + sp.nvec * kVecElems;
+                const int64_t nscalar = sp.head + (n - tail0);
+                for (int64_t j = threadIdx.x; j < nscalar; j += kThreads) {
+                    const int64_t i = j < sp.head ? j : tail0 + (j - sp.head);
+                    y[i] = (uint16_t)(dequant_pair<FMT>(q[i], s) & 0xFFFFu);
+                }
+            }
+        } else {
+            const int64_t base = tile * kTileElems;
+            const int64_t end = min(base + (int64_t)kTileElems, n);
+            for (int64_t i = base + threadIdx.x; i < end; i += kThreads)
+                y[i] = (uint16_t)(dequant_pair<FMT>(q[i], s) & 0xFFFFu);
+        }
+    }
+}
+
+// ----------------------------------------------------------------------------
+// amax history roll + amax selection + scale update
+
+constexpr int kUpdThreads = 256;
+constexpr int kUpdCols = 4;                           // slot columns per CTA
+constexpr int kUpdRows = 4;                           // rows per thread per chunk
+constexpr int kUpdChunk = kUpdThreads * kUpdRows;     // 1024 history rows per chunk
+
+struct UpdArgs {
+    float* hist;
+    const float* amax_new;
+    float* scale;
+    float* scale_inv;
+    const uint8_t* slot_format;
+    int32_t H, S;
+    int32_t fmt, algo, margin;
+};
+
+// Order-preserving integer key of a non-NaN float (so an integer max is a
+// float max); NaN is tracked separately.
+__device__ __forceinline__ int float_key(float f) {
+    const int b = __float_as_int(f);
+    return b ^ ((b >> 31) & 0x7FFFFFFF);
+}
+
+__device__ __forceinline__ float key_float(int k) { return __int_as_float(k ^ ((k >> 31) & 0x7FFFFFFF)); }
+
+template <bool VEC4>
+__device__ __forceinline__ float4 load_row(const UpdArgs& a, int64_t row, int c0, int ncols) {
+    const float* p = a.hist + row * a.S + c0;
+    if (VEC4) return *reinterpret_cast<const float4*>(p);
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (ncols > 0) v.x = p[0];
+    if (ncols > 1) v.y = p[1];
+    if (ncols > 2) v.z = p[2];
+    if (ncols > 3) v.w = p[3];
+    return v;
+}
+
+template <bool VEC4>
+__device__ __forceinline__ void store_row(const UpdArgs& a, int64_t row, int c0, int ncols, float4 v) {
+    float* p = a.hist + row * a.S + c0;
+    if (VEC4) {
+        *reinterpret_cast<float4*>(p) = v;
+        return;
+    }
+    if (ncols > 0) p[0] = v.x;
+    if (ncols > 1) p[1] = v.y;
+    if (ncols > 2) p[2] = v.z;
+    if (ncols > 3) p[3] = v.w;
+}
+
+__device__ __forceinline__ void fold(int (&key)[4], bool (&nan)[4], float4 v) {
+    const float c[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        nan[j] |= isnan(c[j]);
+        key[j] = max(key[j], float_key(c[j]));
+    }
+}
+
+template <bool VEC4>
+__global__ void __launch_bounds__(kUpdThreads) amax_scale_update_kernel(const UpdArgs a) {
+    __shared__ int s_key[kUpdThreads / 32][kUpdCols];
+    __shared__ int s_nan[kUpdThreads / 32][kUpdCols];
+    const int c0 = blockIdx.x * kUpdCols;
+    const int ncols = min(kUpdCols, a.S - c0);
+    const int64_t H = a.H;
+    const bool want_max = (a.algo == FP8Q_ALGO_MAX);
+
+    int key[4] = {INT_MIN, INT_MIN, INT_MIN, INT_MIN};
+    bool nan[4] = {false, false, false, false};
+
+    float4 cur[kUpdRows], nxt[kUpdRows];
+#pragma unroll
+    for (int k = 0; k < kUpdRows; ++k) {
+        const int64_t r = threadIdx.x + (int64_t)k * kUpdThreads;
+        if (r < H) cur[k] = load_row<VEC4>(a, r, c0, ncols);
+    }
+    for (int64_t base = 0; base < H; base += kUpdChunk) {
+        const bool more = base + kUpdChunk < H;
+        if (more) {
+#pragma unroll
+            for (int k = 0; k < kUpdRows; ++k) {
+                const int64_t r = base + kUpdChunk + threadIdx.x + (int64_t)k * kUpdThreads;
+                if (r < H) nxt[k] = load_row<VEC4>(a, r, c0, ncols);
+            }
+        }
+        if (want_max) {
+            // old rows 0..H-2 survive the roll; row H-1 drops out of the window
+#pragma unroll
+            for (int k = 0; k < kUpdRows; ++k) {
+                const int64_t r = base + threadIdx.x + (int64_t)k * kUpdThreads;
+                if (r + 1 < H) fold(key, nan, cur[k]);
+            }
+        }
+        __syncthreads();  // every read of rows <= base + 2*chunk - 1 precedes the writes below
+#pragma unroll
+        for (int k = 0; k < kUpdRows; ++k) {
+            const int64_t r = base + threadIdx.x + (int64_t)k * kUpdThreads;
+            if (r + 1 < H) store_row<VEC4>(a, r + 1, c0, ncols, cur[k]);
+        }
+        if (more) {
+#pragma unroll
+            for (int k = 0; k < kUpdRows; ++k) cur[k] = nxt[k];
+        }
+    }
+    // Row 0 was read before the first barrier; now it receives the new amax.
+    if (threadIdx.x < ncols) a.hist[c0 + threadIdx.x] = a.amax_new[c0 + threadIdx.x];
+
+    if (want_max) {
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int kw = __reduce_max_sync(0xFFFFFFFFu, key[j]);
+            const bool nw = __any_sync(0xFFFFFFFFu, nan[j]);
+            if (lane == 0) {
+                s_key[warp][j] = kw;
+                s_nan[warp][j] = nw;
+            }
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x < ncols) {
+        const int j = threadIdx.x;
+        const int s = c0 + j;
+        const float newest = a.amax_new[s];
+        float amax = newest;
+        if (want_max) {
+            int kb = INT_MIN;
+            bool nb = isnan(newest);
+            for (int w = 0; w < kUpdThreads / 32; ++w) {
+                kb = max(kb, s_key[w][j]);
+                nb |= (s_nan[w][j] != 0);
+            }
+            if (H > 1) amax = fmaxf(amax, key_float(kb));
+            if (nb) amax = __int_as_float(0x7FC00000);
+        }
+        const int f = a.slot_format ? (int)a.slot_format[s] : a.fmt;
+        if ((f == FP8Q_E4M3FN || f == FP8Q_E5M2) && isfinite(amax) && amax > 0.0f) {
+            const float fp8max = (f == FP8Q_E4M3FN) ? 448.0f : 57344.0f;
+            const float pow2m = __uint_as_float((uint32_t)(127 + a.margin) << 23);  // exact 2^margin
+            const float sc = __fmul_rn(__fdiv_rn(amax, fp8max), pow2m);
+            if (sc >= 0x1p-126f && sc <= 0x1.fffffep127f) {  // normal and finite
+                a.scale[s] = sc;
+                a.scale_inv[s] = __frcp_rn(sc);
+            }
+        }
+    }
+}
+
+// ----------------------------------------------------------------------------
+// Host side: grid sizing
+
+int current_device(int* dev) {
+    cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (*dev < 0 || *dev >= kMaxDevices) {
+        std::snprintf(g_last_error, sizeof g_last_error, "device ordinal %d beyond %d", *dev, kMaxDevices);
+        return FP8Q_ERR_CUDA;
+    }
+    return FP8Q_OK;
+}
+
+std::atomic<int> g_sm_count[kMaxDevices];
+
+fp8q_status sm_count(int dev, int* out) {
+    int v = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (v == 0) {
+        cudaError_t e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+        g_sm_count[dev].store(v, std::memory_order_relaxed);
+    }
+    *out = v;
+    return FP8Q_OK;
+}
+
+// Resident CTAs per SM for one kernel instance, cached per device.
+template <typename Kernel>
+fp8q_status blocks_per_sm(Kernel kernel, int threads, int dev, std::atomic<int>* cache, int* out) {
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v == 0) {
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kernel, threads, 0);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+        if (v < 1) v = 1;
+        cache[dev].store(v, std::memory_order_relaxed);
+    }
+    *out = v;
+    return FP8Q_OK;
+}
+
+// Persistent grid: as many CTAs as fit on the GPU at once, never more than tiles.
+template <typename Kernel>
+fp8q_status persistent_grid(Kernel kernel, std::atomic<int>* cache, int64_t tiles, int* grid) {
+    int dev, sms, per_sm;
+    fp8q_status st;
+    if ((st = (fp8q_status)current_device(&dev)) != FP8Q_OK) return st;
+    if ((st = sm_count(dev, &sms)) != FP8Q_OK) return st;
+    if ((st = blocks_per_sm(kernel, kThreads, dev, cache, &per_sm)) != FP8Q_OK) return st;
+    const int64_t full = (int64_t)sms * per_sm;
+    *grid = (int)(tiles < full ? tiles : full);
+    return FP8Q_OK;
+}
+
+bool valid_fmt(int fmt) { return fmt == FP8Q_E4M3FN || fmt == FP8Q_E5M2; }
+
+// ----------------------------------------------------------------------------
+// Host side: quantize launchers
+
+template <int FMT, int MAXT>
+fp8q_status launch_quantize(const fp8q_tensor* list, int32_t count, cudaStream_t stream) {
+    static std::atomic<int> occ[kMaxDevices];
+    QList<MAXT> L;
+    int64_t tiles = 0;
+    int m = 0;
+    for (int32_t i = 0; i < count; ++i) {
+        const fp8q_tensor& t = list[i];
+        const Split sp = split_tensor((uintptr_t)t.x_bf16, (uintptr_t)t.q, t.n, 8);
+        if (sp.tiles == 0) continue;  // empty tensors take no tiles and are skipped
+        QTensor& d = L.t[m++];
+        d.x = static_cast<const uint16_t*>(t.x_bf16);
+        d.q = t.q;
+        d.scale = t.scale;
+        d.amax = t.amax;
+        d.n = t.n;
+        tiles += sp.tiles;
+        d.tile_end = tiles;
+    }
+    if (tiles == 0) return FP8Q_OK;
+    L.total_tiles = tiles;
+    L.count = m;
+    L.pad = 0;
+    int grid;
+    fp8q_status st = persistent_grid(quantize_amax_kernel<FMT, MAXT>, occ, tiles, &grid);
+    if (st != FP8Q_OK) return st;
+    quantize_amax_kernel<FMT, MAXT><<<grid, kThreads, 0, stream>>>(L);
+    return after_launch("quantize_amax_kernel");
+}
+
+template <int FMT>
+fp8q_status dispatch_quantize(const fp8q_tensor* list, int32_t count, cudaStream_t stream) {
+    int32_t live = 0;
+    for (int32_t i = 0; i < count; ++i) live += list[i].n > 0;
+    if (live <= 1) return launch_quantize<FMT, 1>(list, count, stream);
+    if (live <= 8) return launch_quantize<FMT, 8>(list, count, stream);
+    if (live <= 64) return launch_quantize<FMT, 64>(list, count, stream);
+    return launch_quantize<FMT, FP8Q_MAX_TENSORS>(list, count, stream);
+}
+
+fp8q_status check_tensor(const fp8q_tensor& t) {
+    if (t.n < 0) return FP8Q_ERR_INVALID_ARG;
+    if (t.n == 0) return FP8Q_OK;
+    if (!t.x_bf16 || !t.q || !t.scale || !t.amax) return FP8Q_ERR_INVALID_ARG;
+    if (((uintptr_t)t.x_bf16 & 1u) || ((uintptr_t)t.scale & 3u) || ((uintptr_t)t.amax & 3u))
+        return FP8Q_ERR_INVALID_ARG;
+    return FP8Q_OK;
+}
+
+template <int FMT>
+fp8q_status launch_dequantize(const uint8_t* q, void* y, int64_t n, const float* scale,
+                              cudaStream_t stream) {
+    static std::atomic<int> occ[kMaxDevices];
+    const Split sp = split_tensor((uintptr_t)y, (uintptr_t)q, n, 8);
+    int grid;
+    fp8q_status st = persistent_grid(dequantize_kernel<FMT>, occ, sp.tiles, &grid);
+    if (st != FP8Q_OK) return st;
+    dequantize_kernel<FMT><<<grid, kThreads, 0, stream>>>(q, static_cast<uint16_t*>(y), n, scale, sp.tiles);
+    return after_launch("dequantize_kernel");
+}
+
+}  // namespace
+
+// ----------------------------------------------------------------------------
+// C ABI
+
+extern "C" {
+
+fp8q_status fp8q_quantize_amax(const void* x_bf16, uint8_t* q, int64_t n, fp8q_format fmt,
+                               const float* scale, float* amax, void* stream) {
+    if (!valid_fmt(fmt)) return FP8Q_ERR_INVALID_ARG;
+    const fp8q_tensor t = {x_bf16, q, n, scale, amax};
+    fp8q_status st = check_tensor(t);
+    if (st != FP8Q_OK || n == 0) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return fmt == FP8Q_E4M3FN ? launch_quantize<FP8Q_E4M3FN, 1>(&t, 1, s)
+                              : launch_quantize<FP8Q_E5M2, 1>(&t, 1, s);
+}
+
+fp8q_status fp8q_multi_quantize_amax(const fp8q_tensor* list, int32_t count, fp8q_format fmt,
+                                     void* stream) {
+    if (!valid_fmt(fmt) || count < 0) return FP8Q_ERR_INVALID_ARG;
+    if (count > FP8Q_MAX_TENSORS) return FP8Q_ERR_TOO_MANY_TENSORS;
+    if (count == 0) return FP8Q_OK;
+    if (!list) return FP8Q_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < count; ++i) {
+        fp8q_status st = check_tensor(list[i]);
+        if (st != FP8Q_OK) return st;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return fmt == FP8Q_E4M3FN ? dispatch_quantize<FP8Q_E4M3FN>(list, count, s)
+                              : dispatch_quantize<FP8Q_E5M2>(list, count, s);
+}
+
+fp8q_status fp8q_dequantize(const uint8_t* q, void* y_bf16, int64_t n, fp8q_format fmt,
+                            const float* scale, void* stream) {
+    if (!valid_fmt(fmt) || n < 0) return FP8Q_ERR_INVALID_ARG;
+    if (n == 0) return FP8Q_OK;
+    if (!q || !y_bf16 || !scale || ((uintptr_t)y_bf16 & 1u) || ((uintptr_t)scale & 3u))
+        return FP8Q_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return fmt == FP8Q_E4M3FN ? launch_dequantize<FP8Q_E4M3FN>(q, y_bf16, n, scale, s)
+                              : launch_dequantize<FP8Q_E5M2>(q, y_bf16, n, scale, s);
+}
+
+fp8q_status fp8q_amax_scale_update(float* amax_history, int32_t history_len, int32_t num_slots,
+                                   const float* amax_new, float* scale, float* scale_inv,
+                                   const uint8_t* slot_format, fp8q_format fmt,
+                                   fp8q_amax_algo algo, int32_t margin, void* stream) {
+    if (history_len < 1 || num_slots < 1 || !valid_fmt(fmt)) return FP8Q_ERR_INVALID_ARG;
+    if (algo != FP8Q_ALGO_MAX && algo != FP8Q_ALGO_MOST_RECENT) return FP8Q_ERR_INVALID_ARG;
+    if (margin < -64 || margin > 64) return FP8Q_ERR_INVALID_ARG;
+    const void* fp[4] = {amax_history, amax_new, scale, scale_inv};
+    for (const void* p : fp)
+        if (!p || ((uintptr_t)p & 3u)) return FP8Q_ERR_INVALID_ARG;
+    UpdArgs a;
+    a.hist = amax_history;
+    a.amax_new = amax_new;
+    a.scale = scale;
+    a.scale_inv = scale_inv;
+    a.slot_format = slot_format;
+    a.H = history_len;
+    a.S = num_slots;
+    a.fmt = fmt;
+    a.algo = algo;
+    a.margin = margin;
+    const int grid = (num_slots + kUpdCols - 1) / kUpdCols;
+    const bool vec4 = ((uintptr_t)amax_history & 15u) == 0 && (num_slots % kUpdCols) == 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (vec4) amax_scale_update_kernel<true><<<grid, kUpdThreads, 0, s>>>(a);
+    else      amax_scale_update_kernel<false><<<grid, kUpdThreads, 0, s>>>(a);
+    return after_launch("amax_scale_update_kernel");
+}
+
+const char* fp8q_status_string(fp8q_status status) {
+    switch (status) {
+        case FP8Q_OK: return "FP8Q_OK";
+        case FP8Q_ERR_INVALID_ARG: return "FP8Q_ERR_INVALID_ARG";
+        case FP8Q_ERR_UNSUPPORTED: return "FP8Q_ERR_UNSUPPORTED";
+        case FP8Q_ERR_CUDA: return "FP8Q_ERR_CUDA";
+        case FP8Q_ERR_TOO_MANY_TENSORS: return "FP8Q_ERR_TOO_MANY_TENSORS";
+    }
+    return "FP8Q_ERR_UNKNOWN";
+}
+
+const char* fp8q_last_cuda_error(void) { return g_last_error; }
+
+}  // extern "C"

@@ -1,0 +1,188 @@
+"""Thin Python binding of libfp8q's C ABI (include/fp8q.h).
+
+Argument marshalling only: every step of the FP8 path runs in the CUDA
+kernels of libfp8q.so.  Tensors are torch CUDA tensors (torch supplies device
+memory and streams); the functions keep the C names and raise Fp8qError on a
+non-OK status.  If the library has not been built, loading fails loudly --
+there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+E4M3FN = 0
+E5M2 = 1
+ALGO_MAX = 0
+ALGO_MOST_RECENT = 1
+MAX_TENSORS = 512
+
+STATUS = {0: "FP8Q_OK", 1: "FP8Q_ERR_INVALID_ARG", 2: "FP8Q_ERR_UNSUPPORTED", 3: "FP8Q_ERR_CUDA",
+          4: "FP8Q_ERR_TOO_MANY_TENSORS"}
+
+# Every symbol the header declares.
+EXPORTS = ("fp8q_quantize_amax", "fp8q_multi_quantize_amax", "fp8q_dequantize",
+           "fp8q_amax_scale_update", "fp8q_status_string", "fp8q_last_cuda_error")
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfp8q.so")
+
+
+class Fp8qError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str = ""):
+        self.status = status
+        msg = f"{where}: {STATUS.get(status, status)}"
+        if detail:
+            msg += f" ({detail})"
+        super().__init__(msg)
+
+
+class Tensor(ctypes.Structure):
+    """fp8q_tensor: one entry of a ragged list."""
+    _fields_ = [("x_bf16", ctypes.c_void_p), ("q", ctypes.c_void_p), ("n", ctypes.c_int64),
+                ("scale", ctypes.c_void_p), ("amax", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libfp8q.so (built by ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build the CUDA library first "
+                               "(python -c 'import __graft_entry__ as g; g.build()')")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i64, i32, c_int = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int
+        L.fp8q_quantize_amax.argtypes = [vp, vp, i64, c_int, vp, vp, vp]
+        L.fp8q_multi_quantize_amax.argtypes = [vp, i32, c_int, vp]
+        L.fp8q_dequantize.argtypes = [vp, vp, i64, c_int, vp, vp]
+        L.fp8q_amax_scale_update.argtypes = [vp, i32, i32, vp, vp, vp, vp, c_int, c_int, i32, vp]
+        for f in ("fp8q_quantize_amax", "fp8q_multi_quantize_amax", "fp8q_dequantize",
+                  "fp8q_amax_scale_update"):
+            getattr(L, f).restype = c_int
+        L.fp8q_status_string.argtypes = [c_int]
+        L.fp8q_status_string.restype = ctypes.c_char_p
+        L.fp8q_last_cuda_error.argtypes = []
+        L.fp8q_last_cuda_error.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        detail = lib().fp8q_last_cuda_error().decode() if status == 3 else ""
+        raise Fp8qError(status, where, detail)
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+_FP8_DTYPES = None
+
+
+def _dev(t, kind, name):
+    """Reject anything but a contiguous CUDA tensor of the right element type.
+
+    Pointers reach the kernels unchanged, so a host tensor must never get
+    through.  ``kind`` is "bf16", "u8" (uint8 or a float8 dtype) or "f32".
+    """
+    global _FP8_DTYPES
+    if t is None:
+        return
+    import torch
+    if _FP8_DTYPES is None:
+        _FP8_DTYPES = (torch.uint8, torch.float8_e4m3fn, torch.float8_e5m2)
+    ok = {"bf16": (torch.bfloat16,), "u8": _FP8_DTYPES, "f32": (torch.float32,)}[kind]
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype not in ok:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected one of {ok}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _numel(t):
+    return 0 if t is None else t.numel()
+
+
+def fp8q_quantize_amax(x, q, fmt, scale, amax, stream=None):
+    """q = FP8(x / scale) (saturating RNE) and amax = max(amax, max|x|) in one launch."""
+    n = _numel(x)
+    if q is not None and _numel(q) != n:
+        raise ValueError("q must have as many elements as x")
+    for t, k, nm in ((x, "bf16", "x"), (q, "u8", "q"), (scale, "f32", "scale"), (amax, "f32", "amax")):
+        _dev(t, k, nm)
+    _check(lib().fp8q_quantize_amax(_ptr(x), _ptr(q), n, fmt, _ptr(scale), _ptr(amax),
+                                    _stream(stream)), "fp8q_quantize_amax")
+
+
+def fp8q_multi_quantize_amax(xs, qs, fmt, scales, amaxes, stream=None):
+    """fp8q_quantize_amax over a ragged list of tensors, one launch.
+
+    ``scales`` and ``amaxes`` are sequences of one-element float32 tensors (or
+    views into one vector) aligned with ``xs``.
+    """
+    count = len(xs)
+    arr = (Tensor * max(1, count))()
+    for i in range(count):
+        n = _numel(xs[i])
+        if _numel(qs[i]) != n:
+            raise ValueError(f"tensor {i}: q must have as many elements as x")
+        for t, k, nm in ((xs[i], "bf16", "x"), (qs[i], "u8", "q"), (scales[i], "f32", "scale"),
+                         (amaxes[i], "f32", "amax")):
+            _dev(t, k, f"{nm}[{i}]")
+        arr[i].x_bf16 = _ptr(xs[i])
+        arr[i].q = _ptr(qs[i])
+        arr[i].n = n
+        arr[i].scale = _ptr(scales[i])
+        arr[i].amax = _ptr(amaxes[i])
+    _check(lib().fp8q_multi_quantize_amax(ctypes.cast(arr, ctypes.c_void_p), count, fmt,
+                                          _stream(stream)), "fp8q_multi_quantize_amax")
+
+
+def fp8q_dequantize(q, y, fmt, scale, stream=None):
+    """y = bf16_rne(float(q) * scale)."""
+    n = _numel(q)
+    if y is not None and _numel(y) != n:
+        raise ValueError("y must have as many elements as q")
+    for t, k, nm in ((q, "u8", "q"), (y, "bf16", "y"), (scale, "f32", "scale")):
+        _dev(t, k, nm)
+    _check(lib().fp8q_dequantize(_ptr(q), _ptr(y), n, fmt, _ptr(scale), _stream(stream)),
+           "fp8q_dequantize")
+
+
+def fp8q_amax_scale_update(history, amax_new, scale, scale_inv, fmt=E4M3FN, algo=ALGO_MAX,
+                           margin=0, slot_format=None, stream=None):
+    """In-place amax-history roll, amax selection and scale/scale_inv update.
+
+    ``history`` is a float32 [history_len, num_slots] tensor, row 0 newest.
+    """
+    if history.dim() != 2:
+        raise ValueError("history must be [history_len, num_slots]")
+    H, S = history.shape
+    for t, k, nm in ((history, "f32", "history"), (amax_new, "f32", "amax_new"),
+                     (scale, "f32", "scale"), (scale_inv, "f32", "scale_inv"),
+                     (slot_format, "u8", "slot_format")):
+        _dev(t, k, nm)
+    for t, nm in ((amax_new, "amax_new"), (scale, "scale"), (scale_inv, "scale_inv"),
+                  (slot_format, "slot_format")):
+        if t is not None and t.numel() != S:
+            raise ValueError(f"{nm} must have num_slots={S} elements")
+    _check(lib().fp8q_amax_scale_update(_ptr(history), H, S, _ptr(amax_new), _ptr(scale),
+                                        _ptr(scale_inv), _ptr(slot_format), fmt, algo, margin,
+                                        _stream(stream)), "fp8q_amax_scale_update")
+
+
+def status_string(status: int) -> str:
+    return lib().fp8q_status_string(status).decode()

@@ -1,0 +1,137 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every function include/fp8q.h declares, and rejects bad arguments before it
+touches CUDA (so these calls launch nothing)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HDR = os.path.join(ROOT, "include", "fp8q.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from quantize_amax_scaling_gb300 import build, fp8q
+    build.build()
+    return fp8q.lib()
+
+
+def declared_functions():
+    text = open(HDR).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+char\s*\*|fp8q_status)\s+(fp8q_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_four_operations():
+    names = declared_functions()
+    for f in ("fp8q_quantize_amax", "fp8q_multi_quantize_amax", "fp8q_dequantize",
+              "fp8q_amax_scale_update", "fp8q_status_string", "fp8q_last_cuda_error"):
+        assert f in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    from quantize_amax_scaling_gb300 import fp8q
+    names = declared_functions()
+    assert sorted(fp8q.EXPORTS) == names
+    for f in names:
+        assert hasattr(L, f), f
+
+
+def test_status_strings(L):
+    from quantize_amax_scaling_gb300 import fp8q
+    for code, name in fp8q.STATUS.items():
+        assert fp8q.status_string(code) == name
+    assert L.fp8q_last_cuda_error() == b""
+
+
+INVALID, TOO_MANY, OK = 1, 4, 0
+P = ctypes.c_void_p(0x10000)       # never dereferenced: every call below fails validation first
+ODD = ctypes.c_void_p(0x10001)
+
+
+def test_quantize_argument_errors(L):
+    q = L.fp8q_quantize_amax
+    assert q(None, None, 0, 0, None, None, None) == OK            # empty: nothing to do
+    assert q(P, P, -1, 0, P, P, None) == INVALID
+    assert q(P, P, 5, 2, P, P, None) == INVALID                   # unknown format
+    assert q(P, P, 0, 7, P, P, None) == INVALID                   # unknown format even when empty
+    for args in ((None, P, P, P), (P, None, P, P), (P, P, None, P), (P, P, P, None)):
+        x, qq, s, a = args
+        assert q(x, qq, 5, 0, s, a, None) == INVALID
+    assert q(ODD, P, 5, 0, P, P, None) == INVALID                 # bf16 pointer must be even
+    assert q(P, P, 5, 0, ctypes.c_void_p(0x10002), P, None) == INVALID  # float pointer alignment
+
+
+def test_multi_argument_errors(L):
+    from quantize_amax_scaling_gb300.fp8q import Tensor
+    m = L.fp8q_multi_quantize_amax
+    assert m(None, 0, 0, None) == OK
+    assert m(None, -1, 0, None) == INVALID
+    assert m(None, 3, 0, None) == INVALID
+    arr = (Tensor * 600)()
+    assert m(ctypes.cast(arr, ctypes.c_void_p), 513, 0, None) == TOO_MANY
+    assert m(ctypes.cast(arr, ctypes.c_void_p), 600, 1, None) == TOO_MANY
+    # all-empty list: OK, nothing launched
+    assert m(ctypes.cast(arr, ctypes.c_void_p), 512, 0, None) == OK
+    arr[3].n = 10            # one live tensor with NULL pointers
+    assert m(ctypes.cast(arr, ctypes.c_void_p), 5, 0, None) == INVALID
+    arr[3].n = -2
+    assert m(ctypes.cast(arr, ctypes.c_void_p), 5, 0, None) == INVALID
+    assert m(ctypes.cast(arr, ctypes.c_void_p), 5, 9, None) == INVALID
+
+
+def test_dequantize_argument_errors(L):
+    d = L.fp8q_dequantize
+    assert d(None, None, 0, 0, None, None) == OK
+    assert d(P, P, -3, 0, P, None) == INVALID
+    assert d(P, P, 3, 5, P, None) == INVALID
+    assert d(None, P, 3, 0, P, None) == INVALID
+    assert d(P, None, 3, 0, P, None) == INVALID
+    assert d(P, P, 3, 0, None, None) == INVALID
+    assert d(P, ODD, 3, 0, P, None) == INVALID
+
+
+def test_scale_update_argument_errors(L):
+    u = L.fp8q_amax_scale_update
+    good = (P, 16, 4, P, P, P, None, 0, 0, 0, None)
+    def call(i, v):
+        a = list(good)
+        a[i] = v
+        return u(*a)
+    assert call(1, 0) == INVALID          # history_len < 1
+    assert call(2, 0) == INVALID          # num_slots < 1
+    assert call(7, 2) == INVALID          # fmt
+    assert call(8, 2) == INVALID          # algo
+    assert call(9, 65) == INVALID         # margin
+    assert call(9, -65) == INVALID
+    for i in (0, 3, 4, 5):
+        assert call(i, None) == INVALID
+        assert call(i, ctypes.c_void_p(0x10002)) == INVALID
+
+
+def test_binding_refuses_host_tensors():
+    import torch
+    from quantize_amax_scaling_gb300 import fp8q
+    x = torch.zeros(8, dtype=torch.bfloat16)
+    q = torch.zeros(8, dtype=torch.uint8)
+    s = torch.ones(1)
+    with pytest.raises(ValueError):
+        fp8q.fp8q_quantize_amax(x, q, fp8q.E4M3FN, s, s.clone())
+    with pytest.raises(ValueError):
+        fp8q.fp8q_dequantize(q, x, fp8q.E4M3FN, s)
+    with pytest.raises(ValueError):
+        fp8q.fp8q_amax_scale_update(torch.zeros(4, 2), s.expand(2), s.expand(2), s.expand(2))
+
+
+def test_product_code_never_touches_the_oracle():
+    """The package (kernels, binding, build) neither imports, includes nor links the oracle."""
+    pkg = os.path.join(ROOT, "quantize_amax_scaling_gb300")
+    pat = re.compile(r"^\s*(import\s+oracle|from\s+oracle|#\s*include\s*[<\"].*oracle)|fp8q_oracle|orc_",
+                     re.M)
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not pat.search(text), f

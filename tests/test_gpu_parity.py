@@ -1,0 +1,471 @@
+"""GPU parity: libfp8q (through its C ABI) against the CPU oracle.
+
+Bar: bit-exact FP8 codes, amax, history, scale, scale_inv and bf16 dequant.
+Where several encodings are equally correct (a NaN), both sides must agree
+that the value is a NaN.  Small cases compare every element; the full-size
+workloads compare a sample of positions (the oracle is elementwise) plus the
+amax over the whole tensor.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from quantize_amax_scaling_gb300 import fp8q
+from quantize_amax_scaling_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+E4M3FN, E5M2 = fp8q.E4M3FN, fp8q.E5M2
+GUARD = 64
+CANARY = 0xA5
+
+SCALES_ALL = [1.0, 0.5, 2.0 ** -6, 2.0 ** 20, 1.0 / 3.0, 0.012345678, 7.5, 448.0 / 3.9, 3.0e-5,
+              1.7e4, 2.0 ** -60, 2.0 ** 60, float.fromhex("0x1.fffffep-61"), float.fromhex("0x1.000002p60"), 2.0 ** -70, 2.0 ** 70,
+              1.0e-38, 5.0e-45, -2.5, 0.0, -0.0, math.inf, math.nan, 3.4e38, float.fromhex("0x1.fffffep-1"),
+              float.fromhex("0x1.000002p0"), 1.0 / 448.0, 57344.0]
+
+
+@pytest.fixture(scope="module")
+def dev():
+    fp8q.lib()
+    return torch.device("cuda:0")
+
+
+def f32(v, dev):
+    return torch.tensor([v], dtype=torch.float32, device=dev)
+
+
+def is_nan_code(c, fmt):
+    c = np.asarray(c) & 0x7F
+    return c == 0x7F if fmt == E4M3FN else c > 0x7C
+
+
+def assert_codes_equal(got, want, fmt, what=""):
+    got = np.asarray(got, np.uint8).reshape(-1)
+    want = np.asarray(want, np.uint8).reshape(-1)
+    assert got.shape == want.shape
+    nan_w = is_nan_code(want, fmt)
+    assert np.array_equal(is_nan_code(got, fmt), nan_w), f"{what}: NaN codes differ"
+    bad = np.nonzero((got != want) & ~nan_w)[0]
+    assert bad.size == 0, f"{what}: {bad.size} codes differ, first at {bad[:5]}: got {got[bad[:5]]} want {want[bad[:5]]}"
+
+
+def assert_f32_equal(got, want, what=""):
+    g = np.asarray(got, np.float32).reshape(-1)
+    w = np.asarray(want, np.float32).reshape(-1)
+    gn, wn = np.isnan(g), np.isnan(w)
+    assert np.array_equal(gn, wn), f"{what}: NaN positions differ"
+    bad = np.nonzero((g.view(np.uint32) != w.view(np.uint32)) & ~wn)[0]
+    assert bad.size == 0, f"{what}: {bad.size} differ, first {bad[:5]}: got {g[bad[:5]]} want {w[bad[:5]]}"
+
+
+def assert_bf16_equal(got_bits, want_bits, what=""):
+    g = np.asarray(got_bits, np.uint16).reshape(-1)
+    w = np.asarray(want_bits, np.uint16).reshape(-1)
+    gn = ((g & 0x7F80) == 0x7F80) & ((g & 0x7F) != 0)
+    wn = ((w & 0x7F80) == 0x7F80) & ((w & 0x7F) != 0)
+    assert np.array_equal(gn, wn), f"{what}: NaN positions differ"
+    bad = np.nonzero((g != w) & ~wn)[0]
+    assert bad.size == 0, f"{what}: {bad.size} differ, first {bad[:5]}: got {g[bad[:5]]} want {w[bad[:5]]}"
+
+
+def guarded(n, dtype, dev, offset=0, fill=CANARY):
+    """A contiguous view of n elements inside a buffer with canary guards on both sides."""
+    buf = torch.full((n + 2 * GUARD + offset,), fill, dtype=torch.uint8 if dtype == torch.uint8 else torch.int16,
+                     device=dev)
+    if dtype != torch.uint8:
+        buf = buf.view(dtype)
+    return buf, buf[GUARD + offset: GUARD + offset + n]
+
+
+def check_guards(buf, n, offset, fill=CANARY):
+    raw = buf.view(torch.uint8) if buf.dtype != torch.uint8 else buf
+    es = buf.element_size()
+    lo = raw[: (GUARD + offset) * es].cpu().numpy()
+    hi = raw[(GUARD + offset + n) * es:].cpu().numpy()
+    if buf.dtype == torch.uint8:
+        assert np.all(lo == fill) and np.all(hi == fill), "write outside the output"
+    else:
+        lo16 = lo.view(np.uint16)
+        hi16 = hi.view(np.uint16)
+        assert np.all(lo16 == fill) and np.all(hi16 == fill), "write outside the output"
+
+
+def run_quantize(x, fmt, scale, dev, q=None, amax0=0.0):
+    if q is None:
+        q = torch.empty(x.numel(), dtype=torch.uint8, device=dev)
+    am = f32(amax0, dev)
+    fp8q.fp8q_quantize_amax(x.reshape(-1), q, fmt, f32(scale, dev), am)
+    torch.cuda.synchronize()
+    return q, am
+
+
+def oracle_scale_from(amax_prev, fmt):
+    """Delayed scale for the next step, computed by the oracle's own update."""
+    hist = np.zeros((1, 1), np.float32)
+    s = np.ones(1, np.float32)
+    si = np.ones(1, np.float32)
+    oracle.amax_scale_update(hist, np.array([amax_prev], np.float32), s, si, fmt)
+    return np.float32(s[0])
+
+
+def sample_positions(n, k=400_000, seed=0):
+    rng = np.random.default_rng(seed)
+    head = np.arange(min(n, 20000))
+    tail = np.arange(max(0, n - 20000), n)
+    rnd = rng.integers(0, n, min(k, n))
+    return np.unique(np.concatenate([head, tail, rnd]))
+
+
+# --------------------------------------------------------------------------- quantize
+
+@pytest.mark.parametrize("fmt", [E4M3FN, E5M2])
+def test_quantize_every_bf16_pattern_many_scales(dev, fmt):
+    x = W.all_bf16_patterns(dev)
+    xb = W.bf16_bits(x)
+    for s in SCALES_ALL:
+        q, am = run_quantize(x, fmt, s, dev)
+        rq, ra = oracle.quantize_amax(xb, fmt, np.float32(s))
+        assert_codes_equal(q.cpu().numpy(), rq, fmt, f"scale {s!r}")
+        assert math.isnan(float(am)) and math.isnan(float(ra))
+
+
+def test_amax_exact_on_pattern_subsets(dev):
+    allx = W.bf16_bits(W.all_bf16_patterns())
+    f = (allx.astype(np.uint32) << 16).view(np.float32)
+    subsets = {
+        "finite": allx[np.isfinite(f)],
+        "with_inf": allx[~np.isnan(f)],
+        "subnormal": allx[(np.abs(f) < 2.0 ** -126)],
+        "negative_only": allx[np.isfinite(f) & (f < 0)],
+        "zeros": np.array([0x8000, 0x0000, 0x8000], np.uint16),
+    }
+    for name, bits in subsets.items():
+        x = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).to(dev)
+        q, am = run_quantize(x, E4M3FN, 1.0, dev)
+        rq, ra = oracle.quantize_amax(bits, E4M3FN, 1.0)
+        assert_f32_equal([float(am)], [ra], name)
+        assert_codes_equal(q.cpu().numpy(), rq, E4M3FN, name)
+
+
+def test_amax_accumulates_into_seed(dev):
+    x = W.mlp_activation(7, dev, (64, 256))
+    xb = W.bf16_bits(x)
+    for seed in (0.0, 0.5, 1e6, math.inf):
+        _, am = run_quantize(x, E4M3FN, 1.0, dev, amax0=seed)
+        _, ra = oracle.quantize_amax(xb, E4M3FN, 1.0, amax=seed)
+        assert_f32_equal([float(am)], [ra], f"seed {seed}")
+
+
+SIZES = [1, 2, 7, 8, 9, 15, 16, 17, 255, 4095, 4097, 8191, 8192, 8193, 2 * 65536 + 5, (1 << 20) + 3]
+OFFSETS = [(0, 0), (1, 1), (3, 3), (7, 7), (0, 1), (1, 0), (5, 2), (2, 13), (4, 4), (6, 14)]
+
+
+@pytest.mark.parametrize("n", SIZES)
+def test_quantize_ragged_sizes_offsets_with_canaries(dev, n):
+    g = torch.Generator(device=dev)
+    g.manual_seed(n)
+    for k, (xo, qo) in enumerate(OFFSETS if n < 100000 else OFFSETS[:4]):
+        fmt = E4M3FN if k % 2 == 0 else E5M2
+        scale = [0.0123, 1.0, 2.0 ** 70, 3.3e-3][k % 4]   # includes a slow-path scale
+        xbuf = torch.randn(n + 16, generator=g, device=dev).mul_(40.0).to(torch.bfloat16)
+        x = xbuf[xo: xo + n]
+        qbuf, q = guarded(n, torch.uint8, dev, qo)
+        am = f32(0.0, dev)
+        fp8q.fp8q_quantize_amax(x, q, fmt, f32(scale, dev), am)
+        torch.cuda.synchronize()
+        rq, ra = oracle.quantize_amax(W.bf16_bits(x), fmt, np.float32(scale))
+        assert_codes_equal(q.cpu().numpy(), rq, fmt, f"n={n} off={xo},{qo}")
+        assert_f32_equal([float(am)], [ra], f"amax n={n} off={xo},{qo}")
+        check_guards(qbuf, n, qo)
+
+
+def test_quantize_on_a_side_stream(dev):
+    x = W.mlp_activation(3, dev, (512, 1024))
+    s = torch.cuda.Stream()
+    q = torch.empty(x.numel(), dtype=torch.uint8, device=dev)
+    am = f32(0.0, dev)
+    sc = f32(0.05, dev)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        fp8q.fp8q_quantize_amax(x.reshape(-1), q, E4M3FN, sc, am, stream=s)
+    s.synchronize()
+    rq, ra = oracle.quantize_amax(W.bf16_bits(x), E4M3FN, np.float32(0.05))
+    assert_codes_equal(q.cpu().numpy(), rq, E4M3FN)
+    assert float(am) == float(ra)
+
+
+def test_tiny_config_page_example(dev):
+    """bf16 A 16x32 and B 32x64 from U[0,1), e4m3fn with scale 1, amax per tensor,
+    then one scale update (history 16 of zeros, margin 0, max)."""
+    A, B = W.tiny_pair(dev)
+    amax = torch.zeros(2, device=dev)
+    for i, X in enumerate((A, B)):
+        q = torch.empty(X.numel(), dtype=torch.uint8, device=dev)
+        fp8q.fp8q_quantize_amax(X.reshape(-1), q, E4M3FN, f32(1.0, dev), amax[i:i + 1])
+        torch.cuda.synchronize()
+        rq, ra = oracle.quantize_amax(W.bf16_bits(X), E4M3FN, 1.0)
+        assert_codes_equal(q.cpu().numpy(), rq, E4M3FN)
+        assert float(amax[i]) == float(ra)
+    hist = torch.zeros(16, 2, device=dev)
+    sc = torch.ones(2, device=dev)
+    si = torch.ones(2, device=dev)
+    fp8q.fp8q_amax_scale_update(hist, amax, sc, si, E4M3FN, fp8q.ALGO_MAX, 0)
+    torch.cuda.synchronize()
+    rh = np.zeros((16, 2), np.float32)
+    rs, ri = np.ones(2, np.float32), np.ones(2, np.float32)
+    oracle.amax_scale_update(rh, amax.cpu().numpy(), rs, ri)
+    assert_f32_equal(hist.cpu().numpy(), rh, "history")
+    assert_f32_equal(sc.cpu().numpy(), rs, "scale")
+    assert_f32_equal(si.cpu().numpy(), ri, "scale_inv")
+
+
+def test_mlp_activation_full_size_full_compare(dev):
+    """8192x4096 N(0,1) with 0.1% outliers x100, e4m3fn, delayed scale from the
+    previous step's amax -- every byte compared."""
+    prev = W.mlp_activation(W.SEED_MLP + 1, dev)
+    scale = oracle_scale_from(oracle.amax(W.bf16_bits(prev)), E4M3FN)
+    x = W.mlp_activation(W.SEED_MLP, dev)
+    q, am = run_quantize(x, E4M3FN, scale, dev)
+    xb = W.bf16_bits(x)
+    rq, ra = oracle.quantize_amax(xb, E4M3FN, scale)
+    assert_codes_equal(q.cpu().numpy(), rq, E4M3FN, "mlp activation")
+    assert float(am) == float(ra)
+
+
+def _sampled_quantize_check(x, q, am, fmt, scale, what):
+    xb = W.bf16_bits(x)
+    idx = sample_positions(xb.size)
+    rq, _ = oracle.quantize_amax(xb[idx], fmt, scale)
+    assert_codes_equal(q.cpu().numpy()[idx], rq, fmt, what)
+    assert_f32_equal([float(am)], [oracle.amax(xb)], what + " amax")
+
+
+def test_ffn_full_size_multi_tensor_sampled(dev):
+    """gelu activation 8192x16384 + W1 4096x16384 + W2 16384x4096 in one launch,
+    each with its own delayed scale and amax."""
+    xs = W.ffn_tensors(dev)
+    prev = W.ffn_tensors(dev, seed=W.SEED_FFN + 1)
+    scales = [oracle_scale_from(oracle.amax(W.bf16_bits(p)), E4M3FN) for p in prev]
+    del prev
+    qs = [torch.empty(x.numel(), dtype=torch.uint8, device=dev) for x in xs]
+    am = torch.zeros(len(xs), device=dev)
+    sc = torch.tensor(scales, dtype=torch.float32, device=dev)
+    fp8q.fp8q_multi_quantize_amax([x.reshape(-1) for x in xs], qs, E4M3FN,
+                                  [sc[i:i + 1] for i in range(3)], [am[i:i + 1] for i in range(3)])
+    torch.cuda.synchronize()
+    for i, (x, q) in enumerate(zip(xs, qs)):
+        _sampled_quantize_check(x, q, am[i], E4M3FN, scales[i], f"ffn tensor {i}")
+
+
+def test_headline_tensor_single_call_sampled(dev):
+    """The 8192x16384 activation through the single-tensor entry point."""
+    x = W.gelu_activation(W.SEED_FFN, dev)
+    scale = np.float32(0.0091)
+    q, am = run_quantize(x, E4M3FN, scale, dev)
+    _sampled_quantize_check(x, q, am, E4M3FN, scale, "8192x16384")
+
+
+def test_gradients_e5m2_quantize_then_dequantize_sampled(dev):
+    """sign x lognormal(-12, 3) gradients with signed zeros and +-inf, e5m2
+    saturating (amax = inf), then dequantized back to bf16."""
+    grads = W.gradient_tensors(dev)
+    prev = W.gradient_tensors(dev, seed=W.SEED_GRAD + 1)
+    for g, p in zip(grads, prev):
+        pb = W.bf16_bits(p)
+        pf = (pb.astype(np.uint32) << 16).view(np.float32)
+        finite_prev = pb[np.isfinite(pf)]
+        scale = oracle_scale_from(oracle.amax(finite_prev), E5M2)
+        q, am = run_quantize(g, E5M2, scale, dev)
+        assert math.isinf(float(am))
+        _sampled_quantize_check(g, q, am, E5M2, scale, "gradient")
+        y = torch.empty(g.numel(), dtype=torch.bfloat16, device=dev)
+        fp8q.fp8q_dequantize(q, y, E5M2, f32(scale, dev))
+        torch.cuda.synchronize()
+        idx = sample_positions(g.numel(), seed=1)
+        ry = oracle.dequantize(q.cpu().numpy()[idx], E5M2, scale)
+        assert_bf16_equal(W.bf16_bits(y)[idx], ry, "gradient dequant")
+
+
+# --------------------------------------------------------------------------- multi-tensor
+
+def _multi_case(dev, sizes, fmt, seed, offsets=True, share_amax=False):
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    rng = np.random.default_rng(seed)
+    xs, qs, qbufs, qoffs, scales = [], [], [], [], []
+    for i, n in enumerate(sizes):
+        xo = int(rng.integers(0, 8)) if offsets else 0
+        qo = int(rng.integers(0, 16)) if offsets else 0
+        xbuf = (torch.randn(n + 8, generator=g, device=dev) * float(rng.uniform(0.1, 500))).to(torch.bfloat16)
+        xs.append(xbuf[xo: xo + n])
+        qb, q = guarded(n, torch.uint8, dev, qo)
+        qs.append(q)
+        qbufs.append(qb)
+        qoffs.append(qo)
+        scales.append(np.float32([0.01, 1.0, 0.37, 2.0 ** -65, 3.0][i % 5]))
+    T = len(sizes)
+    sc = torch.tensor(scales, dtype=torch.float32, device=dev)
+    am = torch.zeros(T, device=dev)
+    amax_views = [am[0:1] if share_amax else am[i:i + 1] for i in range(T)]
+    fp8q.fp8q_multi_quantize_amax(xs, qs, fmt, [sc[i:i + 1] for i in range(T)], amax_views)
+    torch.cuda.synchronize()
+    rqs, ras = oracle.multi_quantize_amax([W.bf16_bits(x) for x in xs], fmt, scales)
+    for i in range(T):
+        assert_codes_equal(qs[i].cpu().numpy(), rqs[i], fmt, f"tensor {i} of {T}")
+        check_guards(qbufs[i], sizes[i], qoffs[i])
+    amh = am.cpu().numpy()
+    if share_amax:
+        want = max((float(a) for a in ras if not math.isnan(a)), default=0.0)
+        assert amh[0] == np.float32(want)
+    else:
+        assert_f32_equal(amh, ras, "amax")
+
+
+@pytest.mark.parametrize("count", [1, 2, 8, 9, 64, 65, 200, 512])
+def test_multi_tensor_every_bucket(dev, count):
+    rng = np.random.default_rng(count)
+    sizes = [int(v) for v in rng.integers(0, 3000, count)]
+    sizes[0] = max(sizes[0], 1)
+    _multi_case(dev, sizes, E4M3FN if count % 2 else E5M2, seed=count)
+
+
+def test_multi_tensor_mixed_large_and_tiny_with_empty(dev):
+    sizes = [0, 1, 70000, 3, 0, 8192 * 5 + 7, 9, 123457, 0, 16]
+    _multi_case(dev, sizes, E4M3FN, seed=42)
+    _multi_case(dev, sizes, E5M2, seed=43, offsets=False)
+
+
+def test_multi_tensor_shared_amax(dev):
+    _multi_case(dev, [5000, 7000, 11, 90000], E4M3FN, seed=44, share_amax=True)
+
+
+def test_ragged_twelve_tensors_full_size_sampled(dev):
+    """Twelve bf16 N(0,1) tensors 2048x12288 .. 12288x4096 in one launch, with
+    the per-slot scales that a 576-slot update produces."""
+    xs = W.ragged_tensors(dev)
+    hist, new, sc0, si0, sf = W.scale_update_inputs("cpu")
+    hist_np, new_np = hist.numpy().copy(), new.numpy().copy()
+    s_np, si_np = sc0.numpy().copy(), si0.numpy().copy()
+    oracle.amax_scale_update(hist_np, new_np, s_np, si_np, E4M3FN, oracle.ALGO_MAX, 0)
+    scales = [np.float32(s_np[i]) for i in range(len(xs))]
+    qs = [torch.empty(x.numel(), dtype=torch.uint8, device=dev) for x in xs]
+    am = torch.zeros(len(xs), device=dev)
+    sc = torch.tensor(scales, dtype=torch.float32, device=dev)
+    fp8q.fp8q_multi_quantize_amax([x.reshape(-1) for x in xs], qs, E4M3FN,
+                                  [sc[i:i + 1] for i in range(len(xs))],
+                                  [am[i:i + 1] for i in range(len(xs))])
+    torch.cuda.synchronize()
+    for i, (x, q) in enumerate(zip(xs, qs)):
+        xb = W.bf16_bits(x)
+        idx = sample_positions(xb.size, k=60000, seed=i)
+        rq, _ = oracle.quantize_amax(xb[idx], E4M3FN, scales[i])
+        assert_codes_equal(q.cpu().numpy()[idx], rq, E4M3FN, f"ragged {i}")
+        assert_f32_equal([float(am[i])], [oracle.amax(xb)], f"ragged amax {i}")
+
+
+# --------------------------------------------------------------------------- dequantize
+
+@pytest.mark.parametrize("fmt", [E4M3FN, E5M2])
+def test_dequantize_every_code_many_scales(dev, fmt):
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8).repeat(37).to(dev)
+    for s in SCALES_ALL:
+        y = torch.empty(codes.numel(), dtype=torch.bfloat16, device=dev)
+        fp8q.fp8q_dequantize(codes, y, fmt, f32(s, dev))
+        torch.cuda.synchronize()
+        ry = oracle.dequantize(codes.cpu().numpy(), fmt, np.float32(s))
+        assert_bf16_equal(W.bf16_bits(y), ry, f"scale {s!r}")
+
+
+@pytest.mark.parametrize("n", SIZES)
+def test_dequantize_ragged_sizes_offsets_with_canaries(dev, n):
+    rng = np.random.default_rng(n)
+    for k, (qo, yo) in enumerate(OFFSETS if n < 100000 else OFFSETS[:4]):
+        fmt = E4M3FN if k % 2 == 0 else E5M2
+        qbuf = torch.from_numpy(rng.integers(0, 256, n + 16, dtype=np.uint8)).to(dev)
+        q = qbuf[qo: qo + n]
+        ybuf, y = guarded(n, torch.bfloat16, dev, yo, fill=0x5A5A)
+        s = [0.0123, 1.0, 3.0e5, 2.0 ** -100][k % 4]
+        fp8q.fp8q_dequantize(q, y, fmt, f32(s, dev))
+        torch.cuda.synchronize()
+        ry = oracle.dequantize(q.cpu().numpy(), fmt, np.float32(s))
+        assert_bf16_equal(W.bf16_bits(y), ry, f"n={n} off={qo},{yo}")
+        check_guards(ybuf, n, yo, fill=0x5A5A)
+
+
+# --------------------------------------------------------------------------- scale update
+
+def _update_case(dev, hist_np, new_np, fmt=E4M3FN, algo=0, margin=0, slot_format=None, steps=1,
+                 scale0=None, hist_offset=0):
+    H, S = hist_np.shape
+    if hist_offset:
+        buf = torch.zeros(H * S + hist_offset, device=dev)
+        hist = buf[hist_offset:].view(H, S)
+        hist.copy_(torch.from_numpy(hist_np))
+    else:
+        hist = torch.from_numpy(hist_np.copy()).to(dev)
+    sc = torch.from_numpy(scale0.copy() if scale0 is not None else np.ones(S, np.float32)).to(dev)
+    si = torch.from_numpy((1.0 / sc.cpu().numpy()).astype(np.float32)).to(dev)
+    rh = hist_np.copy()
+    rs, ri = sc.cpu().numpy().copy(), si.cpu().numpy().copy()
+    sf_t = None if slot_format is None else torch.from_numpy(slot_format).to(dev)
+    for step in range(steps):
+        new_s = new_np if step == 0 else np.roll(new_np, step) * np.float32(1.5 ** step)
+        new_t = torch.from_numpy(np.ascontiguousarray(new_s, np.float32)).to(dev)
+        fp8q.fp8q_amax_scale_update(hist, new_t, sc, si, fmt, algo, margin, sf_t)
+        oracle.amax_scale_update(rh, new_s, rs, ri, fmt, algo, margin, slot_format)
+    torch.cuda.synchronize()
+    assert_f32_equal(hist.cpu().numpy(), rh, f"history {H}x{S}")
+    assert_f32_equal(sc.cpu().numpy(), rs, f"scale {H}x{S}")
+    assert_f32_equal(si.cpu().numpy(), ri, f"scale_inv {H}x{S}")
+
+
+@pytest.mark.parametrize("algo", [fp8q.ALGO_MAX, fp8q.ALGO_MOST_RECENT])
+@pytest.mark.parametrize("margin", [0, 1])
+@pytest.mark.parametrize("per_slot", [False, True])
+def test_scale_update_576_slots_full(dev, algo, margin, per_slot):
+    """96 layers x 6 slots, history 1024, lognormal(0,2) with 2% zeros."""
+    hist, new, _, _, sf = W.scale_update_inputs("cpu")
+    _update_case(dev, hist.numpy(), new.numpy(), algo=algo, margin=margin,
+                 slot_format=sf.numpy() if per_slot else None, steps=3)
+
+
+SHAPES = [(1, 1), (1, 5), (2, 3), (16, 2), (17, 7), (1023, 577), (1024, 575), (1025, 576),
+          (1024, 4), (2053, 12), (3000, 8), (4096, 4)]
+
+
+@pytest.mark.parametrize("H,S", SHAPES)
+def test_scale_update_shapes(dev, H, S):
+    rng = np.random.default_rng(H * 1000 + S)
+    hist = np.exp(rng.normal(0, 2, (H, S))).astype(np.float32)
+    hist[rng.random((H, S)) < 0.05] = 0.0
+    new = np.exp(rng.normal(0, 2, S)).astype(np.float32)
+    for algo in (0, 1):
+        _update_case(dev, hist, new, algo=algo, margin=(H % 3) - 1, steps=2)
+
+
+def test_scale_update_misaligned_history_uses_scalar_path(dev):
+    rng = np.random.default_rng(8)
+    hist = np.exp(rng.normal(0, 2, (1024, 576))).astype(np.float32)
+    new = np.exp(rng.normal(0, 2, 576)).astype(np.float32)
+    _update_case(dev, hist, new, hist_offset=1, steps=2)
+
+
+def test_scale_update_specials(dev):
+    S = 12
+    hist = np.full((8, S), 2.0, np.float32)
+    hist[3, 0] = np.nan          # NaN inside the window: pass-through under max
+    hist[7, 1] = np.nan          # NaN in the row that drops out: ignored
+    hist[2, 2] = np.inf          # inf in the window
+    hist[:, 3] = 0.0             # all zero, new zero
+    hist[:, 4] = -5.0            # negative history
+    new = np.array([1, 1, 1, 0, 1, np.nan, np.inf, -1, 1e-38, 3e38, 1e-45, 448], np.float32)
+    scale0 = np.full(S, 4.0, np.float32)
+    sf = np.array([0, 1, 0, 0, 1, 0, 1, 0, 0, 1, 0, 5], np.uint8)
+    for algo in (0, 1):
+        for margin in (-64, -3, 0, 2, 64):
+            _update_case(dev, hist, new, algo=algo, margin=margin, slot_format=sf, scale0=scale0,
+                         steps=2)
