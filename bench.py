@@ -252,8 +252,8 @@ def run_gpu(args, ws, rank, local):
         time.sleep(0.002)
     torch.cuda.synchronize(dev)
     barrier()
-    t_rank = start.elapsed_time(end) / 1e3
-    value, t_max = aggregate_throughput(STEP_BYTES, t_rank, ws)
+    t_rank = start.elapsed_time(end) / 1e3          # seconds for all K steps on this rank
+    value, t_max = aggregate_throughput(STEP_BYTES * args.steps, t_rank, ws)
 
     per = {"quantize_amax": [], "multi_quantize_amax": [], "dequantize": [], "amax_scale_update": []}
     for k in range(args.steps):
@@ -364,12 +364,23 @@ def run_e2e(args, step, stream, dev):
 
 
 def read_traffic():
-    """DRAM bytes per launch of the quantize kernel from the committed ncu summary, if current."""
+    """DRAM bytes per launch of the quantize kernel from the committed ncu capture.
+
+    None when there is no capture or when the kernel source has changed since
+    the counters were taken (the record carries the source's sha256).
+    """
+    import hashlib
     p = os.path.join(ROOT, "profiles", "quantize_amax_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
+    src = os.path.join(ROOT, d.get("source", ""))
+    if not os.path.exists(src):
+        return None
+    with open(src, "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest() != d.get("source_sha256"):
+            return None
     return d.get("dram_bytes_per_launch")
 
 
