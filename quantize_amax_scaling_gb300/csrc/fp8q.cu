@@ -64,45 +64,63 @@ fp8q_status after_launch(const char* where) {
 // ----------------------------------------------------------------------------
 // Launch geometry
 
-constexpr int kThreads = 256;                       // threads per CTA (streaming kernels)
-constexpr int kUnroll = 4;                          // 16-byte vectors in flight per thread
-constexpr int kVecElems = 8;                        // bf16 per 16-byte vector
-constexpr int kVecPerTile = kThreads * kUnroll;     // 1024 vectors
-constexpr int kTileElems = kVecPerTile * kVecElems; // 8192 elements per tile
+constexpr int kThreads = 256;  // threads per CTA (streaming kernels)
 constexpr int kMaxDevices = 64;
+
+// Vector geometry of the two streaming kernels.  A thread moves vectors of
+// kVecElems elements; a tile is kVecPerThread vectors per thread.
+//   quantize:   16 bf16 (one 32-byte load) -> 16 codes (one 16-byte store)
+//   dequantize: 8 codes (one 8-byte load)  -> 8 bf16 (one 16-byte store)
+struct QuantGeom {
+    static constexpr int kVecElems = 16;
+    static constexpr int kVecPerThread = 2;
+    static constexpr int kWideAlign = 32;  // bytes, bf16 side
+};
+struct DequantGeom {
+    static constexpr int kVecElems = 8;
+    static constexpr int kVecPerThread = 4;
+    static constexpr int kWideAlign = 16;
+};
+template <class G>
+struct Tile {
+    static constexpr int kVecs = kThreads * G::kVecPerThread;
+    static constexpr int kElems = kVecs * G::kVecElems;  // 8192 for both kernels
+};
 
 enum : int { kModeVec = 0, kModeScalar = 1 };
 
-// How a tensor is split: `head` scalar elements until the bf16 pointer is
-// 16-byte aligned, then `nvec` 8-element vectors, then a scalar tail of
-// fewer than 8.  If the byte pointer is not 8-byte aligned at the same
-// element the whole tensor is processed element by element.  Host and device
-// both call this, so they agree on the tile count.
+// How a tensor is split: `head` scalar elements until the bf16 pointer
+// (`wide`) is G::kWideAlign-byte aligned, then `nvec` vectors, then a scalar
+// tail shorter than one vector.  The FP8 pointer (`narrow`) must then be
+// aligned to one vector's bytes at the same element; otherwise the whole
+// tensor is processed element by element.  Host and device both call this,
+// so they agree on the tile count.
 struct Split {
     int64_t head, nvec, tiles;
     int mode;
 };
 
-__host__ __device__ inline Split split_tensor(uintptr_t wide, uintptr_t narrow, int64_t n,
-                                              int narrow_vec_bytes) {
+template <class G>
+__host__ __device__ inline Split split_tensor(uintptr_t wide, uintptr_t narrow, int64_t n) {
     Split s;
     if (n <= 0) {
         s.head = 0; s.nvec = 0; s.tiles = 0; s.mode = kModeVec;
         return s;
     }
-    int64_t h = (int64_t)(((16u - (unsigned)(wide & 15u)) & 15u) >> 1);
+    const unsigned wa = G::kWideAlign;
+    int64_t h = (int64_t)(((wa - (unsigned)(wide & (wa - 1))) & (wa - 1)) >> 1);
     if (h > n) h = n;
-    if (((narrow + (uintptr_t)h) & (uintptr_t)(narrow_vec_bytes - 1)) == 0) {
+    if (((narrow + (uintptr_t)h) & (uintptr_t)(G::kVecElems - 1)) == 0) {
         s.mode = kModeVec;
         s.head = h;
-        s.nvec = (n - h) / kVecElems;
-        int64_t t = (s.nvec + kVecPerTile - 1) / kVecPerTile;
+        s.nvec = (n - h) / G::kVecElems;
+        int64_t t = (s.nvec + Tile<G>::kVecs - 1) / Tile<G>::kVecs;
         s.tiles = t > 0 ? t : 1;  // tile 0 also carries the scalar head and tail
     } else {
         s.mode = kModeScalar;
         s.head = n;
         s.nvec = 0;
-        s.tiles = (n + kTileElems - 1) / kTileElems;
+        s.tiles = (n + Tile<G>::kElems - 1) / Tile<G>::kElems;
     }
     return s;
 }
@@ -113,12 +131,10 @@ __host__ __device__ inline Split split_tensor(uintptr_t wide, uintptr_t narrow, 
 // are written once: stores are marked streaming (evict-first) so L2 drains them
 // to HBM early instead of holding them against the next kernel.
 
-__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+__device__ __forceinline__ void ld_stream_v8(const void* p, uint4& a, uint4& b) {
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
                  : "l"(p));
-    return v;
 }
 
 __device__ __forceinline__ uint2 ld_stream_v2(const void* p) {
@@ -127,10 +143,6 @@ __device__ __forceinline__ uint2 ld_stream_v2(const void* p) {
                  : "=r"(v.x), "=r"(v.y)
                  : "l"(p));
     return v;
-}
-
-__device__ __forceinline__ void st_v2(void* p, uint2 v) {
-    asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
 }
 
 __device__ __forceinline__ void st_v4(void* p, uint4 v) {
@@ -269,7 +281,7 @@ struct QCursor {
 
 __device__ __forceinline__ QCursor make_cursor(const QTensor& t, int64_t tile_begin) {
     QCursor k;
-    Split sp = split_tensor((uintptr_t)t.x, (uintptr_t)t.q, t.n, 8);
+    Split sp = split_tensor<QuantGeom>((uintptr_t)t.x, (uintptr_t)t.q, t.n);
     k.x = t.x;
     k.q = t.q;
     k.amax = t.amax;
@@ -301,27 +313,38 @@ __device__ __forceinline__ void flush_amax(uint32_t m2, uint32_t ms, float* amax
     __syncthreads();  // `red` is reused by the next flush
 }
 
+// Four bf16 (two words) -> four FP8 codes in one word.
+template <int FMT, bool FAST>
+__device__ __forceinline__ uint32_t quant_quad(uint32_t w0, uint32_t w1, const QScale& c) {
+    return quant_pair<FMT, FAST>(w0, c) | (quant_pair<FMT, FAST>(w1, c) << 16);
+}
+
 template <int FMT, bool FAST>
 __device__ __forceinline__ void quant_vec_tile(const QCursor& k, int64_t local, uint32_t& m2) {
+    constexpr int E = QuantGeom::kVecElems, U = QuantGeom::kVecPerThread;
     const uint16_t* xb = k.x + k.head;
     uint8_t* qb = k.q + k.head;
-    const int64_t v0 = local * kVecPerTile + threadIdx.x;
-    uint4 w[kUnroll];
+    const int64_t v0 = local * Tile<QuantGeom>::kVecs + threadIdx.x;
+    uint4 a[U], b[U];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
+    for (int u = 0; u < U; ++u) {
         const int64_t v = v0 + (int64_t)u * kThreads;
-        if (v < k.nvec) w[u] = ld_stream_v4(xb + v * kVecElems);
+        if (v < k.nvec) ld_stream_v8(xb + v * E, a[u], b[u]);
     }
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
+    for (int u = 0; u < U; ++u) {
         const int64_t v = v0 + (int64_t)u * kThreads;
         if (v < k.nvec) {
-            m2 = bf16x2_absmax(m2, bf16x2_absmax(bf16x2_absmax(w[u].x, w[u].y),
-                                                 bf16x2_absmax(w[u].z, w[u].w)));
-            uint2 o;
-            o.x = quant_pair<FMT, FAST>(w[u].x, k.c) | (quant_pair<FMT, FAST>(w[u].y, k.c) << 16);
-            o.y = quant_pair<FMT, FAST>(w[u].z, k.c) | (quant_pair<FMT, FAST>(w[u].w, k.c) << 16);
-            st_v2(qb + v * kVecElems, o);
+            m2 = bf16x2_absmax(m2, bf16x2_absmax(bf16x2_absmax(bf16x2_absmax(a[u].x, a[u].y),
+                                                               bf16x2_absmax(a[u].z, a[u].w)),
+                                                 bf16x2_absmax(bf16x2_absmax(b[u].x, b[u].y),
+                                                               bf16x2_absmax(b[u].z, b[u].w))));
+            uint4 o;
+            o.x = quant_quad<FMT, FAST>(a[u].x, a[u].y, k.c);
+            o.y = quant_quad<FMT, FAST>(a[u].z, a[u].w, k.c);
+            o.z = quant_quad<FMT, FAST>(b[u].x, b[u].y, k.c);
+            o.w = quant_quad<FMT, FAST>(b[u].z, b[u].w, k.c);
+            st_v4(qb + v * E, o);
         }
     }
 }
@@ -338,15 +361,15 @@ __device__ __forceinline__ void quant_tile(const QCursor& k, int64_t local, uint
                                            uint32_t& ms) {
     if (k.mode == kModeVec) {
         quant_vec_tile<FMT, FAST>(k, local, m2);
-        if (local == 0) {  // scalar head (< 8) and tail (< 8) elements
-            const int64_t tail0 = k.head + k.nvec * kVecElems;
+        if (local == 0) {  // scalar head and tail, each shorter than one vector
+            const int64_t tail0 = k.head + k.nvec * QuantGeom::kVecElems;
             const int64_t nscalar = k.head + (k.n - tail0);
             for (int64_t j = threadIdx.x; j < nscalar; j += kThreads)
                 quant_scalar<FMT, FAST>(k, j < k.head ? j : tail0 + (j - k.head), ms);
         }
     } else {
-        const int64_t base = local * kTileElems;
-        const int64_t end = min(base + (int64_t)kTileElems, k.n);
+        const int64_t base = local * Tile<QuantGeom>::kElems;
+        const int64_t end = min(base + (int64_t)Tile<QuantGeom>::kElems, k.n);
         for (int64_t i = base + threadIdx.x; i < end; i += kThreads) quant_scalar<FMT, FAST>(k, i, ms);
     }
 }
@@ -389,20 +412,21 @@ __global__ void __launch_bounds__(kThreads)
     dequantize_kernel(const uint8_t* __restrict__ q, uint16_t* __restrict__ y, int64_t n,
                       const float* __restrict__ scale, int64_t tiles) {
     const float s = __ldg(scale);
-    const Split sp = split_tensor((uintptr_t)y, (uintptr_t)q, n, 8);
+    const Split sp = split_tensor<DequantGeom>((uintptr_t)y, (uintptr_t)q, n);
+    constexpr int E = DequantGeom::kVecElems, U = DequantGeom::kVecPerThread;
     for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
         if (sp.mode == kModeVec) {
             const uint8_t* qb = q + sp.head;
             uint16_t* yb = y + sp.head;
-            const int64_t v0 = tile * kVecPerTile + threadIdx.x;
-            uint2 w[kUnroll];
+            const int64_t v0 = tile * Tile<DequantGeom>::kVecs + threadIdx.x;
+            uint2 w[U];
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
+            for (int u = 0; u < U; ++u) {
                 const int64_t v = v0 + (int64_t)u * kThreads;
-                if (v < sp.nvec) w[u] = ld_stream_v2(qb + v * kVecElems);
+                if (v < sp.nvec) w[u] = ld_stream_v2(qb + v * E);
             }
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
+            for (int u = 0; u < U; ++u) {
                 const int64_t v = v0 + (int64_t)u * kThreads;
                 if (v < sp.nvec) {
                     uint4 o;
@@ -410,11 +434,11 @@ __global__ void __launch_bounds__(kThreads)
                     o.y = dequant_pair<FMT>(w[u].x >> 16, s);
                     o.z = dequant_pair<FMT>(w[u].y & 0xFFFFu, s);
                     o.w = dequant_pair<FMT>(w[u].y >> 16, s);
-                    st_v4(yb + v * kVecElems, o);
+                    st_v4(yb + v * E, o);
                 }
             }
             if (tile == 0) {
-                const int64_t tail0 = sp.head + sp.nvec * kVecElems;
+                const int64_t tail0 = sp.head + sp.nvec * E;
                 const int64_t nscalar = sp.head + (n - tail0);
                 for (int64_t j = threadIdx.x; j < nscalar; j += kThreads) {
                     const int64_t i = j < sp.head ? j : tail0 + (j - sp.head);
@@ -422,8 +446,8 @@ __global__ void __launch_bounds__(kThreads)
                 }
             }
         } else {
-            const int64_t base = tile * kTileElems;
-            const int64_t end = min(base + (int64_t)kTileElems, n);
+            const int64_t base = tile * Tile<DequantGeom>::kElems;
+            const int64_t end = min(base + (int64_t)Tile<DequantGeom>::kElems, n);
             for (int64_t i = base + threadIdx.x; i < end; i += kThreads)
                 y[i] = (uint16_t)(dequant_pair<FMT>(q[i], s) & 0xFFFFu);
         }
@@ -655,7 +679,7 @@ fp8q_status launch_quantize(const fp8q_tensor* list, int32_t count, cudaStream_t
     int m = 0;
     for (int32_t i = 0; i < count; ++i) {
         const fp8q_tensor& t = list[i];
-        const Split sp = split_tensor((uintptr_t)t.x_bf16, (uintptr_t)t.q, t.n, 8);
+        const Split sp = split_tensor<QuantGeom>((uintptr_t)t.x_bf16, (uintptr_t)t.q, t.n);
         if (sp.tiles == 0) continue;  // empty tensors take no tiles and are skipped
         QTensor& d = L.t[m++];
         d.x = static_cast<const uint16_t*>(t.x_bf16);
@@ -699,7 +723,7 @@ fp8q_status check_tensor(const fp8q_tensor& t) {
 template <int FMT>
 fp8q_status launch_dequantize(const uint8_t* q, void* y, int64_t n, const float* scale,
                               cudaStream_t stream) {
-    const Split sp = split_tensor((uintptr_t)y, (uintptr_t)q, n, 8);
+    const Split sp = split_tensor<DequantGeom>((uintptr_t)y, (uintptr_t)q, n);
     // One CTA per tile: for this write-heavy stream (1 byte read, 2 written)
     // the hardware's in-order CTA dispatch keeps the writes more sequential
     // than a persistent grid-stride loop does (measured ~12% faster on GB300).

@@ -160,8 +160,10 @@ def test_amax_accumulates_into_seed(dev):
         assert_f32_equal([float(am)], [ra], f"seed {seed}")
 
 
-SIZES = [1, 2, 7, 8, 9, 15, 16, 17, 255, 4095, 4097, 8191, 8192, 8193, 2 * 65536 + 5, (1 << 20) + 3]
-OFFSETS = [(0, 0), (1, 1), (3, 3), (7, 7), (0, 1), (1, 0), (5, 2), (2, 13), (4, 4), (6, 14)]
+SIZES = [1, 2, 7, 8, 9, 15, 16, 17, 31, 32, 33, 255, 4095, 4097, 8191, 8192, 8193, 2 * 65536 + 5,
+         (1 << 20) + 3]
+OFFSETS = [(0, 0), (1, 1), (3, 3), (7, 7), (0, 1), (1, 0), (5, 2), (2, 13), (4, 4), (6, 14),
+           (8, 8), (15, 15), (9, 1), (12, 12), (8, 0)]
 
 
 @pytest.mark.parametrize("n", SIZES)
