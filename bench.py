@@ -268,6 +268,9 @@ def run_gpu(args, ws, rank, local):
                for n in per}
     q_gbs = kbytes["quantize_amax"] / (avg["quantize_amax"] * 1e-6) / 1e9
 
+    # ---- rows beyond the step (fused Q->DQ), timed on their own after it
+    next_rows = measure_next_rows(args, step, stream, dev, peak)
+
     # ---- end to end through the public API with host buffers
     e2e = run_e2e(args, step, stream, dev) if not args.no_e2e else None
 
@@ -299,6 +302,7 @@ def run_gpu(args, ws, rank, local):
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
                      else "fallback 6.8 TB/s",
                      "unit": "GB/s", "frac": round(q_gbs / peak, 4), "traffic": traffic},
+        "next_rows": next_rows,
         "gpu_launches": KERNELS_PER_STEP * args.steps,
         "other_launches": {"torch fill (zero the step's 3 amax slots)": args.steps},
         "clocks": clocks.summary(),
@@ -307,6 +311,35 @@ def run_gpu(args, ws, rank, local):
     if not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args.cpu_sample_frac)
     return out
+
+
+def measure_next_rows(args, step, stream, dev, peak):
+    """fp8q_qdq_amax (quantize -> dequantize in one pass) on the 8192x16384 activation.
+
+    Timed with CUDA events on the launching stream over back-to-back launches;
+    4 algorithmic bytes per element (bf16 in, bf16 out), larger than L2.
+    """
+    import torch
+    f = step.fp8q
+    y = torch.empty(step.act.numel(), dtype=torch.bfloat16, device=dev)
+    am = torch.zeros(1, device=dev)
+    n_iter = max(5, min(args.steps, 50))
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            f.fp8q_qdq_amax(step.act, y, f.E4M3FN, step.scale[0:1], am, stream.cuda_stream)
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for _ in range(n_iter):
+            f.fp8q_qdq_amax(step.act, y, f.E4M3FN, step.scale[0:1], am, stream.cuda_stream)
+        e.record(stream)
+    torch.cuda.synchronize(dev)
+    us = s.elapsed_time(e) * 1e3 / n_iter
+    nbytes = 4 * N_ACT
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"qdq_amax": {"workload": "bf16 8192x16384 -> e4m3fn -> bf16 + amax", "launches": n_iter,
+                         "us": round(us, 3), "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+                         "bytes_per_launch": nbytes}}
 
 
 def run_e2e(args, step, stream, dev):

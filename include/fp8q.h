@@ -1,12 +1,13 @@
 /*
  * fp8q.h -- C ABI of libfp8q: FP8 delayed-scaling quantization on one GPU.
  *
- * Four operations, each one kernel launch on the caller's stream:
+ * Five operations, each one kernel launch on the caller's stream:
  *   fp8q_quantize_amax        bf16 -> FP8 bytes, fused with amax = max|x|
  *   fp8q_multi_quantize_amax  the same over a ragged list of tensors
  *   fp8q_dequantize           FP8 bytes -> bf16
  *   fp8q_amax_scale_update    amax-history roll + amax selection + scale and
  *                             scale_inv, for many FP8 metadata slots at once
+ *   fp8q_qdq_amax             quantize then dequantize (bf16 -> bf16) + amax
  *
  * Sources (web pages, by title and section):
  *   "User Guide on Native XLA-FP8" (NVIDIA JAX-Toolbox): opening section
@@ -29,8 +30,8 @@
  *     overlap unless a call says it works in place.
  *   - bf16 tensors are contiguous arrays of 16-bit patterns (any 2-byte
  *     aligned address); FP8 tensors are contiguous byte arrays.  Any
- *     alignment works; 16-byte-aligned bf16 with a matching FP8 offset take
- *     the vectorised path.
+ *     alignment works; tensors whose bf16 and FP8 pointers are aligned alike
+ *     (as allocators return them) take the vectorised path.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
  *     return once the kernel is enqueued; results are ready when the stream
  *     reaches that point.
@@ -157,6 +158,20 @@ fp8q_status fp8q_amax_scale_update(float* amax_history, int32_t history_len, int
                                    const float* amax_new, float* scale, float* scale_inv,
                                    const uint8_t* slot_format, fp8q_format fmt,
                                    fp8q_amax_algo algo, int32_t margin, void* stream);
+
+/*
+ * Fused quantize -> dequantize ("fake quant") with amax, in one pass
+ * ("User Guide on Native XLA-FP8", section "Gradient accumulation of FP8
+ * params": in_qdq passes a value through Q and DQ with its scale):
+ *   y[i]  = bf16_rne( float(FP8(x[i] / *scale)) * *scale )   exactly
+ *           fp8q_dequantize(fp8q_quantize_amax(x)), without the FP8 bytes
+ *   *amax = max(*amax, max_i |x[i]|)
+ * x_bf16: n bf16 (device).  y_bf16: n bf16 (device, written); y_bf16 may equal
+ * x_bf16 (in place) but must not partially overlap it.  scale, amax: as for
+ * fp8q_quantize_amax.  Errors: as for fp8q_quantize_amax, plus an odd y_bf16.
+ */
+fp8q_status fp8q_qdq_amax(const void* x_bf16, void* y_bf16, int64_t n, fp8q_format fmt,
+                          const float* scale, float* amax, void* stream);
 
 /* Static, human-readable name of a status. */
 const char* fp8q_status_string(fp8q_status status);

@@ -55,6 +55,8 @@ def lib():
         L.orc_amax.restype = f32
         L.orc_dequantize.argtypes = [vp, i64, ctypes.c_int, f32, vp]
         L.orc_dequantize.restype = None
+        L.orc_qdq_amax.argtypes = [vp, i64, ctypes.c_int, f32, vp, vp]
+        L.orc_qdq_amax.restype = None
         L.orc_amax_scale_update.argtypes = [vp, i32, i32, vp, vp, vp, vp, ctypes.c_int,
                                             ctypes.c_int, i32]
         L.orc_amax_scale_update.restype = None
@@ -134,6 +136,15 @@ def dequantize(q, fmt, scale):
     y = np.empty(q.shape, np.uint16)
     lib().orc_dequantize(_ptr(q), q.size, fmt, float(np.float32(scale)), _ptr(y))
     return y
+
+
+def qdq_amax(x_bf16, fmt, scale, amax=0.0):
+    """Return (bf16 bits of DQ(Q(x)), amax float32) for one bf16 tensor."""
+    x = _c_u16(x_bf16).reshape(-1)
+    y = np.empty(x.shape, np.uint16)
+    a = np.array([amax], np.float32)
+    lib().orc_qdq_amax(_ptr(x), x.size, fmt, float(np.float32(scale)), _ptr(y), _ptr(a))
+    return y, np.float32(a[0])
 
 
 def amax_scale_update(hist, amax_new, scale, scale_inv, fmt=E4M3FN, algo=ALGO_MAX, margin=0,

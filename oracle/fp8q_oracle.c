@@ -206,6 +206,25 @@ void orc_dequantize(const uint8_t* q, int64_t n, int fmt, float scale, uint16_t*
 }
 
 /* ----------------------------------------------------------------------- */
+/* Fused quantize-then-dequantize ("fake quant") with amax ([XLA-FP8]       */
+/* section "Gradient accumulation of FP8 params": in_qdq passes a value     */
+/* through Q and DQ with the tensor's scale).  Each element is exactly      */
+/* DQ(Q(x)) of the two definitions above.                                   */
+
+void orc_qdq_amax(const uint16_t* x_bf16, int64_t n, int fmt, float scale, uint16_t* y_bf16,
+                  float* amax_inout) {
+    float m = *amax_inout;
+    for (int64_t i = 0; i < n; ++i) {
+        float x = orc_bf16_to_f32(x_bf16[i]);
+        uint8_t code = orc_fp8_encode(x / scale, fmt);
+        float p = (float)orc_fp8_decode(code, fmt) * scale;
+        y_bf16[i] = orc_f32_to_bf16(p);
+        m = amax_combine(m, fabsf(x));
+    }
+    if (n > 0) *amax_inout = m;
+}
+
+/* ----------------------------------------------------------------------- */
 /* amax_and_scale_update ([TE-593]; scale formula from [XLA-FP8] "JAX":     */
 /* scale = max|A| / E4M3_MAX, times 2^margin).                              */
 

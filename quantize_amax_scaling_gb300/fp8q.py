@@ -22,7 +22,8 @@ STATUS = {0: "FP8Q_OK", 1: "FP8Q_ERR_INVALID_ARG", 2: "FP8Q_ERR_UNSUPPORTED", 3:
 
 # Every symbol the header declares.
 EXPORTS = ("fp8q_quantize_amax", "fp8q_multi_quantize_amax", "fp8q_dequantize",
-           "fp8q_amax_scale_update", "fp8q_status_string", "fp8q_last_cuda_error")
+           "fp8q_amax_scale_update", "fp8q_qdq_amax", "fp8q_status_string",
+           "fp8q_last_cuda_error")
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfp8q.so")
 
@@ -58,8 +59,9 @@ def lib() -> ctypes.CDLL:
         L.fp8q_multi_quantize_amax.argtypes = [vp, i32, c_int, vp]
         L.fp8q_dequantize.argtypes = [vp, vp, i64, c_int, vp, vp]
         L.fp8q_amax_scale_update.argtypes = [vp, i32, i32, vp, vp, vp, vp, c_int, c_int, i32, vp]
+        L.fp8q_qdq_amax.argtypes = [vp, vp, i64, c_int, vp, vp, vp]
         for f in ("fp8q_quantize_amax", "fp8q_multi_quantize_amax", "fp8q_dequantize",
-                  "fp8q_amax_scale_update"):
+                  "fp8q_amax_scale_update", "fp8q_qdq_amax"):
             getattr(L, f).restype = c_int
         L.fp8q_status_string.argtypes = [c_int]
         L.fp8q_status_string.restype = ctypes.c_char_p
@@ -125,6 +127,17 @@ def fp8q_quantize_amax(x, q, fmt, scale, amax, stream=None):
         _dev(t, k, nm)
     _check(lib().fp8q_quantize_amax(_ptr(x), _ptr(q), n, fmt, _ptr(scale), _ptr(amax),
                                     _stream(stream)), "fp8q_quantize_amax")
+
+
+def fp8q_qdq_amax(x, y, fmt, scale, amax, stream=None):
+    """y = DQ(Q(x)) in bf16 and amax = max(amax, max|x|) in one launch (y may be x)."""
+    n = _numel(x)
+    if y is not None and _numel(y) != n:
+        raise ValueError("y must have as many elements as x")
+    for t, k, nm in ((x, "bf16", "x"), (y, "bf16", "y"), (scale, "f32", "scale"), (amax, "f32", "amax")):
+        _dev(t, k, nm)
+    _check(lib().fp8q_qdq_amax(_ptr(x), _ptr(y), n, fmt, _ptr(scale), _ptr(amax), _stream(stream)),
+           "fp8q_qdq_amax")
 
 
 def fp8q_multi_quantize_amax(xs, qs, fmt, scales, amaxes, stream=None):

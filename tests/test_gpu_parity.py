@@ -471,3 +471,157 @@ def test_scale_update_specials(dev):
         for margin in (-64, -3, 0, 2, 64):
             _update_case(dev, hist, new, algo=algo, margin=margin, slot_format=sf, scale0=scale0,
                          steps=2)
+
+
+# --------------------------------------------------------------------------- limits and capture
+
+def test_more_than_2_pow_31_elements(dev):
+    """Tile and index arithmetic stays 64-bit: quantize and dequantize 2^31 + 4099 elements."""
+    n = (1 << 31) + 4099
+    g = torch.Generator(device=dev)
+    g.manual_seed(31)
+    x = torch.empty(n, dtype=torch.bfloat16, device=dev)
+    chunk = 1 << 28
+    for i in range(0, n, chunk):          # draw in chunks to bound the float32 temporary
+        m = min(chunk, n - i)
+        x[i:i + m] = (torch.randn(m, generator=g, device=dev) * 3.0).to(torch.bfloat16)
+    x[n - 1] = 1000.0                     # the largest magnitude sits in the last element
+    q = torch.empty(n, dtype=torch.uint8, device=dev)
+    scale = np.float32(0.37)
+    am = f32(0.0, dev)
+    fp8q.fp8q_quantize_amax(x, q, E4M3FN, f32(scale, dev), am)
+    y = torch.empty(n, dtype=torch.bfloat16, device=dev)
+    fp8q.fp8q_dequantize(q, y, E4M3FN, f32(scale, dev))
+    torch.cuda.synchronize()
+    assert float(am) == 1000.0
+    rng = np.random.default_rng(2)
+    idx = np.unique(np.concatenate([np.arange(4096), np.arange(n - 8192, n),
+                                    rng.integers((1 << 31) - 8192, n, 4096),
+                                    rng.integers(0, n, 60000)]))
+    # every index is checked on the host before the device gathers with it
+    assert idx.min() >= 0 and idx.max() < n
+    it = torch.from_numpy(idx).to(dev)
+    xb = W.bf16_bits(x[it])
+    rq, _ = oracle.quantize_amax(xb, E4M3FN, scale)
+    assert_codes_equal(q[it].cpu().numpy(), rq, E4M3FN, "n > 2^31")
+    ry = oracle.dequantize(q[it].cpu().numpy(), E4M3FN, scale)
+    assert_bf16_equal(W.bf16_bits(y[it]), ry, "n > 2^31 dequant")
+    del x, q, y
+    torch.cuda.empty_cache()
+
+
+def test_step_captured_in_a_cuda_graph(dev):
+    """Quantize, ragged quantize, dequantize and the update, captured once and replayed:
+    the calls enqueue device work only, so a graph replays them bit-exactly."""
+    act = W.mlp_activation(11, dev, (256, 1024)).reshape(-1)
+    ws = [W.truncated_normal_weight((64, 1024), 1024, 12, dev).reshape(-1),
+          W.truncated_normal_weight((1024, 33), 1024, 13, dev).reshape(-1)]
+    grad_q = torch.from_numpy(np.random.default_rng(3).integers(0, 256, 5000, dtype=np.uint8)).to(dev)
+    H, S = 16, 8
+    hist = torch.zeros(H, S, device=dev)
+    amax = torch.zeros(S, device=dev)
+    scale = torch.ones(S, device=dev)
+    scale_inv = torch.ones(S, device=dev)
+    q_act = torch.empty(act.numel(), dtype=torch.uint8, device=dev)
+    q_w = [torch.empty(w.numel(), dtype=torch.uint8, device=dev) for w in ws]
+    y = torch.empty(grad_q.numel(), dtype=torch.bfloat16, device=dev)
+    s = torch.cuda.Stream()
+
+    def step():
+        amax[:3].zero_()
+        fp8q.fp8q_quantize_amax(act, q_act, E4M3FN, scale[0:1], amax[0:1], stream=s)
+        fp8q.fp8q_multi_quantize_amax(ws, q_w, E4M3FN, [scale[1:2], scale[2:3]], [amax[1:2], amax[2:3]],
+                                      stream=s)
+        fp8q.fp8q_dequantize(grad_q, y, E5M2, scale[3:4], stream=s)
+        fp8q.fp8q_amax_scale_update(hist, amax, scale, scale_inv, E4M3FN, fp8q.ALGO_MAX, 0, stream=s)
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        step()                      # first call on this device (caches launch geometry)
+    s.synchronize()
+    hist.zero_(); amax.zero_(); scale.fill_(1.0); scale_inv.fill_(1.0)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        step()
+    # oracle: three steps of delayed scaling
+    rh = np.zeros((H, S), np.float32)
+    ra = np.zeros(S, np.float32)
+    rs, ri = np.ones(S, np.float32), np.ones(S, np.float32)
+    xa, xw = W.bf16_bits(act), [W.bf16_bits(w) for w in ws]
+    gq = grad_q.cpu().numpy()
+    for _ in range(3):
+        graph.replay()
+        torch.cuda.synchronize()
+        sc = rs.copy()
+        rq_act, a0 = oracle.quantize_amax(xa, E4M3FN, sc[0])
+        rq_w, aw = oracle.multi_quantize_amax(xw, E4M3FN, [sc[1], sc[2]])
+        ry = oracle.dequantize(gq, E5M2, sc[3])
+        ra[:3] = [a0, aw[0], aw[1]]
+        oracle.amax_scale_update(rh, ra, rs, ri, E4M3FN, oracle.ALGO_MAX, 0)
+        assert_codes_equal(q_act.cpu().numpy(), rq_act, E4M3FN, "graph act")
+        for qq, rr in zip(q_w, rq_w):
+            assert_codes_equal(qq.cpu().numpy(), rr, E4M3FN, "graph weights")
+        assert_bf16_equal(W.bf16_bits(y), ry, "graph dequant")
+        assert_f32_equal(hist.cpu().numpy(), rh, "graph history")
+        assert_f32_equal(scale.cpu().numpy(), rs, "graph scale")
+        assert_f32_equal(scale_inv.cpu().numpy(), ri, "graph scale_inv")
+
+
+# --------------------------------------------------------------------------- fused Q -> DQ
+
+def run_qdq(x, fmt, scale, dev, y=None, amax0=0.0):
+    if y is None:
+        y = torch.empty(x.numel(), dtype=torch.bfloat16, device=dev)
+    am = f32(amax0, dev)
+    fp8q.fp8q_qdq_amax(x.reshape(-1), y, fmt, f32(scale, dev), am)
+    torch.cuda.synchronize()
+    return y, am
+
+
+@pytest.mark.parametrize("fmt", [E4M3FN, E5M2])
+def test_qdq_every_bf16_pattern_many_scales(dev, fmt):
+    x = W.all_bf16_patterns(dev)
+    xb = W.bf16_bits(x)
+    for s in SCALES_ALL:
+        y, am = run_qdq(x, fmt, s, dev)
+        ry, ra = oracle.qdq_amax(xb, fmt, np.float32(s))
+        assert_bf16_equal(W.bf16_bits(y), ry, f"scale {s!r}")
+        assert math.isnan(float(am)) and math.isnan(float(ra))
+
+
+@pytest.mark.parametrize("n", [1, 15, 16, 17, 33, 4095, 8193, (1 << 20) + 3])
+def test_qdq_sizes_offsets_in_place_and_canaries(dev, n):
+    g = torch.Generator(device=dev)
+    g.manual_seed(7 * n)
+    for k, (xo, yo) in enumerate(OFFSETS if n < 100000 else OFFSETS[:4]):
+        fmt = E4M3FN if k % 2 else E5M2
+        scale = [0.0123, 1.0, 2.0 ** 70, 3.3e-3][k % 4]
+        xbuf = (torch.randn(n + 16, generator=g, device=dev) * 30.0).to(torch.bfloat16)
+        x = xbuf[xo: xo + n]
+        ybuf, y = guarded(n, torch.bfloat16, dev, yo, fill=0x5A5A)
+        am = f32(0.0, dev)
+        fp8q.fp8q_qdq_amax(x, y, fmt, f32(scale, dev), am)
+        torch.cuda.synchronize()
+        xb = W.bf16_bits(x)
+        ry, ra = oracle.qdq_amax(xb, fmt, np.float32(scale))
+        assert_bf16_equal(W.bf16_bits(y), ry, f"n={n} off={xo},{yo}")
+        assert_f32_equal([float(am)], [ra], f"amax n={n}")
+        check_guards(ybuf, n, yo, fill=0x5A5A)
+        # in place: y is x
+        am2 = f32(0.0, dev)
+        fp8q.fp8q_qdq_amax(x, x, fmt, f32(scale, dev), am2)
+        torch.cuda.synchronize()
+        assert_bf16_equal(W.bf16_bits(x), ry, f"in place n={n}")
+        assert_f32_equal([float(am2)], [ra], f"in-place amax n={n}")
+
+
+def test_qdq_full_size_activation_sampled(dev):
+    x = W.gelu_activation(W.SEED_FFN, dev).reshape(-1)
+    scale = np.float32(0.0091)
+    y, am = run_qdq(x, E4M3FN, scale, dev)
+    xb = W.bf16_bits(x)
+    idx = sample_positions(xb.size)
+    ry, _ = oracle.qdq_amax(xb[idx], E4M3FN, scale)
+    assert_bf16_equal(W.bf16_bits(y)[idx], ry, "qdq 8192x16384")
+    assert_f32_equal([float(am)], [oracle.amax(xb)], "qdq amax")

@@ -33,12 +33,14 @@ MUTATIONS = [
     ("scale_inv not inverted", "scale_inv[s] = 1.0f / sc;", "scale_inv[s] = sc;"),
     ("subnormal scale accepted", "if (!isnormal(sc)) continue;", "if (!isfinite(sc)) continue;"),
     ("dropped roll insert", "hist[s] = amax_new[s];", "(void)amax_new;"),
+    ("fused Q->DQ divides on the way back", "float p = (float)orc_fp8_decode(code, fmt) * scale;",
+     "float p = (float)orc_fp8_decode(code, fmt) / scale;"),
 ]
 
 
 def _build_mutant(tmp, i, old, new):
     src = open(SRC).read()
-    assert src.count(old) == 1, old
+    assert src.count(old) >= 1, old
     d = os.path.join(tmp, f"m{i}")
     os.makedirs(d)
     with open(os.path.join(d, "fp8q_oracle.c"), "w") as f:

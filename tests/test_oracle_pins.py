@@ -414,3 +414,58 @@ def test_per_slot_formats(orc):
     assert sc[2] == 1.0   # unknown format code: slot left unchanged (started at 1.0)
     _, sc, _ = _run_update(orc, 2, 3, [[57344.0, 57344.0, 448.0]], slot_format=sf, scale0=2.0)
     assert sc[0] == 128.0 and sc[1] == 1.0 and sc[2] == 2.0
+
+
+# --------------------------------------------------------------------------- fused Q -> DQ
+
+QDQ_SCALES = [1.0, 0.25, 2.0 ** 10, 1.0 / 3.0, 0.0123, 7.5, 3.0e-5]
+
+
+@pytest.mark.parametrize("fmt", [E4M3FN, E5M2])
+def test_qdq_matches_library_round_trip_in_range(orc, fmt):
+    """In range, DQ(Q(x)) equals the library's cast to FP8 and back, times the scale, as bf16."""
+    x = ALL_BF16_F32
+    for s in QDQ_SCALES:
+        s32 = np.float32(s)
+        with np.errstate(all="ignore"):
+            yq = (x / s32).astype(np.float32)
+        inr = np.isfinite(yq) & (np.abs(yq) <= FP8_MAX[fmt])
+        fp = torch.from_numpy(np.where(inr, yq, 0).astype(np.float32)).to(TORCH_FP8[fmt]).to(torch.float32)
+        want = (fp * torch.tensor(s32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        got, _ = orc.qdq_amax(ALL_BF16, fmt, s32)
+        assert np.array_equal(got[inr], want[inr]), f"scale {s}"
+
+
+@pytest.mark.parametrize("fmt", [E4M3FN, E5M2])
+def test_qdq_error_bound_saturation_and_idempotence(orc, fmt):
+    x = ALL_BF16_F32
+    fin = np.isfinite(x)
+    for s in (1.0, 2.0 ** -4, 2.0 ** 6):   # powers of two: the fp32 product is exact
+        y, a = orc.qdq_amax(ALL_BF16, fmt, s)
+        yf = (y.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        # saturation: |DQ(Q(x))| never exceeds FP8_MAX * scale (rounded to bf16)
+        assert np.all(np.abs(yf[fin]) <= FP8_MAX[fmt] * s * (1 + 2.0 ** -8))
+        # in range the error is at most half an FP8 step (relative 2^-4 or 2^-3) plus the
+        # subnormal floor, and the bf16 rounding of an exact FP8 value adds nothing
+        xs = x[fin].astype(np.float64)
+        inr = np.abs(xs) <= FP8_MAX[fmt] * s
+        rel = 2.0 ** -4 if fmt == E4M3FN else 2.0 ** -3
+        floor = (2.0 ** -10 if fmt == E4M3FN else 2.0 ** -17) * s
+        err = np.abs(yf[fin][inr] - xs[inr])
+        assert np.all(err <= rel * np.abs(xs[inr]) + floor)
+        # idempotence: QDQ(QDQ(x)) == QDQ(x)
+        y2, _ = orc.qdq_amax(y, fmt, s)
+        nan = np.isnan(yf)
+        assert np.array_equal(y2[~nan], y[~nan])
+        # amax is the plain max|x| (NaN among the inputs makes it NaN)
+        assert math.isnan(float(a))
+
+
+def test_qdq_amax_and_representable_identity(orc):
+    for fmt in (E4M3FN, E5M2):
+        vals = [orc.fp8_decode(c, fmt) for c in range(256)]
+        vals = [v * 8.0 for v in vals if math.isfinite(v)]
+        xb = torch.tensor(vals, dtype=torch.float32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        y, a = orc.qdq_amax(xb, fmt, 8.0)
+        assert np.array_equal(y, xb)
+        assert float(a) == max(abs(v) for v in vals)
