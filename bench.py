@@ -235,8 +235,7 @@ def run_gpu(args, ws, rank, local):
             step.run(stream)
     torch.cuda.synchronize(dev)
 
-    # ---- timed region: K steps back to back, per-kernel events inside
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    # ---- timed region: K steps back to back, CUDA events only at its two ends
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
@@ -244,8 +243,8 @@ def run_gpu(args, ws, rank, local):
     torch.cuda.synchronize(dev)
     with torch.cuda.stream(stream):
         start.record(stream)
-        for k in range(args.steps):
-            step.run(stream, ev[k])
+        for _ in range(args.steps):
+            step.run(stream)
         end.record(stream)
     while not end.query():          # sample clocks while the GPU runs the timed steps
         clocks.sample()
@@ -254,6 +253,19 @@ def run_gpu(args, ws, rank, local):
     barrier()
     t_rank = start.elapsed_time(end) / 1e3          # seconds for all K steps on this rank
     value, t_max = aggregate_throughput(STEP_BYTES * args.steps, t_rank, ws)
+
+    # ---- the same K steps again with an event around every kernel, for the
+    # per-kernel breakdown and the roofline.  An event between two kernels
+    # keeps the second from overlapping the first one's tail, so these times
+    # are a little longer than the kernels' share of the clean region above.
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        for k in range(args.steps):
+            step.run(stream, ev[k])
+    torch.cuda.synchronize(dev)
+    barrier()
 
     per = {"quantize_amax": [], "multi_quantize_amax": [], "dequantize": [], "amax_scale_update": []}
     for k in range(args.steps):
@@ -268,8 +280,11 @@ def run_gpu(args, ws, rank, local):
                for n in per}
     q_gbs = kbytes["quantize_amax"] / (avg["quantize_amax"] * 1e-6) / 1e9
 
-    # ---- rows beyond the step (fused Q->DQ), timed on their own after it
-    next_rows = measure_next_rows(args, step, stream, dev, peak)
+    # ---- the same step as one CUDA graph (no host launches, no events inside)
+    graph = None if args.no_extras else measure_graph(args, step, stream, dev)
+
+    # ---- rows beyond the step (fused Q->DQ, ring history), timed on their own after it
+    next_rows = None if args.no_extras else measure_next_rows(args, step, stream, dev, peak)
 
     # ---- end to end through the public API with host buffers
     e2e = run_e2e(args, step, stream, dev) if not args.no_e2e else None
@@ -291,17 +306,22 @@ def run_gpu(args, ws, rank, local):
         "dtype": "f32",
         "data": "synthetic (seeded; shapes of the FFN/MLP and 96-layer workloads)",
         "config": {"workload": WORKLOAD, "step_bytes": STEP_BYTES,
+                   "timing": "value and ms_per_step: K steps with CUDA events only around the region; "
+                             "kernels and roofline: a second pass of K steps with an event around each kernel",
                    "l2": "inputs larger than L2 (each step streams 1.21 GB; the 129 MB L2 holds none of "
                          "a step's inputs when it is read again)",
                    "parallelism": f"replicas x{ws} (no collective)"},
         "headline": {"quantize_amax_gbs": round(q_gbs, 1), "quantize_amax_frac_of_peak": round(q_gbs / peak, 4),
-                     "scale_update_us": round(avg["amax_scale_update"], 3)},
+                     "scale_update_us": round(avg["amax_scale_update"], 3),
+                     "scale_update_us_in_graph": graph["scale_update_us_after_dequantize"] if graph else None,
+                     "scale_update_launches_per_call": 1},
         "kernels": kernels,
         "roofline": {"kernel": "quantize_amax_kernel (8192x16384 bf16 -> e4m3fn + amax)",
                      "bound": "hbm", "achieved": round(q_gbs, 1), "peak": peak,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
                      else "fallback 6.8 TB/s",
                      "unit": "GB/s", "frac": round(q_gbs / peak, 4), "traffic": traffic},
+        "graph": graph,
         "next_rows": next_rows,
         "gpu_launches": KERNELS_PER_STEP * args.steps,
         "other_launches": {"torch fill (zero the step's 3 amax slots)": args.steps},
@@ -311,6 +331,58 @@ def run_gpu(args, ws, rank, local):
     if not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args.cpu_sample_frac)
     return out
+
+
+def measure_graph(args, step, stream, dev):
+    """The step captured once as a CUDA graph and replayed K times.
+
+    Per-kernel events in the eager loop stop each launch from overlapping the
+    previous kernel's tail, which costs a few microseconds per kernel and shows
+    most on the short scale update.  Here the step runs without host launches
+    or events inside; the update's own cost is taken as the difference between
+    graphs of (dequantize, update) pairs and of dequantize alone.
+    """
+    import torch
+    f = step.fp8q
+    st = stream.cuda_stream
+
+    def timed(fn, reps):
+        with torch.cuda.stream(stream):
+            fn()
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(reps):
+                    fn()
+            for _ in range(2):
+                g.replay()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) * 1e3 / reps  # us per repetition
+
+    reps = max(4, min(args.steps, 50))
+    step_us = timed(lambda: step.run(stream), reps)
+    deq = lambda: f.fp8q_dequantize(step.grad_q, step.y_grad, f.E5M2, step.scale[4:5], st)
+    upd = lambda: f.fp8q_amax_scale_update(step.hist, step.amax_new, step.scale, step.scale_inv, f.E4M3FN,
+                                           f.ALGO_MAX, 0, step.slot_format, st)
+    ring_hist = step.hist.clone()
+    head = torch.full((S,), H - 1, dtype=torch.int32, device=dev)
+    sc, si = step.scale.clone(), step.scale_inv.clone()
+    ring = lambda: f.fp8q_amax_scale_update_ring(ring_hist, head, step.amax_new, sc, si, f.E4M3FN,
+                                                 f.ALGO_MAX, 0, step.slot_format, st)
+    deq_us = timed(deq, 20)
+    pair_us = timed(lambda: (deq(), upd()), 20)
+    ring_pair_us = timed(lambda: (deq(), ring()), 20)
+    return {"ms_per_step": round(step_us / 1e3, 4), "replays_of_step": reps,
+            "GB/s": round(STEP_BYTES / (step_us * 1e-6) / 1e9, 1),
+            "scale_update_us_after_dequantize": round(pair_us - deq_us, 3),
+            "ring_update_us_after_dequantize": round(ring_pair_us - deq_us, 3),
+            "how": "one step captured as a CUDA graph, CUDA events around the replay; the update's "
+                   "time is (dequantize+update) pairs minus dequantize alone, both as graphs"}
 
 
 def measure_next_rows(args, step, stream, dev, peak):
@@ -337,9 +409,41 @@ def measure_next_rows(args, step, stream, dev, peak):
     us = s.elapsed_time(e) * 1e3 / n_iter
     nbytes = 4 * N_ACT
     gbs = nbytes / (us * 1e-6) / 1e9
-    return {"qdq_amax": {"workload": "bf16 8192x16384 -> e4m3fn -> bf16 + amax", "launches": n_iter,
-                         "us": round(us, 3), "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
-                         "bytes_per_launch": nbytes}}
+    out = {"qdq_amax": {"workload": "bf16 8192x16384 -> e4m3fn -> bf16 + amax", "launches": n_iter,
+                        "us": round(us, 3), "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+                        "bytes_per_launch": nbytes}}
+
+    # Ring-buffer update against the rolled one, each timed right after a
+    # dequantize of the 8192x16384 gradient (where the update sits in the step).
+    ring_hist = step.hist.clone()
+    head = torch.full((S,), H - 1, dtype=torch.int32, device=dev)
+    roll_hist = step.hist.clone()
+    sc, si = step.scale.clone(), step.scale_inv.clone()
+    times = {"ring": [], "roll": []}
+    with torch.cuda.stream(stream):
+        for i in range(n_iter + 3):
+            for kind in ("ring", "roll"):
+                f.fp8q_dequantize(step.grad_q, step.y_grad, f.E5M2, step.scale[4:5], stream.cuda_stream)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                if kind == "ring":
+                    f.fp8q_amax_scale_update_ring(ring_hist, head, step.amax_new, sc, si, f.E4M3FN,
+                                                  f.ALGO_MAX, 0, step.slot_format, stream.cuda_stream)
+                else:
+                    f.fp8q_amax_scale_update(roll_hist, step.amax_new, sc, si, f.E4M3FN, f.ALGO_MAX, 0,
+                                             step.slot_format, stream.cuda_stream)
+                e1.record(stream)
+                if i >= 3:
+                    times[kind].append((e0, e1))
+    torch.cuda.synchronize(dev)
+    avg = {k: sum(a.elapsed_time(b) for a, b in v) * 1e3 / len(v) for k, v in times.items()}
+    ring_bytes = H * S * 4 + S * 4 * 2 + S * 4 * 4   # history read, one row + heads, scales
+    out["amax_scale_update_ring"] = {
+        "workload": "576 slots x history 1024, each call right after a 268 MB dequantize",
+        "launches": n_iter, "us": round(avg["ring"], 3), "rolled_us_same_setting": round(avg["roll"], 3),
+        "bytes_per_launch": ring_bytes}
+    return out
 
 
 def run_e2e(args, step, stream, dev):
@@ -491,6 +595,8 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the CUDA-graph and next-row measurements (run after the timed region)")
     ap.add_argument("--cpu-sample-frac", type=float, default=1.0 / 16)
     ap.add_argument("--ref-sample-frac", type=float, default=1.0 / 128)
     args = ap.parse_args(argv)

@@ -1,13 +1,14 @@
 /*
  * fp8q.h -- C ABI of libfp8q: FP8 delayed-scaling quantization on one GPU.
  *
- * Five operations, each one kernel launch on the caller's stream:
+ * Six operations, each one kernel launch on the caller's stream:
  *   fp8q_quantize_amax        bf16 -> FP8 bytes, fused with amax = max|x|
  *   fp8q_multi_quantize_amax  the same over a ragged list of tensors
  *   fp8q_dequantize           FP8 bytes -> bf16
  *   fp8q_amax_scale_update    amax-history roll + amax selection + scale and
  *                             scale_inv, for many FP8 metadata slots at once
  *   fp8q_qdq_amax             quantize then dequantize (bf16 -> bf16) + amax
+ *   fp8q_amax_scale_update_ring  the update over a ring buffer (no roll)
  *
  * Sources (web pages, by title and section):
  *   "User Guide on Native XLA-FP8" (NVIDIA JAX-Toolbox): opening section
@@ -172,6 +173,32 @@ fp8q_status fp8q_amax_scale_update(float* amax_history, int32_t history_len, int
  */
 fp8q_status fp8q_qdq_amax(const void* x_bf16, void* y_bf16, int64_t n, fp8q_format fmt,
                           const float* scale, float* amax, void* stream);
+
+/*
+ * amax_and_scale_update over a ring buffer: the same window, selection and
+ * scale as fp8q_amax_scale_update, without moving the history.  Each slot's
+ * oldest entry is overwritten in place instead of every entry shifting by one
+ * row, so a call reads the history and writes one row.  (Window and scale:
+ * "Implement fused kernel for FP8 scale update"; "User Guide on Native
+ * XLA-FP8", section "JAX", delayed scaling.)  Per slot s, with h = head[s]:
+ *   1. h' = (h + 1) mod H;  hist[h'][s] <- amax_new[s];  head[s] <- h'
+ *   2. select: a = max over all H rows (ALGO_MAX; NaN wins) or amax_new[s]
+ *   3. scale / scale_inv exactly as fp8q_amax_scale_update.
+ * Logical row r (0 = newest) of slot s is physical row (head[s] - r) mod H,
+ * so after any sequence of calls the window and the scales equal those of the
+ * rolled form.  Start with head[s] = H - 1 to fill rows 0, 1, 2, ... in order.
+ * A head outside [0, H) leaves that slot's history, head and scales untouched.
+ *
+ * amax_history: float[H][num_slots] row-major (device, one row per slot
+ * written).  head: int32[num_slots] (device, read and advanced).  Other
+ * arguments and errors: as for fp8q_amax_scale_update (head is checked like
+ * the float pointers).
+ */
+fp8q_status fp8q_amax_scale_update_ring(float* amax_history, int32_t* head, int32_t history_len,
+                                        int32_t num_slots, const float* amax_new, float* scale,
+                                        float* scale_inv, const uint8_t* slot_format,
+                                        fp8q_format fmt, fp8q_amax_algo algo, int32_t margin,
+                                        void* stream);
 
 /* Static, human-readable name of a status. */
 const char* fp8q_status_string(fp8q_status status);

@@ -60,6 +60,9 @@ def lib():
         L.orc_amax_scale_update.argtypes = [vp, i32, i32, vp, vp, vp, vp, ctypes.c_int,
                                             ctypes.c_int, i32]
         L.orc_amax_scale_update.restype = None
+        L.orc_amax_scale_update_ring.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp, ctypes.c_int,
+                                                 ctypes.c_int, i32]
+        L.orc_amax_scale_update_ring.restype = None
         _lib = L
     return _lib
 
@@ -158,3 +161,15 @@ def amax_scale_update(hist, amax_new, scale, scale_inv, fmt=E4M3FN, algo=ALGO_MA
     sf = None if slot_format is None else np.ascontiguousarray(slot_format, np.uint8)
     lib().orc_amax_scale_update(_ptr(hist), H, S, _ptr(amax_new), _ptr(scale), _ptr(scale_inv),
                                 _ptr(sf), fmt, algo, margin)
+
+
+def amax_scale_update_ring(hist, head, amax_new, scale, scale_inv, fmt=E4M3FN, algo=ALGO_MAX,
+                           margin=0, slot_format=None):
+    """In-place ring-buffer update of hist[H][S], head[S] (int32), scale[S], scale_inv[S]."""
+    assert hist.dtype == np.float32 and hist.flags.c_contiguous and hist.ndim == 2
+    H, S = hist.shape
+    assert head.dtype == np.int32 and head.flags.c_contiguous and head.size == S
+    amax_new = np.ascontiguousarray(amax_new, np.float32)
+    sf = None if slot_format is None else np.ascontiguousarray(slot_format, np.uint8)
+    lib().orc_amax_scale_update_ring(_ptr(hist), _ptr(head), H, S, _ptr(amax_new), _ptr(scale),
+                                     _ptr(scale_inv), _ptr(sf), fmt, algo, margin)

@@ -228,6 +228,18 @@ void orc_qdq_amax(const uint16_t* x_bf16, int64_t n, int fmt, float scale, uint1
 /* amax_and_scale_update ([TE-593]; scale formula from [XLA-FP8] "JAX":     */
 /* scale = max|A| / E4M3_MAX, times 2^margin).                              */
 
+/* Scale and scale_inv of one slot from its selected amax, or pass-through. */
+static void slot_scale(float a, int f, int32_t margin, float* scale, float* scale_inv) {
+    if (f != ORC_E4M3FN && f != ORC_E5M2) return; /* unknown format: leave the slot */
+    if (!(isfinite(a) && a > 0.0f)) return;
+    float fp8max = (float)orc_fp8_max(f);
+    float sc = a / fp8max;      /* RN binary32 */
+    sc = ldexpf(sc, margin);    /* times 2^margin, one rounding */
+    if (!isnormal(sc)) return;
+    *scale = sc;
+    *scale_inv = 1.0f / sc;     /* RN binary32 */
+}
+
 void orc_amax_scale_update(float* hist, int32_t H, int32_t S, const float* amax_new,
                            float* scale, float* scale_inv, const uint8_t* slot_format,
                            int fmt, int algo, int32_t margin) {
@@ -242,14 +254,30 @@ void orc_amax_scale_update(float* hist, int32_t H, int32_t S, const float* amax_
             for (int32_t h = 1; h < H; ++h) a = amax_combine(a, hist[(int64_t)h * S + s]);
 
         /* 3. scale and its inverse, or pass-through */
-        int f = slot_format ? slot_format[s] : fmt;
-        if (f != ORC_E4M3FN && f != ORC_E5M2) continue; /* unknown format: leave the slot */
-        if (!(isfinite(a) && a > 0.0f)) continue;
-        float fp8max = (float)orc_fp8_max(f);
-        float sc = a / fp8max;      /* RN binary32 */
-        sc = ldexpf(sc, margin);    /* times 2^margin, one rounding */
-        if (!isnormal(sc)) continue;
-        scale[s] = sc;
-        scale_inv[s] = 1.0f / sc;   /* RN binary32 */
+        slot_scale(a, slot_format ? slot_format[s] : fmt, margin, &scale[s], &scale_inv[s]);
+    }
+}
+
+/*
+ * The same update over a ring buffer (a NEXT item beyond the roll: the window
+ * is kept in place and only the oldest entry is overwritten).  Slot s keeps
+ * its own position head[s] = the physical row of its newest entry; logical
+ * row r (0 = newest) is physical row (head[s] - r) mod H, so after the same
+ * sequence of calls the window holds exactly what the rolled history holds.
+ * A head outside [0, H) leaves the whole slot unchanged.
+ */
+void orc_amax_scale_update_ring(float* hist, int32_t* head, int32_t H, int32_t S,
+                                const float* amax_new, float* scale, float* scale_inv,
+                                const uint8_t* slot_format, int fmt, int algo, int32_t margin) {
+    for (int32_t s = 0; s < S; ++s) {
+        int32_t h = head[s];
+        if (h < 0 || h >= H) continue;
+        h = (h + 1) % H;                   /* the oldest entry's row */
+        hist[(int64_t)h * S + s] = amax_new[s];
+        head[s] = h;
+        float a = hist[(int64_t)h * S + s];
+        if (algo == ORC_ALGO_MAX)
+            for (int32_t r = 0; r < H; ++r) a = amax_combine(a, hist[(int64_t)r * S + s]);
+        slot_scale(a, slot_format ? slot_format[s] : fmt, margin, &scale[s], &scale_inv[s]);
     }
 }

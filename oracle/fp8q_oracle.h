@@ -41,6 +41,9 @@ void orc_qdq_amax(const uint16_t* x_bf16, int64_t n, int fmt, float scale, uint1
 void orc_amax_scale_update(float* hist, int32_t H, int32_t S, const float* amax_new,
                            float* scale, float* scale_inv, const uint8_t* slot_format,
                            int fmt, int algo, int32_t margin);
+void orc_amax_scale_update_ring(float* hist, int32_t* head, int32_t H, int32_t S,
+                                const float* amax_new, float* scale, float* scale_inv,
+                                const uint8_t* slot_format, int fmt, int algo, int32_t margin);
 
 #ifdef __cplusplus
 }

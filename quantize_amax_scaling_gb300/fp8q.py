@@ -22,8 +22,8 @@ STATUS = {0: "FP8Q_OK", 1: "FP8Q_ERR_INVALID_ARG", 2: "FP8Q_ERR_UNSUPPORTED", 3:
 
 # Every symbol the header declares.
 EXPORTS = ("fp8q_quantize_amax", "fp8q_multi_quantize_amax", "fp8q_dequantize",
-           "fp8q_amax_scale_update", "fp8q_qdq_amax", "fp8q_status_string",
-           "fp8q_last_cuda_error")
+           "fp8q_amax_scale_update", "fp8q_qdq_amax", "fp8q_amax_scale_update_ring",
+           "fp8q_status_string", "fp8q_last_cuda_error")
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfp8q.so")
 
@@ -60,8 +60,10 @@ def lib() -> ctypes.CDLL:
         L.fp8q_dequantize.argtypes = [vp, vp, i64, c_int, vp, vp]
         L.fp8q_amax_scale_update.argtypes = [vp, i32, i32, vp, vp, vp, vp, c_int, c_int, i32, vp]
         L.fp8q_qdq_amax.argtypes = [vp, vp, i64, c_int, vp, vp, vp]
+        L.fp8q_amax_scale_update_ring.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp, c_int, c_int, i32,
+                                                  vp]
         for f in ("fp8q_quantize_amax", "fp8q_multi_quantize_amax", "fp8q_dequantize",
-                  "fp8q_amax_scale_update", "fp8q_qdq_amax"):
+                  "fp8q_amax_scale_update", "fp8q_qdq_amax", "fp8q_amax_scale_update_ring"):
             getattr(L, f).restype = c_int
         L.fp8q_status_string.argtypes = [c_int]
         L.fp8q_status_string.restype = ctypes.c_char_p
@@ -195,6 +197,33 @@ def fp8q_amax_scale_update(history, amax_new, scale, scale_inv, fmt=E4M3FN, algo
     _check(lib().fp8q_amax_scale_update(_ptr(history), H, S, _ptr(amax_new), _ptr(scale),
                                         _ptr(scale_inv), _ptr(slot_format), fmt, algo, margin,
                                         _stream(stream)), "fp8q_amax_scale_update")
+
+
+def fp8q_amax_scale_update_ring(history, head, amax_new, scale, scale_inv, fmt=E4M3FN,
+                                algo=ALGO_MAX, margin=0, slot_format=None, stream=None):
+    """Ring-buffer amax history update: overwrite each slot's oldest row, advance head.
+
+    ``history`` is float32 [history_len, num_slots]; ``head`` is int32 [num_slots],
+    the row of each slot's newest entry.
+    """
+    import torch
+    if history.dim() != 2:
+        raise ValueError("history must be [history_len, num_slots]")
+    H, S = history.shape
+    for t, k, nm in ((history, "f32", "history"), (amax_new, "f32", "amax_new"),
+                     (scale, "f32", "scale"), (scale_inv, "f32", "scale_inv"),
+                     (slot_format, "u8", "slot_format")):
+        _dev(t, k, nm)
+    if not (head.is_cuda and head.dtype == torch.int32 and head.is_contiguous()):
+        raise ValueError("head must be a contiguous int32 CUDA tensor")
+    for t, nm in ((head, "head"), (amax_new, "amax_new"), (scale, "scale"), (scale_inv, "scale_inv"),
+                  (slot_format, "slot_format")):
+        if t is not None and t.numel() != S:
+            raise ValueError(f"{nm} must have num_slots={S} elements")
+    _check(lib().fp8q_amax_scale_update_ring(_ptr(history), _ptr(head), H, S, _ptr(amax_new),
+                                             _ptr(scale), _ptr(scale_inv), _ptr(slot_format), fmt,
+                                             algo, margin, _stream(stream)),
+           "fp8q_amax_scale_update_ring")
 
 
 def status_string(status: int) -> str:

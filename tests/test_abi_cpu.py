@@ -27,8 +27,8 @@ def declared_functions():
 def test_header_declares_the_four_operations():
     names = declared_functions()
     for f in ("fp8q_quantize_amax", "fp8q_multi_quantize_amax", "fp8q_dequantize",
-              "fp8q_amax_scale_update", "fp8q_qdq_amax", "fp8q_status_string",
-              "fp8q_last_cuda_error"):
+              "fp8q_amax_scale_update", "fp8q_qdq_amax", "fp8q_amax_scale_update_ring",
+              "fp8q_status_string", "fp8q_last_cuda_error"):
         assert f in names
 
 
@@ -93,6 +93,23 @@ def test_qdq_argument_errors(L):
         assert f(x, y, 4, 0, sc, am, None) == INVALID
     assert f(ODD, P, 4, 0, P, P, None) == INVALID
     assert f(P, ODD, 4, 0, P, P, None) == INVALID
+
+
+def test_ring_update_argument_errors(L):
+    u = L.fp8q_amax_scale_update_ring
+    good = [P, P, 16, 4, P, P, P, None, 0, 0, 0, None]
+    def call(i, v):
+        a = list(good)
+        a[i] = v
+        return u(*a)
+    assert call(2, 0) == INVALID
+    assert call(3, 0) == INVALID
+    assert call(8, 5) == INVALID
+    assert call(9, 7) == INVALID
+    assert call(10, 99) == INVALID
+    for i in (0, 1, 4, 5, 6):
+        assert call(i, None) == INVALID
+        assert call(i, ctypes.c_void_p(0x10002)) == INVALID
 
 
 def test_dequantize_argument_errors(L):

@@ -625,3 +625,96 @@ def test_qdq_full_size_activation_sampled(dev):
     ry, _ = oracle.qdq_amax(xb[idx], E4M3FN, scale)
     assert_bf16_equal(W.bf16_bits(y)[idx], ry, "qdq 8192x16384")
     assert_f32_equal([float(am)], [oracle.amax(xb)], "qdq amax")
+
+
+# --------------------------------------------------------------------------- ring-buffer history
+
+def _ring_case(dev, hist_np, head_np, new_np, algo=0, margin=0, slot_format=None, steps=1,
+               scale0=None, hist_offset=0):
+    H, S = hist_np.shape
+    if hist_offset:
+        buf = torch.zeros(H * S + hist_offset, device=dev)
+        hist = buf[hist_offset:].view(H, S)
+        hist.copy_(torch.from_numpy(hist_np))
+    else:
+        hist = torch.from_numpy(hist_np.copy()).to(dev)
+    head = torch.from_numpy(head_np.copy()).to(dev)
+    s0 = scale0 if scale0 is not None else np.ones(S, np.float32)
+    sc = torch.from_numpy(s0.copy()).to(dev)
+    si = torch.from_numpy((1.0 / s0).astype(np.float32)).to(dev)
+    rh, rhead = hist_np.copy(), head_np.copy()
+    rs, ri = sc.cpu().numpy().copy(), si.cpu().numpy().copy()
+    sf_t = None if slot_format is None else torch.from_numpy(slot_format).to(dev)
+    for step in range(steps):
+        new_s = new_np if step == 0 else (np.roll(new_np, step) * np.float32(1.25 ** step)).astype(np.float32)
+        fp8q.fp8q_amax_scale_update_ring(hist, head, torch.from_numpy(new_s).to(dev), sc, si, E4M3FN, algo,
+                                         margin, sf_t)
+        oracle.amax_scale_update_ring(rh, rhead, new_s, rs, ri, E4M3FN, algo, margin, slot_format)
+    torch.cuda.synchronize()
+    assert np.array_equal(head.cpu().numpy(), rhead), "head"
+    assert_f32_equal(hist.cpu().numpy(), rh, f"ring history {H}x{S}")
+    assert_f32_equal(sc.cpu().numpy(), rs, f"ring scale {H}x{S}")
+    assert_f32_equal(si.cpu().numpy(), ri, f"ring scale_inv {H}x{S}")
+
+
+@pytest.mark.parametrize("algo", [fp8q.ALGO_MAX, fp8q.ALGO_MOST_RECENT])
+@pytest.mark.parametrize("margin", [0, 1])
+@pytest.mark.parametrize("per_slot", [False, True])
+def test_ring_update_576_slots_full(dev, algo, margin, per_slot):
+    hist, new, _, _, sf = W.scale_update_inputs("cpu")
+    H, S = hist.shape
+    head = np.random.default_rng(5).integers(0, H, S).astype(np.int32)
+    _ring_case(dev, hist.numpy(), head, new.numpy(), algo=algo, margin=margin,
+               slot_format=sf.numpy() if per_slot else None, steps=3)
+
+
+@pytest.mark.parametrize("H,S", SHAPES)
+def test_ring_update_shapes(dev, H, S):
+    rng = np.random.default_rng(H * 7 + S)
+    hist = np.exp(rng.normal(0, 2, (H, S))).astype(np.float32)
+    hist[rng.random((H, S)) < 0.05] = 0.0
+    new = np.exp(rng.normal(0, 2, S)).astype(np.float32)
+    head = rng.integers(0, H, S).astype(np.int32)
+    for algo in (0, 1):
+        _ring_case(dev, hist, head, new, algo=algo, margin=(H % 3) - 1, steps=2)
+
+
+def test_ring_update_specials_corrupt_heads_and_scalar_path(dev):
+    S = 12
+    hist = np.full((8, S), 2.0, np.float32)
+    hist[3, 0] = np.nan
+    hist[2, 2] = np.inf
+    hist[:, 3] = 0.0
+    new = np.array([1, 1, 1, 0, 1, np.nan, np.inf, -1, 1e-38, 3e38, 1e-45, 448], np.float32)
+    head = np.array([7, 3, 0, 5, -1, 8, 2, 2, 2, 2, 2, 1000], np.int32)   # -1, 8, 1000 are corrupt
+    sf = np.array([0, 1, 0, 0, 1, 0, 1, 0, 0, 1, 0, 5], np.uint8)
+    for algo in (0, 1):
+        _ring_case(dev, hist, head, new, algo=algo, slot_format=sf, scale0=np.full(S, 4.0, np.float32), steps=2)
+    rng = np.random.default_rng(9)
+    big = np.exp(rng.normal(0, 2, (1024, 576))).astype(np.float32)
+    _ring_case(dev, big, rng.integers(0, 1024, 576).astype(np.int32),
+               np.exp(rng.normal(0, 2, 576)).astype(np.float32), hist_offset=1, steps=2)
+
+
+def test_ring_matches_roll_on_the_gpu(dev):
+    """Both GPU forms, fed the same amaxes, give the same window (unrotated) and scales."""
+    hist, new, _, _, sf = W.scale_update_inputs(dev)
+    H, S = hist.shape
+    roll = hist.clone()
+    ring = hist.flip(0).contiguous()             # newest row at the bottom ...
+    head = torch.full((S,), H - 1, dtype=torch.int32, device=dev)   # ... where head points
+    sc_a, si_a = torch.ones(S, device=dev), torch.ones(S, device=dev)
+    sc_b, si_b = sc_a.clone(), si_a.clone()
+    g = torch.Generator(device=dev)
+    g.manual_seed(77)
+    for _ in range(5):
+        a = torch.exp(torch.randn(S, generator=g, device=dev) * 2)
+        fp8q.fp8q_amax_scale_update(roll, a, sc_a, si_a, E4M3FN, fp8q.ALGO_MAX, 0, sf)
+        fp8q.fp8q_amax_scale_update_ring(ring, head, a, sc_b, si_b, E4M3FN, fp8q.ALGO_MAX, 0, sf)
+    torch.cuda.synchronize()
+    h = head.cpu().numpy()
+    rg = ring.cpu().numpy()
+    logical = np.stack([rg[(h - r) % H, np.arange(S)] for r in range(H)])
+    assert_f32_equal(logical, roll.cpu().numpy(), "ring vs roll window")
+    assert_f32_equal(sc_b.cpu().numpy(), sc_a.cpu().numpy(), "ring vs roll scale")
+    assert_f32_equal(si_b.cpu().numpy(), si_a.cpu().numpy(), "ring vs roll scale_inv")

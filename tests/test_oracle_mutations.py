@@ -30,9 +30,12 @@ MUTATIONS = [
     ("selection algos swapped", "if (algo == ORC_ALGO_MAX)", "if (algo != ORC_ALGO_MAX)"),
     ("subnormal exponent off by one", "v = ldexp((double)m, 1 - bias - mbits);", "v = ldexp((double)m, - bias - mbits);"),
     ("scale inverted", "float sc = a / fp8max;", "float sc = fp8max / a;"),
-    ("scale_inv not inverted", "scale_inv[s] = 1.0f / sc;", "scale_inv[s] = sc;"),
-    ("subnormal scale accepted", "if (!isnormal(sc)) continue;", "if (!isfinite(sc)) continue;"),
+    ("scale_inv not inverted", "*scale_inv = 1.0f / sc;", "*scale_inv = sc;"),
+    ("subnormal scale accepted", "if (!isnormal(sc)) return;", "if (!isfinite(sc)) return;"),
     ("dropped roll insert", "hist[s] = amax_new[s];", "(void)amax_new;"),
+    ("ring overwrites the newest entry", "h = (h + 1) % H;", "h = h % H;"),
+    ("ring window one row short", "for (int32_t r = 0; r < H; ++r) a = amax_combine(a, hist[(int64_t)r * S + s]);",
+     "for (int32_t r = 0; r < H - 1; ++r) a = amax_combine(a, hist[(int64_t)r * S + s]);"),
     ("fused Q->DQ divides on the way back", "float p = (float)orc_fp8_decode(code, fmt) * scale;",
      "float p = (float)orc_fp8_decode(code, fmt) / scale;"),
 ]

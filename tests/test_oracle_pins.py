@@ -469,3 +469,68 @@ def test_qdq_amax_and_representable_identity(orc):
         y, a = orc.qdq_amax(xb, fmt, 8.0)
         assert np.array_equal(y, xb)
         assert float(a) == max(abs(v) for v in vals)
+
+
+# --------------------------------------------------------------------------- ring-buffer history
+
+def _ring_logical(hist, head):
+    """Unrotate a ring history into the rolled layout (row 0 newest)."""
+    H, S = hist.shape
+    out = np.empty_like(hist)
+    for s in range(S):
+        for r in range(H):
+            out[r, s] = hist[(head[s] - r) % H, s]
+    return out
+
+
+def test_ring_equals_roll_for_any_sequence(orc):
+    """Same window contents and the same scales as the rolled history after every call."""
+    rng = np.random.default_rng(21)
+    for H in (1, 2, 3, 5, 8):
+        for S in (1, 3, 6):
+            for algo in (0, 1):
+                hist_r = np.zeros((H, S), np.float32)
+                hist_g = np.zeros((H, S), np.float32)
+                start = rng.integers(0, H, S).astype(np.int32)       # arbitrary starting positions
+                head = start.copy()
+                sc_r, si_r = np.ones(S, np.float32), np.ones(S, np.float32)
+                sc_g, si_g = sc_r.copy(), si_r.copy()
+                sf = (np.arange(S) % 2).astype(np.uint8)
+                for k in range(2 * H + 3):
+                    new = np.exp(rng.normal(0, 3, S)).astype(np.float32)
+                    new[rng.random(S) < 0.15] = 0.0
+                    if k == H:
+                        new[0] = np.nan
+                    margin = int(rng.integers(-2, 3))
+                    orc.amax_scale_update(hist_r, new, sc_r, si_r, E4M3FN, algo, margin, sf)
+                    orc.amax_scale_update_ring(hist_g, head, new, sc_g, si_g, E4M3FN, algo, margin, sf)
+                    assert np.array_equal(head, ((start + k + 1) % H).astype(np.int32))
+                    lg = _ring_logical(hist_g, head)
+                    assert np.array_equal(np.isnan(lg), np.isnan(hist_r))
+                    assert np.array_equal(np.nan_to_num(lg), np.nan_to_num(hist_r)), (H, S, k)
+                    assert np.array_equal(sc_g, sc_r) and np.array_equal(si_g, si_r), (H, S, algo, k)
+
+
+def test_ring_writes_exactly_one_row_per_slot(orc):
+    H, S = 6, 4
+    hist = np.arange(H * S, dtype=np.float32).reshape(H, S) + 1
+    head = np.array([0, 5, 2, 3], np.int32)
+    before = hist.copy()
+    orc.amax_scale_update_ring(hist, head, np.full(S, 99.0, np.float32), np.ones(S, np.float32),
+                               np.ones(S, np.float32))
+    changed = hist != before
+    assert changed.sum() == S
+    for s, h in enumerate([1, 0, 3, 4]):
+        assert changed[h, s] and hist[h, s] == 99.0
+
+
+def test_ring_invalid_head_leaves_slot_alone(orc):
+    H, S = 4, 3
+    hist = np.full((H, S), 2.0, np.float32)
+    head = np.array([-1, 4, 1], np.int32)
+    sc = np.full(S, 5.0, np.float32)
+    si = np.full(S, 0.2, np.float32)
+    orc.amax_scale_update_ring(hist, head, np.full(S, 448.0, np.float32), sc, si)
+    assert list(head) == [-1, 4, 2]
+    assert np.all(hist[:, :2] == 2.0) and sc[0] == 5.0 and sc[1] == 5.0
+    assert hist[2, 2] == 448.0 and sc[2] == 1.0
