@@ -584,9 +584,8 @@ def read_traffic():
     """DRAM bytes per launch of the quantize kernel from the committed ncu capture.
 
     None when there is no capture or when the kernel source has changed since
-    the counters were taken (the record carries the source's sha256).
+    the counters were taken (the record carries a digest of the source's code).
     """
-    import hashlib
     p = os.path.join(ROOT, "profiles", "quantize_amax_traffic.json")
     if not os.path.exists(p):
         return None
@@ -595,10 +594,19 @@ def read_traffic():
     src = os.path.join(ROOT, d.get("source", ""))
     if not os.path.exists(src):
         return None
-    with open(src, "rb") as f:
-        if hashlib.sha256(f.read()).hexdigest() != d.get("source_sha256"):
+    with open(src) as f:
+        if source_digest(f.read()) != d.get("source_code_sha256"):
             return None
     return d.get("dram_bytes_per_launch")
+
+
+def source_digest(text: str) -> str:
+    """sha256 of C/CUDA source with comments and whitespace removed (code changes only)."""
+    import hashlib
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return hashlib.sha256("".join(text.split()).encode()).hexdigest()
 
 
 # --------------------------------------------------------------------------- CPU oracle legs

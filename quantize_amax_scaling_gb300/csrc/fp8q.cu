@@ -11,9 +11,13 @@
 //
 // Every kernel here streams HBM; none is a contraction, so there are no
 // tensor-core instructions.  Design points:
-//   * quantize+amax reads each bf16 once (16-byte vector loads), writes each
-//     FP8 byte once, and reduces |x| with packed NaN-propagating bf16x2 max,
-//     then one warp redux and one atomic per CTA and tensor.
+//   * quantize+amax reads each bf16 once (32-byte vector loads), writes each
+//     FP8 byte once (16-byte stores), and reduces |x| with packed
+//     NaN-propagating bf16x2 max, then one warp redux and one atomic per CTA
+//     and tensor.  It runs as a persistent grid-stride loop (read-heavy).
+//   * the write-heavy streams -- dequantize and the fused quantize ->
+//     dequantize -- launch one CTA per tile instead, which keeps their writes
+//     more sequential.
 //   * the division x / scale is exact IEEE binary32 (round to nearest even)
 //     without a per-element divide: with r = RN(1/s) computed once per CTA,
 //     y0 = RN(x*r), e = fma(y0, s, -x), y = fma(-e, r, y0) is the correctly
@@ -32,7 +36,11 @@
 //   * the scale update gives each CTA four slot columns and every history row
 //     of them, reads all rows into registers, synchronises, then writes the
 //     rows shifted by one; no other CTA touches those columns, so the in-place
-//     roll needs no grid-wide synchronisation.
+//     roll needs no grid-wide synchronisation.  The ring-buffer form keeps the
+//     same layout, overwrites only each slot's oldest row and advances a
+//     per-slot head that only the owning CTA touches.
+//   * no kernel waits on another CTA, a flag or an mbarrier: the only waits are
+//     __syncthreads in uniform control flow.
 
 #include "fp8q.h"
 
