@@ -57,6 +57,12 @@ def lib():
         L.orc_dequantize.restype = None
         L.orc_qdq_amax.argtypes = [vp, i64, ctypes.c_int, f32, vp, vp]
         L.orc_qdq_amax.restype = None
+        L.orc_exp_f32.argtypes = [f32]
+        L.orc_exp_f32.restype = f32
+        L.orc_gelu_f32.argtypes = [f32]
+        L.orc_gelu_f32.restype = f32
+        L.orc_gelu_quantize_amax.argtypes = [vp, i64, ctypes.c_int, f32, vp, vp, vp]
+        L.orc_gelu_quantize_amax.restype = None
         L.orc_amax_scale_update.argtypes = [vp, i32, i32, vp, vp, vp, vp, ctypes.c_int,
                                             ctypes.c_int, i32]
         L.orc_amax_scale_update.restype = None
@@ -173,3 +179,21 @@ def amax_scale_update_ring(hist, head, amax_new, scale, scale_inv, fmt=E4M3FN, a
     sf = None if slot_format is None else np.ascontiguousarray(slot_format, np.uint8)
     lib().orc_amax_scale_update_ring(_ptr(hist), _ptr(head), H, S, _ptr(amax_new), _ptr(scale),
                                      _ptr(scale_inv), _ptr(sf), fmt, algo, margin)
+
+
+def exp_f32(v):
+    return np.float32(lib().orc_exp_f32(float(np.float32(v))))
+
+
+def gelu_f32(x):
+    return np.float32(lib().orc_gelu_f32(float(np.float32(x))))
+
+
+def gelu_quantize_amax(h_bf16, fmt, scale, amax=0.0):
+    """Return (q codes, bf16 bits of y = GELU(h), amax float32)."""
+    h = _c_u16(h_bf16).reshape(-1)
+    q = np.empty(h.shape, np.uint8)
+    y = np.empty(h.shape, np.uint16)
+    a = np.array([amax], np.float32)
+    lib().orc_gelu_quantize_amax(_ptr(h), h.size, fmt, float(np.float32(scale)), _ptr(q), _ptr(y), _ptr(a))
+    return q, y, np.float32(a[0])

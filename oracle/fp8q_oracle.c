@@ -225,6 +225,72 @@ void orc_qdq_amax(const uint16_t* x_bf16, int64_t n, int fmt, float scale, uint1
 }
 
 /* ----------------------------------------------------------------------- */
+/* GELU producer fused with the quantization ([XLA-7432], test.py: the MLP  */
+/* applies nn.gelu, the tanh form, to the first dense layer's output and    */
+/* feeds it to an FP8 dense layer; the issue asks for the quantization to   */
+/* be fused with what produces its input).                                  */
+/*                                                                          */
+/* GELU(tanh) = 0.5 x (1 + tanh(u)) = x / (1 + exp(-2u)),                   */
+/* u = sqrt(2/pi) (x + 0.044715 x^3).  So that a GPU and a CPU agree bit for */
+/* bit, exp is evaluated by additive range reduction (W. J. Cody and W.     */
+/* Waite, "Software Manual for the Elementary Functions", 1980) and a        */
+/* degree-6 Taylor polynomial of e^r, each step one correctly rounded       */
+/* binary32 operation (fmaf where written).  The constants are the binary32 */
+/* roundings of ln 2 split in two (the high part to 16 significant bits, so */
+/* k * LN2_HI is exact for |k| < 2^8), of 1 / ln 2, of -2 sqrt(2/pi), of     */
+/* 0.044715 and of 1/k!.                                                     */
+
+static const float EXP_LN2_HI = 0x1.62e4p-1f;
+static const float EXP_LN2_LO = 0x1.7f7d1cp-20f;
+static const float EXP_INV_LN2 = 0x1.715476p+0f;
+static const float GELU_K = -0x1.988454p+0f;  /* -2 sqrt(2/pi) */
+static const float GELU_C = 0x1.6e4e26p-5f;   /* 0.044715 */
+
+float orc_exp_f32(float v) {
+    if (isnan(v)) return v;
+    if (v > 89.0f) v = 89.0f;      /* e^89 overflows binary32: the result is +inf */
+    if (v < -104.0f) v = -104.0f;  /* e^-104 is below half the least subnormal: +0 */
+    float k = rintf(v * EXP_INV_LN2);              /* nearest integer, ties to even */
+    float r = fmaf(-k, EXP_LN2_HI, v);             /* v - k ln 2, in two parts */
+    r = fmaf(-k, EXP_LN2_LO, r);
+    float p = 0x1.6c16c2p-10f;                     /* 1/720 */
+    p = fmaf(p, r, 0x1.111112p-7f);                /* 1/120 */
+    p = fmaf(p, r, 0x1.555556p-5f);                /* 1/24 */
+    p = fmaf(p, r, 0x1.555556p-3f);                /* 1/6 */
+    p = fmaf(p, r, 0.5f);
+    p = fmaf(p, r, 1.0f);
+    p = fmaf(p, r, 1.0f);
+    int ki = (int)k;
+    int k1 = ki / 2, k2 = ki - k1;                 /* 2^k in two normal factors */
+    return (p * ldexpf(1.0f, k1)) * ldexpf(1.0f, k2);  /* exact, then one rounding */
+}
+
+float orc_gelu_f32(float x) {
+    if (isnan(x)) return x;
+    if (x == -INFINITY) return -0.0f;              /* the limit; x * 0 would be NaN */
+    float x3 = (x * x) * x;
+    float s = fmaf(GELU_C, x3, x);                 /* x + 0.044715 x^3 */
+    float v = GELU_K * s;                          /* -2u */
+    float d = 1.0f + orc_exp_f32(v);
+    return x * (1.0f / d);
+}
+
+/* y = bf16(GELU(h)); q = FP8(y / scale); amax = max(amax, |y|).  The codes
+ * and the amax are those fp8q's quantize gives for the bf16 tensor y. */
+void orc_gelu_quantize_amax(const uint16_t* h_bf16, int64_t n, int fmt, float scale, uint8_t* q,
+                            uint16_t* y_bf16, float* amax_inout) {
+    float m = *amax_inout;
+    for (int64_t i = 0; i < n; ++i) {
+        uint16_t yb = orc_f32_to_bf16(orc_gelu_f32(orc_bf16_to_f32(h_bf16[i])));
+        float y = orc_bf16_to_f32(yb);
+        if (y_bf16) y_bf16[i] = yb;
+        q[i] = orc_fp8_encode(y / scale, fmt);
+        m = amax_combine(m, fabsf(y));
+    }
+    if (n > 0) *amax_inout = m;
+}
+
+/* ----------------------------------------------------------------------- */
 /* amax_and_scale_update ([TE-593]; scale formula from [XLA-FP8] "JAX":     */
 /* scale = max|A| / E4M3_MAX, times 2^margin).                              */
 

@@ -534,3 +534,85 @@ def test_ring_invalid_head_leaves_slot_alone(orc):
     assert list(head) == [-1, 4, 2]
     assert np.all(hist[:, :2] == 2.0) and sc[0] == 5.0 and sc[1] == 5.0
     assert hist[2, 2] == 448.0 and sc[2] == 1.0
+
+
+# --------------------------------------------------------------------------- GELU producer fused with Q
+
+def _ulp32(x):
+    x = np.abs(np.asarray(x, np.float32))
+    return (np.nextafter(x, np.float32(np.inf)) - x).astype(np.float64)
+
+
+def test_exp_within_a_few_ulp_of_the_true_value(orc):
+    rng = np.random.default_rng(31)
+    vs = np.concatenate([np.linspace(-87, 88, 4001), rng.uniform(-87, 88, 4000),
+                         rng.uniform(-1, 1, 2000)]).astype(np.float32)
+    got = np.array([orc.exp_f32(v) for v in vs], np.float64)
+    ref = np.exp(vs.astype(np.float64))
+    assert np.all(np.abs(got - ref) <= 3 * _ulp32(ref))
+    assert orc.exp_f32(0.0) == 1.0
+    assert np.isinf(orc.exp_f32(89.5)) and np.isinf(orc.exp_f32(np.inf))
+    assert orc.exp_f32(-104.5) == 0.0 and orc.exp_f32(-np.inf) == 0.0
+    assert np.isnan(orc.exp_f32(np.nan))
+    # subnormal results are correctly rounded from the binary32 polynomial value
+    assert 0 < orc.exp_f32(-100.0) < 2.0 ** -126
+
+
+def _gelu_tanh_f64(x):
+    """The tanh GELU in float64, written as x / (1 + exp(-2u)): the same function as
+    0.5 x (1 + tanh(u)), without that form's cancellation for negative x."""
+    x = np.asarray(x, np.float64)
+    u = math.sqrt(2.0 / math.pi) * (x + 0.044715 * x ** 3)
+    return x / (1.0 + np.exp(-2.0 * u))
+
+
+def test_gelu_close_to_the_float64_tanh_form(orc):
+    rng = np.random.default_rng(32)
+    xs = np.concatenate([np.linspace(-9, 9, 6001), rng.normal(0, 3, 6000),
+                         rng.uniform(-0.01, 0.01, 500)]).astype(np.float32)
+    got = np.array([orc.gelu_f32(x) for x in xs], np.float64)
+    ref = _gelu_tanh_f64(xs)
+    tiny = np.abs(ref) < 2.0 ** -120
+    rel = np.abs(got - ref)[~tiny] / np.abs(ref[~tiny])
+    assert rel.max() < 2.0 ** -16          # far below bf16's resolution (2^-8)
+    assert np.all(np.abs(got[tiny] - ref[tiny]) < 2.0 ** -110)
+
+
+def test_gelu_bf16_matches_torch_tanh_gelu(orc):
+    """On bf16 inputs, bf16(GELU) equals torch's tanh GELU (in float64) rounded to bf16,
+    except within one bf16 step where the value sits on a rounding tie."""
+    # |x| < 5 keeps torch's 0.5 x (1 + tanh(u)) free of cancellation in float64
+    x = ALL_BF16_F32[np.isfinite(ALL_BF16_F32) & (np.abs(ALL_BF16_F32) < 5)]
+    xb = (x.view(np.uint32) >> 16).astype(np.uint16)
+    _, y, _ = orc.gelu_quantize_amax(xb, E4M3FN, 1.0)
+    ref = torch.nn.functional.gelu(torch.from_numpy(x.astype(np.float64)), approximate="tanh")
+    refb = ref.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    same = y == refb
+    assert same.mean() > 0.995  # ties: |error| < 2^-16 relative against bf16 steps of 2^-8
+    yf = (y.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    rf = (refb.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    step = np.maximum(np.abs(rf), 2.0 ** -126) * 2.0 ** -7
+    assert np.all(np.abs(yf - rf)[~same] <= step[~same])
+
+
+def test_gelu_special_values(orc):
+    assert orc.gelu_f32(0.0) == 0.0
+    assert orc.gelu_f32(np.inf) == np.inf
+    g = orc.gelu_f32(-np.inf)
+    assert g == 0.0 and math.copysign(1, g) < 0
+    g = orc.gelu_f32(-1e30)
+    assert g == 0.0 and math.copysign(1, g) < 0
+    assert orc.gelu_f32(1e30) == np.float32(1e30)
+    assert np.isnan(orc.gelu_f32(np.nan))
+
+
+@pytest.mark.parametrize("fmt", [E4M3FN, E5M2])
+def test_fused_gelu_quantize_is_quantize_of_the_bf16_gelu(orc, fmt):
+    rng = np.random.default_rng(33)
+    h = (rng.normal(0, 2, 5000).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    for s in (1.0, 0.0123, 2.0 ** -70):
+        q, y, a = orc.gelu_quantize_amax(h, fmt, s)
+        q2, a2 = orc.quantize_amax(y, fmt, s)
+        assert np.array_equal(q, q2) and a == a2
+        yf = (y.astype(np.uint32) << 16).view(np.float32)
+        assert a == np.max(np.abs(yf))
