@@ -413,6 +413,46 @@ def measure_next_rows(args, step, stream, dev, peak):
                         "us": round(us, 3), "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
                         "bytes_per_launch": nbytes}}
 
+    # GELU producer fused with the quantization, against the unfused pair
+    # (torch's tanh GELU writing bf16, then fp8q_quantize_amax reading it back).
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    h = torch.randn(N_ACT, generator=g, device=dev).to(torch.bfloat16)
+    q = torch.empty(N_ACT, dtype=torch.uint8, device=dev)
+
+    def timed_loop(fn):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+            s0 = torch.cuda.Event(enable_timing=True)
+            s1 = torch.cuda.Event(enable_timing=True)
+            s0.record(stream)
+            for _ in range(n_iter):
+                fn()
+            s1.record(stream)
+        torch.cuda.synchronize(dev)
+        return s0.elapsed_time(s1) * 1e3 / n_iter
+
+    sc0 = step.scale[0:1]
+    us_q = timed_loop(lambda: f.fp8q_gelu_quantize_amax(h, None, q, f.E4M3FN, sc0, am, stream.cuda_stream))
+    us_yq = timed_loop(lambda: f.fp8q_gelu_quantize_amax(h, y, q, f.E4M3FN, sc0, am, stream.cuda_stream))
+
+    def unfused():
+        y.copy_(torch.nn.functional.gelu(h, approximate="tanh"))
+        f.fp8q_quantize_amax(y, q, f.E4M3FN, sc0, am, stream.cuda_stream)
+    us_unfused = timed_loop(unfused)
+    out["gelu_quantize_amax"] = {
+        "workload": "pre-activation bf16 8192x16384 N(0,1) -> GELU(tanh) -> e4m3fn + amax",
+        "launches": n_iter,
+        "codes_only": {"us": round(us_q, 3), "GB/s": round(3 * N_ACT / (us_q * 1e-6) / 1e9, 1),
+                       "frac_of_peak": round(3 * N_ACT / (us_q * 1e-6) / 1e9 / peak, 4),
+                       "bytes_per_launch": 3 * N_ACT},
+        "with_bf16_y": {"us": round(us_yq, 3), "GB/s": round(5 * N_ACT / (us_yq * 1e-6) / 1e9, 1),
+                        "frac_of_peak": round(5 * N_ACT / (us_yq * 1e-6) / 1e9 / peak, 4),
+                        "bytes_per_launch": 5 * N_ACT},
+        "unfused_torch_gelu_then_quantize_us": round(us_unfused, 3)}
+    del h, q
+
     # Ring-buffer update against the rolled one, each timed right after a
     # dequantize of the 8192x16384 gradient (where the update sits in the step).
     ring_hist = step.hist.clone()

@@ -1,7 +1,7 @@
 /*
  * fp8q.h -- C ABI of libfp8q: FP8 delayed-scaling quantization on one GPU.
  *
- * Six operations, each one kernel launch on the caller's stream:
+ * Seven operations, each one kernel launch on the caller's stream:
  *   fp8q_quantize_amax        bf16 -> FP8 bytes, fused with amax = max|x|
  *   fp8q_multi_quantize_amax  the same over a ragged list of tensors
  *   fp8q_dequantize           FP8 bytes -> bf16
@@ -9,6 +9,7 @@
  *                             scale_inv, for many FP8 metadata slots at once
  *   fp8q_qdq_amax             quantize then dequantize (bf16 -> bf16) + amax
  *   fp8q_amax_scale_update_ring  the update over a ring buffer (no roll)
+ *   fp8q_gelu_quantize_amax   GELU producer fused with quantize + amax
  *
  * Sources (web pages, by title and section):
  *   "User Guide on Native XLA-FP8" (NVIDIA JAX-Toolbox): opening section
@@ -199,6 +200,27 @@ fp8q_status fp8q_amax_scale_update_ring(float* amax_history, int32_t* head, int3
                                         float* scale_inv, const uint8_t* slot_format,
                                         fp8q_format fmt, fp8q_amax_algo algo, int32_t margin,
                                         void* stream);
+
+/*
+ * GELU producer fused with quantize + amax: the first MLP layer's output goes
+ * through GELU and straight into FP8 for the next FP8 dense layer ("Fusion of
+ * Fp8 quantization and amax reduction kernels": the reproducer's
+ * dense -> gelu -> dense pattern, with quantization fused into what produces
+ * its input), in one pass:
+ *   y[i]  = bf16_rne(GELU(h[i]))        tanh form x / (1 + exp(-2u)),
+ *                                        u = sqrt(2/pi)(x + 0.044715 x^3)
+ *   q[i]  = FP8(y[i] / *scale)           exactly fp8q_quantize_amax of y
+ *   *amax = max(*amax, max_i |y[i]|)
+ * GELU is evaluated by a fixed sequence of correctly rounded binary32
+ * operations (exp by additive range reduction and a degree-6 Taylor
+ * polynomial), so it is reproducible bit for bit; it stays within 2^-16
+ * relative of the exact tanh-form GELU.
+ * h_bf16: n bf16 (device).  y_bf16: n bf16 (device, written) or NULL when only
+ * the FP8 codes are wanted.  q, scale, amax: as for fp8q_quantize_amax.
+ * Errors: as for fp8q_quantize_amax, plus an odd y_bf16.
+ */
+fp8q_status fp8q_gelu_quantize_amax(const void* h_bf16, void* y_bf16, uint8_t* q, int64_t n,
+                                    fp8q_format fmt, const float* scale, float* amax, void* stream);
 
 /* Static, human-readable name of a status. */
 const char* fp8q_status_string(fp8q_status status);

@@ -63,6 +63,8 @@ def lib():
         L.orc_gelu_f32.restype = f32
         L.orc_gelu_quantize_amax.argtypes = [vp, i64, ctypes.c_int, f32, vp, vp, vp]
         L.orc_gelu_quantize_amax.restype = None
+        L.orc_gelu_amax.argtypes = [vp, i64]
+        L.orc_gelu_amax.restype = f32
         L.orc_amax_scale_update.argtypes = [vp, i32, i32, vp, vp, vp, vp, ctypes.c_int,
                                             ctypes.c_int, i32]
         L.orc_amax_scale_update.restype = None
@@ -197,3 +199,9 @@ def gelu_quantize_amax(h_bf16, fmt, scale, amax=0.0):
     a = np.array([amax], np.float32)
     lib().orc_gelu_quantize_amax(_ptr(h), h.size, fmt, float(np.float32(scale)), _ptr(q), _ptr(y), _ptr(a))
     return q, y, np.float32(a[0])
+
+
+def gelu_amax(h_bf16):
+    """max|bf16(GELU(h))| over the whole tensor."""
+    h = _c_u16(h_bf16).reshape(-1)
+    return np.float32(lib().orc_gelu_amax(_ptr(h), h.size))

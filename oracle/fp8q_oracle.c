@@ -235,23 +235,31 @@ void orc_qdq_amax(const uint16_t* x_bf16, int64_t n, int fmt, float scale, uint1
 /* bit, exp is evaluated by additive range reduction (W. J. Cody and W.     */
 /* Waite, "Software Manual for the Elementary Functions", 1980) and a        */
 /* degree-6 Taylor polynomial of e^r, each step one correctly rounded       */
-/* binary32 operation (fmaf where written).  The constants are the binary32 */
-/* roundings of ln 2 split in two (the high part to 16 significant bits, so */
-/* k * LN2_HI is exact for |k| < 2^8), of 1 / ln 2, of -2 sqrt(2/pi), of     */
-/* 0.044715 and of 1/k!.                                                     */
+/* binary32 operation (fmaf where written), in a fixed order.  The constants */
+/* are the binary32 roundings of ln 2 split in two (the high part to 16      */
+/* significant bits, so k * LN2_HI is exact for |k| < 2^8), of 1 / ln 2, of   */
+/* -2 sqrt(2/pi), of 0.044715 and of 1/k!.                                   */
 
 static const float EXP_LN2_HI = 0x1.62e4p-1f;
 static const float EXP_LN2_LO = 0x1.7f7d1cp-20f;
 static const float EXP_INV_LN2 = 0x1.715476p+0f;
+static const float EXP_ROUNDER = 0x1.8p23f;   /* 1.5 * 2^23: adding it rounds to an integer */
 static const float GELU_K = -0x1.988454p+0f;  /* -2 sqrt(2/pi) */
 static const float GELU_C = 0x1.6e4e26p-5f;   /* 0.044715 */
 
+/* e^v for the GELU below.  v is clamped to [-20, 89]: under -20, 1 + e^v
+ * rounds to exactly 1 in binary32 whatever e^v is; over 88.73, e^v
+ * overflows to +inf.  k = round(v / ln 2) comes from one fused multiply-add
+ * with 1.5 * 2^23 (the sum's last bit is then the integer), r = v - k ln 2 in
+ * two parts, e^r by a degree-6 Taylor polynomial (Horner, fused), and
+ * e^v = (e^r * 2^(k-1)) * 2: the first product is exact, the second rounds
+ * once (to +inf past the largest float). */
 float orc_exp_f32(float v) {
-    if (isnan(v)) return v;
-    if (v > 89.0f) v = 89.0f;      /* e^89 overflows binary32: the result is +inf */
-    if (v < -104.0f) v = -104.0f;  /* e^-104 is below half the least subnormal: +0 */
-    float k = rintf(v * EXP_INV_LN2);              /* nearest integer, ties to even */
-    float r = fmaf(-k, EXP_LN2_HI, v);             /* v - k ln 2, in two parts */
+    if (v > 89.0f) v = 89.0f;
+    if (!(v >= -20.0f)) v = -20.0f;                /* also NaN: GELU returns x * 1 = NaN */
+    float t = fmaf(v, EXP_INV_LN2, EXP_ROUNDER);   /* rounds v / ln 2 to the nearest integer */
+    float k = t - EXP_ROUNDER;                     /* exact */
+    float r = fmaf(-k, EXP_LN2_HI, v);
     r = fmaf(-k, EXP_LN2_LO, r);
     float p = 0x1.6c16c2p-10f;                     /* 1/720 */
     p = fmaf(p, r, 0x1.111112p-7f);                /* 1/120 */
@@ -260,18 +268,15 @@ float orc_exp_f32(float v) {
     p = fmaf(p, r, 0.5f);
     p = fmaf(p, r, 1.0f);
     p = fmaf(p, r, 1.0f);
-    int ki = (int)k;
-    int k1 = ki / 2, k2 = ki - k1;                 /* 2^k in two normal factors */
-    return (p * ldexpf(1.0f, k1)) * ldexpf(1.0f, k2);  /* exact, then one rounding */
+    int ki = (int)k;                               /* in [-29, 128] */
+    return (p * ldexpf(1.0f, ki - 1)) * 2.0f;
 }
 
 float orc_gelu_f32(float x) {
-    if (isnan(x)) return x;
     if (x == -INFINITY) return -0.0f;              /* the limit; x * 0 would be NaN */
-    float x3 = (x * x) * x;
-    float s = fmaf(GELU_C, x3, x);                 /* x + 0.044715 x^3 */
-    float v = GELU_K * s;                          /* -2u */
-    float d = 1.0f + orc_exp_f32(v);
+    float x2 = x * x;
+    float s = x * fmaf(GELU_C, x2, 1.0f);          /* x (1 + 0.044715 x^2) */
+    float d = 1.0f + orc_exp_f32(GELU_K * s);      /* 1 + exp(-2u) */
     return x * (1.0f / d);
 }
 
@@ -288,6 +293,16 @@ void orc_gelu_quantize_amax(const uint16_t* h_bf16, int64_t n, int fmt, float sc
         m = amax_combine(m, fabsf(y));
     }
     if (n > 0) *amax_inout = m;
+}
+
+/* max|bf16(GELU(h))| alone (the fused op's amax, without the FP8 encoding). */
+float orc_gelu_amax(const uint16_t* h_bf16, int64_t n) {
+    float m = 0.0f;
+    for (int64_t i = 0; i < n; ++i) {
+        float y = orc_bf16_to_f32(orc_f32_to_bf16(orc_gelu_f32(orc_bf16_to_f32(h_bf16[i]))));
+        m = amax_combine(m, fabsf(y));
+    }
+    return m;
 }
 
 /* ----------------------------------------------------------------------- */

@@ -42,6 +42,7 @@ float orc_exp_f32(float v);
 float orc_gelu_f32(float x);
 void orc_gelu_quantize_amax(const uint16_t* h_bf16, int64_t n, int fmt, float scale, uint8_t* q,
                             uint16_t* y_bf16, float* amax_inout);
+float orc_gelu_amax(const uint16_t* h_bf16, int64_t n);
 void orc_amax_scale_update(float* hist, int32_t H, int32_t S, const float* amax_new,
                            float* scale, float* scale_inv, const uint8_t* slot_format,
                            int fmt, int algo, int32_t margin);

@@ -479,6 +479,153 @@ __global__ void __launch_bounds__(kThreads) quantize_amax_kernel(const __grid_co
 }
 
 // ----------------------------------------------------------------------------
+// GELU producer fused with quantize + amax
+//
+// y = bf16(GELU(h)) with GELU(x) = x / (1 + exp(-2u)), u = sqrt(2/pi)(x +
+// 0.044715 x^3) -- the tanh form -- then exactly the quantize above applied to
+// y: FP8 codes of y / scale and amax = max|y|.  exp is evaluated by additive
+// range reduction (Cody and Waite, "Software Manual for the Elementary
+// Functions", 1980) and a degree-6 Taylor polynomial, every step one
+// correctly rounded binary32 operation written out in a fixed order (no
+// contraction, no approximate instruction), so the result is reproducible bit
+// for bit on any IEEE machine.  Constants: binary32 roundings of ln 2 split in
+// two (high part to 16 significant bits), 1/ln 2, -2 sqrt(2/pi), 0.044715, 1/k!.
+
+// e^v on [-20, 89]: under -20, 1 + e^v is exactly 1 in binary32 whatever e^v
+// is; above 88.73 the result overflows to +inf.  k = round(v / ln 2) comes
+// from one fused multiply-add with 1.5 * 2^23 (whose sum's last bit is then
+// the integer, read straight from the bits), r = v - k ln 2 in two parts, e^r
+// by a degree-6 Taylor polynomial, then (e^r * 2^(k-1)) * 2.
+__device__ __forceinline__ float exp_rr(float v) {
+    v = fminf(fmaxf(v, -20.0f), 89.0f);  // fmaxf first: a NaN becomes -20
+    const float t = __fmaf_rn(v, 0x1.715476p+0f, 0x1.8p23f);
+    const float k = __fsub_rn(t, 0x1.8p23f);
+    float r = __fmaf_rn(-k, 0x1.62e4p-1f, v);
+    r = __fmaf_rn(-k, 0x1.7f7d1cp-20f, r);
+    float p = 0x1.6c16c2p-10f;
+    p = __fmaf_rn(p, r, 0x1.111112p-7f);
+    p = __fmaf_rn(p, r, 0x1.555556p-5f);
+    p = __fmaf_rn(p, r, 0x1.555556p-3f);
+    p = __fmaf_rn(p, r, 0.5f);
+    p = __fmaf_rn(p, r, 1.0f);
+    p = __fmaf_rn(p, r, 1.0f);
+    const int ki = __float_as_int(t) - __float_as_int(0x1.8p23f);  // k, in [-29, 128]
+    return __fmul_rn(__fmul_rn(p, __int_as_float((ki + 126) << 23)), 2.0f);
+}
+
+__device__ __forceinline__ float gelu_rr(float x) {
+    const float x2 = __fmul_rn(x, x);
+    const float sx = __fmul_rn(x, __fmaf_rn(0x1.6e4e26p-5f, x2, 1.0f));  // x (1 + 0.044715 x^2)
+    const float d = __fadd_rn(1.0f, exp_rr(__fmul_rn(-0x1.988454p+0f, sx)));
+    const float g = __fmul_rn(x, __frcp_rn(d));
+    return x == -INFINITY ? -0.0f : g;  // the limit (x * 0 would be NaN); NaN stays NaN
+}
+
+// Two bf16 (one word) -> two bf16 of GELU (one word).
+__device__ __forceinline__ uint32_t gelu_pair(uint32_t w) {
+    return cvt_bf16x2(gelu_rr(__uint_as_float(w << 16)), gelu_rr(__uint_as_float(w & 0xFFFF0000u)));
+}
+
+struct GeluGeom {
+    static constexpr int kVecElems = 16;  // 16 bf16 in (32 bytes) -> 16 codes (+ 16 bf16 of y)
+    static constexpr int kVecPerThread = 2;
+    static constexpr int kWideAlign = 32;
+    static constexpr int kNarrowBytes = 1;
+    static constexpr int kNarrowAlign = 16;
+};
+
+struct GeluArgs {
+    const uint16_t* h;
+    uint16_t* y;  // may be null
+    uint8_t* q;
+    const float* scale;
+    float* amax;
+    int64_t n, head, nvec, tiles;
+    int mode;
+};
+
+template <int FMT, bool FAST, bool WRITE_Y>
+__device__ __forceinline__ void gelu_vec_store(const GeluArgs& a, const QScale& c, int64_t v, const uint4& wa,
+                                               const uint4& wb, uint32_t& m2) {
+    constexpr int E = GeluGeom::kVecElems;
+    uint4 ya, yb;
+    ya.x = gelu_pair(wa.x); ya.y = gelu_pair(wa.y); ya.z = gelu_pair(wa.z); ya.w = gelu_pair(wa.w);
+    yb.x = gelu_pair(wb.x); yb.y = gelu_pair(wb.y); yb.z = gelu_pair(wb.z); yb.w = gelu_pair(wb.w);
+    if (WRITE_Y) {
+        uint16_t* yp = a.y + a.head + v * E;
+        st_v4(yp, ya);
+        st_v4(yp + 8, yb);
+    }
+    m2 = bf16x2_absmax(m2, bf16x2_absmax(bf16x2_absmax(bf16x2_absmax(ya.x, ya.y), bf16x2_absmax(ya.z, ya.w)),
+                                         bf16x2_absmax(bf16x2_absmax(yb.x, yb.y), bf16x2_absmax(yb.z, yb.w))));
+    uint4 o;
+    o.x = quant_quad<FMT, FAST>(ya.x, ya.y, c);
+    o.y = quant_quad<FMT, FAST>(ya.z, ya.w, c);
+    o.z = quant_quad<FMT, FAST>(yb.x, yb.y, c);
+    o.w = quant_quad<FMT, FAST>(yb.z, yb.w, c);
+    st_v4(a.q + a.head + v * E, o);
+}
+
+template <int FMT, bool FAST, bool WRITE_Y>
+__device__ __forceinline__ void gelu_scalar(const GeluArgs& a, const QScale& c, int64_t i, uint32_t& ms) {
+    const uint32_t yw = gelu_pair(a.h[i]) & 0xFFFFu;
+    if (WRITE_Y) a.y[i] = (uint16_t)yw;
+    ms = max(ms, abs_bits_lo(yw));
+    a.q[i] = (uint8_t)(quant_pair<FMT, FAST>(yw, c) & 0xFFu);
+}
+
+template <int FMT, bool FAST, bool WRITE_Y>
+__device__ __forceinline__ void gelu_tile(const GeluArgs& a, const QScale& c, int64_t tile, const uint4* wa,
+                                          const uint4* wb, uint32_t& m2, uint32_t& ms) {
+    constexpr int E = GeluGeom::kVecElems, U = GeluGeom::kVecPerThread;
+    if (a.mode == kModeVec) {
+        const int64_t v0 = tile * Tile<GeluGeom>::kVecs + threadIdx.x;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t v = v0 + (int64_t)u * kThreads;
+            if (v < a.nvec) gelu_vec_store<FMT, FAST, WRITE_Y>(a, c, v, wa[u], wb[u], m2);
+        }
+        if (tile == 0) {
+            const int64_t tail0 = a.head + a.nvec * E;
+            const int64_t nscalar = a.head + (a.n - tail0);
+            for (int64_t j = threadIdx.x; j < nscalar; j += kThreads)
+                gelu_scalar<FMT, FAST, WRITE_Y>(a, c, j < a.head ? j : tail0 + (j - a.head), ms);
+        }
+    } else {
+        const int64_t base = tile * Tile<GeluGeom>::kElems;
+        const int64_t end = min(base + (int64_t)Tile<GeluGeom>::kElems, a.n);
+        for (int64_t i = base + threadIdx.x; i < end; i += kThreads) gelu_scalar<FMT, FAST, WRITE_Y>(a, c, i, ms);
+    }
+}
+
+template <int FMT, bool WRITE_Y>
+__global__ void __launch_bounds__(kThreads) gelu_quantize_amax_kernel(const GeluArgs a) {
+    __shared__ uint32_t red[kThreads / 32];
+    constexpr int E = GeluGeom::kVecElems, U = GeluGeom::kVecPerThread;
+    uint32_t m2 = 0, ms = 0;
+    QScale c;
+    bool have_scale = false;
+    for (int64_t tile = blockIdx.x; tile < a.tiles; tile += gridDim.x) {
+        uint4 wa[U], wb[U];
+        if (a.mode == kModeVec) {  // loads first: nothing here waits on the scale
+            const int64_t v0 = tile * Tile<GeluGeom>::kVecs + threadIdx.x;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t v = v0 + (int64_t)u * kThreads;
+                if (v < a.nvec) ld_stream_v8(a.h + a.head + v * E, wa[u], wb[u]);
+            }
+        }
+        if (!have_scale) {
+            c = make_qscale(a.scale);
+            have_scale = true;
+        }
+        if (c.fast) gelu_tile<FMT, true, WRITE_Y>(a, c, tile, wa, wb, m2, ms);
+        else        gelu_tile<FMT, false, WRITE_Y>(a, c, tile, wa, wb, m2, ms);
+    }
+    flush_amax(m2, ms, a.amax, red);
+}
+
+// ----------------------------------------------------------------------------
 // Dequantize
 
 
@@ -882,6 +1029,44 @@ fp8q_status fp8q_multi_quantize_amax(const fp8q_tensor* list, int32_t count, fp8
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return fmt == FP8Q_E4M3FN ? dispatch_quantize<FP8Q_E4M3FN>(list, count, s)
                               : dispatch_quantize<FP8Q_E5M2>(list, count, s);
+}
+
+fp8q_status fp8q_gelu_quantize_amax(const void* h_bf16, void* y_bf16, uint8_t* q, int64_t n,
+                                    fp8q_format fmt, const float* scale, float* amax, void* stream) {
+    if (!valid_fmt(fmt)) return FP8Q_ERR_INVALID_ARG;
+    const fp8q_tensor t = {h_bf16, q, n, scale, amax};
+    fp8q_status st = check_tensor(t);
+    if (st != FP8Q_OK || n == 0) return st;
+    if ((uintptr_t)y_bf16 & 1u) return FP8Q_ERR_INVALID_ARG;
+    Split sp = split_tensor<GeluGeom>((uintptr_t)h_bf16, (uintptr_t)q, n);
+    // the bf16 output rides the vector path only if it is aligned like the input
+    if (y_bf16 && sp.mode == kModeVec && (((uintptr_t)y_bf16 - (uintptr_t)h_bf16) & 31u) != 0) {
+        sp.mode = kModeScalar;
+        sp.head = n;
+        sp.nvec = 0;
+        sp.tiles = (n + Tile<GeluGeom>::kElems - 1) / Tile<GeluGeom>::kElems;
+    }
+    GeluArgs a;
+    a.h = static_cast<const uint16_t*>(h_bf16);
+    a.y = static_cast<uint16_t*>(y_bf16);
+    a.q = q;
+    a.scale = scale;
+    a.amax = amax;
+    a.n = n;
+    a.head = sp.head;
+    a.nvec = sp.nvec;
+    a.tiles = sp.tiles;
+    a.mode = sp.mode;
+    const int grid = (int)(sp.tiles < 0x7FFFFFFF ? sp.tiles : 0x7FFFFFFF);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (fmt == FP8Q_E4M3FN) {
+        if (y_bf16) gelu_quantize_amax_kernel<FP8Q_E4M3FN, true><<<grid, kThreads, 0, s>>>(a);
+        else        gelu_quantize_amax_kernel<FP8Q_E4M3FN, false><<<grid, kThreads, 0, s>>>(a);
+    } else {
+        if (y_bf16) gelu_quantize_amax_kernel<FP8Q_E5M2, true><<<grid, kThreads, 0, s>>>(a);
+        else        gelu_quantize_amax_kernel<FP8Q_E5M2, false><<<grid, kThreads, 0, s>>>(a);
+    }
+    return after_launch("gelu_quantize_amax_kernel");
 }
 
 fp8q_status fp8q_qdq_amax(const void* x_bf16, void* y_bf16, int64_t n, fp8q_format fmt,

@@ -28,7 +28,7 @@ def test_header_declares_the_four_operations():
     names = declared_functions()
     for f in ("fp8q_quantize_amax", "fp8q_multi_quantize_amax", "fp8q_dequantize",
               "fp8q_amax_scale_update", "fp8q_qdq_amax", "fp8q_amax_scale_update_ring",
-              "fp8q_status_string", "fp8q_last_cuda_error"):
+              "fp8q_gelu_quantize_amax", "fp8q_status_string", "fp8q_last_cuda_error"):
         assert f in names
 
 
@@ -81,6 +81,17 @@ def test_multi_argument_errors(L):
     arr[3].n = -2
     assert m(ctypes.cast(arr, ctypes.c_void_p), 5, 0, None) == INVALID
     assert m(ctypes.cast(arr, ctypes.c_void_p), 5, 9, None) == INVALID
+
+
+def test_gelu_quantize_argument_errors(L):
+    f = L.fp8q_gelu_quantize_amax
+    assert f(None, None, None, 0, 0, None, None, None) == OK
+    assert f(P, None, P, -1, 0, P, P, None) == INVALID
+    assert f(P, None, P, 4, 2, P, P, None) == INVALID
+    for h, q, sc, am in ((None, P, P, P), (P, None, P, P), (P, P, None, P), (P, P, P, None)):
+        assert f(h, None, q, 4, 0, sc, am, None) == INVALID
+    assert f(ODD, None, P, 4, 0, P, P, None) == INVALID
+    assert f(P, ODD, P, 4, 0, P, P, None) == INVALID
 
 
 def test_qdq_argument_errors(L):

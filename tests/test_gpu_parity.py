@@ -718,3 +718,74 @@ def test_ring_matches_roll_on_the_gpu(dev):
     assert_f32_equal(logical, roll.cpu().numpy(), "ring vs roll window")
     assert_f32_equal(sc_b.cpu().numpy(), sc_a.cpu().numpy(), "ring vs roll scale")
     assert_f32_equal(si_b.cpu().numpy(), si_a.cpu().numpy(), "ring vs roll scale_inv")
+
+
+# --------------------------------------------------------------------------- GELU producer fused with Q
+
+def run_gelu(h, fmt, scale, dev, want_y=True):
+    n = h.numel()
+    y = torch.empty(n, dtype=torch.bfloat16, device=dev) if want_y else None
+    q = torch.empty(n, dtype=torch.uint8, device=dev)
+    am = f32(0.0, dev)
+    fp8q.fp8q_gelu_quantize_amax(h.reshape(-1), y, q, fmt, f32(scale, dev), am)
+    torch.cuda.synchronize()
+    return y, q, am
+
+
+@pytest.mark.parametrize("fmt", [E4M3FN, E5M2])
+def test_gelu_quantize_every_bf16_pattern(dev, fmt):
+    h = W.all_bf16_patterns(dev)
+    hb = W.bf16_bits(h)
+    for k, s in enumerate(SCALES_ALL):
+        y, q, am = run_gelu(h, fmt, s, dev, want_y=(k % 2 == 0))
+        rq, ry, ra = oracle.gelu_quantize_amax(hb, fmt, np.float32(s))
+        assert_codes_equal(q.cpu().numpy(), rq, fmt, f"scale {s!r}")
+        if y is not None:
+            assert_bf16_equal(W.bf16_bits(y), ry, f"gelu y, scale {s!r}")
+        assert math.isnan(float(am)) and math.isnan(float(ra))
+    # without NaN inputs the amax is exact
+    f = (hb.astype(np.uint32) << 16).view(np.float32)
+    fin = hb[~np.isnan(f)]
+    hx = torch.from_numpy(fin.view(np.int16).copy()).view(torch.bfloat16).to(dev)
+    _, q, am = run_gelu(hx, fmt, 0.37, dev)
+    rq, _, ra = oracle.gelu_quantize_amax(fin, fmt, np.float32(0.37))
+    assert_codes_equal(q.cpu().numpy(), rq, fmt, "no NaN")
+    assert_f32_equal([float(am)], [ra], "gelu amax")
+
+
+@pytest.mark.parametrize("n", [1, 15, 16, 17, 33, 4095, 8193, 70001])
+def test_gelu_quantize_sizes_offsets_canaries(dev, n):
+    g = torch.Generator(device=dev)
+    g.manual_seed(11 * n)
+    for k, (ho, qo) in enumerate(OFFSETS):
+        fmt = E4M3FN if k % 2 else E5M2
+        scale = [0.0123, 1.0, 2.0 ** 70, 3.3e-3][k % 4]
+        hbuf = (torch.randn(n + 16, generator=g, device=dev) * 3.0).to(torch.bfloat16)
+        h = hbuf[ho: ho + n]
+        qbuf, q = guarded(n, torch.uint8, dev, qo)
+        yo = (ho + 7 * k) % 16                   # often not aligned like h: scalar path
+        ybuf, y = guarded(n, torch.bfloat16, dev, yo, fill=0x5A5A)
+        am = f32(0.0, dev)
+        fp8q.fp8q_gelu_quantize_amax(h, y, q, fmt, f32(scale, dev), am)
+        torch.cuda.synchronize()
+        rq, ry, ra = oracle.gelu_quantize_amax(W.bf16_bits(h), fmt, np.float32(scale))
+        assert_codes_equal(q.cpu().numpy(), rq, fmt, f"n={n} off={ho},{qo},{yo}")
+        assert_bf16_equal(W.bf16_bits(y), ry, f"y n={n} off={ho},{yo}")
+        assert_f32_equal([float(am)], [ra], f"amax n={n}")
+        check_guards(qbuf, n, qo)
+        check_guards(ybuf, n, yo, fill=0x5A5A)
+
+
+def test_gelu_quantize_full_size_sampled(dev):
+    """Pre-activation 8192x16384 (N(0,1)), the FFN intermediate of the MLP workload."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(W.SEED_FFN)
+    h = torch.randn((8192, 16384), generator=g, device=dev).to(torch.bfloat16).reshape(-1)
+    scale = np.float32(0.0091)
+    y, q, am = run_gelu(h, E4M3FN, scale, dev)
+    hb = W.bf16_bits(h)
+    idx = sample_positions(hb.size)
+    rq, ry, _ = oracle.gelu_quantize_amax(hb[idx], E4M3FN, scale)
+    assert_codes_equal(q.cpu().numpy()[idx], rq, E4M3FN, "gelu q")
+    assert_bf16_equal(W.bf16_bits(y)[idx], ry, "gelu y")
+    assert_f32_equal([float(am)], [oracle.gelu_amax(hb)], "gelu amax over the whole tensor")

@@ -36,7 +36,7 @@ MUTATIONS = [
     ("ring overwrites the newest entry", "h = (h + 1) % H;", "h = h % H;"),
     ("ring window one row short", "for (int32_t r = 0; r < H; ++r) a = amax_combine(a, hist[(int64_t)r * S + s]);",
      "for (int32_t r = 0; r < H - 1; ++r) a = amax_combine(a, hist[(int64_t)r * S + s]);"),
-    ("GELU cubic term dropped", "float s = fmaf(GELU_C, x3, x);", "float s = x;"),
+    ("GELU cubic term dropped", "float s = x * fmaf(GELU_C, x2, 1.0f);", "float s = x;"),
     ("exp polynomial one term short", "p = fmaf(p, r, 0.5f);", "p = 0.5f;"),
     ("fused Q->DQ divides on the way back", "float p = (float)orc_fp8_decode(code, fmt) * scale;",
      "float p = (float)orc_fp8_decode(code, fmt) / scale;"),
