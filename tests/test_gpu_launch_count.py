@@ -1,0 +1,72 @@
+"""Each entry point is one kernel launch.
+
+Each call is captured into a CUDA graph and the graph's nodes are counted
+through the driver API: a call that launched two kernels, or a kernel plus
+a memset, would show up as more than one node.
+"""
+import ctypes
+
+import pytest
+import torch
+
+from quantize_amax_scaling_gb300 import fp8q
+from quantize_amax_scaling_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+CU_GRAPH_NODE_TYPE_KERNEL = 0
+
+
+def _graph_nodes(fn, stream):
+    """(kernel nodes, all nodes) of a graph that captured fn() on `stream`."""
+    drv = ctypes.CDLL("libcuda.so.1")
+    g = torch.cuda.CUDAGraph(keep_graph=True)
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    handle = ctypes.c_void_p(g.raw_cuda_graph())
+    n = ctypes.c_size_t(0)
+    assert drv.cuGraphGetNodes(handle, None, ctypes.byref(n)) == 0
+    nodes = (ctypes.c_void_p * max(1, n.value))()
+    assert drv.cuGraphGetNodes(handle, nodes, ctypes.byref(n)) == 0
+    kernels = 0
+    for i in range(n.value):
+        t = ctypes.c_int(-1)
+        assert drv.cuGraphNodeGetType(ctypes.c_void_p(nodes[i]), ctypes.byref(t)) == 0
+        kernels += t.value == CU_GRAPH_NODE_TYPE_KERNEL
+    del g
+    return kernels, n.value
+
+
+def test_every_entry_point_is_one_launch():
+    dev = torch.device("cuda:0")
+    s = torch.cuda.Stream()
+    x = W.mlp_activation(1, dev, (256, 4096)).reshape(-1)
+    q = torch.empty(x.numel(), dtype=torch.uint8, device=dev)
+    y = torch.empty(x.numel(), dtype=torch.bfloat16, device=dev)
+    sc = torch.full((4,), 0.05, device=dev)
+    am = torch.zeros(4, device=dev)
+    hist, new, scale, scale_inv, sf = W.scale_update_inputs(dev)
+    head = torch.full((new.numel(),), 1023, dtype=torch.int32, device=dev)
+    third = x.numel() // 3
+    ws, qs = [x[:third], x[third:]], [q[:third], q[third:]]
+    st = s.cuda_stream
+    calls = {
+        "quantize": lambda: fp8q.fp8q_quantize_amax(x, q, fp8q.E4M3FN, sc[0:1], am[0:1], st),
+        "multi (2 tensors)": lambda: fp8q.fp8q_multi_quantize_amax(ws, qs, fp8q.E4M3FN, [sc[1:2], sc[2:3]],
+                                                                   [am[1:2], am[2:3]], st),
+        "dequantize": lambda: fp8q.fp8q_dequantize(q, y, fp8q.E4M3FN, sc[0:1], st),
+        "update, 576 slots": lambda: fp8q.fp8q_amax_scale_update(hist, new, scale, scale_inv, fp8q.E4M3FN,
+                                                                 fp8q.ALGO_MAX, 0, sf, st),
+        "ring update, 576 slots": lambda: fp8q.fp8q_amax_scale_update_ring(hist, head, new, scale, scale_inv,
+                                                                           fp8q.E4M3FN, fp8q.ALGO_MAX, 0, sf,
+                                                                           st),
+        "fused Q->DQ": lambda: fp8q.fp8q_qdq_amax(x, y, fp8q.E4M3FN, sc[3:4], am[3:4], st),
+        "GELU + quantize": lambda: fp8q.fp8q_gelu_quantize_amax(x, y, q, fp8q.E4M3FN, sc[0:1], am[0:1], st),
+    }
+    with torch.cuda.stream(s):
+        for fn in calls.values():
+            fn()                               # first calls outside capture
+    s.synchronize()
+    for name, fn in calls.items():
+        kernels, nodes = _graph_nodes(fn, s)
+        assert (kernels, nodes) == (1, 1), (name, kernels, nodes)
