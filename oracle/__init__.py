@@ -63,6 +63,10 @@ def lib():
         L.orc_gelu_f32.restype = f32
         L.orc_gelu_quantize_amax.argtypes = [vp, i64, ctypes.c_int, f32, vp, vp, vp]
         L.orc_gelu_quantize_amax.restype = None
+        L.orc_layernorm_stats.argtypes = [vp, i32, f32, vp, vp]
+        L.orc_layernorm_stats.restype = None
+        L.orc_layernorm_quantize_amax.argtypes = [vp, i64, i32, vp, vp, f32, ctypes.c_int, f32, vp, vp, vp]
+        L.orc_layernorm_quantize_amax.restype = None
         L.orc_gelu_amax.argtypes = [vp, i64]
         L.orc_gelu_amax.restype = f32
         L.orc_amax_scale_update.argtypes = [vp, i32, i32, vp, vp, vp, vp, ctypes.c_int,
@@ -205,3 +209,26 @@ def gelu_amax(h_bf16):
     """max|bf16(GELU(h))| over the whole tensor."""
     h = _c_u16(h_bf16).reshape(-1)
     return np.float32(lib().orc_gelu_amax(_ptr(h), h.size))
+
+
+def layernorm_stats(row_bf16, eps=1e-6):
+    """(mean, rstd) of one bf16 row, in the fixed summation order."""
+    r = _c_u16(row_bf16).reshape(-1)
+    m = np.zeros(1, np.float32)
+    rs = np.zeros(1, np.float32)
+    lib().orc_layernorm_stats(_ptr(r), r.size, float(np.float32(eps)), _ptr(m), _ptr(rs))
+    return m[0], rs[0]
+
+
+def layernorm_quantize_amax(x_bf16, H, gamma, beta, fmt, scale, eps=1e-6, amax=0.0):
+    """Return (q codes, bf16 bits of y = LayerNorm(x), amax) for rows of H elements."""
+    x = _c_u16(x_bf16).reshape(-1)
+    assert x.size % H == 0
+    g = np.ascontiguousarray(gamma, np.float32)
+    b = np.ascontiguousarray(beta, np.float32)
+    q = np.empty(x.shape, np.uint8)
+    y = np.empty(x.shape, np.uint16)
+    a = np.array([amax], np.float32)
+    lib().orc_layernorm_quantize_amax(_ptr(x), x.size // H, H, _ptr(g), _ptr(b), float(np.float32(eps)), fmt,
+                                      float(np.float32(scale)), _ptr(q), _ptr(y), _ptr(a))
+    return q, y, np.float32(a[0])

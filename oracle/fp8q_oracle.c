@@ -306,6 +306,76 @@ float orc_gelu_amax(const uint16_t* h_bf16, int64_t n) {
 }
 
 /* ----------------------------------------------------------------------- */
+/* LayerNorm producer fused with the quantization ([XLA-7432], test.py: the */
+/* transformer block applies nn.LayerNorm() to its input and feeds the      */
+/* MLP's first FP8 dense layer; the issue asks for the quantization to be   */
+/* fused with what produces its input).                                     */
+/*                                                                          */
+/* Per row of H elements (H a multiple of 16), in binary32, Flax's defaults: */
+/*   mean = S / H, m2 = Q / H with S = sum x, Q = sum x^2,                   */
+/*   var = max(0, m2 - mean^2), rstd = 1 / sqrt(var + eps),                 */
+/*   y = (x - mean) * (rstd * gamma) + beta, then rounded to bf16.          */
+/* S and Q are summed in one fixed association so that any implementation  */
+/* can reproduce them bit for bit: the row is cut into vectors of 16        */
+/* elements and vector v belongs to lane v mod 256; each lane adds its      */
+/* elements in index order (s = s + x, q = fma(x, x, q)); within each group */
+/* of 32 lanes the partial sums are folded pairwise, lanes j and j + o for  */
+/* o = 16, 8, 4, 2, 1; the 8 group totals are then added left to right.     */
+
+static float row_sum_fixed_order(float* lane) {
+    for (int w = 0; w < 8; ++w)
+        for (int o = 16; o >= 1; o /= 2)
+            for (int j = 0; j < o; ++j) lane[32 * w + j] = lane[32 * w + j] + lane[32 * w + j + o];
+    float t = lane[0];
+    for (int w = 1; w < 8; ++w) t = t + lane[32 * w];
+    return t;
+}
+
+void orc_layernorm_stats(const uint16_t* row, int32_t H, float eps, float* mean_out, float* rstd_out) {
+    float s[256], q[256];
+    for (int l = 0; l < 256; ++l) s[l] = q[l] = 0.0f;
+    for (int32_t v = 0; v < H / 16; ++v) {
+        int l = v % 256;
+        for (int e = 0; e < 16; ++e) {
+            float x = orc_bf16_to_f32(row[16 * v + e]);
+            s[l] = s[l] + x;
+            q[l] = fmaf(x, x, q[l]);
+        }
+    }
+    float S = row_sum_fixed_order(s), Q = row_sum_fixed_order(q);
+    float mean = S / (float)H;
+    float m2 = Q / (float)H;
+    float var = m2 - mean * mean;
+    if (!(var > 0.0f)) var = 0.0f;
+    *mean_out = mean;
+    *rstd_out = 1.0f / sqrtf(var + eps);
+}
+
+/* y = bf16(LayerNorm(x) * gamma + beta) row by row; q = FP8(y / scale);
+ * amax = max(amax, |y|).  gamma and beta are float[H]; y may be NULL. */
+void orc_layernorm_quantize_amax(const uint16_t* x_bf16, int64_t rows, int32_t H, const float* gamma,
+                                 const float* beta, float eps, int fmt, float scale, uint8_t* q,
+                                 uint16_t* y_bf16, float* amax_inout) {
+    float m = *amax_inout;
+    for (int64_t r = 0; r < rows; ++r) {
+        const uint16_t* row = x_bf16 + r * H;
+        float mean, rstd;
+        orc_layernorm_stats(row, H, eps, &mean, &rstd);
+        for (int32_t i = 0; i < H; ++i) {
+            float x = orc_bf16_to_f32(row[i]);
+            float mul = rstd * gamma[i];
+            float yf = (x - mean) * mul + beta[i];
+            uint16_t yb = orc_f32_to_bf16(yf);
+            float y = orc_bf16_to_f32(yb);
+            if (y_bf16) y_bf16[r * H + i] = yb;
+            q[r * H + i] = orc_fp8_encode(y / scale, fmt);
+            m = amax_combine(m, fabsf(y));
+        }
+    }
+    if (rows > 0 && H > 0) *amax_inout = m;
+}
+
+/* ----------------------------------------------------------------------- */
 /* amax_and_scale_update ([TE-593]; scale formula from [XLA-FP8] "JAX":     */
 /* scale = max|A| / E4M3_MAX, times 2^margin).                              */
 

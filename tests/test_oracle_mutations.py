@@ -38,6 +38,9 @@ MUTATIONS = [
      "for (int32_t r = 0; r < H - 1; ++r) a = amax_combine(a, hist[(int64_t)r * S + s]);"),
     ("GELU cubic term dropped", "float s = x * fmaf(GELU_C, x2, 1.0f);", "float s = x;"),
     ("exp polynomial one term short", "p = fmaf(p, r, 0.5f);", "p = 0.5f;"),
+    ("LayerNorm without beta", "float yf = (x - mean) * mul + beta[i];", "float yf = (x - mean) * mul;"),
+    ("LayerNorm without eps", "*rstd_out = 1.0f / sqrtf(var + eps);", "*rstd_out = 1.0f / sqrtf(var);"),
+    ("LayerNorm fold skips a level", "for (int o = 16; o >= 1; o /= 2)", "for (int o = 16; o >= 2; o /= 2)"),
     ("fused Q->DQ divides on the way back", "float p = (float)orc_fp8_decode(code, fmt) * scale;",
      "float p = (float)orc_fp8_decode(code, fmt) / scale;"),
 ]

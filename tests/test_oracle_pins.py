@@ -618,3 +618,65 @@ def test_fused_gelu_quantize_is_quantize_of_the_bf16_gelu(orc, fmt):
         assert np.array_equal(q, q2) and a == a2
         yf = (y.astype(np.uint32) << 16).view(np.float32)
         assert a == np.max(np.abs(yf)) == orc.gelu_amax(h)
+
+
+# --------------------------------------------------------------------------- LayerNorm producer fused with Q
+
+def _ln_rows(rng, rows, H, spread=1.0):
+    x = (rng.normal(0, spread, (rows, H)) + rng.normal(0, 2 * spread, (rows, 1))).astype(np.float32)
+    return torch.from_numpy(x).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("H", [16, 272, 4096, 16384])
+def test_layernorm_stats_close_to_float64(orc, H):
+    rng = np.random.default_rng(H)
+    x = _ln_rows(rng, 6, H)
+    xb = x.view(torch.int16).numpy().view(np.uint16)
+    x64 = x.double().numpy()
+    for r in range(6):
+        mean, rstd = orc.layernorm_stats(xb[r])
+        m64 = x64[r].mean()
+        v64 = x64[r].var()
+        assert abs(mean - m64) <= 2.0 ** -18 * np.abs(x64[r]).max()
+        assert abs(rstd * math.sqrt(v64 + 1e-6) - 1.0) <= 2.0 ** -14
+
+
+def test_layernorm_output_close_to_torch(orc):
+    rng = np.random.default_rng(41)
+    H = 4096
+    x = _ln_rows(rng, 16, H)
+    g = rng.uniform(0.5, 1.5, H).astype(np.float32)
+    b = rng.normal(0, 0.2, H).astype(np.float32)
+    _, y, a = orc.layernorm_quantize_amax(x.view(torch.int16).numpy().view(np.uint16), H, g, b, E4M3FN, 1.0)
+    ref = torch.nn.functional.layer_norm(x.double(), (H,), torch.from_numpy(g).double(),
+                                         torch.from_numpy(b).double(), eps=1e-6)
+    refb = ref.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).reshape(-1)
+    same = y == refb
+    assert same.mean() > 0.99                      # the rest: bf16 rounding ties
+    yf = (y.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    rf = ref.numpy().reshape(-1)
+    assert np.all(np.abs(yf - rf) <= 2.0 ** -8 * np.abs(rf) + 2.0 ** -14)
+    assert a == np.max(np.abs(yf))
+
+
+def test_layernorm_constant_rows_give_beta(orc):
+    H = 64
+    x = torch.full((3, H), 2.5).to(torch.bfloat16)
+    g = np.full(H, 3.0, np.float32)
+    b = np.linspace(-1, 1, H).astype(np.float32)
+    _, y, _ = orc.layernorm_quantize_amax(x.view(torch.int16).numpy().view(np.uint16), H, g, b, E4M3FN, 1.0)
+    want = torch.from_numpy(np.tile(b, 3)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(y, want)
+
+
+@pytest.mark.parametrize("fmt", [E4M3FN, E5M2])
+def test_fused_layernorm_quantize_is_quantize_of_its_output(orc, fmt):
+    rng = np.random.default_rng(42)
+    H = 1024
+    x = _ln_rows(rng, 5, H, 3.0)
+    g = rng.uniform(0.5, 1.5, H).astype(np.float32)
+    b = rng.normal(0, 0.2, H).astype(np.float32)
+    for s in (1.0, 0.0123, 7.5):
+        q, y, a = orc.layernorm_quantize_amax(x.view(torch.int16).numpy().view(np.uint16), H, g, b, fmt, s)
+        q2, a2 = orc.quantize_amax(y, fmt, s)
+        assert np.array_equal(q, q2) and a == a2
