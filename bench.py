@@ -453,6 +453,45 @@ def measure_next_rows(args, step, stream, dev, peak):
         "unfused_torch_gelu_then_quantize_us": round(us_unfused, 3)}
     del h, q
 
+    # LayerNorm producer fused with the quantization on the MLP's input
+    # (8192x4096): four input/output sets in rotation so that each launch reads
+    # from HBM (one set is 100 MB, under the 129 MB L2), against torch's
+    # layer_norm writing bf16 followed by fp8q_quantize_amax.
+    from quantize_amax_scaling_gb300 import workloads as W
+    rows, hid = W.SEQ * W.BATCH, W.HIDDEN
+    xs = [W.residual_stream(seed=W.SEED_MLP + 7 + i, device=dev) for i in range(4)]
+    qs = [torch.empty((rows, hid), dtype=torch.uint8, device=dev) for _ in range(4)]
+    ys = [torch.empty((rows, hid), dtype=torch.bfloat16, device=dev) for _ in range(4)]
+    gam, bet = W.layernorm_params(hid, device=dev)
+    gam16, bet16 = gam.to(torch.bfloat16), bet.to(torch.bfloat16)
+    it = [0]
+
+    def ln(with_y):
+        i = it[0] = (it[0] + 1) % 4
+        f.fp8q_layernorm_quantize_amax(xs[i], ys[i] if with_y else None, qs[i], gam, bet, f.E4M3FN, sc0, am,
+                                       stream=stream.cuda_stream)
+
+    def ln_unfused():
+        i = it[0] = (it[0] + 1) % 4
+        ys[i].copy_(torch.nn.functional.layer_norm(xs[i], (hid,), gam16, bet16, eps=1e-6))
+        f.fp8q_quantize_amax(ys[i], qs[i], f.E4M3FN, sc0, am, stream.cuda_stream)
+    n_ln = rows * hid
+    us_lq = timed_loop(lambda: ln(False))
+    us_lyq = timed_loop(lambda: ln(True))
+    us_lu = timed_loop(ln_unfused)
+    out["layernorm_quantize_amax"] = {
+        "workload": "MLP input bf16 8192x4096 -> LayerNorm (f32 gamma, beta) -> e4m3fn + amax; "
+                    "4 buffer sets in rotation (400 MB, larger than L2)",
+        "launches": n_iter,
+        "codes_only": {"us": round(us_lq, 3), "GB/s": round(3 * n_ln / (us_lq * 1e-6) / 1e9, 1),
+                       "frac_of_peak": round(3 * n_ln / (us_lq * 1e-6) / 1e9 / peak, 4),
+                       "bytes_per_launch": 3 * n_ln},
+        "with_bf16_y": {"us": round(us_lyq, 3), "GB/s": round(5 * n_ln / (us_lyq * 1e-6) / 1e9, 1),
+                        "frac_of_peak": round(5 * n_ln / (us_lyq * 1e-6) / 1e9 / peak, 4),
+                        "bytes_per_launch": 5 * n_ln},
+        "unfused_torch_layer_norm_then_quantize_us": round(us_lu, 3)}
+    del xs, qs, ys
+
     # Ring-buffer update against the rolled one, each timed right after a
     # dequantize of the 8192x16384 gradient (where the update sits in the step).
     ring_hist = step.hist.clone()
@@ -623,20 +662,24 @@ def run_e2e(args, step, stream, dev):
 def read_traffic():
     """DRAM bytes per launch of the quantize kernel from the committed ncu capture.
 
-    None when there is no capture or when the kernel source has changed since
-    the counters were taken (the record carries a digest of the source's code).
+    None when there is no capture or when the code the kernel is built from
+    has changed since the counters were taken (the record carries a digest of
+    those sources' code).
     """
     p = os.path.join(ROOT, "profiles", "quantize_amax_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
-    src = os.path.join(ROOT, d.get("source", ""))
-    if not os.path.exists(src):
-        return None
-    with open(src) as f:
-        if source_digest(f.read()) != d.get("source_code_sha256"):
+    text = ""
+    for rel in d.get("sources", []):
+        src = os.path.join(ROOT, rel)
+        if not os.path.exists(src):
             return None
+        with open(src) as f:
+            text += f.read()
+    if not text or source_digest(text) != d.get("source_code_sha256"):
+        return None
     return d.get("dram_bytes_per_launch")
 
 

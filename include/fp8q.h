@@ -1,7 +1,7 @@
 /*
  * fp8q.h -- C ABI of libfp8q: FP8 delayed-scaling quantization on one GPU.
  *
- * Seven operations, each one kernel launch on the caller's stream:
+ * Eight operations, each one kernel launch on the caller's stream:
  *   fp8q_quantize_amax        bf16 -> FP8 bytes, fused with amax = max|x|
  *   fp8q_multi_quantize_amax  the same over a ragged list of tensors
  *   fp8q_dequantize           FP8 bytes -> bf16
@@ -10,6 +10,7 @@
  *   fp8q_qdq_amax             quantize then dequantize (bf16 -> bf16) + amax
  *   fp8q_amax_scale_update_ring  the update over a ring buffer (no roll)
  *   fp8q_gelu_quantize_amax   GELU producer fused with quantize + amax
+ *   fp8q_layernorm_quantize_amax  LayerNorm producer fused with quantize + amax
  *
  * Sources (web pages, by title and section):
  *   "User Guide on Native XLA-FP8" (NVIDIA JAX-Toolbox): opening section
@@ -221,6 +222,45 @@ fp8q_status fp8q_amax_scale_update_ring(float* amax_history, int32_t* head, int3
  */
 fp8q_status fp8q_gelu_quantize_amax(const void* h_bf16, void* y_bf16, uint8_t* q, int64_t n,
                                     fp8q_format fmt, const float* scale, float* amax, void* stream);
+
+/*
+ * LayerNorm producer fused with quantize + amax: the transformer block of the
+ * reproducer in "Fusion of Fp8 quantization and amax reduction kernels"
+ * (test.py) normalises its input with a LayerNorm and feeds the MLP's first
+ * FP8 dense layer; this computes that layer's FP8 input in one pass over x.
+ * Row by row (rows x hidden, row-major), in binary32 with Flax's defaults:
+ *   mean = S / H, var = max(0, Q / H - mean^2), rstd = 1 / sqrt(var + eps)
+ *   y[i]  = bf16_rne((x[i] - mean) * (rstd * gamma[i]) + beta[i])
+ *   q[i]  = FP8(y[i] / *scale)           exactly fp8q_quantize_amax of y
+ *   *amax = max(*amax, max |y|)          over every row
+ * S = sum x and Q = sum x^2 (fma) are added in one fixed order, so results are
+ * reproducible bit for bit: the row is cut into vectors of 16 elements,
+ * vector v is summed in index order by lane v mod 256, lanes fold within each
+ * group of 32 as a butterfly (offsets 16, 8, 4, 2, 1), and the 8 group totals
+ * are added left to right.  Every other step is one correctly rounded
+ * binary32 operation, without contraction.
+ * x_bf16: rows * hidden bf16 (device).  y_bf16: the same (device, written)
+ * or NULL when only the FP8 codes are wanted.  q: rows * hidden bytes
+ * (device).  gamma, beta: hidden floats each (device).  These five must be
+ * 16-byte aligned.  scale, amax: as for fp8q_quantize_amax.  hidden: a
+ * multiple of 16 from 16 to 16384.
+ * The kernel stages rows of x in shared memory with asynchronous bulk copies
+ * and waits for each copy at most one second.  Should a wait ever run out
+ * (it does not in correct operation), the call leaves *amax holding the bit
+ * pattern 0x7FFFFFFF, a NaN that no bf16 data can produce, and the outputs
+ * incomplete.  The first call on a device also sets the kernel's shared-memory
+ * limit (cudaFuncSetAttribute) and reads its occupancy; make it outside CUDA
+ * graph capture.
+ * Errors: FP8Q_ERR_INVALID_ARG for a bad fmt, rows < 0, hidden < 16 or not a
+ * multiple of 16, a NULL pointer (other than y_bf16) with rows > 0, or a
+ * misaligned scale/amax; FP8Q_ERR_UNSUPPORTED for hidden > 16384 or a
+ * misaligned x_bf16, y_bf16, q, gamma or beta; FP8Q_ERR_CUDA if the launch
+ * or its first-call set-up fails.  rows == 0 launches nothing.
+ */
+fp8q_status fp8q_layernorm_quantize_amax(const void* x_bf16, void* y_bf16, uint8_t* q, int64_t rows,
+                                         int32_t hidden, const float* gamma, const float* beta,
+                                         float eps, fp8q_format fmt, const float* scale, float* amax,
+                                         void* stream);
 
 /* Static, human-readable name of a status. */
 const char* fp8q_status_string(fp8q_status status);

@@ -1,23 +1,28 @@
 """Compile libfp8q.so (the CUDA kernels and their C ABI) for sm_103a, in tree.
 
-One translation unit, one -gencode, no cmake: a few seconds with nvcc.  The
-library is written next to this file and git-ignored.
+Four translation units compiled in parallel with one -gencode each, then
+linked; no cmake.  The library and its objects are written next to this file
+and git-ignored.
 """
 import os
 import shutil
 import subprocess
 import sys
+from concurrent.futures import ThreadPoolExecutor
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
-SRC = os.path.join(PKG, "csrc", "fp8q.cu")
-HDR = os.path.join(ROOT, "include", "fp8q.h")
+CSRC = os.path.join(PKG, "csrc")
+UNITS = ["quantize.cu", "producers.cu", "scale_update.cu", "abi.cu"]
+SRCS = [os.path.join(CSRC, u) for u in UNITS]
+DEPS = SRCS + [os.path.join(CSRC, "fp8q_common.cuh"), os.path.join(ROOT, "include", "fp8q.h")]
 LIB = os.path.join(PKG, "libfp8q.so")
+OBJ_DIR = os.path.join(PKG, "_build")
 
-NVCC_FLAGS = [
-    "-gencode", "arch=compute_103a,code=sm_103a",
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+NVCC_FLAGS = ARCH + [
     "-lineinfo", "-O3", "-std=c++17",
-    "-Xcompiler", "-fPIC", "-shared",
+    "-Xcompiler", "-fPIC",
     "-Xptxas", "-warn-spills",
 ]
 
@@ -37,14 +42,27 @@ def nvcc_path() -> str:
 def build(force: bool = False, verbose: bool = False) -> str:
     """Build libfp8q.so if missing or older than its sources; return its path."""
     if not force and os.path.exists(LIB):
-        if os.path.getmtime(LIB) >= max(os.path.getmtime(SRC), os.path.getmtime(HDR)):
+        if os.path.getmtime(LIB) >= max(os.path.getmtime(p) for p in DEPS):
             return LIB
+    os.makedirs(OBJ_DIR, exist_ok=True)
+    nvcc = nvcc_path()
+    tag = f".{os.getpid()}"
+
+    def compile_one(src):
+        obj = os.path.join(OBJ_DIR, os.path.basename(src) + tag + ".o")
+        cmd = [nvcc, *NVCC_FLAGS, "-I", os.path.join(ROOT, "include"), "-c", "-o", obj, src]
+        if verbose:
+            cmd.insert(1, "-Xptxas=-v")
+        subprocess.run(cmd, check=True)
+        return obj
+
+    with ThreadPoolExecutor(len(SRCS)) as ex:
+        objs = list(ex.map(compile_one, SRCS))
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc_path(), *NVCC_FLAGS, "-I", os.path.join(ROOT, "include"), "-o", tmp, SRC]
-    if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-    subprocess.run(cmd, check=True)
+    subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs], check=True)
     os.replace(tmp, LIB)
+    for o in objs:
+        os.remove(o)
     return LIB
 
 

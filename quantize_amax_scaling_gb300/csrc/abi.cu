@@ -1,0 +1,39 @@
+// abi.cu -- libfp8q's error reporting and status strings.
+
+#include "fp8q_common.cuh"
+
+namespace fp8q_detail {
+
+thread_local char g_last_error[256] = "";
+
+fp8q_status cuda_fail(cudaError_t e, const char* where) {
+    std::snprintf(g_last_error, sizeof g_last_error, "%s: %s (%s)", where, cudaGetErrorName(e),
+                  cudaGetErrorString(e));
+    return FP8Q_ERR_CUDA;
+}
+
+fp8q_status after_launch(const char* where) {
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? FP8Q_OK : cuda_fail(e, where);
+}
+
+}  // namespace fp8q_detail
+
+using namespace fp8q_detail;
+
+extern "C" {
+
+const char* fp8q_status_string(fp8q_status status) {
+    switch (status) {
+        case FP8Q_OK: return "FP8Q_OK";
+        case FP8Q_ERR_INVALID_ARG: return "FP8Q_ERR_INVALID_ARG";
+        case FP8Q_ERR_UNSUPPORTED: return "FP8Q_ERR_UNSUPPORTED";
+        case FP8Q_ERR_CUDA: return "FP8Q_ERR_CUDA";
+        case FP8Q_ERR_TOO_MANY_TENSORS: return "FP8Q_ERR_TOO_MANY_TENSORS";
+    }
+    return "FP8Q_ERR_UNKNOWN";
+}
+
+const char* fp8q_last_cuda_error(void) { return g_last_error; }
+
+}  // extern "C"

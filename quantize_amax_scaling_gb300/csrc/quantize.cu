@@ -1,0 +1,298 @@
+// quantize.cu -- quantize + amax (single and ragged multi-tensor),
+// the fused quantize -> dequantize, and dequantize.
+
+#include "fp8q_common.cuh"
+
+namespace {
+
+// A tile's vectors, loaded before anything depends on the scale, so the loads
+// and the scale's own load are in flight together.
+template <int OUT>
+struct TileRegs {
+    uint4 a[GeomOf<OUT>::type::kVecPerThread], b[GeomOf<OUT>::type::kVecPerThread];
+};
+
+template <int OUT>
+__device__ __forceinline__ void quant_vec_load(const QCursor& k, int64_t local, TileRegs<OUT>& r) {
+    using G = typename GeomOf<OUT>::type;
+    const uint16_t* xb = k.x + k.head;
+    const int64_t v0 = local * Tile<G>::kVecs + threadIdx.x;
+#pragma unroll
+    for (int u = 0; u < G::kVecPerThread; ++u) {
+        const int64_t v = v0 + (int64_t)u * kThreads;
+        if (v < k.nvec) ld_stream_v8(xb + v * G::kVecElems, r.a[u], r.b[u]);
+    }
+}
+
+template <int FMT, bool FAST, int OUT>
+__device__ __forceinline__ void quant_vec_store(const QCursor& k, int64_t local, const TileRegs<OUT>& r,
+                                                uint32_t& m2) {
+    using G = typename GeomOf<OUT>::type;
+    constexpr int E = G::kVecElems, U = G::kVecPerThread;
+    uint8_t* qb = k.q + k.head;
+    const int64_t v0 = local * Tile<G>::kVecs + threadIdx.x;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int64_t v = v0 + (int64_t)u * kThreads;
+        if (v < k.nvec) {
+            const uint4& a = r.a[u];
+            const uint4& b = r.b[u];
+            m2 = bf16x2_absmax(m2, bf16x2_absmax(bf16x2_absmax(bf16x2_absmax(a.x, a.y), bf16x2_absmax(a.z, a.w)),
+                                                 bf16x2_absmax(bf16x2_absmax(b.x, b.y), bf16x2_absmax(b.z, b.w))));
+            uint4 o;
+            o.x = quant_quad<FMT, FAST>(a.x, a.y, k.c);
+            o.y = quant_quad<FMT, FAST>(a.z, a.w, k.c);
+            o.z = quant_quad<FMT, FAST>(b.x, b.y, k.c);
+            o.w = quant_quad<FMT, FAST>(b.z, b.w, k.c);
+            if (OUT == kOutFp8) {
+                st_v4(qb + v * E, o);
+            } else {  // widen the fresh codes straight back: y = DQ(Q(x))
+                uint16_t* yb = reinterpret_cast<uint16_t*>(k.q) + k.head + v * E;
+                const float s = k.c.s;
+                st_v4(yb, make_uint4(dequant_pair<FMT>(o.x & 0xFFFFu, s), dequant_pair<FMT>(o.x >> 16, s),
+                                     dequant_pair<FMT>(o.y & 0xFFFFu, s), dequant_pair<FMT>(o.y >> 16, s)));
+                st_v4(yb + 8, make_uint4(dequant_pair<FMT>(o.z & 0xFFFFu, s), dequant_pair<FMT>(o.z >> 16, s),
+                                         dequant_pair<FMT>(o.w & 0xFFFFu, s), dequant_pair<FMT>(o.w >> 16, s)));
+            }
+        }
+    }
+}
+
+template <int FMT, bool FAST, int OUT>
+__device__ __forceinline__ void quant_scalar(const QCursor& k, int64_t i, uint32_t& ms) {
+    const uint32_t w = k.x[i];
+    ms = max(ms, abs_bits_lo(w));
+    const uint32_t code = quant_pair<FMT, FAST>(w, k.c) & 0xFFu;
+    if (OUT == kOutFp8)
+        k.q[i] = (uint8_t)code;
+    else
+        reinterpret_cast<uint16_t*>(k.q)[i] = (uint16_t)(dequant_pair<FMT>(code, k.c.s) & 0xFFFFu);
+}
+
+template <int FMT, bool FAST, int OUT>
+__device__ __forceinline__ void quant_scalars(const QCursor& k, int64_t local, uint32_t& ms) {
+    using G = typename GeomOf<OUT>::type;
+    if (k.mode == kModeVec) {
+        if (local == 0) {  // scalar head and tail, each shorter than one vector
+            const int64_t tail0 = k.head + k.nvec * G::kVecElems;
+            const int64_t nscalar = k.head + (k.n - tail0);
+            for (int64_t j = threadIdx.x; j < nscalar; j += kThreads)
+                quant_scalar<FMT, FAST, OUT>(k, j < k.head ? j : tail0 + (j - k.head), ms);
+        }
+    } else {
+        const int64_t base = local * Tile<G>::kElems;
+        const int64_t end = min(base + (int64_t)Tile<G>::kElems, k.n);
+        for (int64_t i = base + threadIdx.x; i < end; i += kThreads) quant_scalar<FMT, FAST, OUT>(k, i, ms);
+    }
+}
+
+template <int FMT, int OUT>
+__device__ __forceinline__ void quant_tile(const QCursor& k, int64_t local, uint32_t& m2, uint32_t& ms) {
+    TileRegs<OUT> r;
+    if (k.mode == kModeVec) quant_vec_load<OUT>(k, local, r);
+    if (k.c.fast) {
+        if (k.mode == kModeVec) quant_vec_store<FMT, true, OUT>(k, local, r, m2);
+        quant_scalars<FMT, true, OUT>(k, local, ms);
+    } else {
+        if (k.mode == kModeVec) quant_vec_store<FMT, false, OUT>(k, local, r, m2);
+        quant_scalars<FMT, false, OUT>(k, local, ms);
+    }
+}
+
+template <int FMT, int MAXT, int OUT>
+__global__ void __launch_bounds__(kThreads) quantize_amax_kernel(const __grid_constant__ QList<MAXT> L) {
+    __shared__ uint32_t red[kThreads / 32];
+    int64_t tile = blockIdx.x;
+    if (tile >= L.total_tiles) return;
+    // first tensor whose tiles end after this tile (binary search: a CTA starts cold)
+    int lo = 0, hi = L.count - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (tile < L.t[mid].tile_end) hi = mid;
+        else lo = mid + 1;
+    }
+    int ti = lo;
+    QCursor k = make_cursor<OUT>(L.t[ti], ti ? L.t[ti - 1].tile_end : 0);
+    uint32_t m2 = 0, ms = 0;
+    for (; tile < L.total_tiles; tile += gridDim.x) {
+        if (tile >= L.t[ti].tile_end) {  // uniform across the CTA
+            flush_amax(m2, ms, k.amax, red);
+            m2 = 0;
+            ms = 0;
+            do { ++ti; } while (tile >= L.t[ti].tile_end);
+            k = make_cursor<OUT>(L.t[ti], L.t[ti - 1].tile_end);
+        }
+        quant_tile<FMT, OUT>(k, tile - k.tile_begin, m2, ms);
+    }
+    flush_amax(m2, ms, k.amax, red);
+}
+
+// ----------------------------------------------------------------------------
+// Dequantize
+
+
+template <int FMT>
+__global__ void __launch_bounds__(kThreads)
+    dequantize_kernel(const uint8_t* __restrict__ q, uint16_t* __restrict__ y, int64_t n,
+                      const float* __restrict__ scale, int64_t tiles) {
+    const float s = __ldg(scale);
+    const Split sp = split_tensor<DequantGeom>((uintptr_t)y, (uintptr_t)q, n);
+    constexpr int E = DequantGeom::kVecElems, U = DequantGeom::kVecPerThread;
+    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+        if (sp.mode == kModeVec) {
+            const uint8_t* qb = q + sp.head;
+            uint16_t* yb = y + sp.head;
+            const int64_t v0 = tile * Tile<DequantGeom>::kVecs + threadIdx.x;
+            uint2 w[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t v = v0 + (int64_t)u * kThreads;
+                if (v < sp.nvec) w[u] = ld_stream_v2(qb + v * E);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t v = v0 + (int64_t)u * kThreads;
+                if (v < sp.nvec) {
+                    uint4 o;
+                    o.x = dequant_pair<FMT>(w[u].x & 0xFFFFu, s);
+                    o.y = dequant_pair<FMT>(w[u].x >> 16, s);
+                    o.z = dequant_pair<FMT>(w[u].y & 0xFFFFu, s);
+                    o.w = dequant_pair<FMT>(w[u].y >> 16, s);
+                    st_v4(yb + v * E, o);
+                }
+            }
+            if (tile == 0) {
+                const int64_t tail0 = sp.head + sp.nvec * E;
+                const int64_t nscalar = sp.head + (n - tail0);
+                for (int64_t j = threadIdx.x; j < nscalar; j += kThreads) {
+                    const int64_t i = j < sp.head ? j : tail0 + (j - sp.head);
+                    y[i] = (uint16_t)(dequant_pair<FMT>(q[i], s) & 0xFFFFu);
+                }
+            }
+        } else {
+            const int64_t base = tile * Tile<DequantGeom>::kElems;
+            const int64_t end = min(base + (int64_t)Tile<DequantGeom>::kElems, n);
+            for (int64_t i = base + threadIdx.x; i < end; i += kThreads)
+                y[i] = (uint16_t)(dequant_pair<FMT>(q[i], s) & 0xFFFFu);
+        }
+    }
+}
+
+// ----------------------------------------------------------------------------
+// Host side: quantize launchers
+
+// `list[i].q` is the FP8 output, or (OUT == kOutBf16) the bf16 output.
+template <int FMT, int MAXT, int OUT = kOutFp8>
+fp8q_status launch_quantize(const fp8q_tensor* list, int32_t count, cudaStream_t stream) {
+    QList<MAXT> L;
+    int64_t tiles = 0;
+    int m = 0;
+    for (int32_t i = 0; i < count; ++i) {
+        const fp8q_tensor& t = list[i];
+        const Split sp =
+            split_tensor<typename GeomOf<OUT>::type>((uintptr_t)t.x_bf16, (uintptr_t)t.q, t.n);
+        if (sp.tiles == 0) continue;  // empty tensors take no tiles and are skipped
+        QTensor& d = L.t[m++];
+        d.x = static_cast<const uint16_t*>(t.x_bf16);
+        d.q = t.q;
+        d.scale = t.scale;
+        d.amax = t.amax;
+        d.n = t.n;
+        tiles += sp.tiles;
+        d.tile_end = tiles;
+    }
+    if (tiles == 0) return FP8Q_OK;
+    L.total_tiles = tiles;
+    L.count = m;
+    L.pad = 0;
+    // One CTA per tile (16384 elements for quantize, 8192 for the fused
+    // quantize -> dequantize); each CTA flushes its amax once.  Measured on
+    // GB300 against a persistent grid-stride loop: quantize 61.9 vs 65.9 us and
+    // quantize -> dequantize 82.6 vs 110.6 us on 8192x16384.  The kernel's
+    // grid-stride loop still covers tile counts beyond the grid limit.
+    const int grid = (int)(tiles < 0x7FFFFFFF ? tiles : 0x7FFFFFFF);
+    quantize_amax_kernel<FMT, MAXT, OUT><<<grid, kThreads, 0, stream>>>(L);
+    return after_launch("quantize_amax_kernel");
+}
+
+template <int FMT>
+fp8q_status dispatch_quantize(const fp8q_tensor* list, int32_t count, cudaStream_t stream) {
+    int32_t live = 0;
+    for (int32_t i = 0; i < count; ++i) live += list[i].n > 0;
+    if (live <= 1) return launch_quantize<FMT, 1>(list, count, stream);
+    if (live <= 8) return launch_quantize<FMT, 8>(list, count, stream);
+    if (live <= 64) return launch_quantize<FMT, 64>(list, count, stream);
+    return launch_quantize<FMT, FP8Q_MAX_TENSORS>(list, count, stream);
+}
+
+template <int FMT>
+fp8q_status launch_dequantize(const uint8_t* q, void* y, int64_t n, const float* scale,
+                              cudaStream_t stream) {
+    const Split sp = split_tensor<DequantGeom>((uintptr_t)y, (uintptr_t)q, n);
+    // One CTA per tile: for this write-heavy stream (1 byte read, 2 written)
+    // the hardware's in-order CTA dispatch keeps the writes more sequential
+    // than a persistent grid-stride loop does (measured ~12% faster on GB300).
+    // The kernel's loop still covers any tile count beyond the grid limit.
+    const int64_t kMaxGrid = 0x7FFFFFFF;
+    const int grid = (int)(sp.tiles < kMaxGrid ? sp.tiles : kMaxGrid);
+    dequantize_kernel<FMT><<<grid, kThreads, 0, stream>>>(q, static_cast<uint16_t*>(y), n, scale, sp.tiles);
+    return after_launch("dequantize_kernel");
+}
+
+}  // namespace
+
+// ----------------------------------------------------------------------------
+// C ABI
+
+extern "C" {
+
+fp8q_status fp8q_quantize_amax(const void* x_bf16, uint8_t* q, int64_t n, fp8q_format fmt,
+                               const float* scale, float* amax, void* stream) {
+    if (!valid_fmt(fmt)) return FP8Q_ERR_INVALID_ARG;
+    const fp8q_tensor t = {x_bf16, q, n, scale, amax};
+    fp8q_status st = check_tensor(t);
+    if (st != FP8Q_OK || n == 0) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return fmt == FP8Q_E4M3FN ? launch_quantize<FP8Q_E4M3FN, 1>(&t, 1, s)
+                              : launch_quantize<FP8Q_E5M2, 1>(&t, 1, s);
+}
+
+fp8q_status fp8q_multi_quantize_amax(const fp8q_tensor* list, int32_t count, fp8q_format fmt,
+                                     void* stream) {
+    if (!valid_fmt(fmt) || count < 0) return FP8Q_ERR_INVALID_ARG;
+    if (count > FP8Q_MAX_TENSORS) return FP8Q_ERR_TOO_MANY_TENSORS;
+    if (count == 0) return FP8Q_OK;
+    if (!list) return FP8Q_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < count; ++i) {
+        fp8q_status st = check_tensor(list[i]);
+        if (st != FP8Q_OK) return st;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return fmt == FP8Q_E4M3FN ? dispatch_quantize<FP8Q_E4M3FN>(list, count, s)
+                              : dispatch_quantize<FP8Q_E5M2>(list, count, s);
+}
+
+fp8q_status fp8q_qdq_amax(const void* x_bf16, void* y_bf16, int64_t n, fp8q_format fmt,
+                          const float* scale, float* amax, void* stream) {
+    if (!valid_fmt(fmt)) return FP8Q_ERR_INVALID_ARG;
+    const fp8q_tensor t = {x_bf16, static_cast<uint8_t*>(y_bf16), n, scale, amax};
+    fp8q_status st = check_tensor(t);
+    if (st != FP8Q_OK || n == 0) return st;
+    if ((uintptr_t)y_bf16 & 1u) return FP8Q_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return fmt == FP8Q_E4M3FN ? launch_quantize<FP8Q_E4M3FN, 1, kOutBf16>(&t, 1, s)
+                              : launch_quantize<FP8Q_E5M2, 1, kOutBf16>(&t, 1, s);
+}
+
+fp8q_status fp8q_dequantize(const uint8_t* q, void* y_bf16, int64_t n, fp8q_format fmt,
+                            const float* scale, void* stream) {
+    if (!valid_fmt(fmt) || n < 0) return FP8Q_ERR_INVALID_ARG;
+    if (n == 0) return FP8Q_OK;
+    if (!q || !y_bf16 || !scale || ((uintptr_t)y_bf16 & 1u) || ((uintptr_t)scale & 3u))
+        return FP8Q_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return fmt == FP8Q_E4M3FN ? launch_dequantize<FP8Q_E4M3FN>(q, y_bf16, n, scale, s)
+                              : launch_dequantize<FP8Q_E5M2>(q, y_bf16, n, scale, s);
+}
+
+}  // extern "C"

@@ -23,7 +23,8 @@ STATUS = {0: "FP8Q_OK", 1: "FP8Q_ERR_INVALID_ARG", 2: "FP8Q_ERR_UNSUPPORTED", 3:
 # Every symbol the header declares.
 EXPORTS = ("fp8q_quantize_amax", "fp8q_multi_quantize_amax", "fp8q_dequantize",
            "fp8q_amax_scale_update", "fp8q_qdq_amax", "fp8q_amax_scale_update_ring",
-           "fp8q_gelu_quantize_amax", "fp8q_status_string", "fp8q_last_cuda_error")
+           "fp8q_gelu_quantize_amax", "fp8q_layernorm_quantize_amax", "fp8q_status_string",
+           "fp8q_last_cuda_error")
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfp8q.so")
 
@@ -63,9 +64,11 @@ def lib() -> ctypes.CDLL:
         L.fp8q_amax_scale_update_ring.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp, c_int, c_int, i32,
                                                   vp]
         L.fp8q_gelu_quantize_amax.argtypes = [vp, vp, vp, i64, c_int, vp, vp, vp]
+        L.fp8q_layernorm_quantize_amax.argtypes = [vp, vp, vp, i64, i32, vp, vp, ctypes.c_float, c_int,
+                                                   vp, vp, vp]
         for f in ("fp8q_quantize_amax", "fp8q_multi_quantize_amax", "fp8q_dequantize",
                   "fp8q_amax_scale_update", "fp8q_qdq_amax", "fp8q_amax_scale_update_ring",
-                  "fp8q_gelu_quantize_amax"):
+                  "fp8q_gelu_quantize_amax", "fp8q_layernorm_quantize_amax"):
             getattr(L, f).restype = c_int
         L.fp8q_status_string.argtypes = [c_int]
         L.fp8q_status_string.restype = ctypes.c_char_p
@@ -155,6 +158,29 @@ def fp8q_gelu_quantize_amax(h, y, q, fmt, scale, amax, stream=None):
         _dev(t, k, nm)
     _check(lib().fp8q_gelu_quantize_amax(_ptr(h), _ptr(y), _ptr(q), n, fmt, _ptr(scale), _ptr(amax),
                                          _stream(stream)), "fp8q_gelu_quantize_amax")
+
+
+def fp8q_layernorm_quantize_amax(x, y, q, gamma, beta, fmt, scale, amax, eps=1e-6, stream=None):
+    """y = bf16(LayerNorm(x) * gamma + beta) (y may be None), q = FP8(y / scale),
+    amax = max(amax, max|y|), one launch.
+
+    ``x`` is bf16 [rows, hidden]; ``gamma`` and ``beta`` are float32 [hidden].
+    """
+    if x.dim() != 2:
+        raise ValueError("x must be [rows, hidden]")
+    rows, hidden = x.shape
+    for t, nm in ((y, "y"), (q, "q")):
+        if t is not None and _numel(t) != rows * hidden:
+            raise ValueError(f"{nm} must have as many elements as x")
+    for t, nm in ((gamma, "gamma"), (beta, "beta")):
+        if _numel(t) != hidden:
+            raise ValueError(f"{nm} must have hidden={hidden} elements")
+    for t, k, nm in ((x, "bf16", "x"), (y, "bf16", "y"), (q, "u8", "q"), (gamma, "f32", "gamma"),
+                     (beta, "f32", "beta"), (scale, "f32", "scale"), (amax, "f32", "amax")):
+        _dev(t, k, nm)
+    _check(lib().fp8q_layernorm_quantize_amax(_ptr(x), _ptr(y), _ptr(q), rows, hidden, _ptr(gamma),
+                                              _ptr(beta), float(eps), fmt, _ptr(scale), _ptr(amax),
+                                              _stream(stream)), "fp8q_layernorm_quantize_amax")
 
 
 def fp8q_multi_quantize_amax(xs, qs, fmt, scales, amaxes, stream=None):

@@ -80,6 +80,32 @@ def gelu_activation(seed: int = SEED_FFN, device="cpu", shape=(SEQ * BATCH, FFN)
     return torch.nn.functional.gelu(x, approximate="tanh").to(torch.bfloat16)
 
 
+def residual_stream(seed: int = SEED_MLP + 7, device="cpu", shape=(SEQ * BATCH, HIDDEN),
+                    outlier_frac: float = 1e-3, outlier_gain: float = 100.0) -> torch.Tensor:
+    """LayerNorm input: row r is N(mu_r, sigma_r^2) with mu_r ~ U(-2, 2) and
+    sigma_r ~ U(0.5, 4), and a uniformly chosen 0.1% of entries times 100; bf16."""
+    g = _gen(seed, device)
+    rows = shape[0]
+    mu = torch.rand((rows, 1), generator=g, device=device) * 4.0 - 2.0
+    sigma = torch.rand((rows, 1), generator=g, device=device) * 3.5 + 0.5
+    x = torch.randn(shape, generator=g, device=device, dtype=torch.float32) * sigma + mu
+    n = x.numel()
+    k = max(1, int(n * outlier_frac))
+    idx = torch.randint(0, n, (k,), generator=g, device=device)
+    flat = x.view(-1)
+    flat[idx] = flat[idx] * outlier_gain
+    return x.to(torch.bfloat16)
+
+
+def layernorm_params(hidden: int, seed: int = SEED_MLP + 8, device="cpu"):
+    """gamma = 1 + 0.1 N(0,1) and beta = 0.1 N(0,1), float32 [hidden] (a trained-looking
+    perturbation of Flax's ones/zeros initialisation)."""
+    g = _gen(seed, device)
+    gamma = 1.0 + 0.1 * torch.randn(hidden, generator=g, device=device, dtype=torch.float32)
+    beta = 0.1 * torch.randn(hidden, generator=g, device=device, dtype=torch.float32)
+    return gamma, beta
+
+
 def truncated_normal_weight(shape, fan_in: int, seed: int, device="cpu") -> torch.Tensor:
     """Normal truncated at +-2 sigma, rescaled to variance 1/fan_in (variance-scaling init)."""
     g = _gen(seed, device)

@@ -28,7 +28,8 @@ def test_header_declares_the_four_operations():
     names = declared_functions()
     for f in ("fp8q_quantize_amax", "fp8q_multi_quantize_amax", "fp8q_dequantize",
               "fp8q_amax_scale_update", "fp8q_qdq_amax", "fp8q_amax_scale_update_ring",
-              "fp8q_gelu_quantize_amax", "fp8q_status_string", "fp8q_last_cuda_error"):
+              "fp8q_gelu_quantize_amax", "fp8q_layernorm_quantize_amax", "fp8q_status_string",
+              "fp8q_last_cuda_error"):
         assert f in names
 
 
@@ -92,6 +93,29 @@ def test_gelu_quantize_argument_errors(L):
         assert f(h, None, q, 4, 0, sc, am, None) == INVALID
     assert f(ODD, None, P, 4, 0, P, P, None) == INVALID
     assert f(P, ODD, P, 4, 0, P, P, None) == INVALID
+
+
+def test_layernorm_quantize_argument_errors(L):
+    f = L.fp8q_layernorm_quantize_amax
+    UNSUPPORTED = 2
+    #          x  y     q  rows hidden gamma beta eps  fmt sc am  stream
+    good = [P, None, P, 4, 64, P, P, 1e-6, 0, P, P, None]
+    def call(i, v):
+        a = list(good)
+        a[i] = v
+        return f(*a)
+    assert call(3, 0) == OK                          # no rows: nothing launched
+    assert call(3, -1) == INVALID
+    for h in (0, 8, 24, -16):                        # hidden >= 16 and a multiple of 16
+        assert call(4, h) == INVALID
+    assert call(4, 16384 + 16) == UNSUPPORTED        # longest row one CTA holds is 16384
+    assert call(8, 2) == INVALID
+    for i in (0, 2, 5, 6, 9, 10):
+        assert call(i, None) == INVALID
+    assert call(9, ctypes.c_void_p(0x10002)) == INVALID
+    assert call(10, ctypes.c_void_p(0x10002)) == INVALID
+    for i in (0, 1, 2, 5, 6):                  # x (bulk copies), y, q, gamma, beta: 16-byte aligned
+        assert call(i, ctypes.c_void_p(0x10008)) == UNSUPPORTED
 
 
 def test_qdq_argument_errors(L):

@@ -789,3 +789,136 @@ def test_gelu_quantize_full_size_sampled(dev):
     assert_codes_equal(q.cpu().numpy()[idx], rq, E4M3FN, "gelu q")
     assert_bf16_equal(W.bf16_bits(y)[idx], ry, "gelu y")
     assert_f32_equal([float(am)], [oracle.gelu_amax(hb)], "gelu amax over the whole tensor")
+
+
+# --------------------------------------------------------------------------- LayerNorm producer fused with Q
+
+def run_layernorm(x, gamma, beta, fmt, scale, dev, want_y=True, eps=1e-6, amax0=0.0):
+    rows, H = x.shape
+    y = torch.empty((rows, H), dtype=torch.bfloat16, device=dev) if want_y else None
+    q = torch.empty((rows, H), dtype=torch.uint8, device=dev)
+    am = f32(amax0, dev)
+    fp8q.fp8q_layernorm_quantize_amax(x, y, q, gamma, beta, fmt, f32(scale, dev), am, eps=eps)
+    torch.cuda.synchronize()
+    return y, q, am
+
+
+def _ln_check(x, gamma, beta, fmt, scale, dev, want_y=True, eps=1e-6, amax0=0.0, what=""):
+    y, q, am = run_layernorm(x, gamma, beta, fmt, scale, dev, want_y, eps, amax0)
+    rq, ry, ra = oracle.layernorm_quantize_amax(W.bf16_bits(x), x.shape[1], gamma.cpu().numpy(),
+                                                beta.cpu().numpy(), fmt, np.float32(scale), eps=eps,
+                                                amax=amax0)
+    assert_codes_equal(q.cpu().numpy(), rq, fmt, f"ln q {what}")
+    if y is not None:
+        assert_bf16_equal(W.bf16_bits(y), ry, f"ln y {what}")
+    assert_f32_equal([float(am)], [ra], f"ln amax {what}")
+
+
+LN_SHAPES = [(1, 16), (3, 272), (2, 4096), (2, 16384), (7, 4112), (300, 48), (5, 4080), (4, 8208),
+             (33, 1024), (2, 12288)]
+
+
+@pytest.mark.parametrize("rows,H", LN_SHAPES)
+def test_layernorm_quantize_shapes(dev, rows, H):
+    """One row per CTA; 1, 2 and 4 vectors per thread, ragged last pass of vectors."""
+    x = W.residual_stream(seed=rows * 7919 + H, device=dev, shape=(rows, H))
+    gamma, beta = W.layernorm_params(H, seed=H, device=dev)
+    for k, (fmt, scale) in enumerate([(E4M3FN, 0.0123), (E5M2, 1.0), (E4M3FN, 2.0 ** 70),
+                                      (E5M2, 3.3e-3)]):
+        _ln_check(x, gamma, beta, fmt, scale, dev, want_y=(k % 2 == 0), amax0=0.25 * k,
+                  what=f"{rows}x{H} scale {scale}")
+
+
+@pytest.mark.parametrize("rows,H", [(20000, 48), (5000, 4096), (3000, 8192), (1000, 16384), (7001, 272)])
+def test_layernorm_quantize_ring_wraps(dev, rows, H):
+    """More rows than the persistent grid holds in its shared-memory rings, so
+    every stage is refilled several times (parity flips), for each ring depth."""
+    x = W.residual_stream(seed=rows + H, device=dev, shape=(rows, H))
+    gamma, beta = W.layernorm_params(H, seed=H + 1, device=dev)
+    _ln_check(x, gamma, beta, E4M3FN, 0.021, dev, want_y=True, what=f"{rows}x{H}")
+    _ln_check(x, gamma, beta, E5M2, 0.5, dev, want_y=False, what=f"{rows}x{H} e5m2")
+
+
+def test_layernorm_quantize_every_scale_and_flax_defaults(dev):
+    x = W.residual_stream(seed=5, device=dev, shape=(64, 4096))
+    ones = torch.ones(4096, dtype=torch.float32, device=dev)
+    zeros = torch.zeros(4096, dtype=torch.float32, device=dev)
+    for fmt in (E4M3FN, E5M2):
+        for s in SCALES_ALL:
+            _ln_check(x, ones, zeros, fmt, s, dev, want_y=True, what=f"scale {s!r}")
+
+
+def test_layernorm_quantize_degenerate_rows(dev):
+    """Constant rows (var = 0), eps = 0 on a constant row (rstd = inf), rows with
+    inf, NaN, huge values (Q overflows) and subnormal-scale values."""
+    H = 512
+    rows = []
+    rows.append(np.full(H, 0x3F80, np.uint16))                        # all 1.0
+    rows.append(np.zeros(H, np.uint16))                               # all +0
+    r = np.full(H, 0x4000, np.uint16); r[17] = 0x7F80; rows.append(r)   # +inf
+    r = np.full(H, 0x4000, np.uint16); r[300] = 0x7FC1; rows.append(r)  # NaN
+    r = np.full(H, 0x4000, np.uint16); r[5] = 0xFF80; r[6] = 0x7F80; rows.append(r)  # +inf and -inf
+    rows.append(np.where(np.arange(H) % 2 == 0, 0x7F00, 0xFF00).astype(np.uint16))  # +-1.7e38: Q overflows
+    rows.append(np.where(np.arange(H) % 3 == 0, 0x0001, 0x8002).astype(np.uint16))  # bf16 subnormals
+    rows.append((np.arange(H) % 7 + 0x3F80).astype(np.uint16))        # values near 1 (cancellation)
+    xb = np.stack(rows)
+    x = torch.from_numpy(xb.view(np.int16).copy()).view(torch.bfloat16).to(dev)
+    gamma, beta = W.layernorm_params(H, seed=77, device=dev)
+    for eps in (1e-6, 0.0, 1e-2):
+        for fmt in (E4M3FN, E5M2):
+            y, q, am = run_layernorm(x, gamma, beta, fmt, 0.05, dev, eps=eps)
+            rq, ry, _ = oracle.layernorm_quantize_amax(xb, H, gamma.cpu().numpy(), beta.cpu().numpy(),
+                                                       fmt, np.float32(0.05), eps=eps)
+            assert_codes_equal(q.cpu().numpy(), rq, fmt, f"eps {eps}")
+            assert_bf16_equal(W.bf16_bits(y), ry, f"eps {eps}")
+    # per-row mean and rstd agree with the oracle's statistics, through y
+    m, rs = oracle.layernorm_stats(xb[0], 1e-6)
+    assert m == np.float32(1.0) and rs == np.float32(1.0) / np.sqrt(np.float32(1e-6))
+
+
+def test_layernorm_quantize_does_not_write_outside(dev):
+    rows, H = 9, 4112
+    x = W.residual_stream(seed=3, device=dev, shape=(rows, H))
+    gamma, beta = W.layernorm_params(H, device=dev)
+    n = rows * H
+    qbuf, q = guarded(n, torch.uint8, dev, 0)
+    ybuf, y = guarded(n, torch.bfloat16, dev, 0, fill=0x5A5A)
+    am = f32(0.0, dev)
+    fp8q.fp8q_layernorm_quantize_amax(x, y.view(rows, H), q.view(rows, H), gamma, beta, E4M3FN,
+                                      f32(0.02, dev), am)
+    torch.cuda.synchronize()
+    rq, ry, ra = oracle.layernorm_quantize_amax(W.bf16_bits(x), H, gamma.cpu().numpy(), beta.cpu().numpy(),
+                                                E4M3FN, np.float32(0.02))
+    assert_codes_equal(q.cpu().numpy(), rq, E4M3FN, "guarded q")
+    assert_bf16_equal(W.bf16_bits(y), ry, "guarded y")
+    check_guards(qbuf, n, 0)
+    check_guards(ybuf, n, 0, fill=0x5A5A)
+
+
+def test_layernorm_quantize_full_size_sampled(dev):
+    """The MLP's LayerNorm input, 8192x4096: sampled rows compared in full, amax over
+    every row from the oracle."""
+    x = W.residual_stream(device=dev)
+    gamma, beta = W.layernorm_params(x.shape[1], device=dev)
+    scale = np.float32(0.031)
+    y, q, am = run_layernorm(x, gamma, beta, E4M3FN, scale, dev)
+    H = x.shape[1]
+    xb = W.bf16_bits(x).reshape(-1, H)
+    g, b = gamma.cpu().numpy(), beta.cpu().numpy()
+    rows = np.unique(np.concatenate([np.arange(8), np.arange(8184, 8192),
+                                     np.random.default_rng(0).integers(0, 8192, 200)]))
+    rq, ry, _ = oracle.layernorm_quantize_amax(xb[rows], H, g, b, E4M3FN, scale)
+    assert_codes_equal(q.cpu().numpy()[rows], rq, E4M3FN, "ln q")
+    assert_bf16_equal(W.bf16_bits(y).reshape(-1, H)[rows], ry, "ln y")
+    _, _, ra = oracle.layernorm_quantize_amax(xb, H, g, b, E4M3FN, scale)
+    assert_f32_equal([float(am)], [ra], "ln amax over the whole tensor")
+
+
+def test_layernorm_close_to_torch_layer_norm(dev):
+    """Sanity check against torch's float32 layer_norm (different summation order:
+    a few bf16 ulps at most)."""
+    x = W.residual_stream(seed=9, device=dev, shape=(256, 4096))
+    gamma, beta = W.layernorm_params(4096, device=dev)
+    y, _, _ = run_layernorm(x, gamma, beta, E4M3FN, 1.0, dev)
+    ref = torch.nn.functional.layer_norm(x.float(), (4096,), gamma, beta, eps=1e-6)
+    torch.testing.assert_close(y.float(), ref, rtol=2 ** -7, atol=1e-5)
