@@ -162,29 +162,40 @@ __global__ void __launch_bounds__(kThreads) gelu_quantize_amax_kernel(const Gelu
 // rstd = 1 / sqrt(var + eps), y = (x - mean) * (rstd * gamma) + beta rounded
 // to bf16, then the quantize path on y.  S and Q are summed in one fixed
 // association that the CPU reference of this library writes out the same way:
-// vector v (16 elements) belongs to lane v mod 256, each lane adds its
-// elements in index order (s = s + x, q = fma(x, x, q)), warps fold with the
-// xor butterfly (offsets 16 .. 1), and the 8 warp totals are added left to
+// the row is cut into 16-element vectors, vector v belongs to summation lane
+// v mod 256, each lane adds its elements in index order (s = s + x,
+// q = fma(x, x, q)), each group of 32 lanes folds as a butterfly (lanes k and
+// k ^ o for o = 16, 8, 4, 2, 1), and the 8 group totals are added left to
 // right.
 //
-// Persistent grid (as many CTAs as fit on the GPU at once, at most one per
-// row); CTA b takes rows b, b + G, b + 2G, ...  Each CTA keeps a ring of
-// whole rows in shared memory, filled by cp.async.bulk copies that complete
-// on one mbarrier per stage, so up to `stages` rows (64 KB) per CTA are in
-// flight while the CTA computes.  A stage is refilled with the row `stages`
-// ahead as soon as every thread has copied it into registers (the first
-// block-wide reduction's barrier).  With at most 256 vectors per row
-// (H <= 4096) each thread always owns the same 16 columns, so it keeps their
-// gamma and beta in registers for all its rows.
+// Persistent grid (as many CTAs as fit at once, at most one per batch).  A
+// batch is R consecutive rows (R <= 8, chosen so that two batches fit the
+// shared-memory ring); CTA b takes batches b, b + G, ...  A batch arrives by
+// one cp.async.bulk copy completing on the mbarrier of its ring slot, and the
+// slot is refilled with the batch two ahead once the CTA is done with it, so
+// one batch is always in flight while the CTA computes the other.
+//
+// Phase 1: warp w computes the statistics of row w of the batch alone.  Lane
+// p holds the eight summation lanes k0 + 4m (m = 0..7) of summation group
+// p / 4, with k0 = p mod 4, so the butterfly levels 16, 8 and 4 are register
+// adds and only levels 2 and 1 cross lanes; the eight group totals are then
+// gathered with shuffles and added left to right.  No block barrier is
+// involved.
+// Phase 2: after one barrier, all 256 threads normalise and quantize the
+// batch.  Thread t owns the 8-element half-vectors t, t + 256, ... of every
+// row; with H <= 4096 those are at most two, and their gamma and beta stay in
+// registers for the whole launch.  Shared-memory reads are 16 bytes per lane
+// at consecutive addresses (no bank conflicts).
 //
 // Every mbarrier wait has a time limit (kWaitLimitNs).  The CTA agrees on the
 // outcome at the next barrier; if any thread gave up, the CTA stores the
 // pattern 0x7FFFFFFF (a NaN that no bf16 input can produce) into *amax, waits
 // (again bounded) for its copies still in flight and returns.
 
-constexpr int kLnMaxVecPerThread = 4;           // H <= 256 * 16 * 4 = 16384
-constexpr int kLnMaxStages = 16;
-constexpr uint32_t kLnRingBytes = 64u * 1024u;  // shared-memory ring per CTA
+constexpr int kLnMaxHalfPerThread = 8;           // H <= 256 * 8 * 8 = 16384
+constexpr int kLnMaxBatch = kThreads / 32;       // rows per batch: one warp each in phase 1
+constexpr int kLnBufs = 2;                       // batches in the ring
+constexpr uint32_t kLnRingBytes = 64u * 1024u;   // ring per CTA (both batches)
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr int kAmaxTimeoutBits = 0x7FFFFFFF;
 
@@ -198,7 +209,7 @@ struct LnArgs {
     float* amax;
     int64_t rows;
     int32_t H;
-    int32_t stages;  // ring depth, 2 .. kLnMaxStages, at most kLnRingBytes in all
+    int32_t batch;  // rows per batch, 1 .. kLnMaxBatch
     float eps;
 };
 
@@ -247,38 +258,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     }
 }
 
-// Warp part of the fixed-order row sums: the xor butterfly over offsets
-// 16 .. 1, for S and Q side by side.  Lane 0 (every lane) ends with the warp's
-// totals.
-__device__ __forceinline__ float2 warp_sums_fixed_order(float s, float q) {
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-        s = __fadd_rn(s, __shfl_xor_sync(0xFFFFFFFFu, s, o));
-        q = __fadd_rn(q, __shfl_xor_sync(0xFFFFFFFFu, q, o));
-    }
-    return make_float2(s, q);
+// Streaming stores whose target this kernel never reads back: no memory
+// clobber, so shared-memory loads of the next rows may be scheduled across
+// them.
+__device__ __forceinline__ void st_cs_v4(void* p, uint4 v) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
 }
 
-// Row statistics from the 8 warp totals (left to right), as (-mean, rstd).
-__device__ __forceinline__ float2 ln_stats(const float2* part, int H, float eps) {
-    float S = part[0].x, Q = part[0].y;
-#pragma unroll
-    for (int w = 1; w < kThreads / 32; ++w) {
-        S = __fadd_rn(S, part[w].x);
-        Q = __fadd_rn(Q, part[w].y);
-    }
-    const float Hf = (float)H;
-    const float mean = __fdiv_rn(S, Hf);
-    float var = __fsub_rn(__fdiv_rn(Q, Hf), __fmul_rn(mean, mean));
-    var = var > 0.0f ? var : 0.0f;
-    return make_float2(-mean, __frcp_rn(__fsqrt_rn(__fadd_rn(var, eps))));
+__device__ __forceinline__ void st_cs_v2(void* p, uint2 v) {
+    asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y));
 }
 
 // Two-lane binary32 add and multiply (PTX f32x2, sm_100 and later), each lane
 // rounded to nearest even exactly like add.rn.f32 / mul.rn.f32.  A two-lane
 // multiply whose result feeds a two-lane add was measured to come out as one
 // fused multiply-add (a single rounding) on sm_103a even with the explicit
-// rounding mode, so a product that is then added is formed with the scalar
+// rounding mode (and so did a two-lane fma with a -0 addend followed by a
+// two-lane add), so a product that is then added is formed with the scalar
 // __fmul_rn / __fadd_rn pair, which is never contracted.
 __device__ __forceinline__ float2 add2_rn(float2 a, float2 b) {
     float2 d;
@@ -298,6 +294,84 @@ __device__ __forceinline__ float2 mul2_rn(float2 a, float2 b) {
         : "=f"(d.x), "=f"(d.y)
         : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
     return d;
+}
+
+// Phase 1: (-mean, rstd) of one row (nv vectors in shared memory), computed by
+// one warp in the fixed summation order.  Lane p holds summation lanes
+// k0 + 4m of group j (p = 4j + k0); its vectors are those lanes' vectors
+// l, l + 256, ... in index order.  Four vectors are loaded at a time and their
+// four chains advanced element by element, so the adds of different chains
+// overlap.  A vector past the end of the row reads as +0.0: every partial sum
+// starts at +0 and can never become -0, so adding +0 leaves it unchanged.
+template <int VPL>  // most vectors one summation lane owns: ceil(nv / 256)
+__device__ __forceinline__ float2 ln_row_stats(const uint8_t* row, int nv, int H, float eps) {
+    const int lane = threadIdx.x & 31;
+    const int base = 32 * (lane >> 2) + (lane & 3);
+    float s[8], q[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) s[m] = q[m] = 0.0f;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+#pragma unroll
+        for (int m0 = 0; m0 < 8; m0 += 4) {
+            uint32_t w[4][8];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int v = base + 4 * (m0 + m) + 256 * i;
+                uint4 h0 = make_uint4(0u, 0u, 0u, 0u), h1 = h0;
+                if (v < nv) {
+                    const uint4* p = reinterpret_cast<const uint4*>(row + 32 * v);
+                    h0 = p[0];
+                    h1 = p[1];
+                }
+                w[m][0] = h0.x; w[m][1] = h0.y; w[m][2] = h0.z; w[m][3] = h0.w;
+                w[m][4] = h1.x; w[m][5] = h1.y; w[m][6] = h1.z; w[m][7] = h1.w;
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const float x0 = __uint_as_float(w[m][e] << 16);
+                    s[m0 + m] = __fadd_rn(s[m0 + m], x0);
+                    q[m0 + m] = __fmaf_rn(x0, x0, q[m0 + m]);
+                }
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const float x1 = __uint_as_float(w[m][e] & 0xFFFF0000u);
+                    s[m0 + m] = __fadd_rn(s[m0 + m], x1);
+                    q[m0 + m] = __fmaf_rn(x1, x1, q[m0 + m]);
+                }
+            }
+        }
+    }
+    // butterfly levels 16, 8, 4 inside the lane, 2 and 1 across lanes
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        s[m] = __fadd_rn(s[m], s[m + 4]);
+        q[m] = __fadd_rn(q[m], q[m + 4]);
+    }
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+        s[m] = __fadd_rn(s[m], s[m + 2]);
+        q[m] = __fadd_rn(q[m], q[m + 2]);
+    }
+    float st = __fadd_rn(s[0], s[1]), qt = __fadd_rn(q[0], q[1]);
+    st = __fadd_rn(st, __shfl_xor_sync(0xFFFFFFFFu, st, 2));
+    qt = __fadd_rn(qt, __shfl_xor_sync(0xFFFFFFFFu, qt, 2));
+    st = __fadd_rn(st, __shfl_xor_sync(0xFFFFFFFFu, st, 1));
+    qt = __fadd_rn(qt, __shfl_xor_sync(0xFFFFFFFFu, qt, 1));
+    // group totals sit in lanes 0, 4, ..., 28: add them left to right
+    float S = __shfl_sync(0xFFFFFFFFu, st, 0), Q = __shfl_sync(0xFFFFFFFFu, qt, 0);
+#pragma unroll
+    for (int j = 1; j < 8; ++j) {
+        S = __fadd_rn(S, __shfl_sync(0xFFFFFFFFu, st, 4 * j));
+        Q = __fadd_rn(Q, __shfl_sync(0xFFFFFFFFu, qt, 4 * j));
+    }
+    const float Hf = (float)H;
+    const float mean = __fdiv_rn(S, Hf);
+    float var = __fsub_rn(__fdiv_rn(Q, Hf), __fmul_rn(mean, mean));
+    var = var > 0.0f ? var : 0.0f;
+    return make_float2(-mean, __frcp_rn(__fsqrt_rn(__fadd_rn(var, eps))));
 }
 
 // Eight bf16 of x (one uint4) -> eight bf16 of y:
@@ -328,15 +402,23 @@ __device__ __forceinline__ uint32_t quant_pair_x2(uint32_t w, const QScale& c, f
     return cvt_fp8x2<FMT>(__fmaf_rn(-e0, c.r, y0.x), __fmaf_rn(-e1, c.r, y0.y));
 }
 
-template <int FMT, bool FAST>
-__device__ __forceinline__ uint4 ln_quant16(const uint4& ya, const uint4& yb, const QScale& c, float2 r2) {
-    if (FAST)
-        return make_uint4(quant_pair_x2<FMT>(ya.x, c, r2) | (quant_pair_x2<FMT>(ya.y, c, r2) << 16),
-                          quant_pair_x2<FMT>(ya.z, c, r2) | (quant_pair_x2<FMT>(ya.w, c, r2) << 16),
-                          quant_pair_x2<FMT>(yb.x, c, r2) | (quant_pair_x2<FMT>(yb.y, c, r2) << 16),
-                          quant_pair_x2<FMT>(yb.z, c, r2) | (quant_pair_x2<FMT>(yb.w, c, r2) << 16));
-    return make_uint4(quant_quad<FMT, false>(ya.x, ya.y, c), quant_quad<FMT, false>(ya.z, ya.w, c),
-                      quant_quad<FMT, false>(yb.x, yb.y, c), quant_quad<FMT, false>(yb.z, yb.w, c));
+// Eight bf16 of y -> eight FP8 codes.
+template <int FMT>
+__device__ __forceinline__ uint2 ln_quant8(const uint4& y, const QScale& c, float2 r2) {
+    if (c.fast)
+        return make_uint2(quant_pair_x2<FMT>(y.x, c, r2) | (quant_pair_x2<FMT>(y.y, c, r2) << 16),
+                          quant_pair_x2<FMT>(y.z, c, r2) | (quant_pair_x2<FMT>(y.w, c, r2) << 16));
+    return make_uint2(quant_quad<FMT, false>(y.x, y.y, c), quant_quad<FMT, false>(y.z, y.w, c));
+}
+
+// One half-vector of the output: y (optional), its |y| into m2, its FP8 codes.
+template <int FMT, bool WRITE_Y>
+__device__ __forceinline__ void ln_out8(const LnArgs& a, uint4 w, const float2 (&g)[4], const float2 (&b)[4],
+                                        float2 stats, const QScale& c, float2 r2, int64_t off, uint32_t& m2) {
+    const uint4 yv = ln_normalize8(w, g, b, make_float2(stats.x, stats.x), make_float2(stats.y, stats.y));
+    if (WRITE_Y) st_cs_v4(a.y + off, yv);
+    m2 = bf16x2_absmax(m2, bf16x2_absmax(bf16x2_absmax(yv.x, yv.y), bf16x2_absmax(yv.z, yv.w)));
+    st_cs_v2(a.q + off, ln_quant8<FMT>(yv, c, r2));
 }
 
 __device__ __forceinline__ void load4f2(const float* p, float2 (&d)[4]) {
@@ -348,115 +430,99 @@ __device__ __forceinline__ void load4f2(const float* p, float2 (&d)[4]) {
     d[3] = make_float2(v.z, v.w);
 }
 
-template <int FMT, bool WRITE_Y, int VPT>
-__global__ void __launch_bounds__(kThreads) layernorm_quantize_amax_kernel(const LnArgs a) {
-    extern __shared__ __align__(128) uint8_t ring[];  // a.stages rows of 2H bytes
-    __shared__ uint64_t bar[kLnMaxStages];
-    __shared__ float2 part[kThreads / 32];  // per-warp (S, Q)
-    __shared__ float2 stats;                // (-mean, rstd) of the current row
+// HPT: most 8-element half-vectors a thread owns per row (ceil(H / 2048)).
+template <int FMT, bool WRITE_Y, int HPT>
+__global__ void __launch_bounds__(kThreads, 2) layernorm_quantize_amax_kernel(const LnArgs a) {
+    extern __shared__ __align__(128) uint8_t ring[];  // kLnBufs batches of a.batch rows of 2H bytes
+    __shared__ uint64_t bar[kLnBufs];
+    __shared__ float2 stats[kLnMaxBatch];  // (-mean, rstd) of each row of the batch
     __shared__ uint32_t red[kThreads / 32];
-    constexpr bool kGammaInRegs = (VPT == 1);
-    const int nv = a.H / 16;
+    constexpr bool kGammaInRegs = (HPT <= 2);
+    constexpr int VPL = (HPT + 1) / 2;  // vectors per summation lane
+    const int nv = a.H / 16, nh = a.H / 8;
+    const int R = a.batch;
     const uint32_t row_bytes = 2u * (uint32_t)a.H;
+    const uint32_t buf_bytes = (uint32_t)R * row_bytes;
+    const int64_t nb = (a.rows + R - 1) / R;
     const int64_t G = gridDim.x;
-    const int64_t n_mine = (a.rows - 1 - blockIdx.x) / G + 1;  // the launch keeps G <= rows
-    const int stages = a.stages;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t n_mine = (nb - 1 - blockIdx.x) / G + 1;  // the launch keeps G <= nb
+    const int warp = threadIdx.x >> 5;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < stages; ++s) mbar_init(&bar[s]);
+        for (int b = 0; b < kLnBufs; ++b) mbar_init(&bar[b]);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        for (int s = 0; s < stages && s < n_mine; ++s)
-            bulk_load(ring + (size_t)s * row_bytes, a.x + (blockIdx.x + s * G) * a.H, row_bytes, &bar[s]);
+        for (int64_t k = 0; k < kLnBufs && k < n_mine; ++k) {
+            const int64_t r0 = (blockIdx.x + k * G) * R;
+            const int64_t nr = a.rows - r0 < R ? a.rows - r0 : R;
+            bulk_load(ring + (size_t)k * buf_bytes, a.x + r0 * a.H, (uint32_t)nr * row_bytes, &bar[k]);
+        }
     }
     const QScale c = make_qscale(a.scale);
     const float2 r2 = make_float2(c.r, c.r);
-    float2 gr[kGammaInRegs ? 2 : 1][4], br[kGammaInRegs ? 2 : 1][4];
-    if (kGammaInRegs && (int)threadIdx.x < nv) {
-        load4f2(a.gamma + 16 * threadIdx.x, gr[0]);
-        load4f2(a.gamma + 16 * threadIdx.x + 8, gr[kGammaInRegs ? 1 : 0]);
-        load4f2(a.beta + 16 * threadIdx.x, br[0]);
-        load4f2(a.beta + 16 * threadIdx.x + 8, br[kGammaInRegs ? 1 : 0]);
+    float2 gr[kGammaInRegs ? HPT : 1][4], br[kGammaInRegs ? HPT : 1][4];
+    if (kGammaInRegs) {
+#pragma unroll
+        for (int i = 0; i < (kGammaInRegs ? HPT : 0); ++i) {
+            const int u = threadIdx.x + i * kThreads;
+            if (u < nh) {
+                load4f2(a.gamma + 8 * u, gr[i]);
+                load4f2(a.beta + 8 * u, br[i]);
+            }
+        }
     }
     __syncthreads();  // barriers initialised before anyone waits on them
 
     uint32_t m2 = 0;
     bool ok = true;
-    int st = 0;
-    uint32_t parity = 0;
-    int64_t i = 0;
-    for (; i < n_mine; ++i) {
-        const int64_t row = blockIdx.x + i * G;
-        const bool arrived = mbar_wait(&bar[st], parity);
-        const uint8_t* srow = ring + (size_t)st * row_bytes;
-        uint4 wa[VPT], wb[VPT];
-        float s = 0.0f, q = 0.0f;
-#pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-            const int v = threadIdx.x + k * kThreads;
-            if (v < nv) {
-                wa[k] = *reinterpret_cast<const uint4*>(srow + 32 * v);
-                wb[k] = *reinterpret_cast<const uint4*>(srow + 32 * v + 16);
-                const uint32_t w8[8] = {wa[k].x, wa[k].y, wa[k].z, wa[k].w, wb[k].x, wb[k].y, wb[k].z, wb[k].w};
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float x0 = __uint_as_float(w8[e] << 16);
-                    const float x1 = __uint_as_float(w8[e] & 0xFFFF0000u);
-                    s = __fadd_rn(s, x0);
-                    q = __fmaf_rn(x0, x0, q);
-                    s = __fadd_rn(s, x1);
-                    q = __fmaf_rn(x1, x1, q);
-                }
-            }
+    int64_t k = 0;
+    for (; k < n_mine; ++k) {
+        const int buf = (int)(k % kLnBufs);
+        const uint32_t parity = (uint32_t)((k / kLnBufs) & 1);
+        const int64_t r0 = (blockIdx.x + k * G) * R;
+        const int nr = a.rows - r0 < R ? (int)(a.rows - r0) : R;
+        const uint8_t* base = ring + (size_t)buf * buf_bytes;
+        const bool arrived = mbar_wait(&bar[buf], parity);
+        if (arrived && warp < nr) {
+            const float2 st = ln_row_stats<VPL>(base + (size_t)warp * row_bytes, nv, a.H, a.eps);
+            if ((threadIdx.x & 31) == 0) stats[warp] = st;
         }
-        const float2 wsum = warp_sums_fixed_order(s, q);
-        if (lane == 0) part[warp] = wsum;
-        ok = __syncthreads_and(arrived) != 0;  // every thread also holds its part of the row now
-        if (!ok) break;                        // uniform
-        if (warp == 0) {
-            if (lane == 0 && i + stages < n_mine)  // refill the stage just read
-                bulk_load(ring + (size_t)st * row_bytes, a.x + (row + stages * G) * a.H, row_bytes, &bar[st]);
-            const float2 t = ln_stats(part, a.H, a.eps);
-            if (lane == 0) stats = t;
-        }
-        __syncthreads();
-        const float2 sv = stats;
-        const float2 nmean = make_float2(sv.x, sv.x), rstd = make_float2(sv.y, sv.y);
+        ok = __syncthreads_and(arrived) != 0;
+        if (!ok) break;  // uniform
+        // two rows at a time: independent work for the scheduler, gamma and beta read once
+        for (int r = 0; r < nr; r += 2) {
+            const bool pair = r + 1 < nr;
+            const float2 s0 = stats[r], s1 = stats[pair ? r + 1 : r];
+            const uint8_t* srow = base + (size_t)r * row_bytes;
+            const int64_t row_off = (r0 + r) * a.H;
 #pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-            const int v = threadIdx.x + k * kThreads;
-            if (v < nv) {
-                float2 g0[4], g1[4], b0[4], b1[4];
-                if (kGammaInRegs) {
+            for (int i = 0; i < HPT; ++i) {
+                const int u = threadIdx.x + i * kThreads;
+                if (u < nh) {
+                    const uint4 w0 = *reinterpret_cast<const uint4*>(srow + 16 * u);
+                    uint4 w1 = w0;
+                    if (pair) w1 = *reinterpret_cast<const uint4*>(srow + row_bytes + 16 * u);
+                    float2 g[4], b[4];
+                    if (kGammaInRegs) {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        g0[e] = gr[0][e]; g1[e] = gr[kGammaInRegs ? 1 : 0][e];
-                        b0[e] = br[0][e]; b1[e] = br[kGammaInRegs ? 1 : 0][e];
+                        for (int e = 0; e < 4; ++e) {
+                            g[e] = gr[kGammaInRegs ? i : 0][e];
+                            b[e] = br[kGammaInRegs ? i : 0][e];
+                        }
+                    } else {
+                        load4f2(a.gamma + 8 * u, g);
+                        load4f2(a.beta + 8 * u, b);
                     }
-                } else {
-                    load4f2(a.gamma + 16 * v, g0);
-                    load4f2(a.gamma + 16 * v + 8, g1);
-                    load4f2(a.beta + 16 * v, b0);
-                    load4f2(a.beta + 16 * v + 8, b1);
+                    const int64_t off = row_off + 8 * u;
+                    ln_out8<FMT, WRITE_Y>(a, w0, g, b, s0, c, r2, off, m2);
+                    if (pair) ln_out8<FMT, WRITE_Y>(a, w1, g, b, s1, c, r2, off + a.H, m2);
                 }
-                const uint4 ya = ln_normalize8(wa[k], g0, b0, nmean, rstd);
-                const uint4 yb = ln_normalize8(wb[k], g1, b1, nmean, rstd);
-                const int64_t off = row * a.H + 16 * v;
-                if (WRITE_Y) {
-                    st_v4(a.y + off, ya);
-                    st_v4(a.y + off + 8, yb);
-                }
-                m2 = bf16x2_absmax(m2, bf16x2_absmax(bf16x2_absmax(bf16x2_absmax(ya.x, ya.y),
-                                                                   bf16x2_absmax(ya.z, ya.w)),
-                                                     bf16x2_absmax(bf16x2_absmax(yb.x, yb.y),
-                                                                   bf16x2_absmax(yb.z, yb.w))));
-                const uint4 o = c.fast ? ln_quant16<FMT, true>(ya, yb, c, r2) : ln_quant16<FMT, false>(ya, yb, c, r2);
-                st_v4(a.q + off, o);
             }
         }
-        if (++st == stages) {
-            st = 0;
-            parity ^= 1u;
+        __syncthreads();  // every thread is done with this slot and with stats[]
+        if (threadIdx.x == 0 && k + kLnBufs < n_mine) {  // refill the slot, kLnBufs batches ahead
+            const int64_t next_r0 = (blockIdx.x + (k + kLnBufs) * G) * R;
+            const int64_t next_nr = a.rows - next_r0 < R ? a.rows - next_r0 : R;
+            bulk_load(ring + (size_t)buf * buf_bytes, a.x + next_r0 * a.H, (uint32_t)next_nr * row_bytes, &bar[buf]);
         }
     }
     if (!ok) {
@@ -464,10 +530,8 @@ __global__ void __launch_bounds__(kThreads) layernorm_quantize_amax_kernel(const
         // for the copies this CTA still has in flight before leaving.
         if (threadIdx.x == 0) {
             atomicMax(reinterpret_cast<int*>(a.amax), kAmaxTimeoutBits);
-            for (int64_t j = i; j < n_mine && j < i + stages; ++j) {
-                const int64_t d = j - i + st;
-                mbar_wait(&bar[d % stages], parity ^ (uint32_t)((d / stages) & 1));
-            }
+            for (int64_t j = k; j < n_mine && j < k + kLnBufs; ++j)
+                mbar_wait(&bar[j % kLnBufs], (uint32_t)((j / kLnBufs) & 1));
         }
         return;
     }
@@ -488,7 +552,7 @@ struct ResidentCache {
 };
 
 template <class K>
-cudaError_t resident_ctas(K kern, uint32_t smem, ResidentCache& cache, int* ctas) {
+cudaError_t resident_ctas(K kern, int threads, uint32_t smem, ResidentCache& cache, int* ctas) {
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
@@ -502,7 +566,7 @@ cudaError_t resident_ctas(K kern, uint32_t smem, ResidentCache& cache, int* ctas
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLnRingBytes);
     if (err != cudaSuccess) return err;
     int per_sm = 0, sms = 0;
-    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
     if (err != cudaSuccess) return err;
     err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (err != cudaSuccess) return err;
@@ -512,29 +576,31 @@ cudaError_t resident_ctas(K kern, uint32_t smem, ResidentCache& cache, int* ctas
     return cudaSuccess;
 }
 
-template <int FMT, bool WRITE_Y, int VPT>
-fp8q_status launch_layernorm_vpt(LnArgs a, cudaStream_t s) {
+template <int FMT, bool WRITE_Y, int HPT>
+fp8q_status launch_layernorm_hpt(LnArgs a, cudaStream_t s) {
     static ResidentCache cache;
-    auto kern = layernorm_quantize_amax_kernel<FMT, WRITE_Y, VPT>;
+    auto kern = layernorm_quantize_amax_kernel<FMT, WRITE_Y, HPT>;
     const uint32_t row_bytes = 2u * (uint32_t)a.H;
-    int stages = (int)(kLnRingBytes / row_bytes);
-    stages = stages < 2 ? 2 : (stages > kLnMaxStages ? kLnMaxStages : stages);
-    a.stages = stages;
-    const uint32_t smem = (uint32_t)stages * row_bytes;
+    uint32_t batch = kLnRingBytes / (kLnBufs * row_bytes);
+    batch = batch < 1 ? 1 : (batch > (uint32_t)kLnMaxBatch ? (uint32_t)kLnMaxBatch : batch);
+    a.batch = (int32_t)batch;
+    const uint32_t smem = kLnBufs * batch * row_bytes;
     int ctas = 0;
-    const cudaError_t err = resident_ctas(kern, smem, cache, &ctas);
+    const cudaError_t err = resident_ctas(kern, kThreads, smem, cache, &ctas);
     if (err != cudaSuccess) return cuda_fail(err, "layernorm_quantize_amax_kernel setup");
-    const int64_t grid = a.rows < (int64_t)ctas ? a.rows : (int64_t)ctas;
+    const int64_t batches = (a.rows + batch - 1) / batch;
+    const int64_t grid = batches < (int64_t)ctas ? batches : (int64_t)ctas;
     kern<<<(unsigned)grid, kThreads, smem, s>>>(a);
     return after_launch("layernorm_quantize_amax_kernel");
 }
 
 template <int FMT, bool WRITE_Y>
 fp8q_status launch_layernorm(const LnArgs& a, cudaStream_t s) {
-    const int vpt = (a.H / 16 + kThreads - 1) / kThreads;
-    if (vpt <= 1) return launch_layernorm_vpt<FMT, WRITE_Y, 1>(a, s);
-    if (vpt <= 2) return launch_layernorm_vpt<FMT, WRITE_Y, 2>(a, s);
-    return launch_layernorm_vpt<FMT, WRITE_Y, 4>(a, s);
+    const int hpt = (a.H / 8 + kThreads - 1) / kThreads;  // half-vectors per thread
+    if (hpt <= 1) return launch_layernorm_hpt<FMT, WRITE_Y, 1>(a, s);
+    if (hpt <= 2) return launch_layernorm_hpt<FMT, WRITE_Y, 2>(a, s);
+    if (hpt <= 4) return launch_layernorm_hpt<FMT, WRITE_Y, 4>(a, s);
+    return launch_layernorm_hpt<FMT, WRITE_Y, 8>(a, s);
 }
 
 }  // namespace
@@ -586,7 +652,7 @@ fp8q_status fp8q_layernorm_quantize_amax(const void* x_bf16, void* y_bf16, uint8
                                          int32_t hidden, const float* gamma, const float* beta, float eps,
                                          fp8q_format fmt, const float* scale, float* amax, void* stream) {
     if (!valid_fmt(fmt) || rows < 0 || hidden < 16 || (hidden % 16) != 0) return FP8Q_ERR_INVALID_ARG;
-    if (hidden > 16 * kThreads * kLnMaxVecPerThread) return FP8Q_ERR_UNSUPPORTED;
+    if (hidden > 8 * kThreads * kLnMaxHalfPerThread) return FP8Q_ERR_UNSUPPORTED;
     if (rows == 0) return FP8Q_OK;
     if (!x_bf16 || !q || !gamma || !beta || !scale || !amax) return FP8Q_ERR_INVALID_ARG;
     if (((uintptr_t)scale & 3u) || ((uintptr_t)amax & 3u)) return FP8Q_ERR_INVALID_ARG;
@@ -603,7 +669,7 @@ fp8q_status fp8q_layernorm_quantize_amax(const void* x_bf16, void* y_bf16, uint8
     a.amax = amax;
     a.rows = rows;
     a.H = hidden;
-    a.stages = 0;
+    a.batch = 0;
     a.eps = eps;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (fmt == FP8Q_E4M3FN)
