@@ -2,6 +2,7 @@
 // GELU (elementwise) and LayerNorm (row-wise).
 
 #include "fp8q_common.cuh"
+#include "packed_f32.cuh"
 
 #include <mutex>
 
@@ -20,39 +21,43 @@ namespace {
 // for bit on any IEEE machine.  Constants: binary32 roundings of ln 2 split in
 // two (high part to 16 significant bits), 1/ln 2, -2 sqrt(2/pi), 0.044715, 1/k!.
 
-// e^v on [-20, 89]: under -20, 1 + e^v is exactly 1 in binary32 whatever e^v
-// is; above 88.73 the result overflows to +inf.  k = round(v / ln 2) comes
-// from one fused multiply-add with 1.5 * 2^23 (whose sum's last bit is then
-// the integer, read straight from the bits), r = v - k ln 2 in two parts, e^r
-// by a degree-6 Taylor polynomial, then (e^r * 2^(k-1)) * 2.
-__device__ __forceinline__ float exp_rr(float v) {
-    v = fminf(fmaxf(v, -20.0f), 89.0f);  // fmaxf first: a NaN becomes -20
-    const float t = __fmaf_rn(v, 0x1.715476p+0f, 0x1.8p23f);
-    const float k = __fsub_rn(t, 0x1.8p23f);
-    float r = __fmaf_rn(-k, 0x1.62e4p-1f, v);
-    r = __fmaf_rn(-k, 0x1.7f7d1cp-20f, r);
-    float p = 0x1.6c16c2p-10f;
-    p = __fmaf_rn(p, r, 0x1.111112p-7f);
-    p = __fmaf_rn(p, r, 0x1.555556p-5f);
-    p = __fmaf_rn(p, r, 0x1.555556p-3f);
-    p = __fmaf_rn(p, r, 0.5f);
-    p = __fmaf_rn(p, r, 1.0f);
-    p = __fmaf_rn(p, r, 1.0f);
-    const int ki = __float_as_int(t) - __float_as_int(0x1.8p23f);  // k, in [-29, 128]
-    return __fmul_rn(__fmul_rn(p, __int_as_float((ki + 126) << 23)), 2.0f);
-}
-
-__device__ __forceinline__ float gelu_rr(float x) {
-    const float x2 = __fmul_rn(x, x);
-    const float sx = __fmul_rn(x, __fmaf_rn(0x1.6e4e26p-5f, x2, 1.0f));  // x (1 + 0.044715 x^2)
-    const float d = __fadd_rn(1.0f, exp_rr(__fmul_rn(-0x1.988454p+0f, sx)));
-    const float g = __fmul_rn(x, __frcp_rn(d));
-    return x == -INFINITY ? -0.0f : g;  // the limit (x * 0 would be NaN); NaN stays NaN
+// e^v on [-20, 89], two lanes at a time: under -20, 1 + e^v is exactly 1 in
+// binary32 whatever e^v is; above 88.73 the result overflows to +inf.
+// k = round(v / ln 2) comes from one fused multiply-add with 1.5 * 2^23 (whose
+// sum's last bit is then the integer, read straight from the bits),
+// r = v - k ln 2 in two parts (fma(k, -c, v) is fma(-k, c, v) exactly), e^r by
+// a degree-6 Taylor polynomial, then (e^r * 2^(k-1)) * 2.  Every two-lane
+// operation rounds each lane exactly like its scalar form; the one multiply
+// whose result is then added (by 2, before 1 + e) is exact, so no fusion can
+// change a bit.
+__device__ __forceinline__ float2 exp2_rr(float2 v) {
+    v.x = fminf(fmaxf(v.x, -20.0f), 89.0f);  // fmaxf first: a NaN becomes -20
+    v.y = fminf(fmaxf(v.y, -20.0f), 89.0f);
+    const float2 t = fma2_rn(v, splat2(0x1.715476p+0f), splat2(0x1.8p23f));
+    const float2 k = add2_rn(t, splat2(-0x1.8p23f));
+    float2 r = fma2_rn(k, splat2(-0x1.62e4p-1f), v);
+    r = fma2_rn(k, splat2(-0x1.7f7d1cp-20f), r);
+    float2 p = fma2_rn(splat2(0x1.6c16c2p-10f), r, splat2(0x1.111112p-7f));
+    p = fma2_rn(p, r, splat2(0x1.555556p-5f));
+    p = fma2_rn(p, r, splat2(0x1.555556p-3f));
+    p = fma2_rn(p, r, splat2(0.5f));
+    p = fma2_rn(p, r, splat2(1.0f));
+    p = fma2_rn(p, r, splat2(1.0f));
+    const int k0 = __float_as_int(t.x) - __float_as_int(0x1.8p23f);  // k, in [-29, 128]
+    const int k1 = __float_as_int(t.y) - __float_as_int(0x1.8p23f);
+    const float2 s = make_float2(__int_as_float((k0 + 126) << 23), __int_as_float((k1 + 126) << 23));
+    return mul2_rn(mul2_rn(p, s), splat2(2.0f));
 }
 
 // Two bf16 (one word) -> two bf16 of GELU (one word).
 __device__ __forceinline__ uint32_t gelu_pair(uint32_t w) {
-    return cvt_bf16x2(gelu_rr(__uint_as_float(w << 16)), gelu_rr(__uint_as_float(w & 0xFFFF0000u)));
+    const float2 x = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+    const float2 x2 = mul2_rn(x, x);
+    const float2 sx = mul2_rn(x, fma2_rn(splat2(0x1.6e4e26p-5f), x2, splat2(1.0f)));  // x (1 + 0.044715 x^2)
+    const float2 d = add2_rn(splat2(1.0f), exp2_rr(mul2_rn(splat2(-0x1.988454p+0f), sx)));
+    const float2 g = mul2_rn(x, rcp2_rn(d));  // d >= 1
+    // GELU(-inf) is the limit -0 (x * 0 would be NaN); NaN stays NaN
+    return cvt_bf16x2(x.x == -INFINITY ? -0.0f : g.x, x.y == -INFINITY ? -0.0f : g.y);
 }
 
 struct GeluGeom {
@@ -127,8 +132,10 @@ __device__ __forceinline__ void gelu_tile(const GeluArgs& a, const QScale& c, in
     }
 }
 
+// At most 64 registers, so four CTAs share an SM: the exp chain is long, and
+// the extra warps hide its latency (measured 155 us against 175 us with three).
 template <int FMT, bool WRITE_Y>
-__global__ void __launch_bounds__(kThreads) gelu_quantize_amax_kernel(const GeluArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) gelu_quantize_amax_kernel(const GeluArgs a) {
     __shared__ uint32_t red[kThreads / 32];
     constexpr int E = GeluGeom::kVecElems, U = GeluGeom::kVecPerThread;
     uint32_t m2 = 0, ms = 0;
@@ -267,33 +274,6 @@ __device__ __forceinline__ void st_cs_v4(void* p, uint4 v) {
 
 __device__ __forceinline__ void st_cs_v2(void* p, uint2 v) {
     asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y));
-}
-
-// Two-lane binary32 add and multiply (PTX f32x2, sm_100 and later), each lane
-// rounded to nearest even exactly like add.rn.f32 / mul.rn.f32.  A two-lane
-// multiply whose result feeds a two-lane add was measured to come out as one
-// fused multiply-add (a single rounding) on sm_103a even with the explicit
-// rounding mode (and so did a two-lane fma with a -0 addend followed by a
-// two-lane add), so a product that is then added is formed with the scalar
-// __fmul_rn / __fadd_rn pair, which is never contracted.
-__device__ __forceinline__ float2 add2_rn(float2 a, float2 b) {
-    float2 d;
-    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
-        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return d;
-}
-
-__device__ __forceinline__ float2 mul2_rn(float2 a, float2 b) {
-    float2 d;
-    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
-        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return d;
 }
 
 // Phase 1: (-mean, rstd) of one row (nv vectors in shared memory), computed by
