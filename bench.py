@@ -522,6 +522,57 @@ def measure_next_rows(args, step, stream, dev, peak):
         "workload": "576 slots x history 1024, each call right after a 268 MB dequantize",
         "launches": n_iter, "us": round(avg["ring"], 3), "rolled_us_same_setting": round(avg["roll"], 3),
         "bytes_per_launch": ring_bytes}
+
+    # The ring update fused with the next step's first quantize (the 8192x16384
+    # activation with an e4m3fn slot), against the two launches it replaces:
+    # back to back on the stream, and each form captured as a CUDA graph.
+    slot = 6 * 40 + 1
+    hs = [step.hist.clone(), step.hist.clone()]
+    heads = [torch.full((S,), H - 1, dtype=torch.int32, device=dev) for _ in range(3)]
+    scs = [step.scale.clone() for _ in range(2)]
+    sis = [step.scale_inv.clone() for _ in range(2)]
+    qf = torch.empty(N_ACT, dtype=torch.uint8, device=dev)
+    amf = torch.zeros(2, device=dev)
+    par = {"i": 0}
+
+    def two_calls():
+        f.fp8q_amax_scale_update_ring(hs[0], heads[0], step.amax_new, scs[0], sis[0], f.E4M3FN, f.ALGO_MAX, 0,
+                                      step.slot_format, stream.cuda_stream)
+        f.fp8q_quantize_amax(step.act, qf, f.E4M3FN, scs[0][slot:slot + 1], amf[0:1], stream.cuda_stream)
+
+    def fused():
+        i = par["i"] = par["i"] ^ 1
+        f.fp8q_amax_scale_update_ring_quantize(hs[1], heads[1 + i], heads[2 - i], step.amax_new, scs[1], sis[1],
+                                               step.act, qf, slot, amf[1:2], f.E4M3FN, f.ALGO_MAX, 0,
+                                               step.slot_format, stream.cuda_stream)
+
+    def graph_us(fn, reps=10):
+        with torch.cuda.stream(stream):
+            fn()
+            stream.synchronize()
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream):
+                for _ in range(reps):
+                    fn()
+            gr.replay()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            gr.replay()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) * 1e3 / reps
+
+    out["amax_scale_update_ring_quantize"] = {
+        "workload": "ring update of 576 slots x history 1024 + quantize of the bf16 8192x16384 activation "
+                    "with one slot's new scale",
+        "launches": n_iter,
+        "fused_us": round(timed_loop(fused), 3),
+        "two_launches_us": round(timed_loop(two_calls), 3),
+        "fused_us_graph": round(graph_us(fused), 3),
+        "two_launches_us_graph": round(graph_us(two_calls), 3),
+        "bytes_per_call": 3 * N_ACT + ring_bytes}
+    del qf
     return out
 
 

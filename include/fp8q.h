@@ -1,7 +1,7 @@
 /*
  * fp8q.h -- C ABI of libfp8q: FP8 delayed-scaling quantization on one GPU.
  *
- * Eight operations, each one kernel launch on the caller's stream:
+ * Nine operations, each one kernel launch on the caller's stream:
  *   fp8q_quantize_amax        bf16 -> FP8 bytes, fused with amax = max|x|
  *   fp8q_multi_quantize_amax  the same over a ragged list of tensors
  *   fp8q_dequantize           FP8 bytes -> bf16
@@ -11,6 +11,8 @@
  *   fp8q_amax_scale_update_ring  the update over a ring buffer (no roll)
  *   fp8q_gelu_quantize_amax   GELU producer fused with quantize + amax
  *   fp8q_layernorm_quantize_amax  LayerNorm producer fused with quantize + amax
+ *   fp8q_amax_scale_update_ring_quantize  the ring update fused with the next
+ *                             step's first quantize
  *
  * Sources (web pages, by title and section):
  *   "User Guide on Native XLA-FP8" (NVIDIA JAX-Toolbox): opening section
@@ -261,6 +263,34 @@ fp8q_status fp8q_layernorm_quantize_amax(const void* x_bf16, void* y_bf16, uint8
                                          int32_t hidden, const float* gamma, const float* beta,
                                          float eps, fp8q_format fmt, const float* scale, float* amax,
                                          void* stream);
+
+/*
+ * The ring-buffer update fused with the quantize that follows it, in one
+ * launch: the update sits between one step's amax and the next step's casts
+ * ("Implement fused kernel for FP8 scale update": one launch per update; the
+ * next quantize then needs its new scale), so this call does both:
+ *   fp8q_amax_scale_update_ring(history, heads, ...)   for every slot, then
+ *   fp8q_quantize_amax(x, q, n, fmt, &scale[slot], amax)
+ * with identical results.  The heads come in through head_in (read only) and
+ * go out through head_out (written for every slot; swap the two arrays between
+ * steps).  The quantizing CTAs compute slot `slot`'s new scale themselves from
+ * its history column (without the row the update overwrites) and amax_new,
+ * with the update's own arithmetic, so no CTA waits for another.
+ * amax_history, history_len, num_slots, amax_new, scale, scale_inv,
+ * slot_format, algo, margin: as fp8q_amax_scale_update_ring.  fmt: the FP8
+ * format of q, and the format of slots without slot_format (give slot `slot`
+ * the format of q).  x_bf16, q, n, amax: as fp8q_quantize_amax; amax must not
+ * alias amax_new or the history.  slot: 0 <= slot < num_slots.
+ * Errors: those of both calls, plus FP8Q_ERR_INVALID_ARG for a slot out of
+ * range or head_out equal to head_in.  n == 0 runs only the update.
+ */
+fp8q_status fp8q_amax_scale_update_ring_quantize(float* amax_history, const int32_t* head_in,
+                                                 int32_t* head_out, int32_t history_len, int32_t num_slots,
+                                                 const float* amax_new, float* scale, float* scale_inv,
+                                                 const uint8_t* slot_format, fp8q_format fmt,
+                                                 fp8q_amax_algo algo, int32_t margin, const void* x_bf16,
+                                                 uint8_t* q, int64_t n, int32_t slot, float* amax,
+                                                 void* stream);
 
 /* Static, human-readable name of a status. */
 const char* fp8q_status_string(fp8q_status status);

@@ -187,6 +187,15 @@ def amax_scale_update_ring(hist, head, amax_new, scale, scale_inv, fmt=E4M3FN, a
                                      _ptr(scale_inv), _ptr(sf), fmt, algo, margin)
 
 
+def amax_scale_update_ring_quantize(hist, head, amax_new, scale, scale_inv, x_bf16, slot, fmt=E4M3FN,
+                                    algo=ALGO_MAX, margin=0, slot_format=None, amax=0.0):
+    """The update fused with the next quantize, by its definition: the ring
+    update of every slot (in place on hist, head, scale, scale_inv), then the
+    quantize of x with slot `slot`'s scale after the update.  Returns (q, amax)."""
+    amax_scale_update_ring(hist, head, amax_new, scale, scale_inv, fmt, algo, margin, slot_format)
+    return quantize_amax(x_bf16, fmt, scale[slot], amax)
+
+
 def exp_f32(v):
     return np.float32(lib().orc_exp_f32(float(np.float32(v))))
 

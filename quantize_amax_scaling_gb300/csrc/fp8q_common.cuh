@@ -270,9 +270,9 @@ struct QScale {
     bool fast;    // s in [2^-60, 2^60]
 };
 
-__device__ __forceinline__ QScale make_qscale(const float* scale) {
+__device__ __forceinline__ QScale make_qscale_value(float s) {
     QScale q;
-    q.s = __ldg(scale);
+    q.s = s;
     q.fast = (q.s >= 0x1p-60f) && (q.s <= 0x1p60f);  // false for NaN, <= 0, inf, tiny
     q.r = q.fast ? __frcp_rn(q.s) : 1.0f;
     uint32_t tb = q.fast ? __float_as_uint(q.s * 131072.0f) : 0u;  // exact: s * 2^17
@@ -280,6 +280,8 @@ __device__ __forceinline__ QScale make_qscale(const float* scale) {
     q.t2 = (tb >> 16) | tb;
     return q;
 }
+
+__device__ __forceinline__ QScale make_qscale(const float* scale) { return make_qscale_value(__ldg(scale)); }
 
 template <bool FAST>
 __device__ __forceinline__ float divide(float x, const QScale& c) {
@@ -329,8 +331,9 @@ struct QCursor {
     QScale c;
 };
 
+// A cursor whose scale constants are given (t.scale is not read).
 template <int OUT>
-__device__ __forceinline__ QCursor make_cursor(const QTensor& t, int64_t tile_begin) {
+__device__ __forceinline__ QCursor make_cursor_with(const QTensor& t, int64_t tile_begin, const QScale& c) {
     QCursor k;
     Split sp = split_tensor<typename GeomOf<OUT>::type>((uintptr_t)t.x, (uintptr_t)t.q, t.n);
     k.x = t.x;
@@ -341,8 +344,13 @@ __device__ __forceinline__ QCursor make_cursor(const QTensor& t, int64_t tile_be
     k.nvec = sp.nvec;
     k.mode = sp.mode;
     k.tile_begin = tile_begin;
-    k.c = make_qscale(t.scale);
+    k.c = c;
     return k;
+}
+
+template <int OUT>
+__device__ __forceinline__ QCursor make_cursor(const QTensor& t, int64_t tile_begin) {
+    return make_cursor_with<OUT>(t, tile_begin, make_qscale(t.scale));
 }
 
 // CTA-wide max of the per-thread |x| bits, then one atomic into *amax.

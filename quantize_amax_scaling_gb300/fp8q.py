@@ -23,7 +23,8 @@ STATUS = {0: "FP8Q_OK", 1: "FP8Q_ERR_INVALID_ARG", 2: "FP8Q_ERR_UNSUPPORTED", 3:
 # Every symbol the header declares.
 EXPORTS = ("fp8q_quantize_amax", "fp8q_multi_quantize_amax", "fp8q_dequantize",
            "fp8q_amax_scale_update", "fp8q_qdq_amax", "fp8q_amax_scale_update_ring",
-           "fp8q_gelu_quantize_amax", "fp8q_layernorm_quantize_amax", "fp8q_status_string",
+           "fp8q_gelu_quantize_amax", "fp8q_layernorm_quantize_amax",
+           "fp8q_amax_scale_update_ring_quantize", "fp8q_status_string",
            "fp8q_last_cuda_error")
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfp8q.so")
@@ -66,9 +67,12 @@ def lib() -> ctypes.CDLL:
         L.fp8q_gelu_quantize_amax.argtypes = [vp, vp, vp, i64, c_int, vp, vp, vp]
         L.fp8q_layernorm_quantize_amax.argtypes = [vp, vp, vp, i64, i32, vp, vp, ctypes.c_float, c_int,
                                                    vp, vp, vp]
+        L.fp8q_amax_scale_update_ring_quantize.argtypes = [vp, vp, vp, i32, i32, vp, vp, vp, vp, c_int, c_int,
+                                                           i32, vp, vp, i64, i32, vp, vp]
         for f in ("fp8q_quantize_amax", "fp8q_multi_quantize_amax", "fp8q_dequantize",
                   "fp8q_amax_scale_update", "fp8q_qdq_amax", "fp8q_amax_scale_update_ring",
-                  "fp8q_gelu_quantize_amax", "fp8q_layernorm_quantize_amax"):
+                  "fp8q_gelu_quantize_amax", "fp8q_layernorm_quantize_amax",
+                  "fp8q_amax_scale_update_ring_quantize"):
             getattr(L, f).restype = c_int
         L.fp8q_status_string.argtypes = [c_int]
         L.fp8q_status_string.restype = ctypes.c_char_p
@@ -265,6 +269,36 @@ def fp8q_amax_scale_update_ring(history, head, amax_new, scale, scale_inv, fmt=E
                                              _ptr(scale), _ptr(scale_inv), _ptr(slot_format), fmt,
                                              algo, margin, _stream(stream)),
            "fp8q_amax_scale_update_ring")
+
+
+def fp8q_amax_scale_update_ring_quantize(history, head_in, head_out, amax_new, scale, scale_inv, x, q, slot,
+                                         amax, fmt=E4M3FN, algo=ALGO_MAX, margin=0, slot_format=None,
+                                         stream=None):
+    """The ring-buffer update of every slot, then q = FP8(x / scale[slot]) with the
+    new scale and amax = max(amax, max|x|), in one launch.  head_in is read,
+    head_out written (two int32 [num_slots] arrays, swapped between steps)."""
+    import torch
+    if history.dim() != 2:
+        raise ValueError("history must be [history_len, num_slots]")
+    H, S = history.shape
+    n = _numel(x)
+    if q is not None and _numel(q) != n:
+        raise ValueError("q must have as many elements as x")
+    for t, k, nm in ((history, "f32", "history"), (amax_new, "f32", "amax_new"), (scale, "f32", "scale"),
+                     (scale_inv, "f32", "scale_inv"), (slot_format, "u8", "slot_format"), (x, "bf16", "x"),
+                     (q, "u8", "q"), (amax, "f32", "amax")):
+        _dev(t, k, nm)
+    for t, nm in ((head_in, "head_in"), (head_out, "head_out")):
+        if not (t.is_cuda and t.dtype == torch.int32 and t.is_contiguous()):
+            raise ValueError(f"{nm} must be a contiguous int32 CUDA tensor")
+    for t, nm in ((head_in, "head_in"), (head_out, "head_out"), (amax_new, "amax_new"), (scale, "scale"),
+                  (scale_inv, "scale_inv"), (slot_format, "slot_format")):
+        if t is not None and t.numel() != S:
+            raise ValueError(f"{nm} must have num_slots={S} elements")
+    _check(lib().fp8q_amax_scale_update_ring_quantize(
+        _ptr(history), _ptr(head_in), _ptr(head_out), H, S, _ptr(amax_new), _ptr(scale), _ptr(scale_inv),
+        _ptr(slot_format), fmt, algo, margin, _ptr(x), _ptr(q), n, slot, _ptr(amax), _stream(stream)),
+        "fp8q_amax_scale_update_ring_quantize")
 
 
 def status_string(status: int) -> str:

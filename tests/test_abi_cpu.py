@@ -28,8 +28,8 @@ def test_header_declares_the_four_operations():
     names = declared_functions()
     for f in ("fp8q_quantize_amax", "fp8q_multi_quantize_amax", "fp8q_dequantize",
               "fp8q_amax_scale_update", "fp8q_qdq_amax", "fp8q_amax_scale_update_ring",
-              "fp8q_gelu_quantize_amax", "fp8q_layernorm_quantize_amax", "fp8q_status_string",
-              "fp8q_last_cuda_error"):
+              "fp8q_gelu_quantize_amax", "fp8q_layernorm_quantize_amax",
+              "fp8q_amax_scale_update_ring_quantize", "fp8q_status_string", "fp8q_last_cuda_error"):
         assert f in names
 
 
@@ -145,6 +145,32 @@ def test_ring_update_argument_errors(L):
     for i in (0, 1, 4, 5, 6):
         assert call(i, None) == INVALID
         assert call(i, ctypes.c_void_p(0x10002)) == INVALID
+
+
+def test_ring_update_quantize_argument_errors(L):
+    f = L.fp8q_amax_scale_update_ring_quantize
+    P2 = ctypes.c_void_p(0x20000)
+    #       hist head_in head_out H  S  new sc si  sf  fmt algo margin x  q  n  slot amax stream
+    good = [P, P, P2, 16, 4, P, P, P, None, 0, 0, 0, P, P, 64, 1, P, None]
+    def call(i, v):
+        a = list(good)
+        a[i] = v
+        return f(*a)
+    assert call(3, 0) == INVALID                 # history_len
+    assert call(4, 0) == INVALID                 # num_slots
+    assert call(9, 5) == INVALID                 # fmt
+    assert call(10, 3) == INVALID                # algo
+    assert call(11, 65) == INVALID               # margin
+    for slot in (-1, 4):
+        assert call(15, slot) == INVALID
+    assert call(2, P) == INVALID                 # head_out must differ from head_in
+    for i in (0, 1, 2, 5, 6, 7):
+        assert call(i, None) == INVALID
+        assert call(i, ctypes.c_void_p(0x10002)) == INVALID
+    assert call(14, -1) == INVALID               # n
+    for i in (12, 13, 16):                       # x, q, amax with n > 0
+        assert call(i, None) == INVALID
+    assert call(12, ODD) == INVALID              # bf16 x must be even
 
 
 def test_dequantize_argument_errors(L):

@@ -48,6 +48,7 @@ def test_every_entry_point_is_one_launch():
     hist, new, scale, scale_inv, sf = W.scale_update_inputs(dev)
     head = torch.full((new.numel(),), 1023, dtype=torch.int32, device=dev)
     lg, lb = W.layernorm_params(4096, device=dev)
+    head2 = torch.empty_like(head)
     third = x.numel() // 3
     ws, qs = [x[:third], x[third:]], [q[:third], q[third:]]
     st = s.cuda_stream
@@ -63,6 +64,10 @@ def test_every_entry_point_is_one_launch():
                                                                            st),
         "fused Q->DQ": lambda: fp8q.fp8q_qdq_amax(x, y, fp8q.E4M3FN, sc[3:4], am[3:4], st),
         "GELU + quantize": lambda: fp8q.fp8q_gelu_quantize_amax(x, y, q, fp8q.E4M3FN, sc[0:1], am[0:1], st),
+        "ring update + quantize": lambda: fp8q.fp8q_amax_scale_update_ring_quantize(hist, head, head2, new, scale,
+                                                                                     scale_inv, x, q, 7, am[2:3],
+                                                                                     fp8q.E4M3FN, fp8q.ALGO_MAX,
+                                                                                     0, sf, stream=st),
         "LayerNorm + quantize": lambda: fp8q.fp8q_layernorm_quantize_amax(x.view(256, 4096), y.view(256, 4096),
                                                                          q.view(256, 4096), lg, lb, fp8q.E4M3FN,
                                                                          sc[1:2], am[1:2], stream=st),

@@ -922,3 +922,114 @@ def test_layernorm_close_to_torch_layer_norm(dev):
     y, _, _ = run_layernorm(x, gamma, beta, E4M3FN, 1.0, dev)
     ref = torch.nn.functional.layer_norm(x.float(), (4096,), gamma, beta, eps=1e-6)
     torch.testing.assert_close(y.float(), ref, rtol=2 ** -7, atol=1e-5)
+
+
+# --------------------------------------------------------------------------- update fused with the next quantize
+
+def _fused_case(dev, H, S, slot, n, algo=0, margin=0, per_slot=False, steps=2, seed=0, specials=None,
+                scale0=None):
+    """Run fp8q_amax_scale_update_ring_quantize `steps` times (heads swapped between
+    calls, a new x each step) beside the oracle's update-then-quantize."""
+    rng = np.random.default_rng(seed)
+    hist_np = np.exp(rng.normal(0, 2, (H, S))).astype(np.float32)
+    hist_np[rng.random((H, S)) < 0.02] = 0.0
+    head_np = rng.integers(0, H, S).astype(np.int32)
+    sf_np = (np.arange(S) % 6 >= 4).astype(np.uint8) if per_slot else None
+    fmt = int(sf_np[slot]) if per_slot else E4M3FN
+    s0 = scale0 if scale0 is not None else np.exp(rng.normal(0, 1, S)).astype(np.float32)
+    hist = torch.from_numpy(hist_np.copy()).to(dev)
+    heads = [torch.from_numpy(head_np.copy()).to(dev), torch.full((S,), -7, dtype=torch.int32, device=dev)]
+    sc = torch.from_numpy(s0.copy()).to(dev)
+    si = torch.from_numpy((1.0 / s0).astype(np.float32)).to(dev)
+    sf = None if sf_np is None else torch.from_numpy(sf_np).to(dev)
+    rh, rhead, rs, ri = hist_np.copy(), head_np.copy(), s0.copy(), (1.0 / s0).astype(np.float32)
+    g = torch.Generator(device=dev)
+    for step in range(steps):
+        new_np = np.exp(rng.normal(0, 2, S)).astype(np.float32)
+        if specials is not None:
+            specials(step, new_np, heads[step % 2], rhead)
+        g.manual_seed(seed * 100 + step)
+        x = (torch.randn(n, generator=g, device=dev) * 3.0).to(torch.bfloat16)
+        q = torch.empty(n, dtype=torch.uint8, device=dev)
+        am = f32(0.0, dev)
+        head_in, head_out = heads[step % 2], heads[(step + 1) % 2]
+        before_in = head_in.cpu().numpy().copy()
+        fp8q.fp8q_amax_scale_update_ring_quantize(hist, head_in, head_out, torch.from_numpy(new_np).to(dev), sc,
+                                                  si, x, q, slot, am, fmt, algo, margin, sf)
+        torch.cuda.synchronize()
+        rq, ra = oracle.amax_scale_update_ring_quantize(rh, rhead, new_np, rs, ri, W.bf16_bits(x), slot, fmt,
+                                                        algo, margin, sf_np)
+        what = f"{H}x{S} slot {slot} n {n} algo {algo} margin {margin} step {step}"
+        assert np.array_equal(head_in.cpu().numpy(), before_in), "head_in written: " + what
+        assert np.array_equal(head_out.cpu().numpy(), rhead), "head_out: " + what
+        assert_f32_equal(hist.cpu().numpy(), rh, "history: " + what)
+        assert_f32_equal(sc.cpu().numpy(), rs, "scale: " + what)
+        assert_f32_equal(si.cpu().numpy(), ri, "scale_inv: " + what)
+        assert_codes_equal(q.cpu().numpy(), rq, fmt, "q: " + what)
+        assert_f32_equal([float(am)], [ra], "amax: " + what)
+
+
+@pytest.mark.parametrize("algo", [fp8q.ALGO_MAX, fp8q.ALGO_MOST_RECENT])
+@pytest.mark.parametrize("margin", [0, 1])
+@pytest.mark.parametrize("per_slot", [False, True])
+def test_ring_update_quantize_576_slots(dev, algo, margin, per_slot):
+    for k, slot in enumerate((0, 5, 331, 575)):
+        _fused_case(dev, 1024, 576, slot, [8193, 2 * 65536 + 5, 1, 1 << 20][k], algo, margin, per_slot,
+                    steps=3, seed=11 * k + algo)
+
+
+@pytest.mark.parametrize("H,S", [(1, 5), (2, 3), (16, 2), (17, 7), (3, 577), (1025, 576)])
+def test_ring_update_quantize_shapes(dev, H, S):
+    for slot in sorted({0, S // 2, S - 1}):
+        _fused_case(dev, H, S, slot, 70001, steps=H + 2 if H < 20 else 2, seed=H * 1000 + S + slot)
+
+
+def test_ring_update_quantize_empty_tensor_runs_the_update(dev):
+    _fused_case(dev, 64, 12, 3, 0, steps=2, seed=5)
+
+
+def test_ring_update_quantize_pass_through_and_corrupt_heads(dev):
+    """The slot's new amax 0, NaN or inf keeps its old scale (the quantize uses it);
+    a head outside [0, H) leaves the slot alone and copies its head."""
+    S, slot = 10, 4
+
+    def specials(step, new_np, head_in_dev, ref_head):
+        if step == 0:
+            new_np[slot] = 0.0
+        elif step == 1:
+            new_np[slot] = np.nan
+        elif step == 2:
+            new_np[slot] = np.inf
+        elif step == 3:
+            head_in_dev[slot] = -1
+            ref_head[slot] = -1
+        elif step == 4:
+            head_in_dev[slot] = 32
+            ref_head[slot] = 32
+    _fused_case(dev, 32, S, slot, 9000, steps=5, seed=3, specials=specials)
+
+
+def test_ring_update_quantize_equals_the_two_calls(dev):
+    """Against the library's own ring update followed by its quantize, on the 96-layer
+    history and the full 8192x16384 activation."""
+    hist, new, scale, scale_inv, sf = W.scale_update_inputs(dev)
+    S = new.numel()
+    head = torch.randint(0, hist.shape[0], (S,), dtype=torch.int32, device=dev,
+                         generator=torch.Generator(device=dev).manual_seed(1))
+    x = W.gelu_activation(W.SEED_FFN, dev).reshape(-1)
+    slot = 6 * 40 + 1  # an e4m3fn activation slot
+    h1, hd1, s1, i1 = hist.clone(), head.clone(), scale.clone(), scale_inv.clone()
+    q1 = torch.empty(x.numel(), dtype=torch.uint8, device=dev)
+    a1 = f32(0.0, dev)
+    fp8q.fp8q_amax_scale_update_ring(h1, hd1, new, s1, i1, E4M3FN, fp8q.ALGO_MAX, 0, sf)
+    fp8q.fp8q_quantize_amax(x, q1, E4M3FN, s1[slot:slot + 1], a1)
+    h2, s2, i2 = hist.clone(), scale.clone(), scale_inv.clone()
+    hd2 = torch.empty_like(head)
+    q2 = torch.empty_like(q1)
+    a2 = f32(0.0, dev)
+    fp8q.fp8q_amax_scale_update_ring_quantize(h2, head, hd2, new, s2, i2, x, q2, slot, a2, E4M3FN,
+                                              fp8q.ALGO_MAX, 0, sf)
+    torch.cuda.synchronize()
+    assert torch.equal(hd1, hd2) and torch.equal(h1, h2)
+    assert torch.equal(s1, s2) and torch.equal(i1, i2)
+    assert torch.equal(q1, q2) and float(a1) == float(a2)

@@ -536,6 +536,25 @@ def test_ring_invalid_head_leaves_slot_alone(orc):
     assert hist[2, 2] == 448.0 and sc[2] == 1.0
 
 
+def test_ring_update_then_quantize_hand_example(orc):
+    """The update fused with the next quantize: hand-derived values.  H = 4, S = 2,
+    an empty history with both heads at row 3, new amaxes 2 and 3584: the new
+    entries go to row 0, the windows' maxima are 2 and 3584, so scale[1] = 3584 / 448
+    = 8 and scale[0] = 2 / 448.  x = (8, -16, 448, 1e9, -0) quantized with scale 8:
+    1 -> 0x38, -2 -> 0xC0, 56 -> 0x66 (1.75 * 2^5), 1.25e8 saturates -> 0x7E, -0 -> 0x80."""
+    hist = np.zeros((4, 2), np.float32)
+    head = np.array([3, 3], np.int32)
+    sc = np.ones(2, np.float32)
+    si = np.ones(2, np.float32)
+    x = np.array([0x4100, 0xC180, 0x43E0, 0x4E6E, 0x8000], np.uint16)  # 8, -16, 448, ~1e9, -0 in bf16
+    q, a = orc.amax_scale_update_ring_quantize(hist, head, np.array([2.0, 3584.0], np.float32), sc, si, x, 1)
+    assert list(head) == [0, 0]
+    assert hist[0, 0] == 2.0 and hist[0, 1] == 3584.0 and np.all(hist[1:] == 0.0)
+    assert sc[1] == 8.0 and si[1] == 0.125 and sc[0] == np.float32(2.0) / np.float32(448.0)
+    assert list(q) == [0x38, 0xC0, 0x66, 0x7E, 0x80]
+    assert a == np.float32((np.uint32(0x4E6E) << 16).view(np.float32))
+
+
 # --------------------------------------------------------------------------- GELU producer fused with Q
 
 def _ulp32(x):
