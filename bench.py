@@ -235,7 +235,23 @@ def run_gpu(args, ws, rank, local):
             step.run(stream)
     torch.cuda.synchronize(dev)
 
-    # ---- timed region: K steps back to back, CUDA events only at its two ends
+    # The step is captured as CUDA graphs (its four library kernels and the
+    # amax reset): one graph of G consecutive steps and one of a single step,
+    # replayed so that exactly K steps run, with no host launches between them.
+    G = max(1, min(args.steps, 10))
+    graph_g, graph_1 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph_g, stream=stream):
+            for _ in range(G):
+                step.run(stream)
+        with torch.cuda.graph(graph_1, stream=stream):
+            step.run(stream)
+        for _ in range(args.warmup):
+            graph_1.replay()
+        graph_g.replay()
+    torch.cuda.synchronize(dev)
+
+    # ---- timed region: K graph replays back to back, CUDA events only at its two ends
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
@@ -243,8 +259,10 @@ def run_gpu(args, ws, rank, local):
     torch.cuda.synchronize(dev)
     with torch.cuda.stream(stream):
         start.record(stream)
-        for _ in range(args.steps):
-            step.run(stream)
+        for _ in range(args.steps // G):
+            graph_g.replay()
+        for _ in range(args.steps % G):
+            graph_1.replay()
         end.record(stream)
     while not end.query():          # sample clocks while the GPU runs the timed steps
         clocks.sample()
@@ -253,6 +271,20 @@ def run_gpu(args, ws, rank, local):
     barrier()
     t_rank = start.elapsed_time(end) / 1e3          # seconds for all K steps on this rank
     value, t_max = aggregate_throughput(STEP_BYTES * args.steps, t_rank, ws)
+
+    # ---- the same K steps launched kernel by kernel from the host (eager)
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        e_start.record(stream)
+        for _ in range(args.steps):
+            step.run(stream)
+        e_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    eager_value, eager_t = aggregate_throughput(STEP_BYTES * args.steps, e_start.elapsed_time(e_end) / 1e3, ws)
 
     # ---- the same K steps again with an event around every kernel, for the
     # per-kernel breakdown and the roofline.  An event between two kernels
@@ -306,11 +338,16 @@ def run_gpu(args, ws, rank, local):
         "dtype": "f32",
         "data": "synthetic (seeded; shapes of the FFN/MLP and 96-layer workloads)",
         "config": {"workload": WORKLOAD, "step_bytes": STEP_BYTES,
-                   "timing": "value and ms_per_step: K steps with CUDA events only around the region; "
-                             "kernels and roofline: a second pass of K steps with an event around each kernel",
+                   "timing": "value and ms_per_step: K steps replayed from CUDA graphs (10 steps per graph, "
+                             "plus single-step replays for a remainder), CUDA events only around the region; "
+                             "eager: the same K steps launched "
+                             "kernel by kernel; kernels and roofline: a third pass of K eager steps with an "
+                             "event around each kernel",
                    "l2": "inputs larger than L2 (each step streams 1.21 GB; the 129 MB L2 holds none of "
                          "a step's inputs when it is read again)",
                    "parallelism": f"replicas x{ws} (no collective)"},
+        "eager": {"value": round(eager_value, 1), "unit": "GB/s",
+                  "ms_per_step": round(eager_t / args.steps * 1e3, 4)},
         "headline": {"quantize_amax_gbs": round(q_gbs, 1), "quantize_amax_frac_of_peak": round(q_gbs / peak, 4),
                      "scale_update_us": round(avg["amax_scale_update"], 3),
                      "scale_update_us_in_graph": graph["scale_update_us_after_dequantize"] if graph else None,
