@@ -43,10 +43,18 @@ __device__ __forceinline__ float2 exp2_rr(float2 v) {
     p = fma2_rn(p, r, splat2(0.5f));
     p = fma2_rn(p, r, splat2(1.0f));
     p = fma2_rn(p, r, splat2(1.0f));
-    const int k0 = __float_as_int(t.x) - __float_as_int(0x1.8p23f);  // k, in [-29, 128]
-    const int k1 = __float_as_int(t.y) - __float_as_int(0x1.8p23f);
-    const float2 s = make_float2(__int_as_float((k0 + 126) << 23), __int_as_float((k1 + 126) << 23));
+    // 2^(k-1) from the bits of t: k = bits(t) - bits(1.5 * 2^23), in [-29, 128], and
+    // ((k + 126) << 23) = bits(t) * 2^23 + (126 - bits(1.5 * 2^23)) * 2^23 (mod 2^32)
+    constexpr uint32_t kScaleBias = (126u - 0x4B400000u) << 23;
+    const float2 s = make_float2(__uint_as_float(__float_as_uint(t.x) * (1u << 23) + kScaleBias),
+                                 __uint_as_float(__float_as_uint(t.y) * (1u << 23) + kScaleBias));
     return mul2_rn(mul2_rn(p, s), splat2(2.0f));
+}
+
+__device__ __forceinline__ float max_nan(float a, float b) {
+    float d;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+    return d;
 }
 
 // Two bf16 (one word) -> two bf16 of GELU (one word).
@@ -55,9 +63,11 @@ __device__ __forceinline__ uint32_t gelu_pair(uint32_t w) {
     const float2 x2 = mul2_rn(x, x);
     const float2 sx = mul2_rn(x, fma2_rn(splat2(0x1.6e4e26p-5f), x2, splat2(1.0f)));  // x (1 + 0.044715 x^2)
     const float2 d = add2_rn(splat2(1.0f), exp2_rr(mul2_rn(splat2(-0x1.988454p+0f), sx)));
-    const float2 g = mul2_rn(x, rcp2_rn(d));  // d >= 1
-    // GELU(-inf) is the limit -0 (x * 0 would be NaN); NaN stays NaN
-    return cvt_bf16x2(x.x == -INFINITY ? -0.0f : g.x, x.y == -INFINITY ? -0.0f : g.y);
+    // x * (1 / d) with d >= 1.  GELU(-inf) is the limit -0: there d = inf and 1/d = 0,
+    // so x is first raised to -FLT_MAX (-FLT_MAX * 0 = -0); max.NaN keeps a NaN.
+    const float2 g = mul2_rn(make_float2(max_nan(x.x, -0x1.fffffep127f), max_nan(x.y, -0x1.fffffep127f)),
+                             rcp2_rn(d));
+    return cvt_bf16x2(g.x, g.y);
 }
 
 struct GeluGeom {
