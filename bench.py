@@ -367,6 +367,7 @@ def run_gpu(args, ws, rank, local):
     }
     if not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args.cpu_sample_frac)
+        out["cpu_baseline_all_cores"] = cpu_baseline_all_cores(args.cpu_sample_frac)
     return out
 
 
@@ -824,6 +825,39 @@ def cpu_baseline(frac: float):
     return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": desc, "seconds": round(dt, 3),
             "host": f"{os.uname().machine}, {os.cpu_count()} cores present"}
+
+
+def cpu_baseline_all_cores(frac: float):
+    """The same oracle sample split over every host core: each elementwise tensor in
+    contiguous chunks, one thread per chunk (the oracle's C calls release the GIL;
+    amax is a max, so the results are those of the whole-tensor calls), then the
+    576-slot update once."""
+    import numpy as np
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+    inp, nbytes, desc = _oracle_sample(frac)
+    n = max(1, os.cpu_count() or 1)
+    s = np.float32(0.0091)
+
+    def bounds(a, i):
+        return a.size * i // n, a.size * (i + 1) // n
+
+    def work(i):
+        lo, hi = bounds(inp["act"], i)
+        oracle.quantize_amax(inp["act"][lo:hi], oracle.E4M3FN, s)
+        lo, hi = bounds(inp["w"], i)
+        oracle.quantize_amax(inp["w"][lo:hi], oracle.E4M3FN, s)
+        lo, hi = bounds(inp["gq"], i)
+        oracle.dequantize(inp["gq"][lo:hi], oracle.E5M2, s)
+
+    with ThreadPoolExecutor(n) as ex:
+        t0 = time.perf_counter()
+        list(ex.map(work, range(n)))
+        oracle.amax_scale_update(inp["hist"], inp["new"], inp["scale"], inp["scale_inv"], oracle.E4M3FN,
+                                 oracle.ALGO_MAX, 0, inp["sf"])
+        dt = time.perf_counter() - t0
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": n, "kind": "oracle, chunks on threads",
+            "sample": desc, "seconds": round(dt, 3)}
 
 
 def run_reference(args):

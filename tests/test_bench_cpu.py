@@ -70,3 +70,11 @@ def test_warmup_below_three_is_rejected():
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
                           "--warmup", "2"], capture_output=True, text=True, timeout=300, cwd=ROOT)
     assert out.returncode != 0
+
+
+def test_cpu_baseline_all_cores_runs_the_same_sample():
+    import bench
+    one = bench.cpu_baseline(0.002)
+    many = bench.cpu_baseline_all_cores(0.002)
+    assert many["sample"] == one["sample"]
+    assert many["cores"] == (os.cpu_count() or 1) and many["value"] > 0
