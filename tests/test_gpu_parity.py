@@ -1033,3 +1033,23 @@ def test_ring_update_quantize_equals_the_two_calls(dev):
     assert torch.equal(hd1, hd2) and torch.equal(h1, h2)
     assert torch.equal(s1, s2) and torch.equal(i1, i2)
     assert torch.equal(q1, q2) and float(a1) == float(a2)
+
+
+def test_fp32_max_grad_example_on_the_gpu(dev):
+    """The worked example of the section "Gradient accumulation of FP8 params": x = 2,
+    amax history [0, 0, 0], scale 1, three in_qdq iterations accumulating amax with
+    max, then one update of the length-3 history."""
+    x = torch.full((1,), 2.0, dtype=torch.bfloat16, device=dev)
+    y = torch.empty_like(x)
+    am = f32(0.0, dev)
+    for _ in range(3):
+        fp8q.fp8q_qdq_amax(x, y, E4M3FN, f32(1.0, dev), am)
+        torch.cuda.synchronize()
+        assert float(y) == 2.0
+    assert float(am) == 2.0
+    hist = torch.zeros(3, 1, device=dev)
+    sc, si = torch.ones(1, device=dev), torch.ones(1, device=dev)
+    fp8q.fp8q_amax_scale_update(hist, am, sc, si)
+    torch.cuda.synchronize()
+    assert hist[:, 0].tolist() == [2.0, 0.0, 0.0]
+    assert sc.cpu().numpy()[0] == np.float32(2.0) / np.float32(448.0)

@@ -536,6 +536,27 @@ def test_ring_invalid_head_leaves_slot_alone(orc):
     assert hist[2, 2] == 448.0 and sc[2] == 1.0
 
 
+def test_fp32_max_grad_example_accumulates_with_max(orc):
+    """The worked example of "User Guide on Native XLA-FP8", section "Gradient
+    accumulation of FP8 params": x = 2, amax history [0, 0, 0], scaling factor 1,
+    three in_qdq iterations.  Each round trip returns 2 exactly (2 is an e4m3fn
+    value); the amax seen over the three iterations, accumulated with max as the
+    section asks, is 2 (an add would give 6); one update then puts it at the
+    front of the length-3 history and sets the scale to RN(2 / 448)."""
+    x = np.array([0x4000], np.uint16)  # 2.0 in bf16
+    amax = np.float32(0.0)
+    for _ in range(3):
+        y, amax = orc.qdq_amax(x, E4M3FN, np.float32(1.0), amax)
+        assert list(y) == [0x4000]
+    assert amax == np.float32(2.0)
+    hist = np.zeros((3, 1), np.float32)
+    sc = np.ones(1, np.float32)
+    si = np.ones(1, np.float32)
+    orc.amax_scale_update(hist, np.array([amax], np.float32), sc, si)
+    assert list(hist[:, 0]) == [2.0, 0.0, 0.0]
+    assert sc[0] == np.float32(2.0) / np.float32(448.0) and si[0] == np.float32(1.0) / sc[0]
+
+
 def test_ring_update_then_quantize_hand_example(orc):
     """The update fused with the next quantize: hand-derived values.  H = 4, S = 2,
     an empty history with both heads at row 3, new amaxes 2 and 3584: the new
