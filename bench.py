@@ -349,8 +349,13 @@ def run_gpu(args, ws, rank, local):
         "eager": {"value": round(eager_value, 1), "unit": "GB/s",
                   "ms_per_step": round(eager_t / args.steps * 1e3, 4)},
         "headline": {"quantize_amax_gbs": round(q_gbs, 1), "quantize_amax_frac_of_peak": round(q_gbs / peak, 4),
-                     "scale_update_us": round(avg["amax_scale_update"], 3),
-                     "scale_update_us_in_graph": graph["scale_update_us_after_dequantize"] if graph else None,
+                     # device time of one 576-slot call: measured in CUDA graphs when the
+                     # extras run, else the eager figure with its event overhead
+                     "scale_update_us": (graph["scale_update_us_after_dequantize"] if graph
+                                         else round(avg["amax_scale_update"], 3)),
+                     "scale_update_us_how": ("CUDA graphs: (dequantize + update) pairs minus dequantize alone"
+                                             if graph else "eager, an event on each side of the call"),
+                     "scale_update_us_eager_events": round(avg["amax_scale_update"], 3),
                      "scale_update_launches_per_call": 1},
         "kernels": kernels,
         "roofline": {"kernel": "quantize_amax_kernel (8192x16384 bf16 -> e4m3fn + amax)",
