@@ -144,7 +144,8 @@ __device__ __forceinline__ void gelu_tile(const GeluArgs& a, const QScale& c, in
 }
 
 // At most 64 registers, so four CTAs share an SM: the exp chain is long, and
-// the extra warps hide its latency (measured 155 us against 175 us with three).
+// the extra warps hide its latency (measured on 8192x16384 while the kernel
+// still used the IEEE reciprocal: 155 us against 175 us with three).
 template <int FMT, bool WRITE_Y>
 __global__ void __launch_bounds__(kThreads, 4) gelu_quantize_amax_kernel(const GeluArgs a) {
     __shared__ uint32_t red[kThreads / 32];
