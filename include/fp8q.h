@@ -251,8 +251,9 @@ fp8q_status fp8q_gelu_quantize_amax(const void* h_bf16, void* y_bf16, uint8_t* q
  * (it does not in correct operation), the call leaves *amax holding the bit
  * pattern 0x7FFFFFFF, a NaN that no bf16 data can produce, and the outputs
  * incomplete.  The first call on a device also sets the kernel's shared-memory
- * limit (cudaFuncSetAttribute) and reads its occupancy; make it outside CUDA
- * graph capture.
+ * limit (cudaFuncSetAttribute) and reads its occupancy.  Those are host-side
+ * calls, not stream work, so that first call may itself be captured in a CUDA
+ * graph.
  * Errors: FP8Q_ERR_INVALID_ARG for a bad fmt, rows < 0, hidden < 16 or not a
  * multiple of 16, a NULL pointer (other than y_bf16) with rows > 0, or a
  * misaligned scale/amax; FP8Q_ERR_UNSUPPORTED for hidden > 16384 or a

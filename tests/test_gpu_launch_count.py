@@ -5,10 +5,12 @@ through the driver API: a call that launched two kernels, or a kernel plus
 a memset, would show up as more than one node.
 """
 import ctypes
+import os
 
 import pytest
 import torch
 
+from conftest import ROOT
 from quantize_amax_scaling_gb300 import fp8q
 from quantize_amax_scaling_gb300 import workloads as W
 
@@ -79,3 +81,34 @@ def test_every_entry_point_is_one_launch():
     for name, fn in calls.items():
         kernels, nodes = _graph_nodes(fn, s)
         assert (kernels, nodes) == (1, 1), (name, kernels, nodes)
+
+
+@pytest.mark.gpu
+def test_layernorm_first_call_inside_graph_capture():
+    """The LayerNorm call's first use on a device (function attribute, occupancy query)
+    may itself be captured: in a fresh process, capture it, replay, and compare with an
+    eager call."""
+    import subprocess
+    import sys
+    code = r'''
+import torch
+from quantize_amax_scaling_gb300 import fp8q, workloads as W
+dev = torch.device("cuda:0")
+x = W.residual_stream(seed=1, device=dev, shape=(64, 4096))
+g, b = W.layernorm_params(4096, device=dev)
+sc = torch.full((1,), 0.02, device=dev)
+q, am = torch.empty(x.shape, dtype=torch.uint8, device=dev), torch.zeros(1, device=dev)
+gr = torch.cuda.CUDAGraph()
+with torch.cuda.graph(gr, stream=torch.cuda.Stream()):
+    fp8q.fp8q_layernorm_quantize_amax(x, None, q, g, b, fp8q.E4M3FN, sc, am)
+gr.replay()
+torch.cuda.synchronize()
+q2, am2 = torch.empty_like(q), torch.zeros(1, device=dev)
+fp8q.fp8q_layernorm_quantize_amax(x, None, q2, g, b, fp8q.E4M3FN, sc, am2)
+torch.cuda.synchronize()
+assert torch.equal(q, q2) and float(am) == float(am2)
+print("OK")
+'''
+    env = dict(os.environ, PYTHONPATH=ROOT + os.pathsep + os.environ.get("PYTHONPATH", ""))
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300, env=env)
+    assert r.returncode == 0 and r.stdout.strip().endswith("OK"), r.stdout + r.stderr
