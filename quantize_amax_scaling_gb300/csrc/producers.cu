@@ -89,13 +89,12 @@ struct GeluArgs {
     int mode;
 };
 
+// The 16 results y of vector v: store y (optional), fold |y| into m2, store
+// their FP8 codes.
 template <int FMT, bool FAST, bool WRITE_Y>
-__device__ __forceinline__ void gelu_vec_store(const GeluArgs& a, const QScale& c, int64_t v, const uint4& wa,
-                                               const uint4& wb, uint32_t& m2) {
+__device__ __forceinline__ void gelu_emit(const GeluArgs& a, const QScale& c, int64_t v, const uint4& ya,
+                                          const uint4& yb, uint32_t& m2) {
     constexpr int E = GeluGeom::kVecElems;
-    uint4 ya, yb;
-    ya.x = gelu_pair(wa.x); ya.y = gelu_pair(wa.y); ya.z = gelu_pair(wa.z); ya.w = gelu_pair(wa.w);
-    yb.x = gelu_pair(wb.x); yb.y = gelu_pair(wb.y); yb.z = gelu_pair(wb.z); yb.w = gelu_pair(wb.w);
     if (WRITE_Y) {
         uint16_t* yp = a.y + a.head + v * E;
         st_v4(yp, ya);
@@ -109,6 +108,15 @@ __device__ __forceinline__ void gelu_vec_store(const GeluArgs& a, const QScale& 
     o.z = quant_quad<FMT, FAST>(yb.x, yb.y, c);
     o.w = quant_quad<FMT, FAST>(yb.z, yb.w, c);
     st_v4(a.q + a.head + v * E, o);
+}
+
+template <int FMT, bool FAST, bool WRITE_Y>
+__device__ __forceinline__ void gelu_vec_store(const GeluArgs& a, const QScale& c, int64_t v, const uint4& wa,
+                                               const uint4& wb, uint32_t& m2) {
+    uint4 ya, yb;
+    ya.x = gelu_pair(wa.x); ya.y = gelu_pair(wa.y); ya.z = gelu_pair(wa.z); ya.w = gelu_pair(wa.w);
+    yb.x = gelu_pair(wb.x); yb.y = gelu_pair(wb.y); yb.z = gelu_pair(wb.z); yb.w = gelu_pair(wb.w);
+    gelu_emit<FMT, FAST, WRITE_Y>(a, c, v, ya, yb, m2);
 }
 
 template <int FMT, bool FAST, bool WRITE_Y>
@@ -171,6 +179,94 @@ __global__ void __launch_bounds__(kThreads, 4) gelu_quantize_amax_kernel(const G
         else        gelu_tile<FMT, false, WRITE_Y>(a, c, tile, wa, wb, m2, ms);
     }
     flush_amax(m2, ms, a.amax, red);
+}
+
+// ----------------------------------------------------------------------------
+// GELU through a table of every bf16 input
+//
+// y = bf16(GELU(h)) depends only on the 16 bits of h.  For large tensors each
+// CTA first computes all 65536 values with gelu_pair -- the arithmetic of the
+// kernel above, so the same bits -- into shared memory (128 KB), then streams
+// its share of the tensor with one shared-memory lookup per element in place
+// of the GELU arithmetic.  One CTA per SM (the table fills most of the shared
+// memory), looping over the vectors four at a time so that enough loads are in
+// flight.  Building the table costs each SM about what 65536 elements cost
+// the direct kernel, so smaller tensors, and any that take the
+// element-by-element path, use the direct kernel.
+
+// threads per CTA: 1024 for the codes alone; 512 when y is stored too (its
+// extra registers would spill at 1024)
+template <bool WRITE_Y>
+__host__ __device__ constexpr int gelu_table_threads() { return WRITE_Y ? 512 : 1024; }
+constexpr uint32_t kGeluTableBytes = 65536u * 2u;
+// Fewer elements take the direct kernel (measured crossovers on GB300: the
+// table wins from about 2^24 elements for the codes alone, 2^26 with y).
+constexpr int64_t kGeluTableMinElems = (int64_t)1 << 24;
+constexpr int64_t kGeluTableMinElemsWithY = (int64_t)1 << 26;
+constexpr int kGeluTableUnroll = 4;
+
+__device__ __forceinline__ uint32_t gelu_lookup_pair(const uint16_t* tab, uint32_t w) {
+    return (uint32_t)tab[w & 0xFFFFu] | ((uint32_t)tab[w >> 16] << 16);
+}
+
+__device__ __forceinline__ uint4 gelu_lookup4(const uint16_t* tab, const uint4& w) {
+    return make_uint4(gelu_lookup_pair(tab, w.x), gelu_lookup_pair(tab, w.y), gelu_lookup_pair(tab, w.z),
+                      gelu_lookup_pair(tab, w.w));
+}
+
+template <int FMT, bool WRITE_Y>
+__global__ void __launch_bounds__(gelu_table_threads<WRITE_Y>(), 1)
+    gelu_table_quantize_amax_kernel(const GeluArgs a) {
+    constexpr int kGeluTableThreads = gelu_table_threads<WRITE_Y>();
+    extern __shared__ __align__(16) uint32_t tab32[];  // word p: the results for inputs 2p and 2p + 1
+    __shared__ uint32_t red[kGeluTableThreads / 32];
+    for (int p = threadIdx.x; p < 32768; p += kGeluTableThreads)
+        tab32[p] = gelu_pair((uint32_t)(2 * p) | ((uint32_t)(2 * p + 1) << 16));
+    const QScale c = make_qscale(a.scale);
+    __syncthreads();
+    const uint16_t* tab = reinterpret_cast<const uint16_t*>(tab32);
+    constexpr int E = GeluGeom::kVecElems;
+    const int64_t stride = (int64_t)gridDim.x * kGeluTableThreads;
+    uint32_t m2 = 0, ms = 0;
+    for (int64_t v0 = (int64_t)blockIdx.x * kGeluTableThreads + threadIdx.x; v0 < a.nvec;
+         v0 += kGeluTableUnroll * stride) {
+        uint4 wa[kGeluTableUnroll], wb[kGeluTableUnroll];
+#pragma unroll
+        for (int u = 0; u < kGeluTableUnroll; ++u) {
+            const int64_t v = v0 + u * stride;
+            if (v < a.nvec) ld_stream_v8(a.h + a.head + v * E, wa[u], wb[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < kGeluTableUnroll; ++u) {
+            const int64_t v = v0 + u * stride;
+            if (v < a.nvec) {
+                const uint4 ya = gelu_lookup4(tab, wa[u]), yb = gelu_lookup4(tab, wb[u]);
+                if (c.fast) gelu_emit<FMT, true, WRITE_Y>(a, c, v, ya, yb, m2);
+                else        gelu_emit<FMT, false, WRITE_Y>(a, c, v, ya, yb, m2);
+            }
+        }
+    }
+    if (blockIdx.x == 0) {  // scalar head and tail, each shorter than one vector
+        const int64_t tail0 = a.head + a.nvec * E;
+        const int64_t nscalar = a.head + (a.n - tail0);
+        for (int64_t j = threadIdx.x; j < nscalar; j += kGeluTableThreads) {
+            const int64_t i = j < a.head ? j : tail0 + (j - a.head);
+            const uint32_t yw = tab[a.h[i]];
+            if (WRITE_Y) a.y[i] = (uint16_t)yw;
+            ms = max(ms, abs_bits_lo(yw));
+            a.q[i] = (uint8_t)((c.fast ? quant_pair<FMT, true>(yw, c) : quant_pair<FMT, false>(yw, c)) & 0xFFu);
+        }
+    }
+    // CTA-wide max of |y|, one atomic
+    uint32_t m = max(max(abs_bits_lo(m2), m2 & 0x7FFF0000u), ms);
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t b = red[0];
+        for (int w = 1; w < kGeluTableThreads / 32; ++w) b = max(b, red[w]);
+        atomicMax(reinterpret_cast<int*>(a.amax), (int)b);
+    }
 }
 
 // ----------------------------------------------------------------------------
@@ -550,6 +646,40 @@ fp8q_status launch_layernorm(const LnArgs& a, cudaStream_t s) {
     return launch_layernorm_hpt<FMT, WRITE_Y, 8>(a, s);
 }
 
+template <int FMT, bool WRITE_Y>
+fp8q_status launch_gelu_table(const GeluArgs& a, cudaStream_t s) {
+    static ResidentCache cache;
+    constexpr int kGeluTableThreads = gelu_table_threads<WRITE_Y>();
+    auto kern = gelu_table_quantize_amax_kernel<FMT, WRITE_Y>;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    int ctas = 0;
+    if (err == cudaSuccess) {
+        std::lock_guard<std::mutex> lock(cache.mu);
+        for (int k = 0; k < cache.n; ++k)
+            if (cache.e[k].dev == dev) ctas = cache.e[k].ctas;
+        if (ctas == 0) {
+            err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGeluTableBytes);
+            int per_sm = 0, sms = 0;
+            if (err == cudaSuccess)
+                err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kGeluTableThreads,
+                                                                    kGeluTableBytes);
+            if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            if (err == cudaSuccess && per_sm < 1) err = cudaErrorInvalidConfiguration;
+            if (err == cudaSuccess) {
+                ctas = per_sm * sms;
+                if (cache.n < 32) cache.e[cache.n++] = {dev, kGeluTableBytes, ctas};
+            }
+        }
+    }
+    if (err != cudaSuccess) return cuda_fail(err, "gelu_table_quantize_amax_kernel setup");
+    const int64_t per_cta = (int64_t)kGeluTableThreads * kGeluTableUnroll;
+    const int64_t need = (a.nvec + per_cta - 1) / per_cta;
+    const int grid = (int)(need < ctas ? (need > 0 ? need : 1) : ctas);
+    kern<<<grid, kGeluTableThreads, kGeluTableBytes, s>>>(a);
+    return after_launch("gelu_table_quantize_amax_kernel");
+}
+
 }  // namespace
 
 // ----------------------------------------------------------------------------
@@ -585,6 +715,11 @@ fp8q_status fp8q_gelu_quantize_amax(const void* h_bf16, void* y_bf16, uint8_t* q
     a.mode = sp.mode;
     const int grid = (int)(sp.tiles < 0x7FFFFFFF ? sp.tiles : 0x7FFFFFFF);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (sp.mode == kModeVec && n >= (y_bf16 ? kGeluTableMinElemsWithY : kGeluTableMinElems)) {
+        if (fmt == FP8Q_E4M3FN)
+            return y_bf16 ? launch_gelu_table<FP8Q_E4M3FN, true>(a, s) : launch_gelu_table<FP8Q_E4M3FN, false>(a, s);
+        return y_bf16 ? launch_gelu_table<FP8Q_E5M2, true>(a, s) : launch_gelu_table<FP8Q_E5M2, false>(a, s);
+    }
     if (fmt == FP8Q_E4M3FN) {
         if (y_bf16) gelu_quantize_amax_kernel<FP8Q_E4M3FN, true><<<grid, kThreads, 0, s>>>(a);
         else        gelu_quantize_amax_kernel<FP8Q_E4M3FN, false><<<grid, kThreads, 0, s>>>(a);

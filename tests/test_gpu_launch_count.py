@@ -51,6 +51,8 @@ def test_every_entry_point_is_one_launch():
     head = torch.full((new.numel(),), 1023, dtype=torch.int32, device=dev)
     lg, lb = W.layernorm_params(4096, device=dev)
     head2 = torch.empty_like(head)
+    xl = W.mlp_activation(2, dev, (4096, 4096)).reshape(-1)   # 2^24 elements: the GELU table path
+    ql = torch.empty(xl.numel(), dtype=torch.uint8, device=dev)
     third = x.numel() // 3
     ws, qs = [x[:third], x[third:]], [q[:third], q[third:]]
     st = s.cuda_stream
@@ -66,6 +68,8 @@ def test_every_entry_point_is_one_launch():
                                                                            st),
         "fused Q->DQ": lambda: fp8q.fp8q_qdq_amax(x, y, fp8q.E4M3FN, sc[3:4], am[3:4], st),
         "GELU + quantize": lambda: fp8q.fp8q_gelu_quantize_amax(x, y, q, fp8q.E4M3FN, sc[0:1], am[0:1], st),
+        "GELU + quantize, table path": lambda: fp8q.fp8q_gelu_quantize_amax(xl, None, ql, fp8q.E4M3FN, sc[0:1],
+                                                                          am[0:1], st),
         "ring update + quantize": lambda: fp8q.fp8q_amax_scale_update_ring_quantize(hist, head, head2, new, scale,
                                                                                      scale_inv, x, q, 7, am[2:3],
                                                                                      fp8q.E4M3FN, fp8q.ALGO_MAX,

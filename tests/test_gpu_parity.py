@@ -1053,3 +1053,41 @@ def test_fp32_max_grad_example_on_the_gpu(dev):
     torch.cuda.synchronize()
     assert hist[:, 0].tolist() == [2.0, 0.0, 0.0]
     assert sc.cpu().numpy()[0] == np.float32(2.0) / np.float32(448.0)
+
+
+def test_gelu_table_path_every_bf16_pattern(dev):
+    """Large tensors take the table path (every bf16 result computed once per SM into
+    shared memory): 2^24 elements and more for the codes alone, 2^26 with y.  All
+    65536 patterns, repeated to those sizes, against the oracle."""
+    pat = W.all_bf16_patterns(dev)
+    pb = W.bf16_bits(pat)
+    for k, (fmt, s) in enumerate([(E4M3FN, 1.0), (E5M2, 0.37), (E4M3FN, 2.0 ** 70), (E5M2, 3.0e-5),
+                                  (E4M3FN, 0.0), (E4M3FN, math.nan)]):
+        want_y = k % 2 == 0
+        reps = 1024 if want_y else 256                    # 2^26 or 2^24 elements
+        h = pat.repeat(reps)
+        y, q, am = run_gelu(h, fmt, s, dev, want_y=want_y)
+        rq, ry, _ = oracle.gelu_quantize_amax(pb, fmt, np.float32(s))
+        assert_codes_equal(q.cpu().numpy(), np.tile(rq, reps), fmt, f"table q, scale {s!r}")
+        if y is not None:
+            assert_bf16_equal(W.bf16_bits(y), np.tile(ry, reps), f"table y, scale {s!r}")
+        del h, y, q
+
+
+def test_gelu_table_path_unaligned_head_and_tail(dev):
+    n, off = (1 << 26) + 13, 3
+    g = torch.Generator(device=dev)
+    g.manual_seed(17)
+    hbuf = (torch.randn(n + 16, generator=g, device=dev) * 4.0).to(torch.bfloat16)
+    h = hbuf[off: off + n]
+    qbuf, q = guarded(n, torch.uint8, dev, off)
+    ybuf, y = guarded(n, torch.bfloat16, dev, off, fill=0x5A5A)
+    am = f32(0.0, dev)
+    fp8q.fp8q_gelu_quantize_amax(h, y, q, E4M3FN, f32(0.021, dev), am)
+    torch.cuda.synchronize()
+    rq, ry, ra = oracle.gelu_quantize_amax(W.bf16_bits(h), E4M3FN, np.float32(0.021))
+    assert_codes_equal(q.cpu().numpy(), rq, E4M3FN, "table path unaligned q")
+    assert_bf16_equal(W.bf16_bits(y), ry, "table path unaligned y")
+    assert_f32_equal([float(am)], [ra], "table path amax")
+    check_guards(qbuf, n, off)
+    check_guards(ybuf, n, off, fill=0x5A5A)
