@@ -189,7 +189,8 @@ __global__ void __launch_bounds__(kThreads, 4) gelu_quantize_amax_kernel(const G
 // kernel above, so the same bits -- into shared memory (128 KB), then streams
 // its share of the tensor with one shared-memory lookup per element in place
 // of the GELU arithmetic.  One CTA per SM (the table fills most of the shared
-// memory), looping over the vectors four at a time so that enough loads are in
+// memory), looping over the vectors two at a time, with the next two already
+// loading while the current two are converted, so that enough loads are in
 // flight.  Building the table costs each SM about what 65536 elements cost
 // the direct kernel, so smaller tensors, and any that take the
 // element-by-element path, use the direct kernel.
@@ -203,7 +204,7 @@ constexpr uint32_t kGeluTableBytes = 65536u * 2u;
 // table wins from about 2^24 elements for the codes alone, 2^26 with y).
 constexpr int64_t kGeluTableMinElems = (int64_t)1 << 24;
 constexpr int64_t kGeluTableMinElemsWithY = (int64_t)1 << 26;
-constexpr int kGeluTableUnroll = 4;
+constexpr int kGeluTableUnroll = 2;
 
 __device__ __forceinline__ uint32_t gelu_lookup_pair(const uint16_t* tab, uint32_t w) {
     return (uint32_t)tab[w & 0xFFFFu] | ((uint32_t)tab[w >> 16] << 16);
@@ -228,13 +229,20 @@ __global__ void __launch_bounds__(gelu_table_threads<WRITE_Y>(), 1)
     constexpr int E = GeluGeom::kVecElems;
     const int64_t stride = (int64_t)gridDim.x * kGeluTableThreads;
     uint32_t m2 = 0, ms = 0;
-    for (int64_t v0 = (int64_t)blockIdx.x * kGeluTableThreads + threadIdx.x; v0 < a.nvec;
-         v0 += kGeluTableUnroll * stride) {
-        uint4 wa[kGeluTableUnroll], wb[kGeluTableUnroll];
+    int64_t v0 = (int64_t)blockIdx.x * kGeluTableThreads + threadIdx.x;
+    uint4 wa[kGeluTableUnroll], wb[kGeluTableUnroll];
+#pragma unroll
+    for (int u = 0; u < kGeluTableUnroll; ++u) {
+        const int64_t v = v0 + u * stride;
+        if (v < a.nvec) ld_stream_v8(a.h + a.head + v * E, wa[u], wb[u]);
+    }
+    for (; v0 < a.nvec; v0 += kGeluTableUnroll * stride) {
+        uint4 na[kGeluTableUnroll], nb[kGeluTableUnroll];
+        const int64_t v1 = v0 + kGeluTableUnroll * stride;
 #pragma unroll
         for (int u = 0; u < kGeluTableUnroll; ++u) {
-            const int64_t v = v0 + u * stride;
-            if (v < a.nvec) ld_stream_v8(a.h + a.head + v * E, wa[u], wb[u]);
+            const int64_t v = v1 + u * stride;
+            if (v < a.nvec) ld_stream_v8(a.h + a.head + v * E, na[u], nb[u]);
         }
 #pragma unroll
         for (int u = 0; u < kGeluTableUnroll; ++u) {
@@ -244,6 +252,11 @@ __global__ void __launch_bounds__(gelu_table_threads<WRITE_Y>(), 1)
                 if (c.fast) gelu_emit<FMT, true, WRITE_Y>(a, c, v, ya, yb, m2);
                 else        gelu_emit<FMT, false, WRITE_Y>(a, c, v, ya, yb, m2);
             }
+        }
+#pragma unroll
+        for (int u = 0; u < kGeluTableUnroll; ++u) {
+            wa[u] = na[u];
+            wb[u] = nb[u];
         }
     }
     if (blockIdx.x == 0) {  // scalar head and tail, each shorter than one vector
