@@ -352,6 +352,39 @@ __device__ __forceinline__ void st_cs_v2(void* p, uint2 v) {
     asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y));
 }
 
+// s = s + x and q = fma(x, x, q) for x the low (LO) or high half of a word of
+// two bf16, with the mixed-precision add.f32.bf16 / fma.f32.bf16 (PTX,
+// sm_100 and later): the bf16 operand is widened exactly, so the results are
+// those of the binary32 add and fma on the widened value.
+template <bool LO>
+__device__ __forceinline__ void acc_bf16(uint32_t w, float& s, float& q) {
+    if (LO)
+        asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+            "add.rn.f32.bf16 %0, lo, %0;\n\tfma.rn.f32.bf16 %1, lo, lo, %1;\n\t}"
+            : "+f"(s), "+f"(q)
+            : "r"(w));
+    else
+        asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+            "add.rn.f32.bf16 %0, hi, %0;\n\tfma.rn.f32.bf16 %1, hi, hi, %1;\n\t}"
+            : "+f"(s), "+f"(q)
+            : "r"(w));
+}
+
+// x + c for x the low (LO) or high bf16 half of w, widened exactly.
+template <bool LO>
+__device__ __forceinline__ float add_bf16(uint32_t w, float c) {
+    float d;
+    if (LO)
+        asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.bf16 %0, lo, %2;\n\t}"
+            : "=f"(d)
+            : "r"(w), "f"(c));
+    else
+        asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.bf16 %0, hi, %2;\n\t}"
+            : "=f"(d)
+            : "r"(w), "f"(c));
+    return d;
+}
+
 // Phase 1: (-mean, rstd) of one row (nv vectors in shared memory), computed by
 // one warp in the fixed summation order.  Lane p holds summation lanes
 // k0 + 4m of group j (p = 4j + k0); its vectors are those lanes' vectors
@@ -386,17 +419,9 @@ __device__ __forceinline__ float2 ln_row_stats(const uint8_t* row, int nv, int H
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const float x0 = __uint_as_float(w[m][e] << 16);
-                    s[m0 + m] = __fadd_rn(s[m0 + m], x0);
-                    q[m0 + m] = __fmaf_rn(x0, x0, q[m0 + m]);
-                }
+                for (int m = 0; m < 4; ++m) acc_bf16<true>(w[m][e], s[m0 + m], q[m0 + m]);
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const float x1 = __uint_as_float(w[m][e] & 0xFFFF0000u);
-                    s[m0 + m] = __fadd_rn(s[m0 + m], x1);
-                    q[m0 + m] = __fmaf_rn(x1, x1, q[m0 + m]);
-                }
+                for (int m = 0; m < 4; ++m) acc_bf16<false>(w[m][e], s[m0 + m], q[m0 + m]);
             }
         }
     }
@@ -439,8 +464,7 @@ __device__ __forceinline__ uint4 ln_normalize8(uint4 w, const float2 (&g)[4], co
     uint32_t out[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        const float2 x = make_float2(__uint_as_float(in[k] << 16), __uint_as_float(in[k] & 0xFFFF0000u));
-        const float2 d = add2_rn(x, nmean);
+        const float2 d = make_float2(add_bf16<true>(in[k], nmean.x), add_bf16<false>(in[k], nmean.y));
         const float2 m = mul2_rn(rstd, g[k]);
         out[k] = cvt_bf16x2(__fadd_rn(__fmul_rn(d.x, m.x), b[k].x), __fadd_rn(__fmul_rn(d.y, m.y), b[k].y));
     }
