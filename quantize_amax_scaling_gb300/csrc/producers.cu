@@ -457,7 +457,8 @@ __device__ __forceinline__ float2 ln_row_stats(const uint8_t* row, int nv, int H
 
 // Eight bf16 of x (one uint4) -> eight bf16 of y:
 // y = ((x + (-mean)) * (rstd * gamma)) + beta, each step rounded on its own
-// (x + (-mean) is x - mean); the first two steps two lanes at a time.
+// (x + (-mean) is x - mean, taken with x as a bf16 operand; rstd * gamma two
+// lanes at a time).
 __device__ __forceinline__ uint4 ln_normalize8(uint4 w, const float2 (&g)[4], const float2 (&b)[4],
                                                float2 nmean, float2 rstd) {
     const uint32_t in[4] = {w.x, w.y, w.z, w.w};
