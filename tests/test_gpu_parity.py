@@ -1091,3 +1091,34 @@ def test_gelu_table_path_unaligned_head_and_tail(dev):
     assert_f32_equal([float(am)], [ra], "table path amax")
     check_guards(qbuf, n, off)
     check_guards(ybuf, n, off, fill=0x5A5A)
+
+
+def test_gelu_table_path_more_than_2_pow_31_elements(dev):
+    """The table path's vector and tail arithmetic stays 64-bit: 2^31 + 19 elements, with y,
+    made of every finite bf16 pattern repeated, so each output is checked through its
+    pattern and the amax is known exactly."""
+    pat = W.all_bf16_patterns(dev)
+    pb = W.bf16_bits(pat)
+    pf = (pb.astype(np.uint32) << 16).view(np.float32)
+    keep = ~np.isnan(pf)
+    fin = torch.from_numpy(pb[keep].view(np.int16).copy()).view(torch.bfloat16).to(dev)
+    m = fin.numel()
+    n = (1 << 31) + 19
+    h = fin.repeat(n // m + 1)[:n].contiguous()
+    y = torch.empty(n, dtype=torch.bfloat16, device=dev)
+    q = torch.empty(n, dtype=torch.uint8, device=dev)
+    am = f32(0.0, dev)
+    scale = np.float32(0.0123)
+    fp8q.fp8q_gelu_quantize_amax(h, y, q, E4M3FN, f32(scale, dev), am)
+    torch.cuda.synchronize()
+    rq, ry, ra = oracle.gelu_quantize_amax(pb[keep], E4M3FN, scale)
+    assert_f32_equal([float(am)], [ra], "amax over 2^31 + 19 elements")
+    rng = np.random.default_rng(5)
+    idx = np.unique(np.concatenate([np.arange(4096), np.arange(n - 8192, n),
+                                    rng.integers((1 << 31) - 8192, n, 4096), rng.integers(0, n, 60000)]))
+    assert idx.min() >= 0 and idx.max() < n          # checked on the host before the gather
+    it = torch.from_numpy(idx).to(dev)
+    assert_codes_equal(q[it].cpu().numpy(), rq[idx % m], E4M3FN, "table path n > 2^31")
+    assert_bf16_equal(W.bf16_bits(y[it]), ry[idx % m], "table path n > 2^31 y")
+    del h, y, q
+    torch.cuda.empty_cache()
