@@ -307,7 +307,8 @@ def run_gpu(args, ws, rank, local):
     avg = {n: sum(v) / len(v) for n, v in per.items()}
     kbytes = {"quantize_amax": BYTES_QUANT, "multi_quantize_amax": BYTES_MULTI,
               "dequantize": BYTES_DEQ, "amax_scale_update": UPDATE_BYTES}
-    kernels = {n: {"us": round(avg[n], 3), "GB/s": round(kbytes[n] / (avg[n] * 1e-6) / 1e9, 1),
+    kernels = {n: {"us": round(avg[n], 3), "us_median": round(statistics.median(per[n]), 3),
+                   "GB/s": round(kbytes[n] / (avg[n] * 1e-6) / 1e9, 1),
                    "frac_of_peak": round(kbytes[n] / (avg[n] * 1e-6) / 1e9 / peak, 4)}
                for n in per}
     q_gbs = kbytes["quantize_amax"] / (avg["quantize_amax"] * 1e-6) / 1e9
