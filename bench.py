@@ -219,6 +219,30 @@ class Step:
             events[4].record(stream)
 
 
+    def run_branched(self, stream, side):
+        """The same step for graph capture, with the three streaming kernels on parallel
+        branches (they touch disjoint tensors): forked after the amax reset, joined before
+        the update that reads their amaxes, so one kernel's ramp and tail overlap another's."""
+        import torch
+        f = self.fp8q
+        self.amax_new[:3].zero_()
+        fork = torch.cuda.Event()
+        fork.record(stream)
+        for s in side:
+            s.wait_event(fork)
+        f.fp8q_quantize_amax(self.act, self.q_act, f.E4M3FN, self.scale[0:1], self.amax_new[0:1],
+                             stream.cuda_stream)
+        f.fp8q_multi_quantize_amax(self.w, self.q_w, f.E4M3FN, [self.scale[1:2], self.scale[2:3]],
+                                   [self.amax_new[1:2], self.amax_new[2:3]], side[0].cuda_stream)
+        f.fp8q_dequantize(self.grad_q, self.y_grad, f.E5M2, self.scale[4:5], side[1].cuda_stream)
+        for s in side:
+            join = torch.cuda.Event()
+            join.record(s)
+            stream.wait_event(join)
+        f.fp8q_amax_scale_update(self.hist, self.amax_new, self.scale, self.scale_inv, f.E4M3FN,
+                                 f.ALGO_MAX, 0, self.slot_format, stream.cuda_stream)
+
+
 def run_gpu(args, ws, rank, local):
     import torch
     import torch.distributed as dist
@@ -238,14 +262,17 @@ def run_gpu(args, ws, rank, local):
     # The step is captured as CUDA graphs (its four library kernels and the
     # amax reset): one graph of G consecutive steps and one of a single step,
     # replayed so that exactly K steps run, with no host launches between them.
+    # Within a step the three streaming kernels are parallel branches joined
+    # before the update (run_branched); steps follow one another in order.
     G = max(1, min(args.steps, 10))
+    side = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
     graph_g, graph_1 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
         with torch.cuda.graph(graph_g, stream=stream):
             for _ in range(G):
-                step.run(stream)
+                step.run_branched(stream, side)
         with torch.cuda.graph(graph_1, stream=stream):
-            step.run(stream)
+            step.run_branched(stream, side)
         for _ in range(args.warmup):
             graph_1.replay()
         graph_g.replay()
@@ -340,7 +367,9 @@ def run_gpu(args, ws, rank, local):
         "data": "synthetic (seeded; shapes of the FFN/MLP and 96-layer workloads)",
         "config": {"workload": WORKLOAD, "step_bytes": STEP_BYTES,
                    "timing": "value and ms_per_step: K steps replayed from CUDA graphs (10 steps per graph, "
-                             "plus single-step replays for a remainder), CUDA events only around the region; "
+                             "plus single-step replays for a remainder; in each step quantize, multi-tensor "
+                             "quantize and dequantize are parallel branches joined before the update), "
+                             "CUDA events only around the region; "
                              "eager: the same K steps launched "
                              "kernel by kernel; kernels and roofline: a third pass of K eager steps with an "
                              "event around each kernel",
@@ -378,7 +407,7 @@ def run_gpu(args, ws, rank, local):
 
 
 def measure_graph(args, step, stream, dev):
-    """The step captured once as a CUDA graph and replayed K times.
+    """The step captured once as a CUDA graph, kernels in launch order, and replayed.
 
     Per-kernel events in the eager loop stop each launch from overlapping the
     previous kernel's tail, which costs a few microseconds per kernel and shows
@@ -425,8 +454,9 @@ def measure_graph(args, step, stream, dev):
             "GB/s": round(STEP_BYTES / (step_us * 1e-6) / 1e9, 1),
             "scale_update_us_after_dequantize": round(pair_us - deq_us, 3),
             "ring_update_us_after_dequantize": round(ring_pair_us - deq_us, 3),
-            "how": "one step captured as a CUDA graph, CUDA events around the replay; the update's "
-                   "time is (dequantize+update) pairs minus dequantize alone, both as graphs"}
+            "how": "one step captured as a CUDA graph, its kernels in launch order (no branches), "
+                   "CUDA events around the replay; the update's time is (dequantize+update) pairs "
+                   "minus dequantize alone, both as graphs"}
 
 
 def measure_next_rows(args, step, stream, dev, peak):
