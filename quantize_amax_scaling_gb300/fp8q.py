@@ -105,10 +105,13 @@ _FP8_DTYPES = None
 
 
 def _dev(t, kind, name):
-    """Reject anything but a contiguous CUDA tensor of the right element type.
+    """Reject anything but a contiguous CUDA tensor of the right element type
+    on the current CUDA device.
 
     Pointers reach the kernels unchanged, so a host tensor must never get
-    through.  ``kind`` is "bf16", "u8" (uint8 or a float8 dtype) or "f32".
+    through, and the library launches on the current device, so a tensor on
+    another GPU must not either.  ``kind`` is "bf16", "u8" (uint8 or a float8
+    dtype), "f32" or "i32".
     """
     global _FP8_DTYPES
     if t is None:
@@ -116,13 +119,18 @@ def _dev(t, kind, name):
     import torch
     if _FP8_DTYPES is None:
         _FP8_DTYPES = (torch.uint8, torch.float8_e4m3fn, torch.float8_e5m2)
-    ok = {"bf16": (torch.bfloat16,), "u8": _FP8_DTYPES, "f32": (torch.float32,)}[kind]
+    ok = {"bf16": (torch.bfloat16,), "u8": _FP8_DTYPES, "f32": (torch.float32,),
+          "i32": (torch.int32,)}[kind]
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
     if t.dtype not in ok:
         raise ValueError(f"{name} has dtype {t.dtype}, expected one of {ok}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+    cur = torch.cuda.current_device()
+    if t.device.index != cur:
+        raise ValueError(f"{name} is on {t.device} but the current CUDA device is cuda:{cur}; "
+                         "the kernels launch on the current device (wrap the call in torch.cuda.device)")
 
 
 def _numel(t):
@@ -194,6 +202,8 @@ def fp8q_multi_quantize_amax(xs, qs, fmt, scales, amaxes, stream=None):
     views into one vector) aligned with ``xs``.
     """
     count = len(xs)
+    if not (len(qs) == len(scales) == len(amaxes) == count):
+        raise ValueError("xs, qs, scales and amaxes must have the same length")
     arr = (Tensor * max(1, count))()
     for i in range(count):
         n = _numel(xs[i])
@@ -251,16 +261,15 @@ def fp8q_amax_scale_update_ring(history, head, amax_new, scale, scale_inv, fmt=E
     ``history`` is float32 [history_len, num_slots]; ``head`` is int32 [num_slots],
     the row of each slot's newest entry.
     """
-    import torch
     if history.dim() != 2:
         raise ValueError("history must be [history_len, num_slots]")
     H, S = history.shape
-    for t, k, nm in ((history, "f32", "history"), (amax_new, "f32", "amax_new"),
+    for t, k, nm in ((history, "f32", "history"), (head, "i32", "head"), (amax_new, "f32", "amax_new"),
                      (scale, "f32", "scale"), (scale_inv, "f32", "scale_inv"),
                      (slot_format, "u8", "slot_format")):
+        if t is None and nm == "head":
+            raise ValueError("head must be a contiguous int32 CUDA tensor")
         _dev(t, k, nm)
-    if not (head.is_cuda and head.dtype == torch.int32 and head.is_contiguous()):
-        raise ValueError("head must be a contiguous int32 CUDA tensor")
     for t, nm in ((head, "head"), (amax_new, "amax_new"), (scale, "scale"), (scale_inv, "scale_inv"),
                   (slot_format, "slot_format")):
         if t is not None and t.numel() != S:
@@ -277,7 +286,6 @@ def fp8q_amax_scale_update_ring_quantize(history, head_in, head_out, amax_new, s
     """The ring-buffer update of every slot, then q = FP8(x / scale[slot]) with the
     new scale and amax = max(amax, max|x|), in one launch.  head_in is read,
     head_out written (two int32 [num_slots] arrays, swapped between steps)."""
-    import torch
     if history.dim() != 2:
         raise ValueError("history must be [history_len, num_slots]")
     H, S = history.shape
@@ -289,8 +297,9 @@ def fp8q_amax_scale_update_ring_quantize(history, head_in, head_out, amax_new, s
                      (q, "u8", "q"), (amax, "f32", "amax")):
         _dev(t, k, nm)
     for t, nm in ((head_in, "head_in"), (head_out, "head_out")):
-        if not (t.is_cuda and t.dtype == torch.int32 and t.is_contiguous()):
+        if t is None:
             raise ValueError(f"{nm} must be a contiguous int32 CUDA tensor")
+        _dev(t, "i32", nm)
     for t, nm in ((head_in, "head_in"), (head_out, "head_out"), (amax_new, "amax_new"), (scale, "scale"),
                   (scale_inv, "scale_inv"), (slot_format, "slot_format")):
         if t is not None and t.numel() != S:

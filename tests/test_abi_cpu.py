@@ -216,6 +216,25 @@ def test_binding_refuses_host_tensors():
         fp8q.fp8q_amax_scale_update(torch.zeros(4, 2), s.expand(2), s.expand(2), s.expand(2))
 
 
+def test_binding_refuses_tensors_on_another_device(monkeypatch):
+    """The library launches on the current device: a tensor on another GPU is refused."""
+    import types
+    import torch
+    from quantize_amax_scaling_gb300 import fp8q
+
+    def fake(dtype, index):
+        return types.SimpleNamespace(is_cuda=True, dtype=dtype, is_contiguous=lambda: True,
+                                     device=torch.device("cuda", index), numel=lambda: 8)
+
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 0)
+    fp8q._dev(fake(torch.bfloat16, 0), "bf16", "x")  # on the current device: accepted
+    with pytest.raises(ValueError, match="current CUDA device"):
+        fp8q._dev(fake(torch.bfloat16, 1), "bf16", "x")
+    with pytest.raises(ValueError, match="current CUDA device"):
+        fp8q.fp8q_quantize_amax(fake(torch.bfloat16, 0), fake(torch.uint8, 0), fp8q.E4M3FN,
+                                fake(torch.float32, 1), fake(torch.float32, 0))
+
+
 def test_product_code_never_touches_the_oracle():
     """The package (kernels, binding, build) neither imports, includes nor links the oracle."""
     pkg = os.path.join(ROOT, "quantize_amax_scaling_gb300")
