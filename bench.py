@@ -346,6 +346,9 @@ def run_gpu(args, ws, rank, local):
     # ---- rows beyond the step (fused Q->DQ, ring history), timed on their own after it
     next_rows = None if args.no_extras else measure_next_rows(args, step, stream, dev, peak)
 
+    # ---- the other quantize workloads: MLP activation (L2 flushed) and the ragged list
+    other_configs = None if args.no_extras else measure_other_configs(step, stream, dev, peak)
+
     # ---- end to end through the public API with host buffers
     e2e = run_e2e(args, step, stream, dev) if not args.no_e2e else None
 
@@ -395,6 +398,7 @@ def run_gpu(args, ws, rank, local):
                      "unit": "GB/s", "frac": round(q_gbs / peak, 4), "traffic": traffic},
         "graph": graph,
         "next_rows": next_rows,
+        "other_configs": other_configs,
         "gpu_launches": KERNELS_PER_STEP * args.steps,
         "other_launches": {"torch fill (zero the step's 3 amax slots)": args.steps},
         "clocks": clocks.summary(),
@@ -457,6 +461,83 @@ def measure_graph(args, step, stream, dev):
             "how": "one step captured as a CUDA graph, its kernels in launch order (no branches), "
                    "CUDA events around the replay; the update's time is (dequantize+update) pairs "
                    "minus dequantize alone, both as graphs"}
+
+
+def measure_other_configs(step, stream, dev, peak, warm=20, reps=20):
+    """Two more quantize workloads, each launch timed on its own (median of `reps`).
+
+    - The MLP input activation, bf16 8192x4096 N(0,1) with 0.1% outliers x100,
+      e4m3fn with the scale of the previous step's amax: its 100.7 MB of
+      traffic is close to the L2 size, so a 256 MB buffer passes through L2
+      before every launch and the kernel always starts from a cold L2.  Timed
+      twice: after READING the buffer (L2 holds clean lines that leave for
+      free) and after WRITING it (L2 full of dirty lines that the kernel's own
+      traffic has to write back first, as after a producer kernel).
+    - The ragged list of twelve bf16 N(0,1) tensors (2048x12288 .. 12288x4096,
+      465.6 M elements) in one multi-tensor launch with the first twelve slot
+      scales of the step; 1.4 GB per launch, far larger than L2.
+    Algorithmic bytes: 3 per element (bf16 in, FP8 out).
+    """
+    import torch
+    from quantize_amax_scaling_gb300 import workloads as W
+    f = step.fp8q
+    st = stream.cuda_stream
+    out = {}
+
+    def median_us(launch, before=None):
+        times = []
+        with torch.cuda.stream(stream):
+            for _ in range(warm):
+                if before:
+                    before()
+                launch()
+            for _ in range(reps):
+                if before:
+                    before()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                launch()
+                e1.record(stream)
+                times.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        return statistics.median(a.elapsed_time(b) * 1e3 for a, b in times)
+
+    prev = W.mlp_activation(W.SEED_MLP + 1, dev)
+    sc = (prev.float().abs().max() / 448.0).reshape(1)
+    del prev
+    x = W.mlp_activation(W.SEED_MLP, dev).reshape(-1)
+    q = torch.empty(x.numel(), dtype=torch.uint8, device=dev)
+    am = torch.zeros(1, device=dev)
+    flush = torch.zeros(64 * 1024 * 1024, dtype=torch.int32, device=dev)   # 256 MB, twice the L2
+    nbytes = 3 * x.numel()
+    launch = lambda: f.fp8q_quantize_amax(x, q, f.E4M3FN, sc, am, st)
+    for key, before, how in (("mlp_activation", lambda: flush.sum(), "cold, clean: 256 MB read before every launch"),
+                             ("mlp_activation_after_writes", flush.zero_,
+                              "cold, dirty: 256 MB written before every launch")):
+        us = median_us(launch, before=before)
+        gbs = nbytes / (us * 1e-6) / 1e9
+        out[key] = {"workload": "bf16 8192x4096 N(0,1), 0.1% outliers x100 -> e4m3fn + amax",
+                    "l2": how, "launches_timed": reps, "us_median": round(us, 3), "GB/s": round(gbs, 1),
+                    "frac_of_peak": round(gbs / peak, 4), "bytes_per_launch": nbytes}
+    del x, q, flush
+
+    xs = [t.reshape(-1) for t in W.ragged_tensors(dev)]
+    qs = [torch.empty(t.numel(), dtype=torch.uint8, device=dev) for t in xs]
+    ams = torch.zeros(len(xs), device=dev)
+    scales = [step.scale[i:i + 1] for i in range(len(xs))]
+    amaxes = [ams[i:i + 1] for i in range(len(xs))]
+    us = median_us(lambda: f.fp8q_multi_quantize_amax(xs, qs, f.E4M3FN, scales, amaxes, st))
+    nbytes = 3 * sum(t.numel() for t in xs)
+    gbs = nbytes / (us * 1e-6) / 1e9
+    out["ragged_twelve_tensors"] = {"workload": "12 bf16 N(0,1) tensors 2048x12288 .. 12288x4096 "
+                                                "(465.6 M elements) -> e4m3fn + 12 amaxes, one launch",
+                                    "l2": "inputs larger than L2", "launches_timed": reps,
+                                    "us_median": round(us, 3), "GB/s": round(gbs, 1),
+                                    "frac_of_peak": round(gbs / peak, 4), "bytes_per_launch": nbytes}
+    del xs, qs
+    torch.cuda.empty_cache()
+    return out
 
 
 def measure_next_rows(args, step, stream, dev, peak):
