@@ -185,15 +185,16 @@ __global__ void __launch_bounds__(kThreads, 4) gelu_quantize_amax_kernel(const G
 // GELU through a table of every bf16 input
 //
 // y = bf16(GELU(h)) depends only on the 16 bits of h.  For large tensors each
-// CTA first computes all 65536 values with gelu_pair -- the arithmetic of the
-// kernel above, so the same bits -- into shared memory (128 KB), then streams
-// its share of the tensor with one shared-memory lookup per element in place
-// of the GELU arithmetic.  One CTA per SM (the table fills most of the shared
-// memory), looping over the vectors two at a time, with the next two already
-// loading while the current two are converted, so that enough loads are in
-// flight.  Building the table costs each SM about what 65536 elements cost
-// the direct kernel, so smaller tensors, and any that take the
-// element-by-element path, use the direct kernel.
+// CTA first gets all 65536 values, computed with gelu_pair -- the arithmetic
+// of the kernel above, so the same bits -- into shared memory (128 KB); the
+// CTAs of a thread-block cluster compute them once between them.  It then
+// streams its share of the tensor with one shared-memory lookup per element
+// in place of the GELU arithmetic.  One CTA per SM (the table fills most of
+// the shared memory), looping over the vectors two at a time, with the next
+// two already loading while the current two are converted, so that enough
+// loads are in flight.  Building the table costs each cluster about what
+// 65536 elements cost the direct kernel, so smaller tensors, and any that
+// take the element-by-element path, use the direct kernel.
 
 // threads per CTA: 1024 for the codes alone; 512 when y is stored too (its
 // extra registers would spill at 1024)
