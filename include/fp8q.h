@@ -43,7 +43,9 @@
  *   - Errors are returned as fp8q_status, never raised or aborted.  Argument
  *     errors are detected before anything is launched.  FP8Q_ERR_CUDA means
  *     the launch itself failed; fp8q_last_cuda_error() (per thread) then
- *     describes it.  A zero-sized call succeeds and launches nothing.
+ *     describes it, and the error has been taken off the CUDA runtime's
+ *     per-thread last error (cudaGetLastError) so that it is reported once.
+ *     A zero-sized call succeeds and launches nothing.
  */
 #ifndef FP8Q_H
 #define FP8Q_H

@@ -9,6 +9,11 @@ thread_local char g_last_error[256] = "";
 fp8q_status cuda_fail(cudaError_t e, const char* where) {
     std::snprintf(g_last_error, sizeof g_last_error, "%s: %s (%s)", where, cudaGetErrorName(e),
                   cudaGetErrorString(e));
+    // The failing runtime call also left e as the thread's last CUDA error.
+    // Consume it here, where it is reported, so that the next launch check
+    // (this library's or the caller's) does not report it a second time.
+    // A sticky error (a lost context) stays set whatever is done here.
+    (void)cudaGetLastError();
     return FP8Q_ERR_CUDA;
 }
 
