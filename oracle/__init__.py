@@ -8,6 +8,7 @@ bf16 tensors are numpy ``uint16`` arrays of bit patterns; FP8 tensors are
 ``uint8`` code arrays.
 """
 import ctypes
+import math
 import os
 
 import numpy as np
@@ -57,18 +58,16 @@ def lib():
         L.orc_dequantize.restype = None
         L.orc_qdq_amax.argtypes = [vp, i64, ctypes.c_int, f32, vp, vp]
         L.orc_qdq_amax.restype = None
-        L.orc_exp_f32.argtypes = [f32]
-        L.orc_exp_f32.restype = f32
-        L.orc_gelu_f32.argtypes = [f32]
-        L.orc_gelu_f32.restype = f32
-        L.orc_gelu_quantize_amax.argtypes = [vp, i64, ctypes.c_int, f32, vp, vp, vp]
-        L.orc_gelu_quantize_amax.restype = None
-        L.orc_layernorm_stats.argtypes = [vp, i32, f32, vp, vp]
-        L.orc_layernorm_stats.restype = None
-        L.orc_layernorm_quantize_amax.argtypes = [vp, i64, i32, vp, vp, f32, ctypes.c_int, f32, vp, vp, vp]
-        L.orc_layernorm_quantize_amax.restype = None
-        L.orc_gelu_amax.argtypes = [vp, i64]
-        L.orc_gelu_amax.restype = f32
+        L.orc_f64_to_bf16.argtypes = [ctypes.c_double]
+        L.orc_f64_to_bf16.restype = ctypes.c_uint16
+        L.orc_f64_to_bf16_array.argtypes = [vp, i64, vp]
+        L.orc_f64_to_bf16_array.restype = None
+        L.orc_gelu_ref.argtypes = [ctypes.c_double]
+        L.orc_gelu_ref.restype = ctypes.c_double
+        L.orc_gelu_ref_array.argtypes = [vp, i64, vp]
+        L.orc_gelu_ref_array.restype = None
+        L.orc_layernorm_ref.argtypes = [vp, i64, i32, vp, vp, ctypes.c_double, vp, vp, vp]
+        L.orc_layernorm_ref.restype = None
         L.orc_amax_scale_update.argtypes = [vp, i32, i32, vp, vp, vp, vp, ctypes.c_int,
                                             ctypes.c_int, i32]
         L.orc_amax_scale_update.restype = None
@@ -196,48 +195,159 @@ def amax_scale_update_ring_quantize(hist, head, amax_new, scale, scale_inv, x_bf
     return quantize_amax(x_bf16, fmt, scale[slot], amax)
 
 
-def exp_f32(v):
-    return np.float32(lib().orc_exp_f32(float(np.float32(v))))
+def f64_to_bf16(g):
+    """float64 value -> nearest bf16 bit pattern (ties to even), one rounding."""
+    return int(lib().orc_f64_to_bf16(float(g)))
 
 
-def gelu_f32(x):
-    return np.float32(lib().orc_gelu_f32(float(np.float32(x))))
+def gelu_ref(x):
+    """GELU (tanh form) of one value in float64."""
+    return float(lib().orc_gelu_ref(float(x)))
 
 
-def gelu_quantize_amax(h_bf16, fmt, scale, amax=0.0):
-    """Return (q codes, bf16 bits of y = GELU(h), amax float32)."""
+def gelu_ref_array(h_bf16):
+    """GELU (tanh form) in float64 of every bf16 input."""
     h = _c_u16(h_bf16).reshape(-1)
-    q = np.empty(h.shape, np.uint8)
-    y = np.empty(h.shape, np.uint16)
-    a = np.array([amax], np.float32)
-    lib().orc_gelu_quantize_amax(_ptr(h), h.size, fmt, float(np.float32(scale)), _ptr(q), _ptr(y), _ptr(a))
-    return q, y, np.float32(a[0])
+    g = np.empty(h.shape, np.float64)
+    lib().orc_gelu_ref_array(_ptr(h), h.size, _ptr(g))
+    return g
 
 
-def gelu_amax(h_bf16):
-    """max|bf16(GELU(h))| over the whole tensor."""
-    h = _c_u16(h_bf16).reshape(-1)
-    return np.float32(lib().orc_gelu_amax(_ptr(h), h.size))
+def layernorm_ref(x_bf16, H, gamma, beta, eps=1e-6):
+    """LayerNorm (Flax defaults) in float64 of rows of H bf16 values.
 
-
-def layernorm_stats(row_bf16, eps=1e-6):
-    """(mean, rstd) of one bf16 row, in the fixed summation order."""
-    r = _c_u16(row_bf16).reshape(-1)
-    m = np.zeros(1, np.float32)
-    rs = np.zeros(1, np.float32)
-    lib().orc_layernorm_stats(_ptr(r), r.size, float(np.float32(eps)), _ptr(m), _ptr(rs))
-    return m[0], rs[0]
-
-
-def layernorm_quantize_amax(x_bf16, H, gamma, beta, fmt, scale, eps=1e-6, amax=0.0):
-    """Return (q codes, bf16 bits of y = LayerNorm(x), amax) for rows of H elements."""
+    Returns (y float64 [rows*H], mean float64 [rows], rstd float64 [rows])."""
     x = _c_u16(x_bf16).reshape(-1)
     assert x.size % H == 0
+    rows = x.size // H
     g = np.ascontiguousarray(gamma, np.float32)
     b = np.ascontiguousarray(beta, np.float32)
-    q = np.empty(x.shape, np.uint8)
-    y = np.empty(x.shape, np.uint16)
-    a = np.array([amax], np.float32)
-    lib().orc_layernorm_quantize_amax(_ptr(x), x.size // H, H, _ptr(g), _ptr(b), float(np.float32(eps)), fmt,
-                                      float(np.float32(scale)), _ptr(q), _ptr(y), _ptr(a))
-    return q, y, np.float32(a[0])
+    y = np.empty(x.size, np.float64)
+    mean = np.empty(rows, np.float64)
+    rstd = np.empty(rows, np.float64)
+    lib().orc_layernorm_ref(_ptr(x), rows, H, _ptr(g), _ptr(b), float(eps), _ptr(y), _ptr(mean), _ptr(rstd))
+    return y, mean, rstd
+
+
+# --------------------------------------------------------------------------- producer tolerances
+#
+# The fused producers compute in binary32 and round to bf16; the definitions
+# above are float64.  A kernel's y is accepted when it is the bf16 rounding of
+# some value within E of the float64 value r: RN(r - E) <= y <= RN(r + E)
+# (RN is monotone).  Wherever r lies farther than E from every bf16 rounding
+# boundary, that leaves exactly one value, RN(r).  E is derived from the
+# binary32 arithmetic below; u = 2^-24 is binary32's unit roundoff.
+
+U32 = 2.0 ** -24
+GELU_TINY = 2.0 ** -122
+
+
+def gelu_tolerance(h_f64, r):
+    """E for y = bf16(GELU(h)) evaluated in binary32.
+
+    The binary32 evaluation x / (1 + e^v), v = -2 sqrt(2/pi) x (1 + 0.044715 x^2):
+    v carries at most 6u relative error (the constants' roundings and three
+    operations), so e^v carries 6u|v| from its argument plus at most 7u of
+    its own (range reduction, a degree-6 polynomial whose truncation stays
+    under 3u, Horner roundings); 1 + e^v, the reciprocal and the final
+    product add u each.  So |error| <= (6|v| + 10) u |GELU| while
+    1 / (1 + e^v) is a normal binary32.  Where |GELU| < 2^-122 that
+    reciprocal is subnormal or zero (|x| <= 10.6 there), and y may be any
+    value within 2^-122 of r.
+    """
+    h = np.asarray(h_f64, np.float64)
+    r = np.asarray(r, np.float64)
+    with np.errstate(over="ignore", invalid="ignore"):
+        v = np.minimum(np.abs(2.0 * math.sqrt(2.0 / math.pi) * h * (1.0 + 0.044715 * h * h)), 89.0)
+    v = np.where(np.isfinite(v), v, 89.0)
+    e = (6.0 * v + 10.0) * U32 * np.abs(r)
+    return np.where(np.abs(r) < GELU_TINY, np.maximum(e, GELU_TINY), e)
+
+
+def layernorm_chain_bound(H):
+    """D: the longest chain of binary32 additions in either row sum that the
+    tolerance below allows (H / 128 + 32)."""
+    return H // 128 + 32
+
+
+def layernorm_tolerance(x_f64, gamma, beta, eps, mean, rstd, r):
+    """E for y = bf16(LayerNorm(x) * gamma + beta) evaluated in binary32.
+
+    x_f64 [rows, H]; mean, rstd [rows] and r [rows, H] from layernorm_ref.
+    The binary32 evaluation sums S = sum x and Q = sum x^2 (each x^2 exact)
+    in any order whose longest chain has at most D additions, so
+    |dS| <= g sum|x| and |dQ| <= g Q with g = D u / (1 - D u).  Then
+    mean = S / H, mean^2, Q / H and their difference add one rounding each
+    (dmean, dvar below, to first order in u, with the squares kept); the
+    variance error bounds rstd = 1 / sqrt(var + eps) through the exact
+    interval 1 / sqrt(var +- dvar + eps), and the square root and
+    reciprocal add at most 4u.  Each element then takes x - mean,
+    rstd * gamma and the product and sum with beta: at most 3u on
+    t = (x - mean) rstd gamma and u on |y| and |beta| each.  A factor 1.01
+    covers the neglected second-order terms.
+    Rows outside binary32's range for these sums (a non-finite x, Q over
+    2^126, var + eps under 2^-100) have no bound: E = inf there.
+    """
+    x = np.asarray(x_f64, np.float64)
+    rows, H = x.shape
+    D = layernorm_chain_bound(H)
+    g = D * U32 / (1.0 - D * U32)
+    ax = np.abs(x)
+    A = ax.mean(axis=1)
+    M2 = (x * x).mean(axis=1)
+    mean = np.asarray(mean, np.float64)
+    var = np.maximum(M2 - mean * mean, 0.0)
+    dmean = g * A + U32 * (np.abs(mean) + g * A)
+    dm2 = g * M2 + U32 * M2 * (1.0 + g)
+    dsq = 2.0 * np.abs(mean) * dmean + dmean ** 2 + U32 * (np.abs(mean) + dmean) ** 2
+    dvar = dm2 + dsq + U32 * (var + dm2 + dsq)
+    lo = np.maximum(var - dvar, 0.0) + eps
+    hi = var + dvar + eps
+    e_rho = np.maximum(np.sqrt((var + eps) / lo) - 1.0, 1.0 - np.sqrt((var + eps) / hi)) + 4.0 * U32
+    gam = np.abs(np.asarray(gamma, np.float64))[None, :]
+    bet = np.abs(np.asarray(beta, np.float64))[None, :]
+    rs = np.asarray(rstd, np.float64)[:, None]
+    t = np.abs(x - mean[:, None]) * rs * gam
+    E = 1.01 * (dmean[:, None] * rs * gam + t * (e_rho[:, None] + 3.0 * U32)
+                + U32 * (np.abs(np.asarray(r, np.float64).reshape(rows, H)) + bet))
+    bad = ~np.isfinite(x).all(axis=1) | (M2 * H > 2.0 ** 126) | (var + eps < 2.0 ** -100)
+    E[bad] = np.inf
+    return E
+
+
+def f64_to_bf16_array(v):
+    """Nearest bf16 (ties to even) of each float64 value, one rounding."""
+    v = np.ascontiguousarray(v, np.float64).reshape(-1)
+    out = np.empty(v.shape, np.uint16)
+    lib().orc_f64_to_bf16_array(_ptr(v), v.size, _ptr(out))
+    return out
+
+
+def _bf16_order_key(bits):
+    """Integer key in which bf16 values order like the numbers (-0 equal to +0)."""
+    b = np.asarray(bits, np.uint16).astype(np.int32)
+    mag = b & 0x7FFF
+    return np.where(b & 0x8000, -mag, mag)
+
+
+def bf16_within(y_bits, r, E):
+    """Boolean mask: y is the bf16 rounding of some value in [r - E, r + E].
+
+    y_bits are bf16 patterns, r and E float64 of the same size.  A NaN r
+    accepts exactly the NaN patterns; E = inf accepts anything.
+    """
+    y = np.asarray(y_bits, np.uint16).reshape(-1)
+    r = np.asarray(r, np.float64).reshape(-1)
+    E = np.asarray(E, np.float64).reshape(-1)
+    ynan = ((y & 0x7F80) == 0x7F80) & ((y & 0x7F) != 0)
+    rnan = np.isnan(r)
+    ok = np.zeros(y.shape, bool)
+    inf = np.isinf(E)
+    ok[inf] = True
+    ok[rnan & ~inf] = ynan[rnan & ~inf]
+    m = ~inf & ~rnan
+    lo = f64_to_bf16_array(r[m] - E[m])
+    hi = f64_to_bf16_array(r[m] + E[m])
+    k = _bf16_order_key(y[m])
+    ok[m] = ~ynan[m] & (k >= _bf16_order_key(lo)) & (k <= _bf16_order_key(hi))
+    return ok

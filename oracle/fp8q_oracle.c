@@ -225,154 +225,96 @@ void orc_qdq_amax(const uint16_t* x_bf16, int64_t n, int fmt, float scale, uint1
 }
 
 /* ----------------------------------------------------------------------- */
-/* GELU producer fused with the quantization ([XLA-7432], test.py: the MLP  */
-/* applies nn.gelu, the tanh form, to the first dense layer's output and    */
-/* feeds it to an FP8 dense layer; the issue asks for the quantization to   */
-/* be fused with what produces its input).                                  */
+/* The producers fused with the quantization ([XLA-7432], test.py: the      */
+/* transformer block applies nn.LayerNorm() to its input, and the MLP       */
+/* applies nn.gelu to the first dense layer's output; each result feeds an  */
+/* FP8 dense layer, and the issue asks for the quantization to be fused     */
+/* with what produces its input).                                           */
 /*                                                                          */
-/* GELU(tanh) = 0.5 x (1 + tanh(u)) = x / (1 + exp(-2u)),                   */
-/* u = sqrt(2/pi) (x + 0.044715 x^3).  So that a GPU and a CPU agree bit for */
-/* bit, exp is evaluated by additive range reduction (W. J. Cody and W.     */
-/* Waite, "Software Manual for the Elementary Functions", 1980) and a        */
-/* degree-6 Taylor polynomial of e^r, each step one correctly rounded       */
-/* binary32 operation (fmaf where written), in a fixed order.  The constants */
-/* are the binary32 roundings of ln 2 split in two (the high part to 16      */
-/* significant bits, so k * LN2_HI is exact for |k| < 2^8), of 1 / ln 2, of   */
-/* -2 sqrt(2/pi), of 0.044715 and of 1/k!.                                   */
+/* The producers are defined here by their plain formulas in float64.  The  */
+/* fused operation's output is y = bf16(producer(x)); a binary32            */
+/* implementation reaches the float64 value only up to its own rounding,    */
+/* so y is accepted within a tolerance derived from that arithmetic (the    */
+/* Python side of this oracle states it).  The FP8 codes and the amax are   */
+/* then exactly orc_quantize_amax of that y.                                */
 
-static const float EXP_LN2_HI = 0x1.62e4p-1f;
-static const float EXP_LN2_LO = 0x1.7f7d1cp-20f;
-static const float EXP_INV_LN2 = 0x1.715476p+0f;
-static const float EXP_ROUNDER = 0x1.8p23f;   /* 1.5 * 2^23: adding it rounds to an integer */
-static const float GELU_K = -0x1.988454p+0f;  /* -2 sqrt(2/pi) */
-static const float GELU_C = 0x1.6e4e26p-5f;   /* 0.044715 */
-
-/* e^v for the GELU below.  v is clamped to [-20, 89]: under -20, 1 + e^v
- * rounds to exactly 1 in binary32 whatever e^v is; over 88.73, e^v
- * overflows to +inf.  k = round(v / ln 2) comes from one fused multiply-add
- * with 1.5 * 2^23 (the sum's last bit is then the integer), r = v - k ln 2 in
- * two parts, e^r by a degree-6 Taylor polynomial (Horner, fused), and
- * e^v = (e^r * 2^(k-1)) * 2: the first product is exact, the second rounds
- * once (to +inf past the largest float). */
-float orc_exp_f32(float v) {
-    if (v > 89.0f) v = 89.0f;
-    if (!(v >= -20.0f)) v = -20.0f;                /* also NaN: GELU returns x * 1 = NaN */
-    float t = fmaf(v, EXP_INV_LN2, EXP_ROUNDER);   /* rounds v / ln 2 to the nearest integer */
-    float k = t - EXP_ROUNDER;                     /* exact */
-    float r = fmaf(-k, EXP_LN2_HI, v);
-    r = fmaf(-k, EXP_LN2_LO, r);
-    float p = 0x1.6c16c2p-10f;                     /* 1/720 */
-    p = fmaf(p, r, 0x1.111112p-7f);                /* 1/120 */
-    p = fmaf(p, r, 0x1.555556p-5f);                /* 1/24 */
-    p = fmaf(p, r, 0x1.555556p-3f);                /* 1/6 */
-    p = fmaf(p, r, 0.5f);
-    p = fmaf(p, r, 1.0f);
-    p = fmaf(p, r, 1.0f);
-    int ki = (int)k;                               /* in [-29, 128] */
-    return (p * ldexpf(1.0f, ki - 1)) * 2.0f;
+/* Nearest bf16 to a float64 value, ties to the even bf16, in ONE rounding  */
+/* (rounding to binary32 first could round twice).  The two bf16 neighbours */
+/* of |g| are multiples of the bf16 spacing at |g| (2^(e-7) for |g| in      */
+/* [2^e, 2^(e+1)), 2^-133 below 2^-126), so they and their midpoint are     */
+/* exact in double.  At or beyond the midpoint between the largest finite   */
+/* bf16 and 2^128 the result is infinity.                                    */
+uint16_t orc_f64_to_bf16(double g) {
+    if (isnan(g)) return 0x7FC0;
+    uint16_t sign = signbit(g) ? 0x8000 : 0x0000;
+    double a = fabs(g);
+    if (isinf(a)) return (uint16_t)(sign | 0x7F80);
+    int e;
+    (void)frexp(a, &e);                          /* a in [2^(e-1), 2^e) */
+    int q = (e - 1 >= -126) ? (e - 1) - 7 : -133; /* exponent of the spacing */
+    double ulp = ldexp(1.0, q);
+    double m = floor(a / ulp);                   /* a / ulp is exact: a power-of-two scaling */
+    double lo = m * ulp, hi = lo + ulp, mid = lo + 0.5 * ulp;
+    double pick;
+    if (a < mid) pick = lo;
+    else if (a > mid) pick = hi;
+    else pick = (fmod(m, 2.0) == 0.0) ? lo : hi; /* the even last mantissa bit */
+    if (pick >= ldexp(1.0, 128)) return (uint16_t)(sign | 0x7F80);
+    return (uint16_t)(sign | (f32_to_bits((float)pick) >> 16)); /* exact: pick is a bf16 value */
 }
 
-float orc_gelu_f32(float x) {
-    if (x == -INFINITY) return -0.0f;              /* the limit; x * 0 would be NaN */
-    float x2 = x * x;
-    float s = x * fmaf(GELU_C, x2, 1.0f);          /* x (1 + 0.044715 x^2) */
-    float d = 1.0f + orc_exp_f32(GELU_K * s);      /* 1 + exp(-2u) */
-    return x * (1.0f / d);
+/* orc_f64_to_bf16 over an array. */
+void orc_f64_to_bf16_array(const double* g, int64_t n, uint16_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_f64_to_bf16(g[i]);
 }
 
-/* y = bf16(GELU(h)); q = FP8(y / scale); amax = max(amax, |y|).  The codes
- * and the amax are those fp8q's quantize gives for the bf16 tensor y. */
-void orc_gelu_quantize_amax(const uint16_t* h_bf16, int64_t n, int fmt, float scale, uint8_t* q,
-                            uint16_t* y_bf16, float* amax_inout) {
-    float m = *amax_inout;
-    for (int64_t i = 0; i < n; ++i) {
-        uint16_t yb = orc_f32_to_bf16(orc_gelu_f32(orc_bf16_to_f32(h_bf16[i])));
-        float y = orc_bf16_to_f32(yb);
-        if (y_bf16) y_bf16[i] = yb;
-        q[i] = orc_fp8_encode(y / scale, fmt);
-        m = amax_combine(m, fabsf(y));
-    }
-    if (n > 0) *amax_inout = m;
+/* GELU, tanh form (Flax's nn.gelu, approximate=True):                      */
+/*   GELU(x) = 0.5 x (1 + tanh(u)),  u = sqrt(2/pi) (x + 0.044715 x^3).      */
+/* Since 1 + tanh(u) = 2 / (1 + e^(-2u)), this is x / (1 + e^(-2u)), which   */
+/* float64 evaluates without the cancellation that 1 + tanh(u) suffers for */
+/* u << 0 (there the result is tiny but still far inside bf16's range).     */
+/* At +-inf the value is the limit: +inf and -0.                            */
+double orc_gelu_ref(double x) {
+    if (isnan(x)) return x;
+    if (isinf(x)) return x > 0 ? x : -0.0;
+    const double k = sqrt(2.0 / acos(-1.0));
+    const double u = k * (x + 0.044715 * x * x * x);
+    return x / (1.0 + exp(-2.0 * u));
 }
 
-/* max|bf16(GELU(h))| alone (the fused op's amax, without the FP8 encoding). */
-float orc_gelu_amax(const uint16_t* h_bf16, int64_t n) {
-    float m = 0.0f;
-    for (int64_t i = 0; i < n; ++i) {
-        float y = orc_bf16_to_f32(orc_f32_to_bf16(orc_gelu_f32(orc_bf16_to_f32(h_bf16[i]))));
-        m = amax_combine(m, fabsf(y));
-    }
-    return m;
+/* GELU(h) in float64 for n bf16 inputs. */
+void orc_gelu_ref_array(const uint16_t* h_bf16, int64_t n, double* g) {
+    for (int64_t i = 0; i < n; ++i) g[i] = orc_gelu_ref((double)orc_bf16_to_f32(h_bf16[i]));
 }
 
-/* ----------------------------------------------------------------------- */
-/* LayerNorm producer fused with the quantization ([XLA-7432], test.py: the */
-/* transformer block applies nn.LayerNorm() to its input and feeds the      */
-/* MLP's first FP8 dense layer; the issue asks for the quantization to be   */
-/* fused with what produces its input).                                     */
-/*                                                                          */
-/* Per row of H elements (H a multiple of 16), in binary32, Flax's defaults: */
-/*   mean = S / H, m2 = Q / H with S = sum x, Q = sum x^2,                   */
-/*   var = max(0, m2 - mean^2), rstd = 1 / sqrt(var + eps),                 */
-/*   y = (x - mean) * (rstd * gamma) + beta, then rounded to bf16.          */
-/* S and Q are summed in one fixed association so that any implementation  */
-/* can reproduce them bit for bit: the row is cut into vectors of 16        */
-/* elements and vector v belongs to lane v mod 256; each lane adds its      */
-/* elements in index order (s = s + x, q = fma(x, x, q)); within each group */
-/* of 32 lanes the partial sums are folded pairwise, lanes j and j + o for  */
-/* o = 16, 8, 4, 2, 1; the 8 group totals are then added left to right.     */
-
-static float row_sum_fixed_order(float* lane) {
-    for (int w = 0; w < 8; ++w)
-        for (int o = 16; o >= 1; o /= 2)
-            for (int j = 0; j < o; ++j) lane[32 * w + j] = lane[32 * w + j] + lane[32 * w + j + o];
-    float t = lane[0];
-    for (int w = 1; w < 8; ++w) t = t + lane[32 * w];
-    return t;
-}
-
-void orc_layernorm_stats(const uint16_t* row, int32_t H, float eps, float* mean_out, float* rstd_out) {
-    float s[256], q[256];
-    for (int l = 0; l < 256; ++l) s[l] = q[l] = 0.0f;
-    for (int32_t v = 0; v < H / 16; ++v) {
-        int l = v % 256;
-        for (int e = 0; e < 16; ++e) {
-            float x = orc_bf16_to_f32(row[16 * v + e]);
-            s[l] = s[l] + x;
-            q[l] = fmaf(x, x, q[l]);
-        }
-    }
-    float S = row_sum_fixed_order(s), Q = row_sum_fixed_order(q);
-    float mean = S / (float)H;
-    float m2 = Q / (float)H;
-    float var = m2 - mean * mean;
-    if (!(var > 0.0f)) var = 0.0f;
-    *mean_out = mean;
-    *rstd_out = 1.0f / sqrtf(var + eps);
-}
-
-/* y = bf16(LayerNorm(x) * gamma + beta) row by row; q = FP8(y / scale);
- * amax = max(amax, |y|).  gamma and beta are float[H]; y may be NULL. */
-void orc_layernorm_quantize_amax(const uint16_t* x_bf16, int64_t rows, int32_t H, const float* gamma,
-                                 const float* beta, float eps, int fmt, float scale, uint8_t* q,
-                                 uint16_t* y_bf16, float* amax_inout) {
-    float m = *amax_inout;
+/* LayerNorm with Flax's defaults (nn.LayerNorm(): statistics over the last  */
+/* axis, epsilon 1e-6 unless given, learned scale gamma and bias beta),     */
+/* row by row in float64:                                                   */
+/*   mean = (1/H) sum x,   var = max(0, (1/H) sum x^2 - mean^2),            */
+/*   y = (x - mean) * (gamma / sqrt(var + eps)) + beta.                     */
+/* The sums run left to right.  mean_out and rstd_out (1/sqrt(var + eps))   */
+/* may be NULL.  A NaN or infinite input makes the row's y NaN.             */
+void orc_layernorm_ref(const uint16_t* x_bf16, int64_t rows, int32_t H, const float* gamma,
+                       const float* beta, double eps, double* y, double* mean_out, double* rstd_out) {
     for (int64_t r = 0; r < rows; ++r) {
         const uint16_t* row = x_bf16 + r * H;
-        float mean, rstd;
-        orc_layernorm_stats(row, H, eps, &mean, &rstd);
+        double s = 0.0, s2 = 0.0;
         for (int32_t i = 0; i < H; ++i) {
-            float x = orc_bf16_to_f32(row[i]);
-            float mul = rstd * gamma[i];
-            float yf = (x - mean) * mul + beta[i];
-            uint16_t yb = orc_f32_to_bf16(yf);
-            float y = orc_bf16_to_f32(yb);
-            if (y_bf16) y_bf16[r * H + i] = yb;
-            q[r * H + i] = orc_fp8_encode(y / scale, fmt);
-            m = amax_combine(m, fabsf(y));
+            double v = (double)orc_bf16_to_f32(row[i]);
+            s += v;
+            s2 += v * v;
         }
+        double mean = s / H;
+        double var = s2 / H - mean * mean;
+        if (var < 0.0) var = 0.0;                  /* a NaN stays NaN */
+        double rstd = 1.0 / sqrt(var + eps);
+        for (int32_t i = 0; i < H; ++i) {
+            double v = (double)orc_bf16_to_f32(row[i]);
+            y[r * H + i] = (v - mean) * (rstd * (double)gamma[i]) + (double)beta[i];
+        }
+        if (mean_out) mean_out[r] = mean;
+        if (rstd_out) rstd_out[r] = rstd;
     }
-    if (rows > 0 && H > 0) *amax_inout = m;
 }
 
 /* ----------------------------------------------------------------------- */

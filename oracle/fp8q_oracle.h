@@ -38,15 +38,12 @@ float orc_amax(const uint16_t* x_bf16, int64_t n);
 void orc_dequantize(const uint8_t* q, int64_t n, int fmt, float scale, uint16_t* y_bf16);
 void orc_qdq_amax(const uint16_t* x_bf16, int64_t n, int fmt, float scale, uint16_t* y_bf16,
                   float* amax_inout);
-float orc_exp_f32(float v);
-float orc_gelu_f32(float x);
-void orc_gelu_quantize_amax(const uint16_t* h_bf16, int64_t n, int fmt, float scale, uint8_t* q,
-                            uint16_t* y_bf16, float* amax_inout);
-float orc_gelu_amax(const uint16_t* h_bf16, int64_t n);
-void orc_layernorm_stats(const uint16_t* row, int32_t H, float eps, float* mean_out, float* rstd_out);
-void orc_layernorm_quantize_amax(const uint16_t* x_bf16, int64_t rows, int32_t H, const float* gamma,
-                                 const float* beta, float eps, int fmt, float scale, uint8_t* q,
-                                 uint16_t* y_bf16, float* amax_inout);
+uint16_t orc_f64_to_bf16(double g);
+void orc_f64_to_bf16_array(const double* g, int64_t n, uint16_t* out);
+double orc_gelu_ref(double x);
+void orc_gelu_ref_array(const uint16_t* h_bf16, int64_t n, double* g);
+void orc_layernorm_ref(const uint16_t* x_bf16, int64_t rows, int32_t H, const float* gamma,
+                       const float* beta, double eps, double* y, double* mean_out, double* rstd_out);
 void orc_amax_scale_update(float* hist, int32_t H, int32_t S, const float* amax_new,
                            float* scale, float* scale_inv, const uint8_t* slot_format,
                            int fmt, int algo, int32_t margin);

@@ -33,3 +33,29 @@ def orc():
     import oracle
     oracle.lib()
     return oracle
+
+
+@pytest.fixture(scope="session")
+def seq_gelu(tmp_path_factory):
+    """bf16 bits of the GELU producer's fixed binary32 sequence (tests/csrc/gelu_sequence.c):
+    a determinism check of the kernels' bits, not the oracle."""
+    import ctypes
+    import subprocess
+
+    import numpy as np
+
+    d = tmp_path_factory.mktemp("gelu_sequence")
+    so = str(d / "libgelu_sequence.so")
+    subprocess.run(["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared", "-o", so,
+                    os.path.join(ROOT, "tests", "csrc", "gelu_sequence.c"), "-lm"], check=True)
+    L = ctypes.CDLL(so)
+    L.seq_gelu_bf16.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
+    L.seq_gelu_bf16.restype = None
+
+    def run(h_bits):
+        h = np.ascontiguousarray(h_bits, np.uint16).reshape(-1)
+        y = np.empty(h.shape, np.uint16)
+        L.seq_gelu_bf16(h.ctypes.data, h.size, y.ctypes.data)
+        return y
+
+    return run

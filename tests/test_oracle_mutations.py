@@ -36,11 +36,14 @@ MUTATIONS = [
     ("ring overwrites the newest entry", "h = (h + 1) % H;", "h = h % H;"),
     ("ring window one row short", "for (int32_t r = 0; r < H; ++r) a = amax_combine(a, hist[(int64_t)r * S + s]);",
      "for (int32_t r = 0; r < H - 1; ++r) a = amax_combine(a, hist[(int64_t)r * S + s]);"),
-    ("GELU cubic term dropped", "float s = x * fmaf(GELU_C, x2, 1.0f);", "float s = x;"),
-    ("exp polynomial one term short", "p = fmaf(p, r, 0.5f);", "p = 0.5f;"),
-    ("LayerNorm without beta", "float yf = (x - mean) * mul + beta[i];", "float yf = (x - mean) * mul;"),
-    ("LayerNorm without eps", "*rstd_out = 1.0f / sqrtf(var + eps);", "*rstd_out = 1.0f / sqrtf(var);"),
-    ("LayerNorm fold skips a level", "for (int o = 16; o >= 1; o /= 2)", "for (int o = 16; o >= 2; o /= 2)"),
+    ("GELU cubic term dropped", "const double u = k * (x + 0.044715 * x * x * x);", "const double u = k * x;"),
+    ("GELU exponent sign flipped", "return x / (1.0 + exp(-2.0 * u));", "return x / (1.0 + exp(2.0 * u));"),
+    ("bf16 from float64 rounds through binary32 first", "double a = fabs(g);", "double a = fabs((double)(float)g);"),
+    ("bf16 from float64 ties away", "else pick = (fmod(m, 2.0) == 0.0) ? lo : hi;", "else pick = hi;"),
+    ("LayerNorm without beta", "* (rstd * (double)gamma[i]) + (double)beta[i];", "* (rstd * (double)gamma[i]);"),
+    ("LayerNorm without gamma", "* (rstd * (double)gamma[i]) + (double)beta[i];", "* rstd + (double)beta[i];"),
+    ("LayerNorm without eps", "double rstd = 1.0 / sqrt(var + eps);", "double rstd = 1.0 / sqrt(var);"),
+    ("LayerNorm variance without the mean's square", "double var = s2 / H - mean * mean;", "double var = s2 / H;"),
     ("fused Q->DQ divides on the way back", "float p = (float)orc_fp8_decode(code, fmt) * scale;",
      "float p = (float)orc_fp8_decode(code, fmt) / scale;"),
 ]

@@ -576,147 +576,217 @@ def test_ring_update_then_quantize_hand_example(orc):
     assert a == np.float32((np.uint32(0x4E6E) << 16).view(np.float32))
 
 
-# --------------------------------------------------------------------------- GELU producer fused with Q
+# --------------------------------------------------------------------------- producers (float64 definitions)
 
-def _ulp32(x):
-    x = np.abs(np.asarray(x, np.float32))
-    return (np.nextafter(x, np.float32(np.inf)) - x).astype(np.float64)
-
-
-def test_exp_within_a_few_ulp_of_the_true_value(orc):
-    """The GELU's exp: within 3 ulp of e^v on [-20, 88.7]; clamped outside (below -20,
-    1 + e^v is exactly 1 in binary32 whatever e^v is; above 88.73 it overflows)."""
-    rng = np.random.default_rng(31)
-    vs = np.concatenate([np.linspace(-20, 88.7, 4001), rng.uniform(-20, 88.7, 4000),
-                         rng.uniform(-1, 1, 2000)]).astype(np.float32)
-    got = np.array([orc.exp_f32(v) for v in vs], np.float64)
-    ref = np.exp(vs.astype(np.float64))
-    assert np.all(np.abs(got - ref) <= 3 * _ulp32(ref))
-    assert orc.exp_f32(0.0) == 1.0
-    assert np.isinf(orc.exp_f32(88.8)) and np.isinf(orc.exp_f32(np.inf))
-    e20 = orc.exp_f32(-20.0)
-    for v in (-20.5, -100.0, -np.inf, np.nan):
-        assert orc.exp_f32(v) == e20
-    assert np.float32(1.0) + e20 == np.float32(1.0)
+def test_f64_to_bf16_hand_cases(orc):
+    """One rounding from float64 to bf16, hand-derived (tests/golden/bf16_from_f64_cases.txt)."""
+    for expr, want in _golden("bf16_from_f64_cases.txt"):
+        got = orc.f64_to_bf16(_val(expr))
+        assert got == int(want, 16), f"{expr}: got {got:04X} want {want}"
+    assert orc.f64_to_bf16(math.nan) & 0x7FFF > 0x7F80
 
 
-def _gelu_tanh_f64(x):
-    """The tanh GELU in float64, written as x / (1 + exp(-2u)): the same function as
-    0.5 x (1 + tanh(u)), without that form's cancellation for negative x."""
-    x = np.asarray(x, np.float64)
-    u = math.sqrt(2.0 / math.pi) * (x + 0.044715 * x ** 3)
-    return x / (1.0 + np.exp(-2.0 * u))
+def test_f64_to_bf16_on_binary32_values_equals_the_binary32_rounding(orc):
+    """On values exactly representable in binary32, one rounding from float64 is the
+    binary32 -> bf16 rounding (itself pinned by hand cases and torch)."""
+    rng = np.random.default_rng(51)
+    bits = rng.integers(0, 2 ** 32, 20000, dtype=np.uint64).astype(np.uint32)
+    f = bits.view(np.float32)
+    f = f[np.isfinite(f)]
+    got = orc.f64_to_bf16_array(f.astype(np.float64))
+    want = np.array([orc.f32_to_bf16(v) for v in f[:4000]], np.uint16)
+    assert np.array_equal(got[:4000], want)
+    want_t = torch.from_numpy(f).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, want_t)
 
 
-def test_gelu_close_to_the_float64_tanh_form(orc):
-    rng = np.random.default_rng(32)
-    xs = np.concatenate([np.linspace(-9, 9, 6001), rng.normal(0, 3, 6000),
-                         rng.uniform(-0.01, 0.01, 500)]).astype(np.float32)
-    got = np.array([orc.gelu_f32(x) for x in xs], np.float64)
-    ref = _gelu_tanh_f64(xs)
-    tiny = np.abs(ref) < 2.0 ** -120
-    rel = np.abs(got - ref)[~tiny] / np.abs(ref[~tiny])
-    assert rel.max() < 2.0 ** -16          # far below bf16's resolution (2^-8)
-    assert np.all(np.abs(got[tiny] - ref[tiny]) < 2.0 ** -110)
+FINITE_BF16 = ALL_BF16_F32[np.isfinite(ALL_BF16_F32)]
 
 
-def test_gelu_bf16_matches_torch_tanh_gelu(orc):
-    """On bf16 inputs, bf16(GELU) equals torch's tanh GELU (in float64) rounded to bf16,
-    except within one bf16 step where the value sits on a rounding tie."""
-    # |x| < 5 keeps torch's 0.5 x (1 + tanh(u)) free of cancellation in float64
-    x = ALL_BF16_F32[np.isfinite(ALL_BF16_F32) & (np.abs(ALL_BF16_F32) < 5)]
-    xb = (x.view(np.uint32) >> 16).astype(np.uint16)
-    _, y, _ = orc.gelu_quantize_amax(xb, E4M3FN, 1.0)
-    ref = torch.nn.functional.gelu(torch.from_numpy(x.astype(np.float64)), approximate="tanh")
-    refb = ref.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
-    same = y == refb
-    assert same.mean() > 0.995  # ties: |error| < 2^-16 relative against bf16 steps of 2^-8
-    yf = (y.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
-    rf = (refb.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
-    step = np.maximum(np.abs(rf), 2.0 ** -126) * 2.0 ** -7
-    assert np.all(np.abs(yf - rf)[~same] <= step[~same])
+def test_gelu_ref_equals_the_tanh_form_in_high_precision(orc):
+    """The literal formula 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))) evaluated with
+    120 significant digits (mpmath; at x = -12, 1 + tanh(u) is about 1e-62), on every
+    third finite bf16 input with |x| <= 12 (below -10.5 the result is far under bf16's
+    smallest value)."""
+    mp = pytest.importorskip("mpmath")
+    mp.mp.dps = 120
+    xs = FINITE_BF16[np.abs(FINITE_BF16) <= 12.0].astype(np.float64)
+    xs = xs[::3]
+    k = mp.sqrt(2 / mp.pi)
+    worst = 0.0
+    for x in xs:
+        xm = mp.mpf(float(x))
+        want = 0.5 * xm * (1 + mp.tanh(k * (xm + mp.mpf("0.044715") * xm ** 3)))
+        got = orc.gelu_ref(float(x))
+        if want == 0:
+            assert got == 0.0
+            continue
+        rel = abs((mp.mpf(got) - want) / want)
+        worst = max(worst, float(rel))
+    assert worst < 1e-13, worst
 
 
-def test_gelu_special_values(orc):
-    assert orc.gelu_f32(0.0) == 0.0
-    assert orc.gelu_f32(np.inf) == np.inf
-    g = orc.gelu_f32(-np.inf)
-    assert g == 0.0 and math.copysign(1, g) < 0
-    g = orc.gelu_f32(-1e30)
-    assert g == 0.0 and math.copysign(1, g) < 0
-    assert orc.gelu_f32(1e30) == np.float32(1e30)
-    assert np.isnan(orc.gelu_f32(np.nan))
+def test_gelu_ref_odd_part_is_x(orc):
+    """GELU(x) - GELU(-x) = x: the tanh form is x times a sigmoid of an odd argument."""
+    xs = FINITE_BF16[(FINITE_BF16 > 0) & (FINITE_BF16 < 1e4)].astype(np.float64)
+    d = np.array([orc.gelu_ref(x) - orc.gelu_ref(-x) for x in xs[::2]])
+    assert np.all(np.abs(d - xs[::2]) <= 4e-16 * xs[::2])
 
 
-@pytest.mark.parametrize("fmt", [E4M3FN, E5M2])
-def test_fused_gelu_quantize_is_quantize_of_the_bf16_gelu(orc, fmt):
-    rng = np.random.default_rng(33)
-    h = (rng.normal(0, 2, 5000).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
-    for s in (1.0, 0.0123, 2.0 ** -70):
-        q, y, a = orc.gelu_quantize_amax(h, fmt, s)
-        q2, a2 = orc.quantize_amax(y, fmt, s)
-        assert np.array_equal(q, q2) and a == a2
-        yf = (y.astype(np.uint32) << 16).view(np.float32)
-        assert a == np.max(np.abs(yf)) == orc.gelu_amax(h)
+def test_gelu_ref_matches_torch_float64(orc):
+    """torch's tanh GELU in float64 where its 1 + tanh(u) is free of cancellation
+    (x > -2: there 1 + tanh(u) > 0.04, so float64 keeps 14 digits of it)."""
+    x = FINITE_BF16[(FINITE_BF16 > -2) & (FINITE_BF16 < 5)].astype(np.float64)
+    got = orc.gelu_ref_array((x.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16))
+    ref = torch.nn.functional.gelu(torch.from_numpy(x), approximate="tanh").numpy()
+    nz = ref != 0
+    assert np.all(np.abs(got[nz] - ref[nz]) <= 1e-13 * np.abs(ref[nz]))
+    assert np.all(got[~nz] == 0.0)
 
 
-# --------------------------------------------------------------------------- LayerNorm producer fused with Q
+def test_gelu_ref_special_values(orc):
+    assert orc.gelu_ref(0.0) == 0.0
+    assert orc.gelu_ref(math.inf) == math.inf
+    g = orc.gelu_ref(-math.inf)
+    assert g == 0.0 and math.copysign(1, g) < 0          # the limit
+    assert orc.gelu_ref(-1e30) == 0.0
+    assert orc.gelu_ref(1e30) == 1e30
+    assert math.isnan(orc.gelu_ref(math.nan))
+    assert orc.gelu_ref(3.0) == pytest.approx(3.0 * 0.5 * (1 + math.tanh(math.sqrt(2 / math.pi) * (3 + 0.044715 * 27))),
+                                              rel=1e-15)
+
 
 def _ln_rows(rng, rows, H, spread=1.0):
     x = (rng.normal(0, spread, (rows, H)) + rng.normal(0, 2 * spread, (rows, 1))).astype(np.float32)
     return torch.from_numpy(x).to(torch.bfloat16)
 
 
+def _u16(x):
+    return x.view(torch.int16).numpy().view(np.uint16)
+
+
 @pytest.mark.parametrize("H", [16, 272, 4096, 16384])
-def test_layernorm_stats_close_to_float64(orc, H):
+def test_layernorm_ref_matches_torch_float64(orc, H):
+    """torch's layer_norm (two-pass statistics) in float64 on rows with a large mean."""
     rng = np.random.default_rng(H)
     x = _ln_rows(rng, 6, H)
-    xb = x.view(torch.int16).numpy().view(np.uint16)
-    x64 = x.double().numpy()
-    for r in range(6):
-        mean, rstd = orc.layernorm_stats(xb[r])
-        m64 = x64[r].mean()
-        v64 = x64[r].var()
-        assert abs(mean - m64) <= 2.0 ** -18 * np.abs(x64[r]).max()
-        assert abs(rstd * math.sqrt(v64 + 1e-6) - 1.0) <= 2.0 ** -14
-
-
-def test_layernorm_output_close_to_torch(orc):
-    rng = np.random.default_rng(41)
-    H = 4096
-    x = _ln_rows(rng, 16, H)
     g = rng.uniform(0.5, 1.5, H).astype(np.float32)
     b = rng.normal(0, 0.2, H).astype(np.float32)
-    _, y, a = orc.layernorm_quantize_amax(x.view(torch.int16).numpy().view(np.uint16), H, g, b, E4M3FN, 1.0)
+    y, mean, rstd = orc.layernorm_ref(_u16(x), H, g, b, 1e-6)
     ref = torch.nn.functional.layer_norm(x.double(), (H,), torch.from_numpy(g).double(),
-                                         torch.from_numpy(b).double(), eps=1e-6)
-    refb = ref.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).reshape(-1)
-    same = y == refb
-    assert same.mean() > 0.99                      # the rest: bf16 rounding ties
-    yf = (y.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
-    rf = ref.numpy().reshape(-1)
-    assert np.all(np.abs(yf - rf) <= 2.0 ** -8 * np.abs(rf) + 2.0 ** -14)
-    assert a == np.max(np.abs(yf))
+                                         torch.from_numpy(b).double(), eps=1e-6).numpy().reshape(-1)
+    assert np.all(np.abs(y - ref) <= 1e-11 * (np.abs(ref) + 1.0))
+    x64 = x.double().numpy()
+    assert np.allclose(mean, x64.mean(axis=1), rtol=1e-14, atol=1e-14)
+    assert np.allclose(rstd, 1.0 / np.sqrt(x64.var(axis=1) + 1e-6), rtol=1e-12)
 
 
-def test_layernorm_constant_rows_give_beta(orc):
+def test_layernorm_ref_closed_forms(orc):
+    """Constant rows give beta exactly; a row +a, -a, +a, ... has mean 0 and variance a^2."""
     H = 64
-    x = torch.full((3, H), 2.5).to(torch.bfloat16)
-    g = np.full(H, 3.0, np.float32)
     b = np.linspace(-1, 1, H).astype(np.float32)
-    _, y, _ = orc.layernorm_quantize_amax(x.view(torch.int16).numpy().view(np.uint16), H, g, b, E4M3FN, 1.0)
-    want = torch.from_numpy(np.tile(b, 3)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
-    assert np.array_equal(y, want)
+    g = np.full(H, 3.0, np.float32)
+    x = torch.full((3, H), 2.5).to(torch.bfloat16)
+    y, mean, rstd = orc.layernorm_ref(_u16(x), H, g, b, 1e-6)
+    assert np.array_equal(y, np.tile(b.astype(np.float64), 3))
+    assert np.all(mean == 2.5) and np.allclose(rstd, 1000.0, rtol=1e-15)
+    a = 1.5
+    x = torch.tensor(np.where(np.arange(H) % 2 == 0, a, -a), dtype=torch.float32).reshape(1, H).to(torch.bfloat16)
+    for eps in (1e-6, 0.25):
+        y, mean, rstd = orc.layernorm_ref(_u16(x), H, g, b, eps)
+        sgn = np.where(np.arange(H) % 2 == 0, 1.0, -1.0)
+        want = sgn * a / math.sqrt(a * a + eps) * 3.0 + b.astype(np.float64)
+        assert mean[0] == 0.0
+        assert np.allclose(y, want, rtol=1e-15, atol=1e-15)
 
 
-@pytest.mark.parametrize("fmt", [E4M3FN, E5M2])
-def test_fused_layernorm_quantize_is_quantize_of_its_output(orc, fmt):
-    rng = np.random.default_rng(42)
-    H = 1024
-    x = _ln_rows(rng, 5, H, 3.0)
-    g = rng.uniform(0.5, 1.5, H).astype(np.float32)
-    b = rng.normal(0, 0.2, H).astype(np.float32)
-    for s in (1.0, 0.0123, 7.5):
-        q, y, a = orc.layernorm_quantize_amax(x.view(torch.int16).numpy().view(np.uint16), H, g, b, fmt, s)
-        q2, a2 = orc.quantize_amax(y, fmt, s)
-        assert np.array_equal(q, q2) and a == a2
+def test_layernorm_ref_propagates_nan_and_inf(orc):
+    H = 32
+    x = np.full((3, H), 0x3F80, np.uint16)
+    x[0, 3] = 0x7FC0
+    x[1, 4] = 0x7F80
+    x[2, 5] = 0xFF80
+    y, _, _ = orc.layernorm_ref(x, H, np.ones(H, np.float32), np.zeros(H, np.float32), 1e-6)
+    assert np.all(np.isnan(y))
+
+
+def _f32_tree_sum(a):
+    """Row sums of a float32 [rows, H] array (H a multiple of 8) in binary32: runs of
+    8 added left to right, then a pairwise tree (longest chain 8 + log2(H / 8))."""
+    a = a.astype(np.float32)
+    rows, H = a.shape
+    leaves = a.reshape(rows, H // 8, 8)
+    s = np.zeros((rows, H // 8), np.float32)
+    for k in range(8):
+        s = (s + leaves[:, :, k]).astype(np.float32)
+    while s.shape[1] > 1:
+        if s.shape[1] % 2:
+            s = np.concatenate([s, np.zeros((rows, 1), np.float32)], axis=1)
+        s = (s[:, 0::2] + s[:, 1::2]).astype(np.float32)
+    return s[:, 0]
+
+
+def _ln_f32(x, g, b, eps):
+    """LayerNorm in binary32 with Flax's formula and tree-ordered sums."""
+    xf = x.float().numpy().astype(np.float32)
+    H = xf.shape[1]
+    S = _f32_tree_sum(xf)
+    Q = _f32_tree_sum((xf * xf).astype(np.float32))
+    mean = (S / np.float32(H)).astype(np.float32)
+    var = np.maximum((Q / np.float32(H)).astype(np.float32) - (mean * mean).astype(np.float32), np.float32(0))
+    rstd = (np.float32(1) / np.sqrt((var + np.float32(eps)).astype(np.float32))).astype(np.float32)
+    d = (xf - mean[:, None]).astype(np.float32)
+    m = (rstd[:, None] * g[None, :]).astype(np.float32)
+    yf = ((d * m).astype(np.float32) + b[None, :]).astype(np.float32)
+    return torch.from_numpy(yf).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).reshape(-1)
+
+
+@pytest.mark.parametrize("H", [64, 1024, 4096])
+def test_layernorm_tolerance_holds_a_binary32_evaluation(orc, H):
+    """A plain binary32 LayerNorm, sums well within the allowed chain length, lands
+    inside the stated tolerance, also on rows whose mean dwarfs their spread."""
+    rng = np.random.default_rng(61 + H)
+    rows = 8
+    mu = np.array([0.0, 2.0, -2.0, 30.0, 0.5, -40.0, 1.0, 3.0])[:, None]
+    sd = np.array([1.0, 0.5, 0.5, 0.3, 4.0, 1.0, 1e-3, 2.0])[:, None]
+    x = torch.from_numpy((rng.normal(0, 1, (rows, H)) * sd + mu).astype(np.float32)).to(torch.bfloat16)
+    g = (1 + 0.1 * rng.normal(0, 1, H)).astype(np.float32)
+    b = (0.1 * rng.normal(0, 1, H)).astype(np.float32)
+    y32 = _ln_f32(x, g, b, 1e-6)
+    r, mean, rstd = orc.layernorm_ref(_u16(x), H, g, b, 1e-6)
+    E = orc.layernorm_tolerance(x.double().numpy(), g, b, 1e-6, mean, rstd, r)
+    assert np.all(orc.bf16_within(y32, r, E.reshape(-1)))
+    # On rows whose spread is not dwarfed by their mean the tolerance leaves one value
+    # for almost every element (rows 3, 5 and 6 lose most of var = E[x^2] - mean^2 to
+    # cancellation in binary32, and the tolerance widens accordingly).
+    lo = orc.f64_to_bf16_array(r - E.reshape(-1)).reshape(rows, H)
+    hi = orc.f64_to_bf16_array(r + E.reshape(-1)).reshape(rows, H)
+    benign = [0, 1, 2, 4, 7]
+    assert np.mean(lo[benign] == hi[benign]) > 0.9
+
+
+def test_gelu_tolerance_is_not_vacuous(orc):
+    """The GELU tolerance leaves one acceptable value for almost every bf16 input whose
+    GELU is at least 2^-122 (below that, the binary32 reciprocal is subnormal or zero,
+    and any value within 2^-122 is accepted)."""
+    h = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    x = (h.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    fin = np.isfinite(x)
+    r = orc.gelu_ref_array(h)[fin]
+    E = orc.gelu_tolerance(x[fin], r)
+    lo = orc.f64_to_bf16_array(r - E)
+    hi = orc.f64_to_bf16_array(r + E)
+    big = np.abs(r) >= orc.GELU_TINY
+    assert big.sum() > 30000
+    assert np.mean((lo == hi)[big]) > 0.97
+
+
+def test_bf16_within_accepts_only_the_interval(orc):
+    r = np.array([1.0 + 2.0 ** -8, 1.0 + 2.0 ** -9, -3.0, math.nan, 0.0])
+    E = np.array([2.0 ** -30, 2.0 ** -30, 0.0, 0.0, 2.0 ** -140])
+    y_ok = np.array([0x3F81, 0x3F80, 0xC040, 0x7FC1, 0x8000], np.uint16)
+    assert np.all(orc.bf16_within(y_ok, r, E))
+    y_other = np.array([0x3F80, 0x3F81, 0xC041, 0x3F80, 0x0001], np.uint16)
+    ok = orc.bf16_within(y_other, r, E)
+    # 1 + 2^-8 +- 2^-30 straddles the tie: both neighbours are acceptable
+    assert list(ok) == [True, False, False, False, False]
