@@ -253,14 +253,15 @@ def gelu_tolerance(h_f64, r):
     product add u each.  So |error| <= (6|v| + 10) u |GELU| while
     1 / (1 + e^v) is a normal binary32.  Where |GELU| < 2^-122 that
     reciprocal is subnormal or zero (|x| <= 10.6 there), and y may be any
-    value within 2^-122 of r.
+    value within 2^-122 of r.  At x = +inf the result is +inf exactly (E = 0).
     """
     h = np.asarray(h_f64, np.float64)
     r = np.asarray(r, np.float64)
     with np.errstate(over="ignore", invalid="ignore"):
         v = np.minimum(np.abs(2.0 * math.sqrt(2.0 / math.pi) * h * (1.0 + 0.044715 * h * h)), 89.0)
     v = np.where(np.isfinite(v), v, 89.0)
-    e = (6.0 * v + 10.0) * U32 * np.abs(r)
+    with np.errstate(invalid="ignore"):
+        e = np.where(np.isinf(r), 0.0, (6.0 * v + 10.0) * U32 * np.abs(r))   # GELU(+inf) = +inf exactly
     return np.where(np.abs(r) < GELU_TINY, np.maximum(e, GELU_TINY), e)
 
 

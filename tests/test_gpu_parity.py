@@ -2,9 +2,9 @@
 
 Bar: bit-exact FP8 codes, amax, history, scale, scale_inv and bf16 dequant.
 Where several encodings are equally correct (a NaN), both sides must agree
-that the value is a NaN.  Small cases compare every element; the full-size
-workloads compare a sample of positions (the oracle is elementwise) plus the
-amax over the whole tensor.
+that the value is a NaN.  Every case compares every element, the full-size
+workloads included (the oracle runs chunked over all host cores there).
+The producers fused with the quantize are tested in test_gpu_producers.py.
 """
 import math
 
@@ -13,85 +13,21 @@ import pytest
 import torch
 
 import oracle
+from gpu_helpers import (CANARY, GUARD, SCALES_ALL, assert_bf16_equal, assert_codes_equal,  # noqa: F401
+                         assert_f32_equal, check_guards, check_quantize_full, f32, guarded, is_nan_code,
+                         oracle_scale_from, par_dequantize, par_qdq_amax, par_quantize_amax)
 from quantize_amax_scaling_gb300 import fp8q
 from quantize_amax_scaling_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
 
 E4M3FN, E5M2 = fp8q.E4M3FN, fp8q.E5M2
-GUARD = 64
-CANARY = 0xA5
-
-SCALES_ALL = [1.0, 0.5, 2.0 ** -6, 2.0 ** 20, 1.0 / 3.0, 0.012345678, 7.5, 448.0 / 3.9, 3.0e-5,
-              1.7e4, 2.0 ** -60, 2.0 ** 60, float.fromhex("0x1.fffffep-61"), float.fromhex("0x1.000002p60"), 2.0 ** -70, 2.0 ** 70,
-              1.0e-38, 5.0e-45, -2.5, 0.0, -0.0, math.inf, math.nan, 3.4e38, float.fromhex("0x1.fffffep-1"),
-              float.fromhex("0x1.000002p0"), 1.0 / 448.0, 57344.0]
 
 
 @pytest.fixture(scope="module")
 def dev():
     fp8q.lib()
     return torch.device("cuda:0")
-
-
-def f32(v, dev):
-    return torch.tensor([v], dtype=torch.float32, device=dev)
-
-
-def is_nan_code(c, fmt):
-    c = np.asarray(c) & 0x7F
-    return c == 0x7F if fmt == E4M3FN else c > 0x7C
-
-
-def assert_codes_equal(got, want, fmt, what=""):
-    got = np.asarray(got, np.uint8).reshape(-1)
-    want = np.asarray(want, np.uint8).reshape(-1)
-    assert got.shape == want.shape
-    nan_w = is_nan_code(want, fmt)
-    assert np.array_equal(is_nan_code(got, fmt), nan_w), f"{what}: NaN codes differ"
-    bad = np.nonzero((got != want) & ~nan_w)[0]
-    assert bad.size == 0, f"{what}: {bad.size} codes differ, first at {bad[:5]}: got {got[bad[:5]]} want {want[bad[:5]]}"
-
-
-def assert_f32_equal(got, want, what=""):
-    g = np.asarray(got, np.float32).reshape(-1)
-    w = np.asarray(want, np.float32).reshape(-1)
-    gn, wn = np.isnan(g), np.isnan(w)
-    assert np.array_equal(gn, wn), f"{what}: NaN positions differ"
-    bad = np.nonzero((g.view(np.uint32) != w.view(np.uint32)) & ~wn)[0]
-    assert bad.size == 0, f"{what}: {bad.size} differ, first {bad[:5]}: got {g[bad[:5]]} want {w[bad[:5]]}"
-
-
-def assert_bf16_equal(got_bits, want_bits, what=""):
-    g = np.asarray(got_bits, np.uint16).reshape(-1)
-    w = np.asarray(want_bits, np.uint16).reshape(-1)
-    gn = ((g & 0x7F80) == 0x7F80) & ((g & 0x7F) != 0)
-    wn = ((w & 0x7F80) == 0x7F80) & ((w & 0x7F) != 0)
-    assert np.array_equal(gn, wn), f"{what}: NaN positions differ"
-    bad = np.nonzero((g != w) & ~wn)[0]
-    assert bad.size == 0, f"{what}: {bad.size} differ, first {bad[:5]}: got {g[bad[:5]]} want {w[bad[:5]]}"
-
-
-def guarded(n, dtype, dev, offset=0, fill=CANARY):
-    """A contiguous view of n elements inside a buffer with canary guards on both sides."""
-    buf = torch.full((n + 2 * GUARD + offset,), fill, dtype=torch.uint8 if dtype == torch.uint8 else torch.int16,
-                     device=dev)
-    if dtype != torch.uint8:
-        buf = buf.view(dtype)
-    return buf, buf[GUARD + offset: GUARD + offset + n]
-
-
-def check_guards(buf, n, offset, fill=CANARY):
-    raw = buf.view(torch.uint8) if buf.dtype != torch.uint8 else buf
-    es = buf.element_size()
-    lo = raw[: (GUARD + offset) * es].cpu().numpy()
-    hi = raw[(GUARD + offset + n) * es:].cpu().numpy()
-    if buf.dtype == torch.uint8:
-        assert np.all(lo == fill) and np.all(hi == fill), "write outside the output"
-    else:
-        lo16 = lo.view(np.uint16)
-        hi16 = hi.view(np.uint16)
-        assert np.all(lo16 == fill) and np.all(hi16 == fill), "write outside the output"
 
 
 def run_quantize(x, fmt, scale, dev, q=None, amax0=0.0):
@@ -101,23 +37,6 @@ def run_quantize(x, fmt, scale, dev, q=None, amax0=0.0):
     fp8q.fp8q_quantize_amax(x.reshape(-1), q, fmt, f32(scale, dev), am)
     torch.cuda.synchronize()
     return q, am
-
-
-def oracle_scale_from(amax_prev, fmt):
-    """Delayed scale for the next step, computed by the oracle's own update."""
-    hist = np.zeros((1, 1), np.float32)
-    s = np.ones(1, np.float32)
-    si = np.ones(1, np.float32)
-    oracle.amax_scale_update(hist, np.array([amax_prev], np.float32), s, si, fmt)
-    return np.float32(s[0])
-
-
-def sample_positions(n, k=400_000, seed=0):
-    rng = np.random.default_rng(seed)
-    head = np.arange(min(n, 20000))
-    tail = np.arange(max(0, n - 20000), n)
-    rnd = rng.integers(0, n, min(k, n))
-    return np.unique(np.concatenate([head, tail, rnd]))
 
 
 # --------------------------------------------------------------------------- quantize
@@ -185,6 +104,25 @@ def test_quantize_ragged_sizes_offsets_with_canaries(dev, n):
         check_guards(qbuf, n, qo)
 
 
+@pytest.mark.parametrize("n,xo,qo", [(16384 + 17, 0, 0), (3 * 16384 + 5, 3, 3), ((1 << 25) + 7, 1, 1),
+                                     (4096 * 16384, 0, 0), (4096 * 16384 + 16, 0, 0), (4096 * 16384 + 16, 5, 5),
+                                     (4096 * 16384 - 1, 7, 7)])
+def test_quantize_both_grids_around_the_threshold(dev, n, xo, qo):
+    """Single tensors of up to 4096 tiles take the persistent grid of balanced ranges,
+    larger ones one CTA per tile: both sides of the switch, with heads and tails."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(n % 100003)
+    xbuf = (torch.randn(n + 16, generator=g, device=dev) * 7.0).to(torch.bfloat16)
+    x = xbuf[xo: xo + n]
+    qbuf, q = guarded(n, torch.uint8, dev, qo)
+    for fmt, scale in ((E4M3FN, 0.0123), (E5M2, 2.0 ** 70)):
+        am = f32(0.0, dev)
+        fp8q.fp8q_quantize_amax(x, q, fmt, f32(scale, dev), am)
+        torch.cuda.synchronize()
+        check_quantize_full(x, q, am, fmt, np.float32(scale), f"n={n} off={xo},{qo}")
+        check_guards(qbuf, n, qo)
+
+
 def test_quantize_on_a_side_stream(dev):
     x = W.mlp_activation(3, dev, (512, 1024))
     s = torch.cuda.Stream()
@@ -238,17 +176,9 @@ def test_mlp_activation_full_size_full_compare(dev):
     assert float(am) == float(ra)
 
 
-def _sampled_quantize_check(x, q, am, fmt, scale, what):
-    xb = W.bf16_bits(x)
-    idx = sample_positions(xb.size)
-    rq, _ = oracle.quantize_amax(xb[idx], fmt, scale)
-    assert_codes_equal(q.cpu().numpy()[idx], rq, fmt, what)
-    assert_f32_equal([float(am)], [oracle.amax(xb)], what + " amax")
-
-
-def test_ffn_full_size_multi_tensor_sampled(dev):
+def test_ffn_full_size_multi_tensor(dev):
     """gelu activation 8192x16384 + W1 4096x16384 + W2 16384x4096 in one launch,
-    each with its own delayed scale and amax."""
+    each with its own delayed scale and amax: every code compared."""
     xs = W.ffn_tensors(dev)
     prev = W.ffn_tensors(dev, seed=W.SEED_FFN + 1)
     scales = [oracle_scale_from(oracle.amax(W.bf16_bits(p)), E4M3FN) for p in prev]
@@ -260,20 +190,20 @@ def test_ffn_full_size_multi_tensor_sampled(dev):
                                   [sc[i:i + 1] for i in range(3)], [am[i:i + 1] for i in range(3)])
     torch.cuda.synchronize()
     for i, (x, q) in enumerate(zip(xs, qs)):
-        _sampled_quantize_check(x, q, am[i], E4M3FN, scales[i], f"ffn tensor {i}")
+        check_quantize_full(x, q, am[i], E4M3FN, scales[i], f"ffn tensor {i}")
 
 
-def test_headline_tensor_single_call_sampled(dev):
-    """The 8192x16384 activation through the single-tensor entry point."""
+def test_headline_tensor_single_call(dev):
+    """The 8192x16384 activation through the single-tensor entry point: every code."""
     x = W.gelu_activation(W.SEED_FFN, dev)
     scale = np.float32(0.0091)
     q, am = run_quantize(x, E4M3FN, scale, dev)
-    _sampled_quantize_check(x, q, am, E4M3FN, scale, "8192x16384")
+    check_quantize_full(x, q, am, E4M3FN, scale, "8192x16384")
 
 
-def test_gradients_e5m2_quantize_then_dequantize_sampled(dev):
+def test_gradients_e5m2_quantize_then_dequantize(dev):
     """sign x lognormal(-12, 3) gradients with signed zeros and +-inf, e5m2
-    saturating (amax = inf), then dequantized back to bf16."""
+    saturating (amax = inf), then dequantized back to bf16: every element."""
     grads = W.gradient_tensors(dev)
     prev = W.gradient_tensors(dev, seed=W.SEED_GRAD + 1)
     for g, p in zip(grads, prev):
@@ -283,13 +213,11 @@ def test_gradients_e5m2_quantize_then_dequantize_sampled(dev):
         scale = oracle_scale_from(oracle.amax(finite_prev), E5M2)
         q, am = run_quantize(g, E5M2, scale, dev)
         assert math.isinf(float(am))
-        _sampled_quantize_check(g, q, am, E5M2, scale, "gradient")
+        rq = check_quantize_full(g, q, am, E5M2, scale, "gradient")
         y = torch.empty(g.numel(), dtype=torch.bfloat16, device=dev)
         fp8q.fp8q_dequantize(q, y, E5M2, f32(scale, dev))
         torch.cuda.synchronize()
-        idx = sample_positions(g.numel(), seed=1)
-        ry = oracle.dequantize(q.cpu().numpy()[idx], E5M2, scale)
-        assert_bf16_equal(W.bf16_bits(y)[idx], ry, "gradient dequant")
+        assert_bf16_equal(W.bf16_bits(y), par_dequantize(rq, E5M2, scale), "gradient dequant")
 
 
 # --------------------------------------------------------------------------- multi-tensor
@@ -345,9 +273,9 @@ def test_multi_tensor_shared_amax(dev):
     _multi_case(dev, [5000, 7000, 11, 90000], E4M3FN, seed=44, share_amax=True)
 
 
-def test_ragged_twelve_tensors_full_size_sampled(dev):
+def test_ragged_twelve_tensors_full_size(dev):
     """Twelve bf16 N(0,1) tensors 2048x12288 .. 12288x4096 in one launch, with
-    the per-slot scales that a 576-slot update produces."""
+    the per-slot scales that a 576-slot update produces: every code."""
     xs = W.ragged_tensors(dev)
     hist, new, sc0, si0, sf = W.scale_update_inputs("cpu")
     hist_np, new_np = hist.numpy().copy(), new.numpy().copy()
@@ -362,11 +290,7 @@ def test_ragged_twelve_tensors_full_size_sampled(dev):
                                   [am[i:i + 1] for i in range(len(xs))])
     torch.cuda.synchronize()
     for i, (x, q) in enumerate(zip(xs, qs)):
-        xb = W.bf16_bits(x)
-        idx = sample_positions(xb.size, k=60000, seed=i)
-        rq, _ = oracle.quantize_amax(xb[idx], E4M3FN, scales[i])
-        assert_codes_equal(q.cpu().numpy()[idx], rq, E4M3FN, f"ragged {i}")
-        assert_f32_equal([float(am[i])], [oracle.amax(xb)], f"ragged amax {i}")
+        check_quantize_full(x, q, am[i], E4M3FN, scales[i], f"ragged {i}")
 
 
 # --------------------------------------------------------------------------- dequantize
@@ -495,18 +419,12 @@ def test_more_than_2_pow_31_elements(dev):
     fp8q.fp8q_dequantize(q, y, E4M3FN, f32(scale, dev))
     torch.cuda.synchronize()
     assert float(am) == 1000.0
-    rng = np.random.default_rng(2)
-    idx = np.unique(np.concatenate([np.arange(4096), np.arange(n - 8192, n),
-                                    rng.integers((1 << 31) - 8192, n, 4096),
-                                    rng.integers(0, n, 60000)]))
-    # every index is checked on the host before the device gathers with it
-    assert idx.min() >= 0 and idx.max() < n
-    it = torch.from_numpy(idx).to(dev)
-    xb = W.bf16_bits(x[it])
-    rq, _ = oracle.quantize_amax(xb, E4M3FN, scale)
-    assert_codes_equal(q[it].cpu().numpy(), rq, E4M3FN, "n > 2^31")
-    ry = oracle.dequantize(q[it].cpu().numpy(), E4M3FN, scale)
-    assert_bf16_equal(W.bf16_bits(y[it]), ry, "n > 2^31 dequant")
+    chunk = 1 << 28
+    for i in range(0, n, chunk):          # every element, a host chunk at a time
+        m = min(chunk, n - i)
+        rq, _ = par_quantize_amax(W.bf16_bits(x[i:i + m]), E4M3FN, scale)
+        assert_codes_equal(q[i:i + m].cpu().numpy(), rq, E4M3FN, f"n > 2^31, chunk at {i}")
+        assert_bf16_equal(W.bf16_bits(y[i:i + m]), par_dequantize(rq, E4M3FN, scale), f"dequant chunk at {i}")
     del x, q, y
     torch.cuda.empty_cache()
 
@@ -617,15 +535,13 @@ def test_qdq_sizes_offsets_in_place_and_canaries(dev, n):
         assert_f32_equal([float(am2)], [ra], f"in-place amax n={n}")
 
 
-def test_qdq_full_size_activation_sampled(dev):
+def test_qdq_full_size_activation(dev):
     x = W.gelu_activation(W.SEED_FFN, dev).reshape(-1)
     scale = np.float32(0.0091)
     y, am = run_qdq(x, E4M3FN, scale, dev)
-    xb = W.bf16_bits(x)
-    idx = sample_positions(xb.size)
-    ry, _ = oracle.qdq_amax(xb[idx], E4M3FN, scale)
-    assert_bf16_equal(W.bf16_bits(y)[idx], ry, "qdq 8192x16384")
-    assert_f32_equal([float(am)], [oracle.amax(xb)], "qdq amax")
+    ry, ra = par_qdq_amax(W.bf16_bits(x), E4M3FN, scale)
+    assert_bf16_equal(W.bf16_bits(y), ry, "qdq 8192x16384")
+    assert_f32_equal([float(am)], [ra], "qdq amax")
 
 
 # --------------------------------------------------------------------------- ring-buffer history
@@ -720,210 +636,6 @@ def test_ring_matches_roll_on_the_gpu(dev):
     assert_f32_equal(logical, roll.cpu().numpy(), "ring vs roll window")
     assert_f32_equal(sc_b.cpu().numpy(), sc_a.cpu().numpy(), "ring vs roll scale")
     assert_f32_equal(si_b.cpu().numpy(), si_a.cpu().numpy(), "ring vs roll scale_inv")
-
-
-# --------------------------------------------------------------------------- GELU producer fused with Q
-
-def run_gelu(h, fmt, scale, dev, want_y=True):
-    n = h.numel()
-    y = torch.empty(n, dtype=torch.bfloat16, device=dev) if want_y else None
-    q = torch.empty(n, dtype=torch.uint8, device=dev)
-    am = f32(0.0, dev)
-    fp8q.fp8q_gelu_quantize_amax(h.reshape(-1), y, q, fmt, f32(scale, dev), am)
-    torch.cuda.synchronize()
-    return y, q, am
-
-
-@pytest.mark.parametrize("fmt", [E4M3FN, E5M2])
-def test_gelu_quantize_every_bf16_pattern(dev, fmt):
-    h = W.all_bf16_patterns(dev)
-    hb = W.bf16_bits(h)
-    for k, s in enumerate(SCALES_ALL):
-        y, q, am = run_gelu(h, fmt, s, dev, want_y=(k % 2 == 0))
-        rq, ry, ra = oracle.gelu_quantize_amax(hb, fmt, np.float32(s))
-        assert_codes_equal(q.cpu().numpy(), rq, fmt, f"scale {s!r}")
-        if y is not None:
-            assert_bf16_equal(W.bf16_bits(y), ry, f"gelu y, scale {s!r}")
-        assert math.isnan(float(am)) and math.isnan(float(ra))
-    # without NaN inputs the amax is exact
-    f = (hb.astype(np.uint32) << 16).view(np.float32)
-    fin = hb[~np.isnan(f)]
-    hx = torch.from_numpy(fin.view(np.int16).copy()).view(torch.bfloat16).to(dev)
-    _, q, am = run_gelu(hx, fmt, 0.37, dev)
-    rq, _, ra = oracle.gelu_quantize_amax(fin, fmt, np.float32(0.37))
-    assert_codes_equal(q.cpu().numpy(), rq, fmt, "no NaN")
-    assert_f32_equal([float(am)], [ra], "gelu amax")
-
-
-@pytest.mark.parametrize("n", [1, 15, 16, 17, 33, 4095, 8193, 70001])
-def test_gelu_quantize_sizes_offsets_canaries(dev, n):
-    g = torch.Generator(device=dev)
-    g.manual_seed(11 * n)
-    for k, (ho, qo) in enumerate(OFFSETS):
-        fmt = E4M3FN if k % 2 else E5M2
-        scale = [0.0123, 1.0, 2.0 ** 70, 3.3e-3][k % 4]
-        hbuf = (torch.randn(n + 16, generator=g, device=dev) * 3.0).to(torch.bfloat16)
-        h = hbuf[ho: ho + n]
-        qbuf, q = guarded(n, torch.uint8, dev, qo)
-        yo = (ho + 7 * k) % 16                   # often not aligned like h: scalar path
-        ybuf, y = guarded(n, torch.bfloat16, dev, yo, fill=0x5A5A)
-        am = f32(0.0, dev)
-        fp8q.fp8q_gelu_quantize_amax(h, y, q, fmt, f32(scale, dev), am)
-        torch.cuda.synchronize()
-        rq, ry, ra = oracle.gelu_quantize_amax(W.bf16_bits(h), fmt, np.float32(scale))
-        assert_codes_equal(q.cpu().numpy(), rq, fmt, f"n={n} off={ho},{qo},{yo}")
-        assert_bf16_equal(W.bf16_bits(y), ry, f"y n={n} off={ho},{yo}")
-        assert_f32_equal([float(am)], [ra], f"amax n={n}")
-        check_guards(qbuf, n, qo)
-        check_guards(ybuf, n, yo, fill=0x5A5A)
-
-
-def test_gelu_quantize_full_size_sampled(dev):
-    """Pre-activation 8192x16384 (N(0,1)), the FFN intermediate of the MLP workload."""
-    g = torch.Generator(device=dev)
-    g.manual_seed(W.SEED_FFN)
-    h = torch.randn((8192, 16384), generator=g, device=dev).to(torch.bfloat16).reshape(-1)
-    scale = np.float32(0.0091)
-    y, q, am = run_gelu(h, E4M3FN, scale, dev)
-    hb = W.bf16_bits(h)
-    idx = sample_positions(hb.size)
-    rq, ry, _ = oracle.gelu_quantize_amax(hb[idx], E4M3FN, scale)
-    assert_codes_equal(q.cpu().numpy()[idx], rq, E4M3FN, "gelu q")
-    assert_bf16_equal(W.bf16_bits(y)[idx], ry, "gelu y")
-    assert_f32_equal([float(am)], [oracle.gelu_amax(hb)], "gelu amax over the whole tensor")
-
-
-# --------------------------------------------------------------------------- LayerNorm producer fused with Q
-
-def run_layernorm(x, gamma, beta, fmt, scale, dev, want_y=True, eps=1e-6, amax0=0.0):
-    rows, H = x.shape
-    y = torch.empty((rows, H), dtype=torch.bfloat16, device=dev) if want_y else None
-    q = torch.empty((rows, H), dtype=torch.uint8, device=dev)
-    am = f32(amax0, dev)
-    fp8q.fp8q_layernorm_quantize_amax(x, y, q, gamma, beta, fmt, f32(scale, dev), am, eps=eps)
-    torch.cuda.synchronize()
-    return y, q, am
-
-
-def _ln_check(x, gamma, beta, fmt, scale, dev, want_y=True, eps=1e-6, amax0=0.0, what=""):
-    y, q, am = run_layernorm(x, gamma, beta, fmt, scale, dev, want_y, eps, amax0)
-    rq, ry, ra = oracle.layernorm_quantize_amax(W.bf16_bits(x), x.shape[1], gamma.cpu().numpy(),
-                                                beta.cpu().numpy(), fmt, np.float32(scale), eps=eps,
-                                                amax=amax0)
-    assert_codes_equal(q.cpu().numpy(), rq, fmt, f"ln q {what}")
-    if y is not None:
-        assert_bf16_equal(W.bf16_bits(y), ry, f"ln y {what}")
-    assert_f32_equal([float(am)], [ra], f"ln amax {what}")
-
-
-LN_SHAPES = [(1, 16), (3, 272), (2, 4096), (2, 16384), (7, 4112), (300, 48), (5, 4080), (4, 8208),
-             (33, 1024), (2, 12288)]
-
-
-@pytest.mark.parametrize("rows,H", LN_SHAPES)
-def test_layernorm_quantize_shapes(dev, rows, H):
-    """One row per CTA; 1, 2 and 4 vectors per thread, ragged last pass of vectors."""
-    x = W.residual_stream(seed=rows * 7919 + H, device=dev, shape=(rows, H))
-    gamma, beta = W.layernorm_params(H, seed=H, device=dev)
-    for k, (fmt, scale) in enumerate([(E4M3FN, 0.0123), (E5M2, 1.0), (E4M3FN, 2.0 ** 70),
-                                      (E5M2, 3.3e-3)]):
-        _ln_check(x, gamma, beta, fmt, scale, dev, want_y=(k % 2 == 0), amax0=0.25 * k,
-                  what=f"{rows}x{H} scale {scale}")
-
-
-@pytest.mark.parametrize("rows,H", [(20000, 48), (5000, 4096), (3000, 8192), (1000, 16384), (7001, 272)])
-def test_layernorm_quantize_ring_wraps(dev, rows, H):
-    """More rows than the persistent grid holds in its shared-memory rings, so
-    every stage is refilled several times (parity flips), for each ring depth."""
-    x = W.residual_stream(seed=rows + H, device=dev, shape=(rows, H))
-    gamma, beta = W.layernorm_params(H, seed=H + 1, device=dev)
-    _ln_check(x, gamma, beta, E4M3FN, 0.021, dev, want_y=True, what=f"{rows}x{H}")
-    _ln_check(x, gamma, beta, E5M2, 0.5, dev, want_y=False, what=f"{rows}x{H} e5m2")
-
-
-def test_layernorm_quantize_every_scale_and_flax_defaults(dev):
-    x = W.residual_stream(seed=5, device=dev, shape=(64, 4096))
-    ones = torch.ones(4096, dtype=torch.float32, device=dev)
-    zeros = torch.zeros(4096, dtype=torch.float32, device=dev)
-    for fmt in (E4M3FN, E5M2):
-        for s in SCALES_ALL:
-            _ln_check(x, ones, zeros, fmt, s, dev, want_y=True, what=f"scale {s!r}")
-
-
-def test_layernorm_quantize_degenerate_rows(dev):
-    """Constant rows (var = 0), eps = 0 on a constant row (rstd = inf), rows with
-    inf, NaN, huge values (Q overflows) and subnormal-scale values."""
-    H = 512
-    rows = []
-    rows.append(np.full(H, 0x3F80, np.uint16))                        # all 1.0
-    rows.append(np.zeros(H, np.uint16))                               # all +0
-    r = np.full(H, 0x4000, np.uint16); r[17] = 0x7F80; rows.append(r)   # +inf
-    r = np.full(H, 0x4000, np.uint16); r[300] = 0x7FC1; rows.append(r)  # NaN
-    r = np.full(H, 0x4000, np.uint16); r[5] = 0xFF80; r[6] = 0x7F80; rows.append(r)  # +inf and -inf
-    rows.append(np.where(np.arange(H) % 2 == 0, 0x7F00, 0xFF00).astype(np.uint16))  # +-1.7e38: Q overflows
-    rows.append(np.where(np.arange(H) % 3 == 0, 0x0001, 0x8002).astype(np.uint16))  # bf16 subnormals
-    rows.append((np.arange(H) % 7 + 0x3F80).astype(np.uint16))        # values near 1 (cancellation)
-    xb = np.stack(rows)
-    x = torch.from_numpy(xb.view(np.int16).copy()).view(torch.bfloat16).to(dev)
-    gamma, beta = W.layernorm_params(H, seed=77, device=dev)
-    for eps in (1e-6, 0.0, 1e-2):
-        for fmt in (E4M3FN, E5M2):
-            y, q, am = run_layernorm(x, gamma, beta, fmt, 0.05, dev, eps=eps)
-            rq, ry, _ = oracle.layernorm_quantize_amax(xb, H, gamma.cpu().numpy(), beta.cpu().numpy(),
-                                                       fmt, np.float32(0.05), eps=eps)
-            assert_codes_equal(q.cpu().numpy(), rq, fmt, f"eps {eps}")
-            assert_bf16_equal(W.bf16_bits(y), ry, f"eps {eps}")
-    # per-row mean and rstd agree with the oracle's statistics, through y
-    m, rs = oracle.layernorm_stats(xb[0], 1e-6)
-    assert m == np.float32(1.0) and rs == np.float32(1.0) / np.sqrt(np.float32(1e-6))
-
-
-def test_layernorm_quantize_does_not_write_outside(dev):
-    rows, H = 9, 4112
-    x = W.residual_stream(seed=3, device=dev, shape=(rows, H))
-    gamma, beta = W.layernorm_params(H, device=dev)
-    n = rows * H
-    qbuf, q = guarded(n, torch.uint8, dev, 0)
-    ybuf, y = guarded(n, torch.bfloat16, dev, 0, fill=0x5A5A)
-    am = f32(0.0, dev)
-    fp8q.fp8q_layernorm_quantize_amax(x, y.view(rows, H), q.view(rows, H), gamma, beta, E4M3FN,
-                                      f32(0.02, dev), am)
-    torch.cuda.synchronize()
-    rq, ry, ra = oracle.layernorm_quantize_amax(W.bf16_bits(x), H, gamma.cpu().numpy(), beta.cpu().numpy(),
-                                                E4M3FN, np.float32(0.02))
-    assert_codes_equal(q.cpu().numpy(), rq, E4M3FN, "guarded q")
-    assert_bf16_equal(W.bf16_bits(y), ry, "guarded y")
-    check_guards(qbuf, n, 0)
-    check_guards(ybuf, n, 0, fill=0x5A5A)
-
-
-def test_layernorm_quantize_full_size_sampled(dev):
-    """The MLP's LayerNorm input, 8192x4096: sampled rows compared in full, amax over
-    every row from the oracle."""
-    x = W.residual_stream(device=dev)
-    gamma, beta = W.layernorm_params(x.shape[1], device=dev)
-    scale = np.float32(0.031)
-    y, q, am = run_layernorm(x, gamma, beta, E4M3FN, scale, dev)
-    H = x.shape[1]
-    xb = W.bf16_bits(x).reshape(-1, H)
-    g, b = gamma.cpu().numpy(), beta.cpu().numpy()
-    rows = np.unique(np.concatenate([np.arange(8), np.arange(8184, 8192),
-                                     np.random.default_rng(0).integers(0, 8192, 200)]))
-    rq, ry, _ = oracle.layernorm_quantize_amax(xb[rows], H, g, b, E4M3FN, scale)
-    assert_codes_equal(q.cpu().numpy()[rows], rq, E4M3FN, "ln q")
-    assert_bf16_equal(W.bf16_bits(y).reshape(-1, H)[rows], ry, "ln y")
-    _, _, ra = oracle.layernorm_quantize_amax(xb, H, g, b, E4M3FN, scale)
-    assert_f32_equal([float(am)], [ra], "ln amax over the whole tensor")
-
-
-def test_layernorm_close_to_torch_layer_norm(dev):
-    """Sanity check against torch's float32 layer_norm (different summation order:
-    a few bf16 ulps at most)."""
-    x = W.residual_stream(seed=9, device=dev, shape=(256, 4096))
-    gamma, beta = W.layernorm_params(4096, device=dev)
-    y, _, _ = run_layernorm(x, gamma, beta, E4M3FN, 1.0, dev)
-    ref = torch.nn.functional.layer_norm(x.float(), (4096,), gamma, beta, eps=1e-6)
-    torch.testing.assert_close(y.float(), ref, rtol=2 ** -7, atol=1e-5)
 
 
 # --------------------------------------------------------------------------- update fused with the next quantize
@@ -1055,72 +767,3 @@ def test_fp32_max_grad_example_on_the_gpu(dev):
     torch.cuda.synchronize()
     assert hist[:, 0].tolist() == [2.0, 0.0, 0.0]
     assert sc.cpu().numpy()[0] == np.float32(2.0) / np.float32(448.0)
-
-
-def test_gelu_table_path_every_bf16_pattern(dev):
-    """Large tensors take the table path (every bf16 result computed once per SM into
-    shared memory): 2^24 elements and more for the codes alone, 2^26 with y.  All
-    65536 patterns, repeated to those sizes, against the oracle."""
-    pat = W.all_bf16_patterns(dev)
-    pb = W.bf16_bits(pat)
-    for k, (fmt, s) in enumerate([(E4M3FN, 1.0), (E5M2, 0.37), (E4M3FN, 2.0 ** 70), (E5M2, 3.0e-5),
-                                  (E4M3FN, 0.0), (E4M3FN, math.nan)]):
-        want_y = k % 2 == 0
-        reps = 1024 if want_y else 256                    # 2^26 or 2^24 elements
-        h = pat.repeat(reps)
-        y, q, am = run_gelu(h, fmt, s, dev, want_y=want_y)
-        rq, ry, _ = oracle.gelu_quantize_amax(pb, fmt, np.float32(s))
-        assert_codes_equal(q.cpu().numpy(), np.tile(rq, reps), fmt, f"table q, scale {s!r}")
-        if y is not None:
-            assert_bf16_equal(W.bf16_bits(y), np.tile(ry, reps), f"table y, scale {s!r}")
-        del h, y, q
-
-
-def test_gelu_table_path_unaligned_head_and_tail(dev):
-    n, off = (1 << 26) + 13, 3
-    g = torch.Generator(device=dev)
-    g.manual_seed(17)
-    hbuf = (torch.randn(n + 16, generator=g, device=dev) * 4.0).to(torch.bfloat16)
-    h = hbuf[off: off + n]
-    qbuf, q = guarded(n, torch.uint8, dev, off)
-    ybuf, y = guarded(n, torch.bfloat16, dev, off, fill=0x5A5A)
-    am = f32(0.0, dev)
-    fp8q.fp8q_gelu_quantize_amax(h, y, q, E4M3FN, f32(0.021, dev), am)
-    torch.cuda.synchronize()
-    rq, ry, ra = oracle.gelu_quantize_amax(W.bf16_bits(h), E4M3FN, np.float32(0.021))
-    assert_codes_equal(q.cpu().numpy(), rq, E4M3FN, "table path unaligned q")
-    assert_bf16_equal(W.bf16_bits(y), ry, "table path unaligned y")
-    assert_f32_equal([float(am)], [ra], "table path amax")
-    check_guards(qbuf, n, off)
-    check_guards(ybuf, n, off, fill=0x5A5A)
-
-
-def test_gelu_table_path_more_than_2_pow_31_elements(dev):
-    """The table path's vector and tail arithmetic stays 64-bit: 2^31 + 19 elements, with y,
-    made of every finite bf16 pattern repeated, so each output is checked through its
-    pattern and the amax is known exactly."""
-    pat = W.all_bf16_patterns(dev)
-    pb = W.bf16_bits(pat)
-    pf = (pb.astype(np.uint32) << 16).view(np.float32)
-    keep = ~np.isnan(pf)
-    fin = torch.from_numpy(pb[keep].view(np.int16).copy()).view(torch.bfloat16).to(dev)
-    m = fin.numel()
-    n = (1 << 31) + 19
-    h = fin.repeat(n // m + 1)[:n].contiguous()
-    y = torch.empty(n, dtype=torch.bfloat16, device=dev)
-    q = torch.empty(n, dtype=torch.uint8, device=dev)
-    am = f32(0.0, dev)
-    scale = np.float32(0.0123)
-    fp8q.fp8q_gelu_quantize_amax(h, y, q, E4M3FN, f32(scale, dev), am)
-    torch.cuda.synchronize()
-    rq, ry, ra = oracle.gelu_quantize_amax(pb[keep], E4M3FN, scale)
-    assert_f32_equal([float(am)], [ra], "amax over 2^31 + 19 elements")
-    rng = np.random.default_rng(5)
-    idx = np.unique(np.concatenate([np.arange(4096), np.arange(n - 8192, n),
-                                    rng.integers((1 << 31) - 8192, n, 4096), rng.integers(0, n, 60000)]))
-    assert idx.min() >= 0 and idx.max() < n          # checked on the host before the gather
-    it = torch.from_numpy(idx).to(dev)
-    assert_codes_equal(q[it].cpu().numpy(), rq[idx % m], E4M3FN, "table path n > 2^31")
-    assert_bf16_equal(W.bf16_bits(y[it]), ry[idx % m], "table path n > 2^31 y")
-    del h, y, q
-    torch.cuda.empty_cache()

@@ -765,6 +765,14 @@ def test_layernorm_tolerance_holds_a_binary32_evaluation(orc, H):
     assert np.mean(lo[benign] == hi[benign]) > 0.9
 
 
+def test_gelu_tolerance_at_infinity_is_exact(orc):
+    r = orc.gelu_ref_array(np.array([0x7F80, 0xFF80], np.uint16))
+    E = orc.gelu_tolerance(np.array([math.inf, -math.inf]), r)
+    assert E[0] == 0.0 and E[1] == orc.GELU_TINY
+    assert list(orc.bf16_within(np.array([0x7F80, 0x8000], np.uint16), r, E)) == [True, True]
+    assert not orc.bf16_within(np.array([0x7F7F], np.uint16), r[:1], E[:1])[0]
+
+
 def test_gelu_tolerance_is_not_vacuous(orc):
     """The GELU tolerance leaves one acceptable value for almost every bf16 input whose
     GELU is at least 2^-122 (below that, the binary32 reciprocal is subnormal or zero,
