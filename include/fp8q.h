@@ -45,6 +45,8 @@
  *     the launch itself failed; fp8q_last_cuda_error() (per thread) then
  *     describes it, and the error has been taken off the CUDA runtime's
  *     per-thread last error (cudaGetLastError) so that it is reported once.
+ *     Each call checks only its own launch: a runtime error that an earlier,
+ *     unrelated call left pending is neither reported nor cleared.
  *     A zero-sized call succeeds and launches nothing.
  */
 #ifndef FP8Q_H
@@ -218,8 +220,11 @@ fp8q_status fp8q_amax_scale_update_ring(float* amax_history, int32_t* head, int3
  *   *amax = max(*amax, max_i |y[i]|)
  * GELU is evaluated by a fixed sequence of correctly rounded binary32
  * operations (exp by additive range reduction and a degree-6 Taylor
- * polynomial), so it is reproducible bit for bit; it stays within 2^-16
- * relative of the exact tanh-form GELU.
+ * polynomial), so it is reproducible bit for bit: y is the bf16 rounding of a
+ * value within (6|v| + 10) 2^-24 relative of the exact tanh-form GELU, with
+ * v = 2 sqrt(2/pi) x (1 + 0.044715 x^2) (and within 2^-122 absolute where
+ * |GELU| < 2^-122).  The codes and the amax are exactly those of quantizing
+ * the y returned.
  * h_bf16: n bf16 (device).  y_bf16: n bf16 (device, written) or NULL when only
  * the FP8 codes are wanted.  q, scale, amax: as for fp8q_quantize_amax.
  * Errors: as for fp8q_quantize_amax, plus an odd y_bf16.
@@ -237,25 +242,22 @@ fp8q_status fp8q_gelu_quantize_amax(const void* h_bf16, void* y_bf16, uint8_t* q
  *   y[i]  = bf16_rne((x[i] - mean) * (rstd * gamma[i]) + beta[i])
  *   q[i]  = FP8(y[i] / *scale)           exactly fp8q_quantize_amax of y
  *   *amax = max(*amax, max |y|)          over every row
- * S = sum x and Q = sum x^2 (fma) are added in one fixed order, so results are
- * reproducible bit for bit: the row is cut into vectors of 16 elements,
- * vector v is summed in index order by lane v mod 256, lanes fold within each
- * group of 32 as a butterfly (offsets 16, 8, 4, 2, 1), and the 8 group totals
- * are added left to right.  Every other step is one correctly rounded
- * binary32 operation, without contraction.
+ * with S = sum x and Q = sum x^2.  Precision: y is the bf16 rounding of a
+ * value within a stated bound of the exact (float64) LayerNorm; the bound
+ * follows binary32 error analysis with row sums whose longest chain of
+ * additions is at most 42 (rows are summed in a fixed order, so a call is
+ * reproducible bit for bit), and y is that exact value rounded once to bf16
+ * unless it lies close to a bf16 rounding boundary.  The codes and the amax
+ * are always exactly those of quantizing the y returned.  A NaN or infinite
+ * x makes its row's y NaN.
  * x_bf16: rows * hidden bf16 (device).  y_bf16: the same (device, written)
  * or NULL when only the FP8 codes are wanted.  q: rows * hidden bytes
  * (device).  gamma, beta: hidden floats each (device).  These five must be
  * 16-byte aligned.  scale, amax: as for fp8q_quantize_amax.  hidden: a
  * multiple of 16 from 16 to 16384.
- * The kernel stages rows of x in shared memory with asynchronous bulk copies
- * and waits for each copy at most one second.  Should a wait ever run out
- * (it does not in correct operation), the call leaves *amax holding the bit
- * pattern 0x7FFFFFFF, a NaN that no bf16 data can produce, and the outputs
- * incomplete.  The first call on a device also sets the kernel's shared-memory
- * limit (cudaFuncSetAttribute) and reads its occupancy.  Those are host-side
- * calls, not stream work, so that first call may itself be captured in a CUDA
- * graph.
+ * The first call on a device reads the kernel's occupancy
+ * (cudaOccupancyMaxActiveBlocksPerMultiprocessor), a host-side query, not
+ * stream work, so that first call may itself be captured in a CUDA graph.
  * Errors: FP8Q_ERR_INVALID_ARG for a bad fmt, rows < 0, hidden < 16 or not a
  * multiple of 16, a NULL pointer (other than y_bf16) with rows > 0, or a
  * misaligned scale/amax; FP8Q_ERR_UNSUPPORTED for hidden > 16384 or a

@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 UNITS = ["quantize.cu", "producers.cu", "scale_update.cu", "abi.cu"]
 SRCS = [os.path.join(CSRC, u) for u in UNITS]
 DEPS = SRCS + [os.path.join(CSRC, h) for h in ("fp8q_common.cuh", "packed_f32.cuh", "quant_tile.cuh",
-                                                "slot_math.cuh", "mbarrier.cuh")] + [os.path.join(ROOT, "include", "fp8q.h")]
+                                                "slot_math.cuh")] + [os.path.join(ROOT, "include", "fp8q.h")]
 LIB = os.path.join(PKG, "libfp8q.so")
 OBJ_DIR = os.path.join(PKG, "_build")
 

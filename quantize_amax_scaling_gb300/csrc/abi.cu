@@ -10,16 +10,11 @@ fp8q_status cuda_fail(cudaError_t e, const char* where) {
     std::snprintf(g_last_error, sizeof g_last_error, "%s: %s (%s)", where, cudaGetErrorName(e),
                   cudaGetErrorString(e));
     // The failing runtime call also left e as the thread's last CUDA error.
-    // Consume it here, where it is reported, so that the next launch check
-    // (this library's or the caller's) does not report it a second time.
-    // A sticky error (a lost context) stays set whatever is done here.
+    // Consume it here, where it is reported, so that the caller's own next
+    // check (cudaGetLastError) does not report it a second time.  A sticky
+    // error (a lost context) stays set whatever is done here.
     (void)cudaGetLastError();
     return FP8Q_ERR_CUDA;
-}
-
-fp8q_status after_launch(const char* where) {
-    cudaError_t e = cudaGetLastError();
-    return e == cudaSuccess ? FP8Q_OK : cuda_fail(e, where);
 }
 
 }  // namespace fp8q_detail

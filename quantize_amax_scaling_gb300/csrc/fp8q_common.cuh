@@ -64,8 +64,22 @@
 // Host-side error reporting, shared by every translation unit (abi.cu).
 namespace fp8q_detail {
 fp8q_status cuda_fail(cudaError_t e, const char* where);   // records the text, returns FP8Q_ERR_CUDA
-fp8q_status after_launch(const char* where);               // cudaGetLastError -> status
 extern thread_local char g_last_error[256];
+
+// Launch `kern` on `s` and report that launch's own status.  A runtime error
+// that an earlier, unrelated call left pending is neither reported nor
+// cleared here: only a failure of this launch becomes FP8Q_ERR_CUDA.
+template <typename... KArgs, typename... Args>
+fp8q_status launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                          const char* where, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+    return e == cudaSuccess ? FP8Q_OK : cuda_fail(e, where);
+}
 
 inline bool valid_fmt(int fmt) { return fmt == FP8Q_E4M3FN || fmt == FP8Q_E5M2; }
 

@@ -2,7 +2,6 @@
 // GELU (elementwise) and LayerNorm (row-wise).
 
 #include "fp8q_common.cuh"
-#include "mbarrier.cuh"
 #include "packed_f32.cuh"
 
 #include <mutex>
@@ -215,6 +214,10 @@ constexpr int kGeluTableUnroll = 2;
 template <bool WRITE_Y>
 __host__ __device__ constexpr int gelu_table_cluster() { return WRITE_Y ? 4 : 2; }
 
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -231,6 +234,15 @@ __device__ __forceinline__ uint32_t cluster_map(uint32_t cta_addr, uint32_t rank
 __device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
+
+// The split cluster barrier: every thread of every CTA of the cluster arrives
+// (relaxed: no memory ordering), and a later wait returns once all have
+// arrived -- in particular once every CTA of the cluster is running.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
 
 // Every thread of every CTA of the cluster arrives; the stores made before
 // are visible to all of them afterwards.
@@ -255,15 +267,24 @@ __global__ void __launch_bounds__(gelu_table_threads<WRITE_Y>(), 1)
     __shared__ uint32_t red[kGeluTableThreads / 32];
     {
         constexpr int kGeluTableCluster = gelu_table_cluster<WRITE_Y>();
-        constexpr int kShare = 32768 / kGeluTableCluster;
+        constexpr int kShare = 32768 / kGeluTableCluster;  // at least the CTA's thread count
+        // No CTA may touch another's shared memory before that CTA is known to
+        // be running: arrive on the cluster barrier now, and wait on it just
+        // before the first remote store, with the first pair computed meanwhile.
+        cluster_arrive_relaxed();
         const uint32_t rank = cluster_ctarank();
         uint32_t dst[kGeluTableCluster];
 #pragma unroll
         for (int r = 0; r < kGeluTableCluster; ++r) dst[r] = cluster_map(smem_addr(tab32), (uint32_t)r);
-        for (int p = (int)rank * kShare + threadIdx.x; p < ((int)rank + 1) * kShare; p += kGeluTableThreads) {
-            const uint32_t y = gelu_pair((uint32_t)(2 * p) | ((uint32_t)(2 * p + 1) << 16));
+        int p = (int)rank * kShare + threadIdx.x;
+        uint32_t y = gelu_pair((uint32_t)(2 * p) | ((uint32_t)(2 * p + 1) << 16));
+        cluster_wait();
+        for (;;) {
 #pragma unroll
             for (int r = 0; r < kGeluTableCluster; ++r) st_cluster_u32(dst[r] + 4u * (uint32_t)p, y);
+            p += kGeluTableThreads;
+            if (p >= ((int)rank + 1) * kShare) break;
+            y = gelu_pair((uint32_t)(2 * p) | ((uint32_t)(2 * p + 1) << 16));
         }
     }
     const QScale c = make_qscale(a.scale);
@@ -328,46 +349,34 @@ __global__ void __launch_bounds__(gelu_table_threads<WRITE_Y>(), 1)
 // ----------------------------------------------------------------------------
 // LayerNorm producer fused with quantize + amax
 //
-// Flax's default LayerNorm in binary32, row by row (H elements, H a multiple
-// of 16, at most 16384): mean = S / H, var = max(0, Q / H - mean^2),
+// Flax's default LayerNorm in binary32, row by row (H elements, a multiple of
+// 16, at most 16384): mean = S / H, var = max(0, Q / H - mean^2) (a NaN kept),
 // rstd = 1 / sqrt(var + eps), y = (x - mean) * (rstd * gamma) + beta rounded
-// to bf16, then the quantize path on y.  S and Q are summed in one fixed
-// association that the CPU reference of this library writes out the same way:
-// the row is cut into 16-element vectors, vector v belongs to summation lane
-// v mod 256, each lane adds its elements in index order (s = s + x,
-// q = fma(x, x, q)), each group of 32 lanes folds as a butterfly (lanes k and
-// k ^ o for o = 16, 8, 4, 2, 1), and the 8 group totals are added left to
-// right.
+// to bf16, then the quantize path on y: FP8 codes of y / scale and
+// amax = max |y|.
 //
-// Persistent grid (as many CTAs as fit at once, at most one per batch).  A
-// batch is R consecutive rows (R <= 8, chosen so that two batches fit the
-// shared-memory ring); CTA b takes batches b, b + G, ...  A batch arrives by
-// one cp.async.bulk copy completing on the mbarrier of its ring slot, and the
-// slot is refilled with the batch two ahead once the CTA is done with it, so
-// one batch is always in flight while the CTA computes the other.
+// A row belongs to a group of G = ceil(H / 4096) warps.  Lane l of warp g of
+// the group holds the 8-element vectors l + 32 (g + G i), i < KV, of the row
+// in registers (KV = H / (256 G), rounded up to a power of two; vectors past
+// the row read as +0), so x comes from HBM once and nothing is staged in
+// shared memory.  The sums S = sum x and Q = sum x^2 (an exact product inside
+// each fma) run in four chains per lane (2 KV elements each), fold pairwise,
+// fold across the warp as an xor butterfly (the two lanes of each exchange
+// add the same two values, so every lane ends with the same bits), and for
+// G > 1 the warp totals are added in warp order after a named barrier of the
+// group.  The longest chain of additions is 2 KV + 2 + 5 + (G - 1) <= 42.
+// The output step then normalises each pair of elements with the bf16 operand
+// taken straight from its word (add.f32.bf16), rstd * gamma and the fused
+// multiply-add with beta two lanes at a time, rounds to bf16 and quantizes.
 //
-// Phase 1: warp w computes the statistics of row w of the batch alone.  Lane
-// p holds the eight summation lanes k0 + 4m (m = 0..7) of summation group
-// p / 4, with k0 = p mod 4, so the butterfly levels 16, 8 and 4 are register
-// adds and only levels 2 and 1 cross lanes; the eight group totals are then
-// gathered with shuffles and added left to right.  No block barrier is
-// involved.
-// Phase 2: after one barrier, all 256 threads normalise and quantize the
-// batch.  Thread t owns the 8-element half-vectors t, t + 256, ... of every
-// row; with H <= 4096 those are at most two, and their gamma and beta stay in
-// registers for the whole launch.  Shared-memory reads are 16 bytes per lane
-// at consecutive addresses (no bank conflicts).
-//
-// Every mbarrier wait has a time limit (kWaitLimitNs).  The CTA agrees on the
-// outcome at the next barrier; if any thread gave up, the CTA stores the
-// pattern 0x7FFFFFFF (a NaN that no bf16 input can produce) into *amax, waits
-// (again bounded) for its copies still in flight and returns.
+// Each CTA takes a contiguous, balanced range of rows, and its groups take
+// every (8 / G)-th row of it; a group asks L2 for its next row (one bulk
+// prefetch) before it loads the current one, so HBM keeps streaming while the
+// group computes.  No thread waits on anything but the group's named barrier
+// and one CTA barrier at the end, both in uniform control flow.
 
-constexpr int kLnMaxHalfPerThread = 8;           // H <= 256 * 8 * 8 = 16384
-constexpr int kLnMaxBatch = kThreads / 32;       // rows per batch: one warp each in phase 1
-constexpr int kLnBufs = 2;                       // batches in the ring
-constexpr uint32_t kLnRingBytes = 64u * 1024u;   // ring per CTA (both batches)
-constexpr int kAmaxTimeoutBits = 0x7FFFFFFF;
+constexpr int kLnMaxH = 16384;
+constexpr int kLnWarpCols = 4096;  // columns per warp at most (KV <= 16)
 
 struct LnArgs {
     const uint16_t* x;
@@ -379,20 +388,35 @@ struct LnArgs {
     float* amax;
     int64_t rows;
     int32_t H;
-    int32_t batch;  // rows per batch, 1 .. kLnMaxBatch
     float eps;
 };
 
-
 // Streaming stores whose target this kernel never reads back: no memory
-// clobber, so shared-memory loads of the next rows may be scheduled across
-// them.
+// clobber, so the loads of later rows may be scheduled across them.
 __device__ __forceinline__ void st_cs_v4(void* p, uint4 v) {
     asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
 }
 
 __device__ __forceinline__ void st_cs_v2(void* p, uint2 v) {
     asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y));
+}
+
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// Ask L2 to fetch `bytes` (a multiple of 16, 16-byte aligned) starting at p.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Named barrier `id` over `threads` threads (whole warps).
+__device__ __forceinline__ void named_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 // s = s + x and q = fma(x, x, q) for x the low (LO) or high half of a word of
@@ -428,303 +452,201 @@ __device__ __forceinline__ float add_bf16(uint32_t w, float c) {
     return d;
 }
 
-// Phase 1: (-mean, rstd) of one row (nv vectors in shared memory), computed by
-// one warp in the fixed summation order.  Lane p holds summation lanes
-// k0 + 4m of group j (p = 4j + k0); its vectors are those lanes' vectors
-// l, l + 256, ... in index order.  Four vectors are loaded at a time and their
-// four chains advanced element by element, so the adds of different chains
-// overlap.  A vector past the end of the row reads as +0.0: every partial sum
-// starts at +0 and can never become -0, so adding +0 leaves it unchanged.
-template <int VPL>  // most vectors one summation lane owns: ceil(nv / 256)
-__device__ __forceinline__ float2 ln_row_stats(const uint8_t* row, int nv, int H, float eps) {
-    const int lane = threadIdx.x & 31;
-    const int base = 32 * (lane >> 2) + (lane & 3);
-    float s[8], q[8];
-#pragma unroll
-    for (int m = 0; m < 8; ++m) s[m] = q[m] = 0.0f;
-#pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-#pragma unroll
-        for (int m0 = 0; m0 < 8; m0 += 4) {
-            uint32_t w[4][8];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const int v = base + 4 * (m0 + m) + 256 * i;
-                uint4 h0 = make_uint4(0u, 0u, 0u, 0u), h1 = h0;
-                if (v < nv) {
-                    const uint4* p = reinterpret_cast<const uint4*>(row + 32 * v);
-                    h0 = p[0];
-                    h1 = p[1];
-                }
-                w[m][0] = h0.x; w[m][1] = h0.y; w[m][2] = h0.z; w[m][3] = h0.w;
-                w[m][4] = h1.x; w[m][5] = h1.y; w[m][6] = h1.z; w[m][7] = h1.w;
-            }
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-#pragma unroll
-                for (int m = 0; m < 4; ++m) acc_bf16<true>(w[m][e], s[m0 + m], q[m0 + m]);
-#pragma unroll
-                for (int m = 0; m < 4; ++m) acc_bf16<false>(w[m][e], s[m0 + m], q[m0 + m]);
-            }
-        }
-    }
-    // butterfly levels 16, 8, 4 inside the lane, 2 and 1 across lanes
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-        s[m] = __fadd_rn(s[m], s[m + 4]);
-        q[m] = __fadd_rn(q[m], q[m + 4]);
-    }
-#pragma unroll
-    for (int m = 0; m < 2; ++m) {
-        s[m] = __fadd_rn(s[m], s[m + 2]);
-        q[m] = __fadd_rn(q[m], q[m + 2]);
-    }
-    float st = __fadd_rn(s[0], s[1]), qt = __fadd_rn(q[0], q[1]);
-    st = __fadd_rn(st, __shfl_xor_sync(0xFFFFFFFFu, st, 2));
-    qt = __fadd_rn(qt, __shfl_xor_sync(0xFFFFFFFFu, qt, 2));
-    st = __fadd_rn(st, __shfl_xor_sync(0xFFFFFFFFu, st, 1));
-    qt = __fadd_rn(qt, __shfl_xor_sync(0xFFFFFFFFu, qt, 1));
-    // group totals sit in lanes 0, 4, ..., 28: add them left to right
-    float S = __shfl_sync(0xFFFFFFFFu, st, 0), Q = __shfl_sync(0xFFFFFFFFu, qt, 0);
-#pragma unroll
-    for (int j = 1; j < 8; ++j) {
-        S = __fadd_rn(S, __shfl_sync(0xFFFFFFFFu, st, 4 * j));
-        Q = __fadd_rn(Q, __shfl_sync(0xFFFFFFFFu, qt, 4 * j));
-    }
-    const float Hf = (float)H;
-    const float mean = __fdiv_rn(S, Hf);
-    float var = __fsub_rn(__fdiv_rn(Q, Hf), __fmul_rn(mean, mean));
-    var = var > 0.0f ? var : 0.0f;
-    return make_float2(-mean, __frcp_rn(__fsqrt_rn(__fadd_rn(var, eps))));
+// One word of two bf16 of x -> one word of two bf16 of y.
+__device__ __forceinline__ uint32_t ln_pair(uint32_t w, float nmean, float2 rstd2, float2 g, float2 b) {
+    const float2 d = make_float2(add_bf16<true>(w, nmean), add_bf16<false>(w, nmean));
+    const float2 y = fma2_rn(d, mul2_rn(rstd2, g), b);
+    return cvt_bf16x2(y.x, y.y);
 }
 
-// Eight bf16 of x (one uint4) -> eight bf16 of y:
-// y = ((x + (-mean)) * (rstd * gamma)) + beta, each step rounded on its own
-// (x + (-mean) is x - mean, taken with x as a bf16 operand; rstd * gamma two
-// lanes at a time).
-__device__ __forceinline__ uint4 ln_normalize8(uint4 w, const float2 (&g)[4], const float2 (&b)[4],
-                                               float2 nmean, float2 rstd) {
-    const uint32_t in[4] = {w.x, w.y, w.z, w.w};
-    uint32_t out[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const float2 d = make_float2(add_bf16<true>(in[k], nmean.x), add_bf16<false>(in[k], nmean.y));
-        const float2 m = mul2_rn(rstd, g[k]);
-        out[k] = cvt_bf16x2(__fadd_rn(__fmul_rn(d.x, m.x), b[k].x), __fadd_rn(__fmul_rn(d.y, m.y), b[k].y));
-    }
-    return make_uint4(out[0], out[1], out[2], out[3]);
-}
-
-// quant_pair (fast path) with the first product taken two lanes at a time.
+// quant_pair's fast path, two lanes at a time: y0 = RN(x r), e = fma(y0, s, -x),
+// y = fma(-e, r, y0) is the correctly rounded quotient in each lane.
 template <int FMT>
-__device__ __forceinline__ uint32_t quant_pair_x2(uint32_t w, const QScale& c, float2 r2) {
+__device__ __forceinline__ uint32_t quant_pair_x2(uint32_t w, const QScale& c) {
     w = bf16x2_clamp(w, c.t2);
     const float2 x = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
-    const float2 y0 = mul2_rn(x, r2);
-    const float e0 = __fmaf_rn(y0.x, c.s, -x.x);
-    const float e1 = __fmaf_rn(y0.y, c.s, -x.y);
-    return cvt_fp8x2<FMT>(__fmaf_rn(-e0, c.r, y0.x), __fmaf_rn(-e1, c.r, y0.y));
+    const float2 y0 = mul2_rn(x, splat2(c.r));
+    const float2 e = fma2_rn(y0, splat2(c.s), make_float2(-x.x, -x.y));
+    const float2 y = fma2_rn(make_float2(-e.x, -e.y), splat2(c.r), y0);
+    return cvt_fp8x2<FMT>(y.x, y.y);
 }
 
 // Eight bf16 of y -> eight FP8 codes.
-template <int FMT>
-__device__ __forceinline__ uint2 ln_quant8(const uint4& y, const QScale& c, float2 r2) {
-    if (c.fast)
-        return make_uint2(quant_pair_x2<FMT>(y.x, c, r2) | (quant_pair_x2<FMT>(y.y, c, r2) << 16),
-                          quant_pair_x2<FMT>(y.z, c, r2) | (quant_pair_x2<FMT>(y.w, c, r2) << 16));
+template <int FMT, bool FAST>
+__device__ __forceinline__ uint2 ln_quant8(const uint4& y, const QScale& c) {
+    if (FAST)
+        return make_uint2(quant_pair_x2<FMT>(y.x, c) | (quant_pair_x2<FMT>(y.y, c) << 16),
+                          quant_pair_x2<FMT>(y.z, c) | (quant_pair_x2<FMT>(y.w, c) << 16));
     return make_uint2(quant_quad<FMT, false>(y.x, y.y, c), quant_quad<FMT, false>(y.z, y.w, c));
 }
 
-// One half-vector of the output: y (optional), its |y| into m2, its FP8 codes.
-template <int FMT, bool WRITE_Y>
-__device__ __forceinline__ void ln_out8(const LnArgs& a, uint4 w, const float2 (&g)[4], const float2 (&b)[4],
-                                        float2 stats, const QScale& c, float2 r2, int64_t off, uint32_t& m2) {
-    const uint4 yv = ln_normalize8(w, g, b, make_float2(stats.x, stats.x), make_float2(stats.y, stats.y));
-    if (WRITE_Y) st_cs_v4(a.y + off, yv);
-    m2 = bf16x2_absmax(m2, bf16x2_absmax(bf16x2_absmax(yv.x, yv.y), bf16x2_absmax(yv.z, yv.w)));
-    st_cs_v2(a.q + off, ln_quant8<FMT>(yv, c, r2));
+__device__ __forceinline__ float max_nan_f32(float a, float b) {
+    float d;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+    return d;
 }
 
-__device__ __forceinline__ void load4f2(const float* p, float2 (&d)[4]) {
-    const float4 u = __ldg(reinterpret_cast<const float4*>(p));
-    const float4 v = __ldg(reinterpret_cast<const float4*>(p) + 1);
-    d[0] = make_float2(u.x, u.y);
-    d[1] = make_float2(u.z, u.w);
-    d[2] = make_float2(v.x, v.y);
-    d[3] = make_float2(v.z, v.w);
-}
+template <int G>
+__host__ __device__ constexpr int ln_threads() { return 32 * G * (8 / G); }
 
-// HPT: most 8-element half-vectors a thread owns per row (ceil(H / 2048)).
-template <int FMT, bool WRITE_Y, int HPT>
-__global__ void __launch_bounds__(kThreads, 2) layernorm_quantize_amax_kernel(const LnArgs a) {
-    extern __shared__ __align__(128) uint8_t ring[];  // kLnBufs batches of a.batch rows of 2H bytes
-    __shared__ uint64_t bar[kLnBufs];
-    __shared__ float2 stats[kLnMaxBatch];  // (-mean, rstd) of each row of the batch
-    __shared__ uint32_t red[kThreads / 32];
-    constexpr bool kGammaInRegs = (HPT <= 2);
-    constexpr int VPL = (HPT + 1) / 2;  // vectors per summation lane
-    const int nv = a.H / 16, nh = a.H / 8;
-    const int R = a.batch;
-    const uint32_t row_bytes = 2u * (uint32_t)a.H;
-    const uint32_t buf_bytes = (uint32_t)R * row_bytes;
-    const int64_t nb = (a.rows + R - 1) / R;
-    const int64_t G = gridDim.x;
-    const int64_t n_mine = (nb - 1 - blockIdx.x) / G + 1;  // the launch keeps G <= nb
-    const int warp = threadIdx.x >> 5;
-
-    if (threadIdx.x == 0) {
-        for (int b = 0; b < kLnBufs; ++b) mbar_init(&bar[b]);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        for (int64_t k = 0; k < kLnBufs && k < n_mine; ++k) {
-            const int64_t r0 = (blockIdx.x + k * G) * R;
-            const int64_t nr = a.rows - r0 < R ? a.rows - r0 : R;
-            bulk_load(ring + (size_t)k * buf_bytes, a.x + r0 * a.H, (uint32_t)nr * row_bytes, &bar[k]);
+// The output of one row: y (optional), |y| into m2, the FP8 codes.
+template <int FMT, bool WRITE_Y, int KV, int G, bool FAST>
+__device__ __forceinline__ void ln_emit_row(const LnArgs& a, const uint4 (&v)[KV], int64_t row, int gw, int lane,
+                                            int nv, float nmean, float rstd, const QScale& c, uint32_t& m2) {
+    const float2 rstd2 = splat2(rstd);
+#pragma unroll
+    for (int i = 0; i < KV; ++i) {
+        const int j = lane + 32 * (gw + G * i);
+        if (j < nv) {
+            const float4 g0 = __ldg(reinterpret_cast<const float4*>(a.gamma) + 2 * j);
+            const float4 g1 = __ldg(reinterpret_cast<const float4*>(a.gamma) + 2 * j + 1);
+            const float4 b0 = __ldg(reinterpret_cast<const float4*>(a.beta) + 2 * j);
+            const float4 b1 = __ldg(reinterpret_cast<const float4*>(a.beta) + 2 * j + 1);
+            uint4 yv;
+            yv.x = ln_pair(v[i].x, nmean, rstd2, make_float2(g0.x, g0.y), make_float2(b0.x, b0.y));
+            yv.y = ln_pair(v[i].y, nmean, rstd2, make_float2(g0.z, g0.w), make_float2(b0.z, b0.w));
+            yv.z = ln_pair(v[i].z, nmean, rstd2, make_float2(g1.x, g1.y), make_float2(b1.x, b1.y));
+            yv.w = ln_pair(v[i].w, nmean, rstd2, make_float2(g1.z, g1.w), make_float2(b1.z, b1.w));
+            const int64_t off = row * a.H + 8 * (int64_t)j;
+            if (WRITE_Y) st_cs_v4(a.y + off, yv);
+            m2 = bf16x2_absmax(m2, bf16x2_absmax(bf16x2_absmax(yv.x, yv.y), bf16x2_absmax(yv.z, yv.w)));
+            st_cs_v2(a.q + off, ln_quant8<FMT, FAST>(yv, c));
         }
     }
+}
+
+template <int FMT, bool WRITE_Y, int KV, int G>
+__global__ void __launch_bounds__(ln_threads<G>(), 2) layernorm_quantize_amax_kernel(const LnArgs a) {
+    constexpr int kGroups = 8 / G;
+    constexpr int kWarps = G * kGroups;
+    __shared__ float2 part[kGroups][2][G];  // (S, Q) of each warp of a group, by row parity
+    __shared__ uint32_t red[kWarps];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int grp = warp / G, gw = warp % G;
+    const int nv = a.H >> 3;
+    const int64_t r_begin = a.rows * (int64_t)blockIdx.x / gridDim.x;
+    const int64_t r_end = a.rows * ((int64_t)blockIdx.x + 1) / gridDim.x;
     const QScale c = make_qscale(a.scale);
-    const float2 r2 = make_float2(c.r, c.r);
-    float2 gr[kGammaInRegs ? HPT : 1][4], br[kGammaInRegs ? HPT : 1][4];
-    if (kGammaInRegs) {
-#pragma unroll
-        for (int i = 0; i < (kGammaInRegs ? HPT : 0); ++i) {
-            const int u = threadIdx.x + i * kThreads;
-            if (u < nh) {
-                load4f2(a.gamma + 8 * u, gr[i]);
-                load4f2(a.beta + 8 * u, br[i]);
-            }
-        }
-    }
-    __syncthreads();  // barriers initialised before anyone waits on them
-
+    const float Hf = (float)a.H;
+    const uint32_t row_bytes = 2u * (uint32_t)a.H;
     uint32_t m2 = 0;
-    bool ok = true;
-    int64_t k = 0;
-    for (; k < n_mine; ++k) {
-        const int buf = (int)(k % kLnBufs);
-        const uint32_t parity = (uint32_t)((k / kLnBufs) & 1);
-        const int64_t r0 = (blockIdx.x + k * G) * R;
-        const int nr = a.rows - r0 < R ? (int)(a.rows - r0) : R;
-        const uint8_t* base = ring + (size_t)buf * buf_bytes;
-        const bool arrived = mbar_wait(&bar[buf], parity);
-        if (arrived && warp < nr) {
-            const float2 st = ln_row_stats<VPL>(base + (size_t)warp * row_bytes, nv, a.H, a.eps);
-            if ((threadIdx.x & 31) == 0) stats[warp] = st;
+    int parity = 0;
+    for (int64_t row = r_begin + grp; row < r_end; row += kGroups, parity ^= 1) {
+        if (gw == 0 && lane == 0 && row + kGroups < r_end)
+            prefetch_l2_bulk(a.x + (row + kGroups) * a.H, row_bytes);
+        const uint16_t* xr = a.x + row * a.H;
+        uint4 v[KV];
+#pragma unroll
+        for (int i = 0; i < KV; ++i) {
+            const int j = lane + 32 * (gw + G * i);
+            v[i] = j < nv ? ld_stream_v4(xr + 8 * j) : make_uint4(0u, 0u, 0u, 0u);
         }
-        ok = __syncthreads_and(arrived) != 0;
-        if (!ok) break;  // uniform
-        // two rows at a time: independent work for the scheduler, gamma and beta read once
-        for (int r = 0; r < nr; r += 2) {
-            const bool pair = r + 1 < nr;
-            const float2 s0 = stats[r], s1 = stats[pair ? r + 1 : r];
-            const uint8_t* srow = base + (size_t)r * row_bytes;
-            const int64_t row_off = (r0 + r) * a.H;
+        float s[4] = {0.0f, 0.0f, 0.0f, 0.0f}, q[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-            for (int i = 0; i < HPT; ++i) {
-                const int u = threadIdx.x + i * kThreads;
-                if (u < nh) {
-                    const uint4 w0 = *reinterpret_cast<const uint4*>(srow + 16 * u);
-                    uint4 w1 = w0;
-                    if (pair) w1 = *reinterpret_cast<const uint4*>(srow + row_bytes + 16 * u);
-                    float2 g[4], b[4];
-                    if (kGammaInRegs) {
+        for (int i = 0; i < KV; ++i) {
+            acc_bf16<true>(v[i].x, s[0], q[0]);
+            acc_bf16<true>(v[i].y, s[1], q[1]);
+            acc_bf16<true>(v[i].z, s[2], q[2]);
+            acc_bf16<true>(v[i].w, s[3], q[3]);
+            acc_bf16<false>(v[i].x, s[0], q[0]);
+            acc_bf16<false>(v[i].y, s[1], q[1]);
+            acc_bf16<false>(v[i].z, s[2], q[2]);
+            acc_bf16<false>(v[i].w, s[3], q[3]);
+        }
+        float S = __fadd_rn(__fadd_rn(s[0], s[1]), __fadd_rn(s[2], s[3]));
+        float Q = __fadd_rn(__fadd_rn(q[0], q[1]), __fadd_rn(q[2], q[3]));
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            g[e] = gr[kGammaInRegs ? i : 0][e];
-                            b[e] = br[kGammaInRegs ? i : 0][e];
-                        }
-                    } else {
-                        load4f2(a.gamma + 8 * u, g);
-                        load4f2(a.beta + 8 * u, b);
-                    }
-                    const int64_t off = row_off + 8 * u;
-                    ln_out8<FMT, WRITE_Y>(a, w0, g, b, s0, c, r2, off, m2);
-                    if (pair) ln_out8<FMT, WRITE_Y>(a, w1, g, b, s1, c, r2, off + a.H, m2);
-                }
+        for (int o = 16; o >= 1; o >>= 1) {
+            S = __fadd_rn(S, __shfl_xor_sync(0xFFFFFFFFu, S, o));
+            Q = __fadd_rn(Q, __shfl_xor_sync(0xFFFFFFFFu, Q, o));
+        }
+        if (G > 1) {
+            if (lane == 0) part[grp][parity][gw] = make_float2(S, Q);
+            named_sync(1 + grp, 32 * G);
+            // every warp of the group adds the warp totals in the same order
+            float2 t = part[grp][parity][0];
+#pragma unroll
+            for (int k = 1; k < G; ++k) {
+                const float2 u = part[grp][parity][k];
+                t.x = __fadd_rn(t.x, u.x);
+                t.y = __fadd_rn(t.y, u.y);
             }
+            S = t.x;
+            Q = t.y;
         }
-        __syncthreads();  // every thread is done with this slot and with stats[]
-        if (threadIdx.x == 0 && k + kLnBufs < n_mine) {  // refill the slot, kLnBufs batches ahead
-            const int64_t next_r0 = (blockIdx.x + (k + kLnBufs) * G) * R;
-            const int64_t next_nr = a.rows - next_r0 < R ? a.rows - next_r0 : R;
-            bulk_load(ring + (size_t)buf * buf_bytes, a.x + next_r0 * a.H, (uint32_t)next_nr * row_bytes, &bar[buf]);
-        }
+        const float mean = __fdiv_rn(S, Hf);
+        const float var = max_nan_f32(__fsub_rn(__fdiv_rn(Q, Hf), __fmul_rn(mean, mean)), 0.0f);
+        const float rstd = __frsqrt_rn(__fadd_rn(var, a.eps));
+        if (c.fast) ln_emit_row<FMT, WRITE_Y, KV, G, true>(a, v, row, gw, lane, nv, -mean, rstd, c, m2);
+        else        ln_emit_row<FMT, WRITE_Y, KV, G, false>(a, v, row, gw, lane, nv, -mean, rstd, c, m2);
     }
-    if (!ok) {
-        // A copy did not arrive in time: mark the result, then wait (bounded)
-        // for the copies this CTA still has in flight before leaving.
-        if (threadIdx.x == 0) {
-            atomicMax(reinterpret_cast<int*>(a.amax), kAmaxTimeoutBits);
-            for (int64_t j = k; j < n_mine && j < k + kLnBufs; ++j)
-                mbar_wait(&bar[j % kLnBufs], (uint32_t)((j / kLnBufs) & 1));
-        }
-        return;
+    // CTA-wide max of |y|, one atomic
+    uint32_t m = max(abs_bits_lo(m2), m2 & 0x7FFF0000u);
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t b = red[0];
+#pragma unroll
+        for (int w = 1; w < kWarps; ++w) b = max(b, red[w]);
+        atomicMax(reinterpret_cast<int*>(a.amax), (int)b);
     }
-    flush_amax(m2, 0u, a.amax, red);
 }
 
-// Resident CTAs of one kernel instantiation at a given dynamic shared-memory
-// size, per device (the persistent LayerNorm grid).  The first use on a device
-// also raises the kernel's dynamic shared-memory limit to kLnRingBytes.
+// Resident CTAs of one kernel per device, taken on the first launch there
+// (the persistent LayerNorm grid and the GELU table path).
 struct ResidentCache {
     std::mutex mu;
     struct Entry {
         int dev;
-        uint32_t smem;
         int ctas;
     } e[32];
     int n = 0;
 };
 
-template <class K>
-cudaError_t resident_ctas(K kern, int threads, uint32_t smem, ResidentCache& cache, int* ctas) {
-    int dev = 0;
+template <int FMT, bool WRITE_Y, int KV, int G>
+fp8q_status launch_layernorm_kv(const LnArgs& a, cudaStream_t s) {
+    static ResidentCache cache;
+    auto kern = layernorm_quantize_amax_kernel<FMT, WRITE_Y, KV, G>;
+    constexpr int threads = ln_threads<G>();
+    int dev = 0, ctas = 0;
     cudaError_t err = cudaGetDevice(&dev);
-    if (err != cudaSuccess) return err;
-    std::lock_guard<std::mutex> lock(cache.mu);
-    for (int k = 0; k < cache.n; ++k) {
-        if (cache.e[k].dev == dev && cache.e[k].smem == smem) {
-            *ctas = cache.e[k].ctas;
-            return cudaSuccess;
+    if (err == cudaSuccess) {
+        std::lock_guard<std::mutex> lock(cache.mu);
+        for (int k = 0; k < cache.n; ++k)
+            if (cache.e[k].dev == dev) ctas = cache.e[k].ctas;
+        if (ctas == 0) {
+            int per_sm = 0, sms = 0;
+            err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, 0);
+            if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            if (err == cudaSuccess && per_sm < 1) err = cudaErrorInvalidConfiguration;
+            if (err == cudaSuccess) {
+                ctas = per_sm * sms;
+                if (cache.n < 32) cache.e[cache.n++] = {dev, ctas};
+            }
         }
     }
-    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLnRingBytes);
-    if (err != cudaSuccess) return err;
-    int per_sm = 0, sms = 0;
-    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
-    if (err != cudaSuccess) return err;
-    err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (err != cudaSuccess) return err;
-    if (per_sm < 1) return cudaErrorInvalidConfiguration;
-    *ctas = per_sm * sms;
-    if (cache.n < 32) cache.e[cache.n++] = {dev, smem, *ctas};
-    return cudaSuccess;
-}
-
-template <int FMT, bool WRITE_Y, int HPT>
-fp8q_status launch_layernorm_hpt(LnArgs a, cudaStream_t s) {
-    static ResidentCache cache;
-    auto kern = layernorm_quantize_amax_kernel<FMT, WRITE_Y, HPT>;
-    const uint32_t row_bytes = 2u * (uint32_t)a.H;
-    uint32_t batch = kLnRingBytes / (kLnBufs * row_bytes);
-    batch = batch < 1 ? 1 : (batch > (uint32_t)kLnMaxBatch ? (uint32_t)kLnMaxBatch : batch);
-    a.batch = (int32_t)batch;
-    const uint32_t smem = kLnBufs * batch * row_bytes;
-    int ctas = 0;
-    const cudaError_t err = resident_ctas(kern, kThreads, smem, cache, &ctas);
     if (err != cudaSuccess) return cuda_fail(err, "layernorm_quantize_amax_kernel setup");
-    const int64_t batches = (a.rows + batch - 1) / batch;
-    const int64_t grid = batches < (int64_t)ctas ? batches : (int64_t)ctas;
-    kern<<<(unsigned)grid, kThreads, smem, s>>>(a);
-    return after_launch("layernorm_quantize_amax_kernel");
+    // as many CTAs as fit at once, but no more than give each group a row
+    const int64_t want = (a.rows + (8 / G) - 1) / (8 / G);
+    const int grid = (int)(want < (int64_t)ctas ? want : (int64_t)ctas);
+    return launch_kernel(kern, dim3((unsigned)grid), dim3(threads), 0, s, "layernorm_quantize_amax_kernel", a);
 }
 
 template <int FMT, bool WRITE_Y>
 fp8q_status launch_layernorm(const LnArgs& a, cudaStream_t s) {
-    const int hpt = (a.H / 8 + kThreads - 1) / kThreads;  // half-vectors per thread
-    if (hpt <= 1) return launch_layernorm_hpt<FMT, WRITE_Y, 1>(a, s);
-    if (hpt <= 2) return launch_layernorm_hpt<FMT, WRITE_Y, 2>(a, s);
-    if (hpt <= 4) return launch_layernorm_hpt<FMT, WRITE_Y, 4>(a, s);
-    return launch_layernorm_hpt<FMT, WRITE_Y, 8>(a, s);
+    const int G = (a.H + kLnWarpCols - 1) / kLnWarpCols;
+    const int kv = (a.H / 8 + 32 * G - 1) / (32 * G);  // vectors per lane
+    if (G == 1) {
+        if (kv <= 1) return launch_layernorm_kv<FMT, WRITE_Y, 1, 1>(a, s);
+        if (kv <= 2) return launch_layernorm_kv<FMT, WRITE_Y, 2, 1>(a, s);
+        if (kv <= 4) return launch_layernorm_kv<FMT, WRITE_Y, 4, 1>(a, s);
+        if (kv <= 8) return launch_layernorm_kv<FMT, WRITE_Y, 8, 1>(a, s);
+        return launch_layernorm_kv<FMT, WRITE_Y, 16, 1>(a, s);
+    }
+    if (G == 2) return launch_layernorm_kv<FMT, WRITE_Y, 16, 2>(a, s);
+    if (G == 3) return launch_layernorm_kv<FMT, WRITE_Y, 16, 3>(a, s);
+    return launch_layernorm_kv<FMT, WRITE_Y, 16, 4>(a, s);
 }
 
 template <int FMT, bool WRITE_Y>
@@ -761,7 +683,7 @@ fp8q_status launch_gelu_table(const GeluArgs& a, cudaStream_t s) {
             if (err == cudaSuccess && clusters < 1) err = cudaErrorInvalidConfiguration;
             if (err == cudaSuccess) {
                 ctas = clusters * kGeluTableCluster;
-                if (cache.n < 32) cache.e[cache.n++] = {dev, kGeluTableBytes, ctas};
+                if (cache.n < 32) cache.e[cache.n++] = {dev, ctas};
             }
         }
     }
@@ -772,8 +694,7 @@ fp8q_status launch_gelu_table(const GeluArgs& a, cudaStream_t s) {
     grid = (grid + kGeluTableCluster - 1) / kGeluTableCluster * kGeluTableCluster;  // whole clusters
     cfg.gridDim = dim3((unsigned)grid);
     err = cudaLaunchKernelEx(&cfg, kern, a);
-    if (err != cudaSuccess) return cuda_fail(err, "gelu_table_quantize_amax_kernel launch");
-    return after_launch("gelu_table_quantize_amax_kernel");
+    return err == cudaSuccess ? FP8Q_OK : cuda_fail(err, "gelu_table_quantize_amax_kernel launch");
 }
 
 }  // namespace
@@ -816,21 +737,18 @@ fp8q_status fp8q_gelu_quantize_amax(const void* h_bf16, void* y_bf16, uint8_t* q
             return y_bf16 ? launch_gelu_table<FP8Q_E4M3FN, true>(a, s) : launch_gelu_table<FP8Q_E4M3FN, false>(a, s);
         return y_bf16 ? launch_gelu_table<FP8Q_E5M2, true>(a, s) : launch_gelu_table<FP8Q_E5M2, false>(a, s);
     }
-    if (fmt == FP8Q_E4M3FN) {
-        if (y_bf16) gelu_quantize_amax_kernel<FP8Q_E4M3FN, true><<<grid, kThreads, 0, s>>>(a);
-        else        gelu_quantize_amax_kernel<FP8Q_E4M3FN, false><<<grid, kThreads, 0, s>>>(a);
-    } else {
-        if (y_bf16) gelu_quantize_amax_kernel<FP8Q_E5M2, true><<<grid, kThreads, 0, s>>>(a);
-        else        gelu_quantize_amax_kernel<FP8Q_E5M2, false><<<grid, kThreads, 0, s>>>(a);
-    }
-    return after_launch("gelu_quantize_amax_kernel");
+    auto kern = fmt == FP8Q_E4M3FN ? (y_bf16 ? gelu_quantize_amax_kernel<FP8Q_E4M3FN, true>
+                                             : gelu_quantize_amax_kernel<FP8Q_E4M3FN, false>)
+                                    : (y_bf16 ? gelu_quantize_amax_kernel<FP8Q_E5M2, true>
+                                             : gelu_quantize_amax_kernel<FP8Q_E5M2, false>);
+    return launch_kernel(kern, dim3((unsigned)grid), dim3(kThreads), 0, s, "gelu_quantize_amax_kernel", a);
 }
 
 fp8q_status fp8q_layernorm_quantize_amax(const void* x_bf16, void* y_bf16, uint8_t* q, int64_t rows,
                                          int32_t hidden, const float* gamma, const float* beta, float eps,
                                          fp8q_format fmt, const float* scale, float* amax, void* stream) {
     if (!valid_fmt(fmt) || rows < 0 || hidden < 16 || (hidden % 16) != 0) return FP8Q_ERR_INVALID_ARG;
-    if (hidden > 8 * kThreads * kLnMaxHalfPerThread) return FP8Q_ERR_UNSUPPORTED;
+    if (hidden > kLnMaxH) return FP8Q_ERR_UNSUPPORTED;
     if (rows == 0) return FP8Q_OK;
     if (!x_bf16 || !q || !gamma || !beta || !scale || !amax) return FP8Q_ERR_INVALID_ARG;
     if (((uintptr_t)scale & 3u) || ((uintptr_t)amax & 3u)) return FP8Q_ERR_INVALID_ARG;
@@ -847,7 +765,6 @@ fp8q_status fp8q_layernorm_quantize_amax(const void* x_bf16, void* y_bf16, uint8
     a.amax = amax;
     a.rows = rows;
     a.H = hidden;
-    a.batch = 0;
     a.eps = eps;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (fmt == FP8Q_E4M3FN)

@@ -27,37 +27,40 @@ __device__ __forceinline__ void quant_vec_load(const QCursor& k, int64_t local, 
     }
 }
 
+// Vector v of the tensor (16 bf16 in a and b): |x| into m2, the 16 codes out
+// (or, for the fused quantize -> dequantize, their bf16 values).
+template <int FMT, bool FAST, int OUT>
+__device__ __forceinline__ void quant_vec1(const QCursor& k, int64_t v, const uint4& a, const uint4& b, uint32_t& m2) {
+    constexpr int E = GeomOf<OUT>::type::kVecElems;
+    m2 = bf16x2_absmax(m2, bf16x2_absmax(bf16x2_absmax(bf16x2_absmax(a.x, a.y), bf16x2_absmax(a.z, a.w)),
+                                         bf16x2_absmax(bf16x2_absmax(b.x, b.y), bf16x2_absmax(b.z, b.w))));
+    uint4 o;
+    o.x = quant_quad<FMT, FAST>(a.x, a.y, k.c);
+    o.y = quant_quad<FMT, FAST>(a.z, a.w, k.c);
+    o.z = quant_quad<FMT, FAST>(b.x, b.y, k.c);
+    o.w = quant_quad<FMT, FAST>(b.z, b.w, k.c);
+    if (OUT == kOutFp8) {
+        st_v4(k.q + k.head + v * E, o);
+    } else {  // widen the fresh codes straight back: y = DQ(Q(x))
+        uint16_t* yb = reinterpret_cast<uint16_t*>(k.q) + k.head + v * E;
+        const float s = k.c.s;
+        st_v4(yb, make_uint4(dequant_pair<FMT>(o.x & 0xFFFFu, s), dequant_pair<FMT>(o.x >> 16, s),
+                             dequant_pair<FMT>(o.y & 0xFFFFu, s), dequant_pair<FMT>(o.y >> 16, s)));
+        st_v4(yb + 8, make_uint4(dequant_pair<FMT>(o.z & 0xFFFFu, s), dequant_pair<FMT>(o.z >> 16, s),
+                                 dequant_pair<FMT>(o.w & 0xFFFFu, s), dequant_pair<FMT>(o.w >> 16, s)));
+    }
+}
+
 template <int FMT, bool FAST, int OUT>
 __device__ __forceinline__ void quant_vec_store(const QCursor& k, int64_t local, const TileRegs<OUT>& r,
                                                 uint32_t& m2) {
     using G = typename GeomOf<OUT>::type;
-    constexpr int E = G::kVecElems, U = G::kVecPerThread;
-    uint8_t* qb = k.q + k.head;
+    constexpr int U = G::kVecPerThread;
     const int64_t v0 = local * Tile<G>::kVecs + threadIdx.x;
 #pragma unroll
     for (int u = 0; u < U; ++u) {
         const int64_t v = v0 + (int64_t)u * kThreads;
-        if (v < k.nvec) {
-            const uint4& a = r.a[u];
-            const uint4& b = r.b[u];
-            m2 = bf16x2_absmax(m2, bf16x2_absmax(bf16x2_absmax(bf16x2_absmax(a.x, a.y), bf16x2_absmax(a.z, a.w)),
-                                                 bf16x2_absmax(bf16x2_absmax(b.x, b.y), bf16x2_absmax(b.z, b.w))));
-            uint4 o;
-            o.x = quant_quad<FMT, FAST>(a.x, a.y, k.c);
-            o.y = quant_quad<FMT, FAST>(a.z, a.w, k.c);
-            o.z = quant_quad<FMT, FAST>(b.x, b.y, k.c);
-            o.w = quant_quad<FMT, FAST>(b.z, b.w, k.c);
-            if (OUT == kOutFp8) {
-                st_v4(qb + v * E, o);
-            } else {  // widen the fresh codes straight back: y = DQ(Q(x))
-                uint16_t* yb = reinterpret_cast<uint16_t*>(k.q) + k.head + v * E;
-                const float s = k.c.s;
-                st_v4(yb, make_uint4(dequant_pair<FMT>(o.x & 0xFFFFu, s), dequant_pair<FMT>(o.x >> 16, s),
-                                     dequant_pair<FMT>(o.y & 0xFFFFu, s), dequant_pair<FMT>(o.y >> 16, s)));
-                st_v4(yb + 8, make_uint4(dequant_pair<FMT>(o.z & 0xFFFFu, s), dequant_pair<FMT>(o.z >> 16, s),
-                                         dequant_pair<FMT>(o.w & 0xFFFFu, s), dequant_pair<FMT>(o.w >> 16, s)));
-            }
-        }
+        if (v < k.nvec) quant_vec1<FMT, FAST, OUT>(k, v, r.a[u], r.b[u], m2);
     }
 }
 

@@ -4,6 +4,8 @@
 #include "fp8q_common.cuh"
 #include "quant_tile.cuh"
 
+#include <mutex>
+
 namespace {
 
 template <int FMT, int MAXT, int OUT>
@@ -32,6 +34,68 @@ __global__ void __launch_bounds__(kThreads) quantize_amax_kernel(const __grid_co
         quant_tile<FMT, OUT>(k, tile - k.tile_begin, m2, ms);
     }
     flush_amax(m2, ms, k.amax, red);
+}
+
+// ----------------------------------------------------------------------------
+// Quantize + amax of one tensor by a persistent grid of balanced, contiguous
+// ranges: CTA b converts vectors [b * per, (b + 1) * per) of the tensor, its
+// threads taking every 256th vector, and each thread keeps its next two
+// vectors loading while it converts the current two.  With one CTA per tile,
+// a tensor of a few waves of tiles ends on a partial wave that leaves most
+// SMs idle (2048 tiles over 608 resident CTAs is 3.4 waves); here every CTA
+// streams the same amount.  The launcher picks it for vector-path tensors of
+// at most kStreamMaxTiles tiles.
+
+constexpr int kStreamCtasPerSm = 4;
+constexpr int kStreamUnroll = 2;
+
+template <int FMT, bool FAST>
+__device__ __forceinline__ void stream_range(const QCursor& k, int64_t v0, int64_t end, uint4 (&a)[kStreamUnroll],
+                                             uint4 (&b)[kStreamUnroll], uint32_t& m2) {
+    const uint16_t* xb = k.x + k.head;
+    for (; v0 < end; v0 += kStreamUnroll * kThreads) {
+        uint4 na[kStreamUnroll], nb[kStreamUnroll];
+#pragma unroll
+        for (int u = 0; u < kStreamUnroll; ++u) {
+            const int64_t v = v0 + (kStreamUnroll + u) * kThreads;
+            if (v < end) ld_stream_v8(xb + v * QuantGeom::kVecElems, na[u], nb[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < kStreamUnroll; ++u) {
+            const int64_t v = v0 + u * kThreads;
+            if (v < end) quant_vec1<FMT, FAST, kOutFp8>(k, v, a[u], b[u], m2);
+        }
+#pragma unroll
+        for (int u = 0; u < kStreamUnroll; ++u) {
+            a[u] = na[u];
+            b[u] = nb[u];
+        }
+    }
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) quantize_amax_stream_kernel(const QTensor t, int64_t per) {
+    __shared__ uint32_t red[kThreads / 32];
+    const Split sp = split_tensor<QuantGeom>((uintptr_t)t.x, (uintptr_t)t.q, t.n);  // the vector path
+    const int64_t beg = (int64_t)blockIdx.x * per;
+    const int64_t end = min(beg + per, sp.nvec);
+    uint4 a[kStreamUnroll], b[kStreamUnroll];
+    const int64_t v0 = beg + threadIdx.x;
+#pragma unroll
+    for (int u = 0; u < kStreamUnroll; ++u) {  // loads first: nothing here waits on the scale
+        const int64_t v = v0 + u * kThreads;
+        if (v < end) ld_stream_v8(t.x + sp.head + v * QuantGeom::kVecElems, a[u], b[u]);
+    }
+    const QCursor k = make_cursor<kOutFp8>(t, 0);
+    uint32_t m2 = 0, ms = 0;
+    if (k.c.fast) {
+        stream_range<FMT, true>(k, v0, end, a, b, m2);
+        if (blockIdx.x == 0) quant_scalars<FMT, true, kOutFp8>(k, 0, ms);  // scalar head and tail
+    } else {
+        stream_range<FMT, false>(k, v0, end, a, b, m2);
+        if (blockIdx.x == 0) quant_scalars<FMT, false, kOutFp8>(k, 0, ms);
+    }
+    flush_amax(m2, ms, t.amax, red);
 }
 
 // ----------------------------------------------------------------------------
@@ -118,8 +182,54 @@ fp8q_status launch_quantize(const fp8q_tensor* list, int32_t count, cudaStream_t
     // quantize -> dequantize 82.6 vs 110.6 us on 8192x16384.  The kernel's
     // grid-stride loop still covers tile counts beyond the grid limit.
     const int grid = (int)(tiles < 0x7FFFFFFF ? tiles : 0x7FFFFFFF);
-    quantize_amax_kernel<FMT, MAXT, OUT><<<grid, kThreads, 0, stream>>>(L);
-    return after_launch("quantize_amax_kernel");
+    return launch_kernel(quantize_amax_kernel<FMT, MAXT, OUT>, dim3((unsigned)grid), dim3(kThreads), 0, stream,
+                         "quantize_amax_kernel", L);
+}
+
+// Most tiles (16384 elements each) of a tensor that takes the persistent
+// grid; larger tensors run one CTA per tile, which measured faster once the
+// partial last wave is a small part of the launch (see quantize_amax_stream_kernel).
+constexpr int64_t kStreamMaxTiles = 4096;
+
+// Resident CTAs of the persistent grid per device (multiprocessors x
+// kStreamCtasPerSm), read on the first call there.
+std::mutex g_sm_mu;
+int g_sm_count[64] = {};
+
+cudaError_t sm_count(int* sms) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    std::lock_guard<std::mutex> lock(g_sm_mu);
+    if (dev < 0 || dev >= 64) return cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
+    if (g_sm_count[dev] == 0) {
+        err = cudaDeviceGetAttribute(&g_sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
+        if (err != cudaSuccess) return err;
+    }
+    *sms = g_sm_count[dev];
+    return cudaSuccess;
+}
+
+template <int FMT>
+fp8q_status launch_quantize_one(const fp8q_tensor& t, cudaStream_t stream) {
+    const Split sp = split_tensor<QuantGeom>((uintptr_t)t.x_bf16, (uintptr_t)t.q, t.n);
+    if (sp.mode != kModeVec || sp.tiles < 2 || sp.tiles > kStreamMaxTiles)
+        return launch_quantize<FMT, 1>(&t, 1, stream);
+    int sms = 0;
+    const cudaError_t err = sm_count(&sms);
+    if (err != cudaSuccess) return cuda_fail(err, "quantize_amax_stream_kernel setup");
+    const int64_t ctas = (int64_t)sms * kStreamCtasPerSm;
+    const int64_t per = (sp.nvec + ctas - 1) / ctas;  // >= 1: at least two tiles of vectors
+    const int64_t grid = (sp.nvec + per - 1) / per;
+    QTensor d;
+    d.x = static_cast<const uint16_t*>(t.x_bf16);
+    d.q = t.q;
+    d.scale = t.scale;
+    d.amax = t.amax;
+    d.n = t.n;
+    d.tile_end = 0;
+    return launch_kernel(quantize_amax_stream_kernel<FMT>, dim3((unsigned)grid), dim3(kThreads), 0, stream,
+                         "quantize_amax_stream_kernel", d, per);
 }
 
 template <int FMT>
@@ -142,8 +252,8 @@ fp8q_status launch_dequantize(const uint8_t* q, void* y, int64_t n, const float*
     // The kernel's loop still covers any tile count beyond the grid limit.
     const int64_t kMaxGrid = 0x7FFFFFFF;
     const int grid = (int)(sp.tiles < kMaxGrid ? sp.tiles : kMaxGrid);
-    dequantize_kernel<FMT><<<grid, kThreads, 0, stream>>>(q, static_cast<uint16_t*>(y), n, scale, sp.tiles);
-    return after_launch("dequantize_kernel");
+    return launch_kernel(dequantize_kernel<FMT>, dim3((unsigned)grid), dim3(kThreads), 0, stream, "dequantize_kernel",
+                         q, static_cast<uint16_t*>(y), n, scale, sp.tiles);
 }
 
 }  // namespace
@@ -160,8 +270,7 @@ fp8q_status fp8q_quantize_amax(const void* x_bf16, uint8_t* q, int64_t n, fp8q_f
     fp8q_status st = check_tensor(t);
     if (st != FP8Q_OK || n == 0) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return fmt == FP8Q_E4M3FN ? launch_quantize<FP8Q_E4M3FN, 1>(&t, 1, s)
-                              : launch_quantize<FP8Q_E5M2, 1>(&t, 1, s);
+    return fmt == FP8Q_E4M3FN ? launch_quantize_one<FP8Q_E4M3FN>(t, s) : launch_quantize_one<FP8Q_E5M2>(t, s);
 }
 
 fp8q_status fp8q_multi_quantize_amax(const fp8q_tensor* list, int32_t count, fp8q_format fmt,

@@ -366,9 +366,10 @@ fp8q_status fp8q_amax_scale_update(float* amax_history, int32_t history_len, int
     const int grid = (num_slots + kUpdCols - 1) / kUpdCols;
     const bool vec4 = ((uintptr_t)amax_history & 15u) == 0 && (num_slots % kUpdCols) == 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (vec4) amax_scale_update_kernel<true><<<grid, kUpdThreads, 0, s>>>(a);
-    else      amax_scale_update_kernel<false><<<grid, kUpdThreads, 0, s>>>(a);
-    return after_launch("amax_scale_update_kernel");
+    return vec4 ? launch_kernel(amax_scale_update_kernel<true>, dim3(grid), dim3(kUpdThreads), 0, s,
+                                "amax_scale_update_kernel", a)
+                : launch_kernel(amax_scale_update_kernel<false>, dim3(grid), dim3(kUpdThreads), 0, s,
+                                "amax_scale_update_kernel", a);
 }
 
 fp8q_status fp8q_amax_scale_update_ring_quantize(float* amax_history, const int32_t* head_in,
@@ -413,14 +414,12 @@ fp8q_status fp8q_amax_scale_update_ring_quantize(float* amax_history, const int3
     const int grid = n_upd + (int)(sp.tiles < max_q ? sp.tiles : max_q);
     const bool vec4 = ((uintptr_t)amax_history & 15u) == 0 && (num_slots % kUpdCols) == 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (fmt == FP8Q_E4M3FN) {
-        if (vec4) ring_update_quantize_kernel<FP8Q_E4M3FN, true><<<grid, kThreads, 0, s>>>(a, head_in, head_out, n_upd, t, slot, sp.tiles);
-        else      ring_update_quantize_kernel<FP8Q_E4M3FN, false><<<grid, kThreads, 0, s>>>(a, head_in, head_out, n_upd, t, slot, sp.tiles);
-    } else {
-        if (vec4) ring_update_quantize_kernel<FP8Q_E5M2, true><<<grid, kThreads, 0, s>>>(a, head_in, head_out, n_upd, t, slot, sp.tiles);
-        else      ring_update_quantize_kernel<FP8Q_E5M2, false><<<grid, kThreads, 0, s>>>(a, head_in, head_out, n_upd, t, slot, sp.tiles);
-    }
-    return after_launch("ring_update_quantize_kernel");
+    auto kern = fmt == FP8Q_E4M3FN ? (vec4 ? ring_update_quantize_kernel<FP8Q_E4M3FN, true>
+                                           : ring_update_quantize_kernel<FP8Q_E4M3FN, false>)
+                                    : (vec4 ? ring_update_quantize_kernel<FP8Q_E5M2, true>
+                                           : ring_update_quantize_kernel<FP8Q_E5M2, false>);
+    return launch_kernel(kern, dim3(grid), dim3(kThreads), 0, s, "ring_update_quantize_kernel", a, head_in, head_out,
+                         n_upd, t, slot, sp.tiles);
 }
 
 fp8q_status fp8q_amax_scale_update_ring(float* amax_history, int32_t* head, int32_t history_len,
@@ -447,9 +446,8 @@ fp8q_status fp8q_amax_scale_update_ring(float* amax_history, int32_t* head, int3
     const int grid = (num_slots + kUpdCols - 1) / kUpdCols;
     const bool vec4 = ((uintptr_t)amax_history & 15u) == 0 && (num_slots % kUpdCols) == 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (vec4) amax_scale_update_ring_kernel<true><<<grid, kUpdThreads, 0, s>>>(a, head);
-    else      amax_scale_update_ring_kernel<false><<<grid, kUpdThreads, 0, s>>>(a, head);
-    return after_launch("amax_scale_update_ring_kernel");
+    return launch_kernel(vec4 ? amax_scale_update_ring_kernel<true> : amax_scale_update_ring_kernel<false>, dim3(grid),
+                         dim3(kUpdThreads), 0, s, "amax_scale_update_ring_kernel", a, head);
 }
 
 }  // extern "C"
