@@ -245,19 +245,26 @@ fp8q_status fp8q_gelu_quantize_amax(const void* h_bf16, void* y_bf16, uint8_t* q
  * with S = sum x and Q = sum x^2.  Precision: y is the bf16 rounding of a
  * value within a stated bound of the exact (float64) LayerNorm; the bound
  * follows binary32 error analysis with row sums whose longest chain of
- * additions is at most 42 (rows are summed in a fixed order, so a call is
+ * additions is at most 32 (rows are summed in a fixed order, so a call is
  * reproducible bit for bit), and y is that exact value rounded once to bf16
  * unless it lies close to a bf16 rounding boundary.  The codes and the amax
  * are always exactly those of quantizing the y returned.  A NaN or infinite
  * x makes its row's y NaN.
+ * The kernel stages rows of x in shared memory with asynchronous bulk copies
+ * and waits for each copy at most one second.  Should a wait ever run out
+ * (correct operation never gets there), the call stops early, leaving the
+ * outputs incomplete and *amax holding the bit pattern 0x7FFFFFFF: a NaN that
+ * no bf16 data can produce (a NaN input gives the canonical 0x7FC00000 or
+ * another pattern below 0x7FFFFFFF).  A caller that must tell this apart reads
+ * *amax's bits after the stream has reached the call.
  * x_bf16: rows * hidden bf16 (device).  y_bf16: the same (device, written)
  * or NULL when only the FP8 codes are wanted.  q: rows * hidden bytes
  * (device).  gamma, beta: hidden floats each (device).  These five must be
  * 16-byte aligned.  scale, amax: as for fp8q_quantize_amax.  hidden: a
  * multiple of 16 from 16 to 16384.
- * The first call on a device reads the kernel's occupancy
- * (cudaOccupancyMaxActiveBlocksPerMultiprocessor), a host-side query, not
- * stream work, so that first call may itself be captured in a CUDA graph.
+ * The first call on a device also sets the kernel's shared-memory limit
+ * (cudaFuncSetAttribute) and reads its occupancy.  Those are host-side calls,
+ * not stream work, so that first call may itself be captured in a CUDA graph.
  * Errors: FP8Q_ERR_INVALID_ARG for a bad fmt, rows < 0, hidden < 16 or not a
  * multiple of 16, a NULL pointer (other than y_bf16) with rows > 0, or a
  * misaligned scale/amax; FP8Q_ERR_UNSUPPORTED for hidden > 16384 or a

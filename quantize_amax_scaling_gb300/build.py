@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 UNITS = ["quantize.cu", "producers.cu", "scale_update.cu", "abi.cu"]
 SRCS = [os.path.join(CSRC, u) for u in UNITS]
 DEPS = SRCS + [os.path.join(CSRC, h) for h in ("fp8q_common.cuh", "packed_f32.cuh", "quant_tile.cuh",
-                                                "slot_math.cuh")] + [os.path.join(ROOT, "include", "fp8q.h")]
+                                                "slot_math.cuh", "mbarrier.cuh")] + [os.path.join(ROOT, "include", "fp8q.h")]
 LIB = os.path.join(PKG, "libfp8q.so")
 OBJ_DIR = os.path.join(PKG, "_build")
 
@@ -65,6 +65,29 @@ def build(force: bool = False, verbose: bool = False) -> str:
     for o in objs:
         os.remove(o)
     return LIB
+
+
+def build_variant(lib_path: str, defines) -> str:
+    """Compile the same sources with extra preprocessor definitions into lib_path.
+
+    Only tests use this: it builds libraries whose test hooks (for example
+    FP8Q_TEST_LN_GIVE_UP_AT) exercise paths that correct operation never takes.
+    """
+    nvcc = nvcc_path()
+    out_dir = os.path.dirname(os.path.abspath(lib_path))
+    os.makedirs(out_dir, exist_ok=True)
+    flags = [f"-D{d}" for d in defines]
+
+    def compile_one(src):
+        obj = os.path.join(out_dir, os.path.basename(src) + ".o")
+        subprocess.run([nvcc, *NVCC_FLAGS, *flags, "-I", os.path.join(ROOT, "include"), "-c", "-o", obj, src],
+                       check=True)
+        return obj
+
+    with ThreadPoolExecutor(len(SRCS)) as ex:
+        objs = list(ex.map(compile_one, SRCS))
+    subprocess.run([nvcc, *ARCH, "-shared", "-o", lib_path, *objs], check=True)
+    return lib_path
 
 
 if __name__ == "__main__":

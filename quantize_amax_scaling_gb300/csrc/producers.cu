@@ -2,6 +2,7 @@
 // GELU (elementwise) and LayerNorm (row-wise).
 
 #include "fp8q_common.cuh"
+#include "mbarrier.cuh"
 #include "packed_f32.cuh"
 
 #include <mutex>
@@ -202,8 +203,13 @@ __host__ __device__ constexpr int gelu_table_threads() { return WRITE_Y ? 512 : 
 constexpr uint32_t kGeluTableBytes = 65536u * 2u;
 // Fewer elements take the direct kernel (measured crossovers on GB300: the
 // table wins from about 2^24 elements for the codes alone, 2^26 with y).
+#ifdef FP8Q_TEST_GELU_TABLE_MIN_ELEMS  // test-only build: small tensors take the table path too
+constexpr int64_t kGeluTableMinElems = FP8Q_TEST_GELU_TABLE_MIN_ELEMS;
+constexpr int64_t kGeluTableMinElemsWithY = FP8Q_TEST_GELU_TABLE_MIN_ELEMS;
+#else
 constexpr int64_t kGeluTableMinElems = (int64_t)1 << 24;
 constexpr int64_t kGeluTableMinElemsWithY = (int64_t)1 << 26;
+#endif
 constexpr int kGeluTableUnroll = 2;
 // CTAs of one thread-block cluster (on as many SMs) build their tables
 // together: each computes its share of the entries and stores each into the
@@ -213,10 +219,6 @@ constexpr int kGeluTableUnroll = 2;
 // without, 117.4 with 2).  Clusters of 8 leave SMs idle (86.4 us codes only).
 template <bool WRITE_Y>
 __host__ __device__ constexpr int gelu_table_cluster() { return WRITE_Y ? 4 : 2; }
-
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
@@ -355,28 +357,46 @@ __global__ void __launch_bounds__(gelu_table_threads<WRITE_Y>(), 1)
 // to bf16, then the quantize path on y: FP8 codes of y / scale and
 // amax = max |y|.
 //
-// A row belongs to a group of G = ceil(H / 4096) warps.  Lane l of warp g of
-// the group holds the 8-element vectors l + 32 (g + G i), i < KV, of the row
-// in registers (KV = H / (256 G), rounded up to a power of two; vectors past
-// the row read as +0), so x comes from HBM once and nothing is staged in
-// shared memory.  The sums S = sum x and Q = sum x^2 (an exact product inside
-// each fma) run in four chains per lane (2 KV elements each), fold pairwise,
-// fold across the warp as an xor butterfly (the two lanes of each exchange
-// add the same two values, so every lane ends with the same bits), and for
-// G > 1 the warp totals are added in warp order after a named barrier of the
-// group.  The longest chain of additions is 2 KV + 2 + 5 + (G - 1) <= 42.
-// The output step then normalises each pair of elements with the bf16 operand
-// taken straight from its word (add.f32.bf16), rstd * gamma and the fused
-// multiply-add with beta two lanes at a time, rounds to bf16 and quantizes.
+// Persistent grid (as many CTAs as fit at once, at most one per batch).  A
+// batch is R consecutive rows (R a power of two up to 8, chosen so that two
+// batches fit the 64 KB shared-memory ring); CTA b takes batches b, b + G, ...
+// A batch arrives by one cp.async.bulk copy completing on the mbarrier of its
+// ring slot, and the slot is refilled with the batch two ahead once the CTA is
+// done with it, so one batch is always in flight while the CTA computes the
+// other.
 //
-// Each CTA takes a contiguous, balanced range of rows, and its groups take
-// every (8 / G)-th row of it; a group asks L2 for its next row (one bulk
-// prefetch) before it loads the current one, so HBM keeps streaming while the
-// group computes.  No thread waits on anything but the group's named barrier
-// and one CTA barrier at the end, both in uniform control flow.
+// Phase 1, statistics: all 8 warps work, 8 / R on each row.  Warp part p of a
+// row sums the row's 8-element vectors p, p + 8/R, ... of its lanes in four
+// chains per lane (S = sum x and Q = sum x^2, the product exact inside each
+// fma), folds them and the lanes (an xor butterfly, whose two lanes per
+// exchange add the same two values, so every lane gets the same bits), and
+// the row's warps add their totals in warp order after a named barrier.  The
+// longest chain of additions is 2 ceil(H / (256 (8 / R))) + 6 + 8 / R, at most
+// H / 128 + 32.  The row's first warp stores (-mean, rstd).
+// Phase 2, output: after one CTA barrier, all 256 threads normalise, round to
+// bf16, store y (optional) and quantize, two rows at a time.  Thread t owns
+// the 8-element half-vectors t, t + 256, ... of every row; with H <= 4096
+// those are at most two, and their gamma and beta stay in registers for the
+// whole launch.  Shared-memory reads are 16 bytes per lane at consecutive
+// addresses (no bank conflicts).  The normalisation takes the bf16 operand
+// straight from its word (add.f32.bf16), then rstd * gamma and the fused
+// multiply-add with beta two lanes at a time.
+//
+// Every mbarrier wait gives up after one second (kWaitLimitNs).  The CTA
+// agrees on the outcome at its phase barrier; if any thread gave up, the CTA
+// stores the pattern 0x7FFFFFFF (a NaN that no bf16 input can produce) into
+// *amax, waits (again bounded) for its copies still in flight and returns.
+// Correct operation never gets there; a test-only build
+// (FP8Q_TEST_LN_GIVE_UP_AT) makes the wait of a CTA's batch of that index
+// report failure, to exercise the path without any fault.
 
 constexpr int kLnMaxH = 16384;
-constexpr int kLnWarpCols = 4096;  // columns per warp at most (KV <= 16)
+constexpr int kLnMaxHalfPerThread = 8;  // H <= 256 * 8 * 8
+constexpr int kLnWarps = kThreads / 32;
+constexpr int kLnMaxBatch = kLnWarps;
+constexpr int kLnBufs = 2;                      // batches in the ring
+constexpr uint32_t kLnRingBytes = 64u * 1024u;  // ring per CTA (both batches)
+constexpr int kLnTimeoutBits = 0x7FFFFFFF;
 
 struct LnArgs {
     const uint16_t* x;
@@ -388,30 +408,19 @@ struct LnArgs {
     float* amax;
     int64_t rows;
     int32_t H;
+    int32_t batch;  // rows per batch: 1, 2, 4 or 8
     float eps;
 };
 
 // Streaming stores whose target this kernel never reads back: no memory
-// clobber, so the loads of later rows may be scheduled across them.
+// clobber, so shared-memory loads of the next rows may be scheduled across
+// them.
 __device__ __forceinline__ void st_cs_v4(void* p, uint4 v) {
     asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
 }
 
 __device__ __forceinline__ void st_cs_v2(void* p, uint2 v) {
     asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y));
-}
-
-__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-
-// Ask L2 to fetch `bytes` (a multiple of 16, 16-byte aligned) starting at p.
-__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // Named barrier `id` over `threads` threads (whole warps).
@@ -486,111 +495,191 @@ __device__ __forceinline__ float max_nan_f32(float a, float b) {
     return d;
 }
 
-template <int G>
-__host__ __device__ constexpr int ln_threads() { return 32 * G * (8 / G); }
+// One half-vector of the output: y (optional), its |y| into m2, its FP8 codes.
+template <int FMT, bool WRITE_Y, bool FAST>
+__device__ __forceinline__ void ln_out8(const LnArgs& a, uint4 w, const float2 (&g)[4], const float2 (&b)[4],
+                                        float2 stats, const QScale& c, int64_t off, uint32_t& m2) {
+    const float2 rstd2 = splat2(stats.y);
+    uint4 yv;
+    yv.x = ln_pair(w.x, stats.x, rstd2, g[0], b[0]);
+    yv.y = ln_pair(w.y, stats.x, rstd2, g[1], b[1]);
+    yv.z = ln_pair(w.z, stats.x, rstd2, g[2], b[2]);
+    yv.w = ln_pair(w.w, stats.x, rstd2, g[3], b[3]);
+    if (WRITE_Y) st_cs_v4(a.y + off, yv);
+    m2 = bf16x2_absmax(m2, bf16x2_absmax(bf16x2_absmax(yv.x, yv.y), bf16x2_absmax(yv.z, yv.w)));
+    st_cs_v2(a.q + off, ln_quant8<FMT, FAST>(yv, c));
+}
 
-// The output of one row: y (optional), |y| into m2, the FP8 codes.
-template <int FMT, bool WRITE_Y, int KV, int G, bool FAST>
-__device__ __forceinline__ void ln_emit_row(const LnArgs& a, const uint4 (&v)[KV], int64_t row, int gw, int lane,
-                                            int nv, float nmean, float rstd, const QScale& c, uint32_t& m2) {
-    const float2 rstd2 = splat2(rstd);
+__device__ __forceinline__ void load4f2(const float* p, float2 (&d)[4]) {
+    const float4 u = __ldg(reinterpret_cast<const float4*>(p));
+    const float4 v = __ldg(reinterpret_cast<const float4*>(p) + 1);
+    d[0] = make_float2(u.x, u.y);
+    d[1] = make_float2(u.z, u.w);
+    d[2] = make_float2(v.x, v.y);
+    d[3] = make_float2(v.z, v.w);
+}
+
+// Phase 2 over one batch: rows two at a time.
+template <int FMT, bool WRITE_Y, int HPT, bool FAST>
+__device__ __forceinline__ void ln_emit_batch(const LnArgs& a, const uint8_t* base, const float2* stats, int nr,
+                                              int64_t r0, const float2 (&gr)[HPT <= 2 ? HPT : 1][4],
+                                              const float2 (&br)[HPT <= 2 ? HPT : 1][4], const QScale& c,
+                                              uint32_t& m2) {
+    constexpr bool kGammaInRegs = (HPT <= 2);
+    const int nh = a.H / 8;
+    const uint32_t row_bytes = 2u * (uint32_t)a.H;
+    for (int r = 0; r < nr; r += 2) {
+        const bool pair = r + 1 < nr;
+        const float2 s0 = stats[r], s1 = stats[pair ? r + 1 : r];
+        const uint8_t* srow = base + (size_t)r * row_bytes;
+        const int64_t row_off = (r0 + r) * a.H;
 #pragma unroll
-    for (int i = 0; i < KV; ++i) {
-        const int j = lane + 32 * (gw + G * i);
-        if (j < nv) {
-            const float4 g0 = __ldg(reinterpret_cast<const float4*>(a.gamma) + 2 * j);
-            const float4 g1 = __ldg(reinterpret_cast<const float4*>(a.gamma) + 2 * j + 1);
-            const float4 b0 = __ldg(reinterpret_cast<const float4*>(a.beta) + 2 * j);
-            const float4 b1 = __ldg(reinterpret_cast<const float4*>(a.beta) + 2 * j + 1);
-            uint4 yv;
-            yv.x = ln_pair(v[i].x, nmean, rstd2, make_float2(g0.x, g0.y), make_float2(b0.x, b0.y));
-            yv.y = ln_pair(v[i].y, nmean, rstd2, make_float2(g0.z, g0.w), make_float2(b0.z, b0.w));
-            yv.z = ln_pair(v[i].z, nmean, rstd2, make_float2(g1.x, g1.y), make_float2(b1.x, b1.y));
-            yv.w = ln_pair(v[i].w, nmean, rstd2, make_float2(g1.z, g1.w), make_float2(b1.z, b1.w));
-            const int64_t off = row * a.H + 8 * (int64_t)j;
-            if (WRITE_Y) st_cs_v4(a.y + off, yv);
-            m2 = bf16x2_absmax(m2, bf16x2_absmax(bf16x2_absmax(yv.x, yv.y), bf16x2_absmax(yv.z, yv.w)));
-            st_cs_v2(a.q + off, ln_quant8<FMT, FAST>(yv, c));
+        for (int i = 0; i < HPT; ++i) {
+            const int u = threadIdx.x + i * kThreads;
+            if (u < nh) {
+                const uint4 w0 = *reinterpret_cast<const uint4*>(srow + 16 * u);
+                uint4 w1 = w0;
+                if (pair) w1 = *reinterpret_cast<const uint4*>(srow + row_bytes + 16 * u);
+                float2 g[4], b[4];
+                if (kGammaInRegs) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        g[e] = gr[kGammaInRegs ? i : 0][e];
+                        b[e] = br[kGammaInRegs ? i : 0][e];
+                    }
+                } else {
+                    load4f2(a.gamma + 8 * u, g);
+                    load4f2(a.beta + 8 * u, b);
+                }
+                const int64_t off = row_off + 8 * u;
+                ln_out8<FMT, WRITE_Y, FAST>(a, w0, g, b, s0, c, off, m2);
+                if (pair) ln_out8<FMT, WRITE_Y, FAST>(a, w1, g, b, s1, c, off + a.H, m2);
+            }
         }
     }
 }
 
-template <int FMT, bool WRITE_Y, int KV, int G>
-__global__ void __launch_bounds__(ln_threads<G>(), 2) layernorm_quantize_amax_kernel(const LnArgs a) {
-    constexpr int kGroups = 8 / G;
-    constexpr int kWarps = G * kGroups;
-    __shared__ float2 part[kGroups][2][G];  // (S, Q) of each warp of a group, by row parity
-    __shared__ uint32_t red[kWarps];
+// HPT: most 8-element half-vectors a thread owns per row (ceil(H / 2048)).
+template <int FMT, bool WRITE_Y, int HPT>
+__global__ void __launch_bounds__(kThreads, 2) layernorm_quantize_amax_kernel(const LnArgs a) {
+    extern __shared__ __align__(128) uint8_t ring[];  // kLnBufs batches of a.batch rows of 2H bytes
+    __shared__ uint64_t bar[kLnBufs];
+    __shared__ float2 part[kLnWarps];     // (S, Q) of each warp's part of its row
+    __shared__ float2 stats[kLnMaxBatch];  // (-mean, rstd) of each row of the batch
+    __shared__ uint32_t red[kLnWarps];
+    constexpr bool kGammaInRegs = (HPT <= 2);
+    const int nv8 = a.H / 8, nh = a.H / 8;
+    const int R = a.batch;
+    const int wpr = kLnWarps / R;  // warps per row in phase 1
+    const uint32_t row_bytes = 2u * (uint32_t)a.H;
+    const uint32_t buf_bytes = (uint32_t)R * row_bytes;
+    const int64_t nb = (a.rows + R - 1) / R;
+    const int64_t G = gridDim.x;
+    const int64_t n_mine = (nb - 1 - blockIdx.x) / G + 1;  // the launch keeps G <= nb
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int grp = warp / G, gw = warp % G;
-    const int nv = a.H >> 3;
-    const int64_t r_begin = a.rows * (int64_t)blockIdx.x / gridDim.x;
-    const int64_t r_end = a.rows * ((int64_t)blockIdx.x + 1) / gridDim.x;
+    const int prow = warp / wpr, ppart = warp % wpr;        // phase 1: this warp's row and part
+
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < kLnBufs; ++b) mbar_init(&bar[b]);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        for (int64_t k = 0; k < kLnBufs && k < n_mine; ++k) {
+            const int64_t r0 = (blockIdx.x + k * G) * R;
+            const int64_t nr = a.rows - r0 < R ? a.rows - r0 : R;
+            bulk_load(ring + (size_t)k * buf_bytes, a.x + r0 * a.H, (uint32_t)nr * row_bytes, &bar[k]);
+        }
+    }
     const QScale c = make_qscale(a.scale);
     const float Hf = (float)a.H;
-    const uint32_t row_bytes = 2u * (uint32_t)a.H;
-    uint32_t m2 = 0;
-    int parity = 0;
-    for (int64_t row = r_begin + grp; row < r_end; row += kGroups, parity ^= 1) {
-        if (gw == 0 && lane == 0 && row + kGroups < r_end)
-            prefetch_l2_bulk(a.x + (row + kGroups) * a.H, row_bytes);
-        const uint16_t* xr = a.x + row * a.H;
-        uint4 v[KV];
+    float2 gr[kGammaInRegs ? HPT : 1][4], br[kGammaInRegs ? HPT : 1][4];
+    if (kGammaInRegs) {
 #pragma unroll
-        for (int i = 0; i < KV; ++i) {
-            const int j = lane + 32 * (gw + G * i);
-            v[i] = j < nv ? ld_stream_v4(xr + 8 * j) : make_uint4(0u, 0u, 0u, 0u);
-        }
-        float s[4] = {0.0f, 0.0f, 0.0f, 0.0f}, q[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-        for (int i = 0; i < KV; ++i) {
-            acc_bf16<true>(v[i].x, s[0], q[0]);
-            acc_bf16<true>(v[i].y, s[1], q[1]);
-            acc_bf16<true>(v[i].z, s[2], q[2]);
-            acc_bf16<true>(v[i].w, s[3], q[3]);
-            acc_bf16<false>(v[i].x, s[0], q[0]);
-            acc_bf16<false>(v[i].y, s[1], q[1]);
-            acc_bf16<false>(v[i].z, s[2], q[2]);
-            acc_bf16<false>(v[i].w, s[3], q[3]);
-        }
-        float S = __fadd_rn(__fadd_rn(s[0], s[1]), __fadd_rn(s[2], s[3]));
-        float Q = __fadd_rn(__fadd_rn(q[0], q[1]), __fadd_rn(q[2], q[3]));
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) {
-            S = __fadd_rn(S, __shfl_xor_sync(0xFFFFFFFFu, S, o));
-            Q = __fadd_rn(Q, __shfl_xor_sync(0xFFFFFFFFu, Q, o));
-        }
-        if (G > 1) {
-            if (lane == 0) part[grp][parity][gw] = make_float2(S, Q);
-            named_sync(1 + grp, 32 * G);
-            // every warp of the group adds the warp totals in the same order
-            float2 t = part[grp][parity][0];
-#pragma unroll
-            for (int k = 1; k < G; ++k) {
-                const float2 u = part[grp][parity][k];
-                t.x = __fadd_rn(t.x, u.x);
-                t.y = __fadd_rn(t.y, u.y);
+        for (int i = 0; i < (kGammaInRegs ? HPT : 0); ++i) {
+            const int u = threadIdx.x + i * kThreads;
+            if (u < nh) {
+                load4f2(a.gamma + 8 * u, gr[i]);
+                load4f2(a.beta + 8 * u, br[i]);
             }
-            S = t.x;
-            Q = t.y;
         }
-        const float mean = __fdiv_rn(S, Hf);
-        const float var = max_nan_f32(__fsub_rn(__fdiv_rn(Q, Hf), __fmul_rn(mean, mean)), 0.0f);
-        const float rstd = __frsqrt_rn(__fadd_rn(var, a.eps));
-        if (c.fast) ln_emit_row<FMT, WRITE_Y, KV, G, true>(a, v, row, gw, lane, nv, -mean, rstd, c, m2);
-        else        ln_emit_row<FMT, WRITE_Y, KV, G, false>(a, v, row, gw, lane, nv, -mean, rstd, c, m2);
     }
-    // CTA-wide max of |y|, one atomic
-    uint32_t m = max(abs_bits_lo(m2), m2 & 0x7FFF0000u);
-    m = __reduce_max_sync(0xFFFFFFFFu, m);
-    if (lane == 0) red[warp] = m;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        uint32_t b = red[0];
+    __syncthreads();  // barriers initialised before anyone waits on them
+
+    uint32_t m2 = 0;
+    bool ok = true;
+    int64_t k = 0;
+    for (; k < n_mine; ++k) {
+        const int buf = (int)(k % kLnBufs);
+        const uint32_t parity = (uint32_t)((k / kLnBufs) & 1);
+        const int64_t r0 = (blockIdx.x + k * G) * R;
+        const int nr = a.rows - r0 < R ? (int)(a.rows - r0) : R;
+        const uint8_t* base = ring + (size_t)buf * buf_bytes;
+        bool arrived = mbar_wait(&bar[buf], parity);
+#ifdef FP8Q_TEST_LN_GIVE_UP_AT
+        if (k == FP8Q_TEST_LN_GIVE_UP_AT) arrived = false;
+#endif
+        // Every warp of a row's group reaches the group's named barrier whatever
+        // its own wait saw (a warp whose copy is missing reads nothing); the
+        // CTA then agrees on the outcome at its barrier below.
+        const bool warp_arrived = __all_sync(0xFFFFFFFFu, arrived);
+        if (prow < nr) {
+            const uint8_t* xr = base + (size_t)prow * row_bytes;
+            float s[4] = {0.0f, 0.0f, 0.0f, 0.0f}, q[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            for (int j = lane + 32 * ppart; warp_arrived && j < nv8; j += 32 * wpr) {
+                const uint4 w = *reinterpret_cast<const uint4*>(xr + 16 * j);
+                acc_bf16<true>(w.x, s[0], q[0]);
+                acc_bf16<true>(w.y, s[1], q[1]);
+                acc_bf16<true>(w.z, s[2], q[2]);
+                acc_bf16<true>(w.w, s[3], q[3]);
+                acc_bf16<false>(w.x, s[0], q[0]);
+                acc_bf16<false>(w.y, s[1], q[1]);
+                acc_bf16<false>(w.z, s[2], q[2]);
+                acc_bf16<false>(w.w, s[3], q[3]);
+            }
+            float S = __fadd_rn(__fadd_rn(s[0], s[1]), __fadd_rn(s[2], s[3]));
+            float Q = __fadd_rn(__fadd_rn(q[0], q[1]), __fadd_rn(q[2], q[3]));
 #pragma unroll
-        for (int w = 1; w < kWarps; ++w) b = max(b, red[w]);
-        atomicMax(reinterpret_cast<int*>(a.amax), (int)b);
+            for (int o = 16; o >= 1; o >>= 1) {
+                S = __fadd_rn(S, __shfl_xor_sync(0xFFFFFFFFu, S, o));
+                Q = __fadd_rn(Q, __shfl_xor_sync(0xFFFFFFFFu, Q, o));
+            }
+            if (wpr > 1) {
+                if (lane == 0) part[warp] = make_float2(S, Q);
+                named_sync(1 + prow, 32 * wpr);
+                if (ppart == 0) {  // the row's warp totals, in warp order
+                    for (int p = 1; p < wpr; ++p) {
+                        S = __fadd_rn(S, part[warp + p].x);
+                        Q = __fadd_rn(Q, part[warp + p].y);
+                    }
+                }
+            }
+            if (ppart == 0 && lane == 0) {
+                const float mean = __fdiv_rn(S, Hf);
+                const float var = max_nan_f32(__fsub_rn(__fdiv_rn(Q, Hf), __fmul_rn(mean, mean)), 0.0f);
+                stats[prow] = make_float2(-mean, __frsqrt_rn(__fadd_rn(var, a.eps)));
+            }
+        }
+        ok = __syncthreads_and(arrived) != 0;
+        if (!ok) break;  // uniform
+        if (c.fast) ln_emit_batch<FMT, WRITE_Y, HPT, true>(a, base, stats, nr, r0, gr, br, c, m2);
+        else        ln_emit_batch<FMT, WRITE_Y, HPT, false>(a, base, stats, nr, r0, gr, br, c, m2);
+        __syncthreads();  // every thread is done with this slot and with stats[] and part[]
+        if (threadIdx.x == 0 && k + kLnBufs < n_mine) {  // refill the slot, kLnBufs batches ahead
+            const int64_t next_r0 = (blockIdx.x + (k + kLnBufs) * G) * R;
+            const int64_t next_nr = a.rows - next_r0 < R ? a.rows - next_r0 : R;
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            bulk_load(ring + (size_t)buf * buf_bytes, a.x + next_r0 * a.H, (uint32_t)next_nr * row_bytes, &bar[buf]);
+        }
     }
+    if (!ok) {
+        // A copy did not arrive in time: mark the result, then wait (bounded)
+        // for the copies this CTA still has in flight before leaving.
+        if (threadIdx.x == 0) {
+            atomicMax(reinterpret_cast<int*>(a.amax), kLnTimeoutBits);
+            for (int64_t j = k; j < n_mine && j < k + kLnBufs; ++j)
+                mbar_wait(&bar[j % kLnBufs], (uint32_t)((j / kLnBufs) & 1));
+        }
+        return;
+    }
+    flush_amax(m2, 0u, a.amax, red);
 }
 
 // Resident CTAs of one kernel per device, taken on the first launch there
@@ -604,11 +693,15 @@ struct ResidentCache {
     int n = 0;
 };
 
-template <int FMT, bool WRITE_Y, int KV, int G>
-fp8q_status launch_layernorm_kv(const LnArgs& a, cudaStream_t s) {
+template <int FMT, bool WRITE_Y, int HPT>
+fp8q_status launch_layernorm_hpt(LnArgs a, cudaStream_t s) {
     static ResidentCache cache;
-    auto kern = layernorm_quantize_amax_kernel<FMT, WRITE_Y, KV, G>;
-    constexpr int threads = ln_threads<G>();
+    auto kern = layernorm_quantize_amax_kernel<FMT, WRITE_Y, HPT>;
+    const uint32_t row_bytes = 2u * (uint32_t)a.H;
+    uint32_t batch = kLnRingBytes / (kLnBufs * row_bytes);
+    batch = batch >= 8 ? 8 : batch >= 4 ? 4 : batch >= 2 ? 2 : 1;  // a power of two: 8 / batch warps a row
+    a.batch = (int32_t)batch;
+    const uint32_t smem = kLnBufs * batch * row_bytes;
     int dev = 0, ctas = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err == cudaSuccess) {
@@ -617,7 +710,9 @@ fp8q_status launch_layernorm_kv(const LnArgs& a, cudaStream_t s) {
             if (cache.e[k].dev == dev) ctas = cache.e[k].ctas;
         if (ctas == 0) {
             int per_sm = 0, sms = 0;
-            err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, 0);
+            err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLnRingBytes);
+            if (err == cudaSuccess)
+                err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, kLnRingBytes);
             if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
             if (err == cudaSuccess && per_sm < 1) err = cudaErrorInvalidConfiguration;
             if (err == cudaSuccess) {
@@ -627,26 +722,18 @@ fp8q_status launch_layernorm_kv(const LnArgs& a, cudaStream_t s) {
         }
     }
     if (err != cudaSuccess) return cuda_fail(err, "layernorm_quantize_amax_kernel setup");
-    // as many CTAs as fit at once, but no more than give each group a row
-    const int64_t want = (a.rows + (8 / G) - 1) / (8 / G);
-    const int grid = (int)(want < (int64_t)ctas ? want : (int64_t)ctas);
-    return launch_kernel(kern, dim3((unsigned)grid), dim3(threads), 0, s, "layernorm_quantize_amax_kernel", a);
+    const int64_t batches = (a.rows + batch - 1) / batch;
+    const int grid = (int)(batches < (int64_t)ctas ? batches : (int64_t)ctas);
+    return launch_kernel(kern, dim3((unsigned)grid), dim3(kThreads), smem, s, "layernorm_quantize_amax_kernel", a);
 }
 
 template <int FMT, bool WRITE_Y>
 fp8q_status launch_layernorm(const LnArgs& a, cudaStream_t s) {
-    const int G = (a.H + kLnWarpCols - 1) / kLnWarpCols;
-    const int kv = (a.H / 8 + 32 * G - 1) / (32 * G);  // vectors per lane
-    if (G == 1) {
-        if (kv <= 1) return launch_layernorm_kv<FMT, WRITE_Y, 1, 1>(a, s);
-        if (kv <= 2) return launch_layernorm_kv<FMT, WRITE_Y, 2, 1>(a, s);
-        if (kv <= 4) return launch_layernorm_kv<FMT, WRITE_Y, 4, 1>(a, s);
-        if (kv <= 8) return launch_layernorm_kv<FMT, WRITE_Y, 8, 1>(a, s);
-        return launch_layernorm_kv<FMT, WRITE_Y, 16, 1>(a, s);
-    }
-    if (G == 2) return launch_layernorm_kv<FMT, WRITE_Y, 16, 2>(a, s);
-    if (G == 3) return launch_layernorm_kv<FMT, WRITE_Y, 16, 3>(a, s);
-    return launch_layernorm_kv<FMT, WRITE_Y, 16, 4>(a, s);
+    const int hpt = (a.H / 8 + kThreads - 1) / kThreads;  // half-vectors per thread
+    if (hpt <= 1) return launch_layernorm_hpt<FMT, WRITE_Y, 1>(a, s);
+    if (hpt <= 2) return launch_layernorm_hpt<FMT, WRITE_Y, 2>(a, s);
+    if (hpt <= 4) return launch_layernorm_hpt<FMT, WRITE_Y, 4>(a, s);
+    return launch_layernorm_hpt<FMT, WRITE_Y, 8>(a, s);
 }
 
 template <int FMT, bool WRITE_Y>
@@ -765,6 +852,7 @@ fp8q_status fp8q_layernorm_quantize_amax(const void* x_bf16, void* y_bf16, uint8
     a.amax = amax;
     a.rows = rows;
     a.H = hidden;
+    a.batch = 0;
     a.eps = eps;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (fmt == FP8Q_E4M3FN)

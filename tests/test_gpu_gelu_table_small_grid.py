@@ -1,0 +1,57 @@
+"""The GELU table kernel on small tensors, through the test-hooks build in which
+every vector-path tensor takes the table path (FP8Q_TEST_GELU_TABLE_MIN_ELEMS=1).
+
+The table kernel's grid is the CTAs the tensor needs, rounded up to whole
+thread-block clusters (2 CTAs for the codes alone, 4 with y), so here some CTAs
+have no vectors to convert but still take part in the cluster's table build;
+CTA 0 also converts the scalar head and tail.  Every output is compared: y with
+the fixed binary32 sequence (which the GPU GELU tests hold to the float64
+tolerance), the codes and the amax with the oracle's quantize of that y.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import assert_bf16_equal, assert_codes_equal, assert_f32_equal, check_guards, guarded
+from quantize_amax_scaling_gb300 import fp8q
+from quantize_amax_scaling_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+# vectors of 16 elements per CTA: 1024 threads x 2 (codes only), 512 x 2 (with y)
+CASES = [  # (elements, offset, with y)
+    (16 * 2048 + 7, 0, False),            # 1 CTA needed, grid 2 (one whole cluster)
+    (16 * (2048 * 2 + 5) + 3, 3, False),  # 3 CTAs needed, grid rounded up to 4
+    (16 * 100 + 9, 5, False),             # 1 CTA needed, grid 2
+    (16 * 1024 + 1, 1, True),             # 1 CTA needed, grid rounded up to 4
+    (16 * (1024 * 5 - 7) + 11, 2, True),  # 5 CTAs needed, grid 8
+]
+
+
+@pytest.mark.parametrize("n,off,with_y", CASES)
+def test_gelu_table_path_rounded_grid(hooks_lib, seq_gelu, n, off, with_y):
+    dev = torch.device("cuda:0")
+    g = torch.Generator(device=dev)
+    g.manual_seed(n)
+    hbuf = (torch.randn(n + 16, generator=g, device=dev) * 3.0).to(torch.bfloat16)
+    h = hbuf[off: off + n]
+    qbuf, q = guarded(n, torch.uint8, dev, off)
+    ybuf, y = guarded(n, torch.bfloat16, dev, off, fill=0x5A5A) if with_y else (None, None)
+    am = torch.zeros(1, device=dev)
+    scale = np.float32(0.0123)
+    sc = torch.full((1,), float(scale), device=dev)
+    st = torch.cuda.current_stream().cuda_stream
+    status = hooks_lib.fp8q_gelu_quantize_amax(h.data_ptr(), y.data_ptr() if with_y else None, q.data_ptr(), n,
+                                               fp8q.E4M3FN, sc.data_ptr(), am.data_ptr(), st)
+    assert status == 0
+    torch.cuda.synchronize()
+    hb = W.bf16_bits(h)
+    want_y = seq_gelu(hb)
+    rq, ra = oracle.quantize_amax(want_y, fp8q.E4M3FN, scale)
+    assert_codes_equal(q.cpu().numpy(), rq, fp8q.E4M3FN, f"table q n={n}")
+    assert_f32_equal([float(am)], [ra], f"table amax n={n}")
+    check_guards(qbuf, n, off)
+    if with_y:
+        assert_bf16_equal(W.bf16_bits(y), want_y, f"table y n={n}")
+        check_guards(ybuf, n, off, fill=0x5A5A)

@@ -105,10 +105,10 @@ def test_quantize_ragged_sizes_offsets_with_canaries(dev, n):
 
 
 @pytest.mark.parametrize("n,xo,qo", [(16384 + 17, 0, 0), (3 * 16384 + 5, 3, 3), ((1 << 25) + 7, 1, 1),
-                                     (4096 * 16384, 0, 0), (4096 * 16384 + 16, 0, 0), (4096 * 16384 + 16, 5, 5),
-                                     (4096 * 16384 - 1, 7, 7)])
+                                     (2560 * 16384, 0, 0), (2560 * 16384 + 16, 0, 0), (2560 * 16384 + 16, 5, 5),
+                                     (2560 * 16384 - 1, 7, 7)])
 def test_quantize_both_grids_around_the_threshold(dev, n, xo, qo):
-    """Single tensors of up to 4096 tiles take the persistent grid of balanced ranges,
+    """Single tensors of up to 2560 tiles take the persistent grid of balanced ranges,
     larger ones one CTA per tile: both sides of the switch, with heads and tails."""
     g = torch.Generator(device=dev)
     g.manual_seed(n % 100003)
