@@ -355,6 +355,16 @@ def run_gpu(args, ws, rank, local):
     if rank != 0:
         return None
     traffic = read_traffic()
+    upd_graph = graph["scale_update_us_after_dequantize"] if graph else None
+    detail = {
+        "eager": {"value": round(eager_value, 1), "unit": "GB/s", "ms_per_step": round(eager_t / args.steps * 1e3, 4)},
+        "kernels": kernels, "graph": graph, "next_rows": next_rows, "other_configs": other_configs, "e2e": e2e,
+        "timing": "value and ms_per_step: K steps replayed from CUDA graphs (10 steps per graph, plus single-step "
+                  "replays for a remainder; in each step quantize, multi-tensor quantize and dequantize are "
+                  "parallel branches joined before the update), CUDA events only around the region; eager: the "
+                  "same K steps launched kernel by kernel; kernels and roofline: a third pass of K eager steps "
+                  "with an event around each kernel",
+    }
     out = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -369,45 +379,62 @@ def run_gpu(args, ws, rank, local):
         "dtype": "f32",
         "data": "synthetic (seeded; shapes of the FFN/MLP and 96-layer workloads)",
         "config": {"workload": WORKLOAD, "step_bytes": STEP_BYTES,
-                   "timing": "value and ms_per_step: K steps replayed from CUDA graphs (10 steps per graph, "
-                             "plus single-step replays for a remainder; in each step quantize, multi-tensor "
-                             "quantize and dequantize are parallel branches joined before the update), "
-                             "CUDA events only around the region; "
-                             "eager: the same K steps launched "
-                             "kernel by kernel; kernels and roofline: a third pass of K eager steps with an "
-                             "event around each kernel",
-                   "l2": "inputs larger than L2 (each step streams 1.21 GB; the 129 MB L2 holds none of "
-                         "a step's inputs when it is read again)",
+                   "l2": "inputs larger than L2 (a step streams 1.21 GB)",
                    "parallelism": f"replicas x{ws} (no collective)"},
-        "eager": {"value": round(eager_value, 1), "unit": "GB/s",
-                  "ms_per_step": round(eager_t / args.steps * 1e3, 4)},
-        "headline": {"quantize_amax_gbs": round(q_gbs, 1), "quantize_amax_frac_of_peak": round(q_gbs / peak, 4),
-                     # device time of one 576-slot call: measured in CUDA graphs when the
-                     # extras run, else the eager figure with its event overhead
-                     "scale_update_us": (graph["scale_update_us_after_dequantize"] if graph
-                                         else round(avg["amax_scale_update"], 3)),
-                     "scale_update_us_how": ("CUDA graphs: (dequantize + update) pairs minus dequantize alone"
-                                             if graph else "eager, an event on each side of the call"),
-                     "scale_update_us_eager_events": round(avg["amax_scale_update"], 3),
-                     "scale_update_launches_per_call": 1},
-        "kernels": kernels,
-        "roofline": {"kernel": "quantize_amax_kernel (8192x16384 bf16 -> e4m3fn + amax)",
-                     "bound": "hbm", "achieved": round(q_gbs, 1), "peak": peak,
-                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
-                     else "fallback 6.8 TB/s",
-                     "unit": "GB/s", "frac": round(q_gbs / peak, 4), "traffic": traffic},
-        "graph": graph,
-        "next_rows": next_rows,
-        "other_configs": other_configs,
+        # the metric's two halves: the quantize+amax kernel on the 8192x16384
+        # activation, and the 576-slot update's device time (CUDA graphs)
+        "quantize_amax_gbs": round(q_gbs, 1),
+        "quantize_amax_frac": round(q_gbs / peak, 4),
+        "scale_update_us": upd_graph if upd_graph is not None else round(avg["amax_scale_update"], 3),
+        "scale_update_us_eager": round(avg["amax_scale_update"], 3),
+        "scale_update_launches": 1,
+        "roofline": {"kernel": "quantize_amax_kernel 8192x16384", "bound": "hbm", "achieved": round(q_gbs, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(q_gbs / peak, 4), "traffic": traffic,
+                     "peak_source": "measured" if peak_src == "measured" else "fallback"},
+        "rows": compact_rows(kernels, next_rows, other_configs),
         "gpu_launches": KERNELS_PER_STEP * args.steps,
-        "other_launches": {"torch fill (zero the step's 3 amax slots)": args.steps},
         "clocks": clocks.summary(),
-        "e2e": e2e,
+        "e2e": None if e2e is None else {k: e2e[k] for k in ("value", "unit", "h2d_bytes_per_step",
+                                                             "d2h_bytes_per_step", "link_gbs", "frac_of_link")},
     }
     if not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(args.cpu_sample_frac)
-        out["cpu_baseline_all_cores"] = cpu_baseline_all_cores(args.cpu_sample_frac)
+        cb = cpu_baseline(args.cpu_sample_frac)
+        cba = cpu_baseline_all_cores(args.cpu_sample_frac)
+        pc = cpu_per_config(args.cpu_config_seconds)
+        detail["cpu_baseline"], detail["cpu_baseline_all_cores"], detail["cpu_per_config"] = cb, cba, pc
+        out["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        out["cpu_baseline"]["all_cores"] = {"value": cba["value"], "cores": cba["cores"]}
+        out["cpu_baseline"]["per_config"] = pc["compact"]
+    out["detail"] = write_detail(detail)
     return out
+
+
+def compact_rows(kernels, next_rows, other_configs):
+    """Fractions of the measured HBM peak for the other kernels (full figures in the detail file)."""
+    r = {"multi_quantize_frac": kernels["multi_quantize_amax"]["frac_of_peak"],
+         "dequantize_frac": kernels["dequantize"]["frac_of_peak"]}
+    if other_configs:
+        r["mlp_activation_8192x4096_frac"] = other_configs["mlp_activation"]["frac_of_peak"]
+        r["ragged_12_frac"] = other_configs["ragged_twelve_tensors"]["frac_of_peak"]
+    if next_rows:
+        r["qdq_frac"] = next_rows["qdq_amax"]["frac_of_peak"]
+        r["gelu_codes_frac"] = next_rows["gelu_quantize_amax"]["codes_only"]["frac_of_peak"]
+        r["layernorm_codes_frac"] = next_rows["layernorm_quantize_amax"]["codes_only"]["frac_of_peak"]
+        r["ring_update_us"] = next_rows["amax_scale_update_ring"]["us"]
+    return r
+
+
+def write_detail(detail):
+    """Every figure of the run, as JSON, beside the printed line; returns its path."""
+    d = os.path.join(ROOT, "gpurun_out")
+    try:
+        os.makedirs(d, exist_ok=True)
+        p = os.path.join(d, "bench_detail.json")
+        with open(p, "w") as f:
+            json.dump(detail, f, indent=1)
+        return os.path.relpath(p, ROOT)
+    except OSError as e:
+        return f"not written: {e}"
 
 
 def measure_graph(args, step, stream, dev):
@@ -718,6 +745,29 @@ def measure_next_rows(args, step, stream, dev, peak):
         torch.cuda.synchronize(dev)
         return e0.elapsed_time(e1) * 1e3 / reps
 
+    # The same pair on a small tensor (1024x1024), launched eagerly: the regime in
+    # which one launch instead of two matters (the update's cost is launch overhead).
+    xs_small = step.act[: 1 << 20]
+    qs_small = torch.empty(1 << 20, dtype=torch.uint8, device=dev)
+
+    def two_small():
+        f.fp8q_amax_scale_update_ring(hs[0], heads[0], step.amax_new, scs[0], sis[0], f.E4M3FN, f.ALGO_MAX, 0,
+                                      step.slot_format, stream.cuda_stream)
+        f.fp8q_quantize_amax(xs_small, qs_small, f.E4M3FN, scs[0][slot:slot + 1], amf[0:1], stream.cuda_stream)
+
+    def fused_small():
+        i = par["i"] = par["i"] ^ 1
+        f.fp8q_amax_scale_update_ring_quantize(hs[1], heads[1 + i], heads[2 - i], step.amax_new, scs[1], sis[1],
+                                               xs_small, qs_small, slot, amf[1:2], f.E4M3FN, f.ALGO_MAX, 0,
+                                               step.slot_format, stream.cuda_stream)
+    out["amax_scale_update_ring_quantize_small"] = {
+        "workload": "ring update of 576 slots x history 1024 + quantize of a bf16 1024x1024 tensor, launched "
+                    "eagerly back to back (per call: device time between events over the loop)",
+        "fused_us": round(timed_loop(fused_small), 3),
+        "two_launches_us": round(timed_loop(two_small), 3),
+        "fused_us_graph": round(graph_us(fused_small), 3),
+        "two_launches_us_graph": round(graph_us(two_small), 3)}
+
     out["amax_scale_update_ring_quantize"] = {
         "workload": "ring update of 576 slots x history 1024 + quantize of the bf16 8192x16384 activation "
                     "with one slot's new scale",
@@ -858,11 +908,59 @@ def run_e2e(args, step, stream, dev):
     torch.cuda.synchronize(dev)
     barrier()
     ws = dist_env()[0]
-    v, t = aggregate_throughput(STEP_BYTES, s.elapsed_time(e) / 1e3 / steps, ws)
+    t_step = s.elapsed_time(e) / 1e3 / steps
+    v, t = aggregate_throughput(STEP_BYTES, t_step, ws)
+    link = measure_link(step, host_in, host_out, pipe, dev)
     return {"value": round(v, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": steps, "ms_per_step": round(t * 1e3, 3),
+            "link_gbs": link["both_gbs"], "frac_of_link": round(link["both_ms"] / (t_step * 1e3), 4),
+            "link": link,
             "how": f"pinned host buffers; {_HostPipeline.CHUNK >> 20}M-element pieces copied in, converted "
-                   "and copied out on three streams"}
+                   "and copied out on three streams; frac_of_link = time of the step's copies alone (both "
+                   "directions at once, no kernels) / time of the step"}
+
+
+def measure_link(step, host_in, host_out, pipe, dev, reps=3):
+    """The host link alone: the step's copies (the same tensors and byte counts, whole
+    tensors, pinned host memory) with no kernels, host-to-device alone, device-to-host
+    alone, and both at once on two streams."""
+    import torch
+    pairs_in = [(step.act, host_in["act"]), (step.w[0], host_in["w1"]), (step.w[1], host_in["w2"]),
+                (step.grad_q, host_in["grad_q"]), (step.amax_new, host_in["amax_new"])]
+    pairs_out = [(host_out["q_act"], step.q_act), (host_out["q_w1"], step.q_w[0]), (host_out["q_w2"], step.q_w[1]),
+                 (host_out["y_grad"], step.y_grad), (host_out["scale"], step.scale),
+                 (host_out["scale_inv"], step.scale_inv)]
+    h2d = sum(h.numel() * h.element_size() for _, h in pairs_in)
+    d2h = sum(h.numel() * h.element_size() for h, _ in pairs_out)
+
+    def run(do_in, do_out):
+        torch.cuda.synchronize(dev)
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        main = torch.cuda.current_stream(dev)
+        s.record(main)
+        pipe.cin.wait_event(s)
+        pipe.cout.wait_event(s)
+        for _ in range(reps):
+            if do_in:
+                with torch.cuda.stream(pipe.cin):
+                    for d, h in pairs_in:
+                        d.copy_(h, non_blocking=True)
+            if do_out:
+                with torch.cuda.stream(pipe.cout):
+                    for h, d in pairs_out:
+                        h.copy_(d, non_blocking=True)
+        main.wait_stream(pipe.cin)
+        main.wait_stream(pipe.cout)
+        e.record(main)
+        torch.cuda.synchronize(dev)
+        return s.elapsed_time(e) / reps      # ms per step's copies
+
+    run(True, True)                          # warm
+    t_in, t_out, t_both = run(True, False), run(False, True), run(True, True)
+    return {"h2d_gbs": round(h2d / t_in / 1e6, 1), "d2h_gbs": round(d2h / t_out / 1e6, 1),
+            "both_gbs": round((h2d + d2h) / t_both / 1e6, 1), "both_ms": round(t_both, 3),
+            "h2d_bytes": h2d, "d2h_bytes": d2h}
 
 
 def read_traffic():
@@ -977,6 +1075,88 @@ def cpu_baseline_all_cores(frac: float):
             "sample": desc, "seconds": round(dt, 3)}
 
 
+def cpu_per_config(seconds: float):
+    """The oracle, as it stands, on a bounded sample of each configured workload:
+    single-threaded, and split over every host core (contiguous chunks on threads;
+    the oracle's C calls release the GIL; amax is a max, so the results are those of
+    the whole-tensor calls).  Each sample is sized to about `seconds` of
+    single-threaded work from a measured rate; GB/s counts 3 algorithmic bytes per
+    element, as on the GPU.  The 576-slot update runs whole, single-threaded (its
+    history is row-major over slots, so it does not split into contiguous chunks),
+    for both selection algorithms and both margins."""
+    import numpy as np
+    import torch
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+    from quantize_amax_scaling_gb300 import workloads as W
+    cores = max(1, os.cpu_count() or 1)
+    probe = W.bf16_bits(torch.randn(1 << 20).to(torch.bfloat16))
+    t0 = time.perf_counter()
+    oracle.quantize_amax(probe, oracle.E4M3FN, np.float32(0.01))
+    rate = probe.size / (time.perf_counter() - t0)            # elements per second, one core
+    n_s = max(1 << 16, int(rate * seconds))
+
+    def prefix(make, cols, n):
+        rows = n // cols + 1
+        return W.bf16_bits(make(rows, cols)).reshape(-1)[:n]
+
+    def timed(fn, arrays):
+        """(seconds on one core, seconds on all cores) of fn over every array."""
+        t0 = time.perf_counter()
+        for a in arrays:
+            fn(a)
+        t1 = time.perf_counter() - t0
+
+        def work(i):
+            for a in arrays:
+                lo, hi = a.size * i // cores, a.size * (i + 1) // cores
+                fn(a[lo:hi])
+        with ThreadPoolExecutor(cores) as ex:
+            t0 = time.perf_counter()
+            list(ex.map(work, range(cores)))
+            tn = time.perf_counter() - t0
+        return t1, tn
+
+    q4 = lambda a: oracle.quantize_amax(a, oracle.E4M3FN, np.float32(0.0091))
+    q5 = lambda a: oracle.quantize_amax(a, oracle.E5M2, np.float32(2.0 ** -20))
+    dq5 = lambda a: oracle.dequantize(a, oracle.E5M2, np.float32(2.0 ** -20))
+    cases = {}
+    mlp = prefix(lambda r, c: W.mlp_activation(W.SEED_MLP, "cpu", (r, c)), W.HIDDEN, n_s)
+    cases["mlp_activation"] = (q4, [mlp], "bf16 8192x4096 N(0,1) with outliers -> e4m3fn + amax")
+    third = n_s // 3
+    ffn = [prefix(lambda r, c: W.gelu_activation(W.SEED_FFN, "cpu", (r, c)), W.FFN, third),
+           prefix(lambda r, c: W.truncated_normal_weight((r, c), W.HIDDEN, W.SEED_FFN + 10, "cpu"), W.FFN, third),
+           prefix(lambda r, c: W.truncated_normal_weight((r, c), W.FFN, W.SEED_FFN + 20, "cpu"), W.HIDDEN, third)]
+    cases["ffn"] = (q4, ffn, "act 8192x16384 + W1 + W2 -> e4m3fn, one amax each")
+    grad = prefix(lambda r, c: W.gradient((r, c), W.SEED_GRAD, "cpu"), W.FFN, n_s)
+    cases["grad_quantize"] = (q5, [grad], "gradients sign x lognormal(-12, 3) -> e5m2 saturating")
+    gq, _ = oracle.quantize_amax(grad, oracle.E5M2, np.float32(2.0 ** -20))
+    cases["grad_dequantize"] = (dq5, [gq], "e5m2 codes -> bf16")
+    per = max(1, n_s // 12)
+    rag = [W.bf16_bits(t).reshape(-1)[:per] for t in W.ragged_tensors("cpu", scale_down=max(1, (2048 * 12288) // per))]
+    cases["ragged_12"] = (q4, rag, "12 ragged bf16 tensors -> e4m3fn, one amax each")
+    out, compact = {}, {"cores": cores}
+    for name, (fn, arrays, what) in cases.items():
+        n = sum(a.size for a in arrays)
+        t1, tn = timed(fn, arrays)
+        g1, gn = 3 * n / t1 / 1e9, 3 * n / tn / 1e9
+        out[name] = {"workload": what, "elements_sampled": int(n), "GB/s_1_core": round(g1, 4),
+                     f"GB/s_{cores}_cores": round(gn, 4), "seconds_1_core": round(t1, 3)}
+        compact[name] = [round(g1, 4), round(gn, 4)]
+    hist, new, sc, si, sf = W.scale_update_inputs("cpu")
+    ups = {}
+    for algo in (oracle.ALGO_MAX, oracle.ALGO_MOST_RECENT):
+        for margin in (0, 1):
+            h, a, b = hist.numpy().copy(), sc.numpy().copy(), si.numpy().copy()
+            t0 = time.perf_counter()
+            oracle.amax_scale_update(h, new.numpy(), a, b, oracle.E4M3FN, algo, margin, sf.numpy())
+            ups[f"{'max' if algo == 0 else 'most_recent'}_m{margin}"] = round((time.perf_counter() - t0) * 1e6, 1)
+    out["update_576x1024_us_1_core"] = ups
+    compact["update_us"] = list(ups.values())
+    return {"configs": out, "compact": compact, "sample_seconds": seconds,
+            "host": f"{os.uname().machine}, {cores} cores"}
+
+
 def run_reference(args):
     """The CPU oracle, as it stands, timed on the host on a bounded sample per step."""
     inp, nbytes, desc = _oracle_sample(args.ref_sample_frac)
@@ -996,6 +1176,67 @@ def run_reference(args):
             "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+CASES = ("quantize_8192x16384", "quantize_8192x4096", "dequantize_8192x16384", "update_576x1024",
+         "gelu_8192x16384", "layernorm_8192x4096", "qdq_8192x16384")
+
+
+def run_case(name: str, launches: int):
+    """One kernel on its benchmark workload, `launches` times back to back, then exit:
+    the program a profiler captures (ncu -k <kernel> -s 1 -c 1 ...).  The 100 MB
+    quantize case reads 256 MB before each launch, so that it starts from a cold L2,
+    as in the bench's other_configs."""
+    import torch
+    from quantize_amax_scaling_gb300 import fp8q as f
+    from quantize_amax_scaling_gb300 import workloads as W
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    sc = torch.full((1,), 0.0091, device=dev)
+    am = torch.zeros(1, device=dev)
+    before = None
+    if name == "quantize_8192x16384":
+        x = W.gelu_activation(W.SEED_FFN, dev).reshape(-1)
+        q = torch.empty(x.numel(), dtype=torch.uint8, device=dev)
+        launch = lambda: f.fp8q_quantize_amax(x, q, f.E4M3FN, sc, am)
+    elif name == "quantize_8192x4096":
+        x = W.mlp_activation(W.SEED_MLP, dev).reshape(-1)
+        q = torch.empty(x.numel(), dtype=torch.uint8, device=dev)
+        flush = torch.zeros(64 * 1024 * 1024, dtype=torch.int32, device=dev)
+        before = lambda: flush.sum()
+        launch = lambda: f.fp8q_quantize_amax(x, q, f.E4M3FN, sc, am)
+    elif name == "dequantize_8192x16384":
+        g = W.gradient(GRAD, W.SEED_GRAD, dev).reshape(-1)
+        q = torch.empty(g.numel(), dtype=torch.uint8, device=dev)
+        f.fp8q_quantize_amax(g, q, f.E5M2, sc, am)
+        y = torch.empty(g.numel(), dtype=torch.bfloat16, device=dev)
+        launch = lambda: f.fp8q_dequantize(q, y, f.E5M2, sc)
+    elif name == "update_576x1024":
+        hist, new, scale, scale_inv, sf = W.scale_update_inputs(dev)
+        launch = lambda: f.fp8q_amax_scale_update(hist, new, scale, scale_inv, f.E4M3FN, f.ALGO_MAX, 0, sf)
+    elif name == "gelu_8192x16384":
+        g = torch.Generator(device=dev)
+        g.manual_seed(7)
+        h = torch.randn(N_ACT, generator=g, device=dev).to(torch.bfloat16)
+        q = torch.empty(N_ACT, dtype=torch.uint8, device=dev)
+        launch = lambda: f.fp8q_gelu_quantize_amax(h, None, q, f.E4M3FN, sc, am)
+    elif name == "layernorm_8192x4096":
+        x = W.residual_stream(device=dev)
+        gam, bet = W.layernorm_params(x.shape[1], device=dev)
+        q = torch.empty(x.shape, dtype=torch.uint8, device=dev)
+        launch = lambda: f.fp8q_layernorm_quantize_amax(x, None, q, gam, bet, f.E4M3FN, sc, am)
+    elif name == "qdq_8192x16384":
+        x = W.gelu_activation(W.SEED_FFN, dev).reshape(-1)
+        y = torch.empty(x.numel(), dtype=torch.bfloat16, device=dev)
+        launch = lambda: f.fp8q_qdq_amax(x, y, f.E4M3FN, sc, am)
+    else:
+        raise ValueError(name)
+    for _ in range(launches):
+        if before:
+            before()
+        launch()
+    torch.cuda.synchronize(dev)
+    return {"case": name, "launches": launches, "amax": float(am)}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -1009,10 +1250,18 @@ def main(argv=None):
                     help="skip the CUDA-graph and next-row measurements (run after the timed region)")
     ap.add_argument("--cpu-sample-frac", type=float, default=0.4)  # about 10 s of oracle work
     ap.add_argument("--ref-sample-frac", type=float, default=1.0 / 128)
+    ap.add_argument("--case", choices=CASES, default=None,
+                    help="launch one kernel on its benchmark workload --launches times and exit (for profilers)")
+    ap.add_argument("--launches", type=int, default=2)
+    ap.add_argument("--cpu-config-seconds", type=float, default=1.0,
+                    help="about this much single-core oracle work per config of the per-config CPU baseline")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     ws, rank, local = dist_env()
+    if args.case:
+        print(json.dumps(run_case(args.case, args.launches)), flush=True)
+        return 0
     if args.impl == "reference":
         if rank != 0:
             return 0

@@ -468,24 +468,31 @@ __device__ __forceinline__ uint32_t ln_pair(uint32_t w, float nmean, float2 rstd
     return cvt_bf16x2(y.x, y.y);
 }
 
-// quant_pair's fast path, two lanes at a time: y0 = RN(x r), e = fma(y0, s, -x),
-// y = fma(-e, r, y0) is the correctly rounded quotient in each lane.
+// quant_pair's fast path, two lanes at a time, returning the codes of -y.
+// quant_pair computes y0 = RN(x r), e = fma(y0, s, -x), y = fma(-e, r, y0),
+// the correctly rounded quotient.  With every sign carried by an operand
+// instead (two-lane operations cannot fold a negation): n0 = RN(x (-r)) = -y0,
+// n1 = fma(n0, s, x) = -e and t = fma(n1, -r, n0) = -y, each exactly the
+// negation of the original step, since rounding to nearest is symmetric.  The
+// caller flips the codes' sign bits, which maps the codes of -y to those of y
+// (a NaN code stays a NaN code).
 template <int FMT>
-__device__ __forceinline__ uint32_t quant_pair_x2(uint32_t w, const QScale& c) {
+__device__ __forceinline__ uint32_t quant_pair_x2_neg(uint32_t w, const QScale& c) {
     w = bf16x2_clamp(w, c.t2);
     const float2 x = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
-    const float2 y0 = mul2_rn(x, splat2(c.r));
-    const float2 e = fma2_rn(y0, splat2(c.s), make_float2(-x.x, -x.y));
-    const float2 y = fma2_rn(make_float2(-e.x, -e.y), splat2(c.r), y0);
-    return cvt_fp8x2<FMT>(y.x, y.y);
+    const float2 nr = splat2(-c.r);
+    const float2 n0 = mul2_rn(x, nr);
+    const float2 n1 = fma2_rn(n0, splat2(c.s), x);
+    const float2 t = fma2_rn(n1, nr, n0);
+    return cvt_fp8x2<FMT>(t.x, t.y);
 }
 
 // Eight bf16 of y -> eight FP8 codes.
 template <int FMT, bool FAST>
 __device__ __forceinline__ uint2 ln_quant8(const uint4& y, const QScale& c) {
     if (FAST)
-        return make_uint2(quant_pair_x2<FMT>(y.x, c) | (quant_pair_x2<FMT>(y.y, c) << 16),
-                          quant_pair_x2<FMT>(y.z, c) | (quant_pair_x2<FMT>(y.w, c) << 16));
+        return make_uint2((quant_pair_x2_neg<FMT>(y.x, c) | (quant_pair_x2_neg<FMT>(y.y, c) << 16)) ^ 0x80808080u,
+                          (quant_pair_x2_neg<FMT>(y.z, c) | (quant_pair_x2_neg<FMT>(y.w, c) << 16)) ^ 0x80808080u);
     return make_uint2(quant_quad<FMT, false>(y.x, y.y, c), quant_quad<FMT, false>(y.z, y.w, c));
 }
 
