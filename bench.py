@@ -405,7 +405,7 @@ def run_gpu(args, ws, rank, local):
         out["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
         out["cpu_baseline"]["all_cores"] = {"value": cba["value"], "cores": cba["cores"]}
         out["cpu_baseline"]["per_config"] = pc["compact"]
-    out["detail"] = write_detail(detail)
+    out["detail"] = write_detail(detail, args.detail)
     return out
 
 
@@ -424,12 +424,11 @@ def compact_rows(kernels, next_rows, other_configs):
     return r
 
 
-def write_detail(detail):
+def write_detail(detail, path):
     """Every figure of the run, as JSON, beside the printed line; returns its path."""
-    d = os.path.join(ROOT, "gpurun_out")
+    p = path if os.path.isabs(path) else os.path.join(ROOT, path)
     try:
-        os.makedirs(d, exist_ok=True)
-        p = os.path.join(d, "bench_detail.json")
+        os.makedirs(os.path.dirname(p), exist_ok=True)
         with open(p, "w") as f:
             json.dump(detail, f, indent=1)
         return os.path.relpath(p, ROOT)
@@ -1154,7 +1153,27 @@ def cpu_per_config(seconds: float):
     out["update_576x1024_us_1_core"] = ups
     compact["update_us"] = list(ups.values())
     return {"configs": out, "compact": compact, "sample_seconds": seconds,
-            "host": f"{os.uname().machine}, {cores} cores"}
+            "host": f"{os.uname().machine}, {cores} cores, {cpu_model()}"}
+
+
+def cpu_model() -> str:
+    """The host CPU's model name, as lscpu or /proc/cpuinfo give it ("" if neither)."""
+    import subprocess
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return ""
 
 
 def run_reference(args):
@@ -1253,6 +1272,8 @@ def main(argv=None):
     ap.add_argument("--case", choices=CASES, default=None,
                     help="launch one kernel on its benchmark workload --launches times and exit (for profilers)")
     ap.add_argument("--launches", type=int, default=2)
+    ap.add_argument("--detail", default="bench_detail.json",
+                    help="where every figure of the run is written as JSON (the printed line is the summary)")
     ap.add_argument("--cpu-config-seconds", type=float, default=1.0,
                     help="about this much single-core oracle work per config of the per-config CPU baseline")
     args = ap.parse_args(argv)
