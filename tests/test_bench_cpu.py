@@ -78,3 +78,44 @@ def test_cpu_baseline_all_cores_runs_the_same_sample():
     many = bench.cpu_baseline_all_cores(0.002)
     assert many["sample"] == one["sample"]
     assert many["cores"] == (os.cpu_count() or 1) and many["value"] > 0
+
+
+def test_cpu_per_config_covers_every_workload():
+    """The per-config CPU baseline times the oracle on each configured workload, on one core
+    and on all cores, and the 576-slot update for both algorithms and both margins."""
+    import bench
+    r = bench.cpu_per_config(0.02)
+    c = r["compact"]
+    assert c["cores"] == (os.cpu_count() or 1)
+    for k in ("mlp_activation", "ffn", "grad_quantize", "grad_dequantize", "ragged_12"):
+        one, many = c[k]
+        assert one > 0 and many > 0
+        assert r["configs"][k]["elements_sampled"] > 0
+    assert len(c["update_us"]) == 4 and all(u > 0 for u in c["update_us"])
+    assert len(json.dumps(c)) < 400          # it rides on the printed line
+
+
+def test_compact_rows_and_detail_file(tmp_path):
+    import bench
+    kernels = {"multi_quantize_amax": {"frac_of_peak": 0.95}, "dequantize": {"frac_of_peak": 0.94}}
+    other = {"mlp_activation": {"frac_of_peak": 0.9}, "ragged_twelve_tensors": {"frac_of_peak": 1.04}}
+    nxt = {"qdq_amax": {"frac_of_peak": 0.99}, "gelu_quantize_amax": {"codes_only": {"frac_of_peak": 0.82}},
+           "layernorm_quantize_amax": {"codes_only": {"frac_of_peak": 0.6}},
+           "amax_scale_update_ring": {"us": 7.6}}
+    rows = bench.compact_rows(kernels, nxt, other)
+    assert rows == {"multi_quantize_frac": 0.95, "dequantize_frac": 0.94, "mlp_activation_8192x4096_frac": 0.9,
+                    "ragged_12_frac": 1.04, "qdq_frac": 0.99, "gelu_codes_frac": 0.82,
+                    "layernorm_codes_frac": 0.6, "ring_update_us": 7.6}
+    assert bench.compact_rows(kernels, None, None) == {"multi_quantize_frac": 0.95, "dequantize_frac": 0.94}
+    p = tmp_path / "sub" / "detail.json"
+    where = bench.write_detail({"a": 1}, str(p))
+    assert json.loads(p.read_text()) == {"a": 1} and where.endswith("detail.json")
+
+
+def test_profile_cases_are_listed_in_the_help():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--help"], capture_output=True,
+                         text=True, timeout=300, cwd=ROOT)
+    assert out.returncode == 0
+    import bench
+    for case in bench.CASES:
+        assert case in out.stdout

@@ -53,11 +53,14 @@ def test_every_entry_point_is_one_launch():
     head2 = torch.empty_like(head)
     xl = W.mlp_activation(2, dev, (4096, 4096)).reshape(-1)   # 2^24 elements: the GELU table path
     ql = torch.empty(xl.numel(), dtype=torch.uint8, device=dev)
+    xt = W.mlp_activation(3, dev, (3000, 16384)).reshape(-1)  # 3000 tiles: one CTA per tile
+    qt = torch.empty(xt.numel(), dtype=torch.uint8, device=dev)
     third = x.numel() // 3
     ws, qs = [x[:third], x[third:]], [q[:third], q[third:]]
     st = s.cuda_stream
     calls = {
-        "quantize": lambda: fp8q.fp8q_quantize_amax(x, q, fp8q.E4M3FN, sc[0:1], am[0:1], st),
+        "quantize, persistent grid": lambda: fp8q.fp8q_quantize_amax(x, q, fp8q.E4M3FN, sc[0:1], am[0:1], st),
+        "quantize, one CTA per tile": lambda: fp8q.fp8q_quantize_amax(xt, qt, fp8q.E4M3FN, sc[0:1], am[0:1], st),
         "multi (2 tensors)": lambda: fp8q.fp8q_multi_quantize_amax(ws, qs, fp8q.E4M3FN, [sc[1:2], sc[2:3]],
                                                                    [am[1:2], am[2:3]], st),
         "dequantize": lambda: fp8q.fp8q_dequantize(q, y, fp8q.E4M3FN, sc[0:1], st),
@@ -89,9 +92,10 @@ def test_every_entry_point_is_one_launch():
 
 @pytest.mark.gpu
 def test_layernorm_first_call_inside_graph_capture():
-    """The LayerNorm call's first use on a device (function attribute, occupancy query)
-    may itself be captured: in a fresh process, capture it, replay, and compare with an
-    eager call."""
+    """The first use on a device of the calls that query the device (the LayerNorm call:
+    function attribute and occupancy; the quantize of a mid-size tensor: the SM count) may
+    itself be captured: in a fresh process, capture them, replay, and compare with eager
+    calls."""
     import subprocess
     import sys
     code = r'''
@@ -102,15 +106,21 @@ x = W.residual_stream(seed=1, device=dev, shape=(64, 4096))
 g, b = W.layernorm_params(4096, device=dev)
 sc = torch.full((1,), 0.02, device=dev)
 q, am = torch.empty(x.shape, dtype=torch.uint8, device=dev), torch.zeros(1, device=dev)
+xm = W.mlp_activation(5, dev, (512, 4096)).reshape(-1)
+qm, amm = torch.empty(xm.numel(), dtype=torch.uint8, device=dev), torch.zeros(1, device=dev)
 gr = torch.cuda.CUDAGraph()
 with torch.cuda.graph(gr, stream=torch.cuda.Stream()):
     fp8q.fp8q_layernorm_quantize_amax(x, None, q, g, b, fp8q.E4M3FN, sc, am)
+    fp8q.fp8q_quantize_amax(xm, qm, fp8q.E4M3FN, sc, amm)
 gr.replay()
 torch.cuda.synchronize()
 q2, am2 = torch.empty_like(q), torch.zeros(1, device=dev)
 fp8q.fp8q_layernorm_quantize_amax(x, None, q2, g, b, fp8q.E4M3FN, sc, am2)
+qm2, amm2 = torch.empty_like(qm), torch.zeros(1, device=dev)
+fp8q.fp8q_quantize_amax(xm, qm2, fp8q.E4M3FN, sc, amm2)
 torch.cuda.synchronize()
 assert torch.equal(q, q2) and float(am) == float(am2)
+assert torch.equal(qm, qm2) and float(amm) == float(amm2)
 print("OK")
 '''
     env = dict(os.environ, PYTHONPATH=ROOT + os.pathsep + os.environ.get("PYTHONPATH", ""))
