@@ -192,9 +192,10 @@ __global__ void __launch_bounds__(kThreads, 4) gelu_quantize_amax_kernel(const G
 // in place of the GELU arithmetic.  One CTA per SM (the table fills most of
 // the shared memory), looping over the vectors two at a time, with the next
 // two already loading while the current two are converted, so that enough
-// loads are in flight.  Building the table costs each cluster about what
-// 65536 elements cost the direct kernel, so smaller tensors, and any that
-// take the element-by-element path, use the direct kernel.
+// loads are in flight; the first two go out before the table is built.
+// Building the table costs each cluster about what 65536 elements cost the
+// direct kernel, so smaller tensors, and any that take the element-by-element
+// path, use the direct kernel.
 
 // threads per CTA: 1024 for the codes alone; 512 when y is stored too (its
 // extra registers would spill at 1024)
@@ -267,6 +268,18 @@ __global__ void __launch_bounds__(gelu_table_threads<WRITE_Y>(), 1)
     constexpr int kGeluTableThreads = gelu_table_threads<WRITE_Y>();
     extern __shared__ __align__(16) uint32_t tab32[];  // word p: the results for inputs 2p and 2p + 1
     __shared__ uint32_t red[kGeluTableThreads / 32];
+    constexpr int E = GeluGeom::kVecElems;
+    const int64_t stride = (int64_t)gridDim.x * kGeluTableThreads;
+    uint32_t m2 = 0, ms = 0;
+    int64_t v0 = (int64_t)blockIdx.x * kGeluTableThreads + threadIdx.x;
+    // The first vectors' loads go out before the table is built, so the build
+    // hides their latency.
+    uint4 wa[kGeluTableUnroll], wb[kGeluTableUnroll];
+#pragma unroll
+    for (int u = 0; u < kGeluTableUnroll; ++u) {
+        const int64_t v = v0 + u * stride;
+        if (v < a.nvec) ld_stream_v8(a.h + a.head + v * E, wa[u], wb[u]);
+    }
     {
         constexpr int kGeluTableCluster = gelu_table_cluster<WRITE_Y>();
         constexpr int kShare = 32768 / kGeluTableCluster;  // at least the CTA's thread count
@@ -292,16 +305,6 @@ __global__ void __launch_bounds__(gelu_table_threads<WRITE_Y>(), 1)
     const QScale c = make_qscale(a.scale);
     cluster_sync_all();  // every CTA's table is complete; no remote store comes after this
     const uint16_t* tab = reinterpret_cast<const uint16_t*>(tab32);
-    constexpr int E = GeluGeom::kVecElems;
-    const int64_t stride = (int64_t)gridDim.x * kGeluTableThreads;
-    uint32_t m2 = 0, ms = 0;
-    int64_t v0 = (int64_t)blockIdx.x * kGeluTableThreads + threadIdx.x;
-    uint4 wa[kGeluTableUnroll], wb[kGeluTableUnroll];
-#pragma unroll
-    for (int u = 0; u < kGeluTableUnroll; ++u) {
-        const int64_t v = v0 + u * stride;
-        if (v < a.nvec) ld_stream_v8(a.h + a.head + v * E, wa[u], wb[u]);
-    }
     for (; v0 < a.nvec; v0 += kGeluTableUnroll * stride) {
         uint4 na[kGeluTableUnroll], nb[kGeluTableUnroll];
         const int64_t v1 = v0 + kGeluTableUnroll * stride;
@@ -468,31 +471,24 @@ __device__ __forceinline__ uint32_t ln_pair(uint32_t w, float nmean, float2 rstd
     return cvt_bf16x2(y.x, y.y);
 }
 
-// quant_pair's fast path, two lanes at a time, returning the codes of -y.
-// quant_pair computes y0 = RN(x r), e = fma(y0, s, -x), y = fma(-e, r, y0),
-// the correctly rounded quotient.  With every sign carried by an operand
-// instead (two-lane operations cannot fold a negation): n0 = RN(x (-r)) = -y0,
-// n1 = fma(n0, s, x) = -e and t = fma(n1, -r, n0) = -y, each exactly the
-// negation of the original step, since rounding to nearest is symmetric.  The
-// caller flips the codes' sign bits, which maps the codes of -y to those of y
-// (a NaN code stays a NaN code).
+// quant_pair's fast path, two lanes at a time: y0 = RN(x r), e = fma(y0, s, -x),
+// y = fma(-e, r, y0) is the correctly rounded quotient in each lane.
 template <int FMT>
-__device__ __forceinline__ uint32_t quant_pair_x2_neg(uint32_t w, const QScale& c) {
+__device__ __forceinline__ uint32_t quant_pair_x2(uint32_t w, const QScale& c) {
     w = bf16x2_clamp(w, c.t2);
     const float2 x = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
-    const float2 nr = splat2(-c.r);
-    const float2 n0 = mul2_rn(x, nr);
-    const float2 n1 = fma2_rn(n0, splat2(c.s), x);
-    const float2 t = fma2_rn(n1, nr, n0);
-    return cvt_fp8x2<FMT>(t.x, t.y);
+    const float2 y0 = mul2_rn(x, splat2(c.r));
+    const float2 e = fma2_rn(y0, splat2(c.s), make_float2(-x.x, -x.y));
+    const float2 y = fma2_rn(make_float2(-e.x, -e.y), splat2(c.r), y0);
+    return cvt_fp8x2<FMT>(y.x, y.y);
 }
 
 // Eight bf16 of y -> eight FP8 codes.
 template <int FMT, bool FAST>
 __device__ __forceinline__ uint2 ln_quant8(const uint4& y, const QScale& c) {
     if (FAST)
-        return make_uint2((quant_pair_x2_neg<FMT>(y.x, c) | (quant_pair_x2_neg<FMT>(y.y, c) << 16)) ^ 0x80808080u,
-                          (quant_pair_x2_neg<FMT>(y.z, c) | (quant_pair_x2_neg<FMT>(y.w, c) << 16)) ^ 0x80808080u);
+        return make_uint2(quant_pair_x2<FMT>(y.x, c) | (quant_pair_x2<FMT>(y.y, c) << 16),
+                          quant_pair_x2<FMT>(y.z, c) | (quant_pair_x2<FMT>(y.w, c) << 16));
     return make_uint2(quant_quad<FMT, false>(y.x, y.y, c), quant_quad<FMT, false>(y.z, y.w, c));
 }
 
