@@ -397,7 +397,7 @@ def run_gpu(args, ws, rank, local):
         "e2e": None if e2e is None else {k: e2e[k] for k in ("value", "unit", "h2d_bytes_per_step",
                                                              "d2h_bytes_per_step", "link_gbs", "frac_of_link")},
     }
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and ws == 1:  # the CPU baseline runs at N = 1 only
         cb = cpu_baseline(args.cpu_sample_frac)
         cba = cpu_baseline_all_cores(args.cpu_sample_frac)
         pc = cpu_per_config(args.cpu_config_seconds)

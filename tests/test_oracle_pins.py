@@ -798,3 +798,45 @@ def test_bf16_within_accepts_only_the_interval(orc):
     ok = orc.bf16_within(y_other, r, E)
     # 1 + 2^-8 +- 2^-30 straddles the tie: both neighbours are acceptable
     assert list(ok) == [True, False, False, False, False]
+
+
+def test_gelu_tolerance_rejects_a_wrong_gelu(orc):
+    """The GELU bar is discriminating: a binary32 GELU whose cubic coefficient is off by
+    0.01% (0.04471) lands outside the tolerance on some bf16 inputs, and so does one that
+    goes through a tanh accurate to only 2^-11 (as a hardware approximation is)."""
+    h = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    x = (h.astype(np.uint32) << 16).view(np.float32)
+    fin = np.isfinite(x) & (np.abs(x) < 8)
+    hf, xf = h[fin], x[fin].astype(np.float64)
+    r = orc.gelu_ref_array(hf)
+    E = orc.gelu_tolerance(xf, r)
+
+    def bf16(v):
+        return torch.from_numpy(np.asarray(v, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+    x32 = x[fin].astype(np.float32)
+    k = np.float32(math.sqrt(2.0 / math.pi))
+    wrong_c = x32 * np.float32(0.5) * (np.float32(1) + np.tanh(k * (x32 + np.float32(0.04471) * x32 ** 3)))
+    assert (~orc.bf16_within(bf16(wrong_c), r, E)).sum() > 20
+    t = np.tanh(xf * math.sqrt(2 / math.pi) * (1 + 0.044715 * xf * xf))
+    coarse = 0.5 * xf * (1 + t * (1 + 2.0 ** -11))
+    assert (~orc.bf16_within(bf16(coarse), r, E)).sum() > 20
+
+
+def test_layernorm_tolerance_rejects_a_wrong_layernorm(orc):
+    """The LayerNorm bar is discriminating: rows normalised with eps = 1e-5 instead of
+    1e-6, or with the unbiased variance (divided by H - 1), land outside it."""
+    rng = np.random.default_rng(71)
+    H, rows = 1024, 16
+    x = torch.from_numpy((rng.normal(0, 1, (rows, H)) * rng.uniform(0.05, 3, (rows, 1))
+                          + rng.normal(0, 1, (rows, 1))).astype(np.float32)).to(torch.bfloat16)
+    g = (1 + 0.1 * rng.normal(0, 1, H)).astype(np.float32)
+    b = (0.1 * rng.normal(0, 1, H)).astype(np.float32)
+    r, mean, rstd = orc.layernorm_ref(_u16(x), H, g, b, 1e-6)
+    E = orc.layernorm_tolerance(x.double().numpy(), g, b, 1e-6, mean, rstd, r)
+    x64 = x.double().numpy()
+    for wrong in (torch.nn.functional.layer_norm(x.double(), (H,), torch.from_numpy(g).double(),
+                                                 torch.from_numpy(b).double(), eps=1e-5).numpy(),
+                  (x64 - x64.mean(1, keepdims=True)) / np.sqrt(x64.var(1, ddof=1, keepdims=True) + 1e-6) * g + b):
+        yb = torch.from_numpy(wrong.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        assert (~orc.bf16_within(yb.reshape(-1), r, E.reshape(-1))).sum() > 20
