@@ -7,7 +7,34 @@
 
 #include <mutex>
 
+
 namespace {
+
+// quant_pair's fast path, two lanes at a time: y0 = RN(x r), e = fma(y0, s, -x),
+// y = fma(-e, r, y0) is the correctly rounded quotient in each lane.
+template <int FMT>
+__device__ __forceinline__ uint32_t quant_pair_x2(uint32_t w, const QScale& c) {
+    w = bf16x2_clamp(w, c.t2);
+    const float2 x = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+    const float2 y0 = mul2_rn(x, splat2(c.r));
+    const float2 e = fma2_rn(y0, splat2(c.s), make_float2(-x.x, -x.y));
+    const float2 y = fma2_rn(make_float2(-e.x, -e.y), splat2(c.r), y0);
+    return cvt_fp8x2<FMT>(y.x, y.y);
+}
+
+// Four bf16 (two words) -> four FP8 codes in one word; the fast path two lanes
+// at a time.
+template <int FMT, bool FAST>
+__device__ __forceinline__ uint32_t quant_quad_x2(uint32_t w0, uint32_t w1, const QScale& c) {
+    if (FAST) return quant_pair_x2<FMT>(w0, c) | (quant_pair_x2<FMT>(w1, c) << 16);
+    return quant_quad<FMT, false>(w0, w1, c);
+}
+
+// Eight bf16 of y -> eight FP8 codes.
+template <int FMT, bool FAST>
+__device__ __forceinline__ uint2 quant8(const uint4& y, const QScale& c) {
+    return make_uint2(quant_quad_x2<FMT, FAST>(y.x, y.y, c), quant_quad_x2<FMT, FAST>(y.z, y.w, c));
+}
 
 // ----------------------------------------------------------------------------
 // GELU producer fused with quantize + amax
@@ -184,24 +211,30 @@ __global__ void __launch_bounds__(kThreads, 4) gelu_quantize_amax_kernel(const G
 // ----------------------------------------------------------------------------
 // GELU through a table of every bf16 input
 //
-// y = bf16(GELU(h)) depends only on the 16 bits of h.  For large tensors each
-// CTA first gets all 65536 values, computed with gelu_pair -- the arithmetic
-// of the kernel above, so the same bits -- into shared memory (128 KB); the
-// CTAs of a thread-block cluster compute them once between them.  It then
-// streams its share of the tensor with one shared-memory lookup per element
-// in place of the GELU arithmetic.  One CTA per SM (the table fills most of
-// the shared memory), looping over the vectors two at a time, with the next
-// two already loading while the current two are converted, so that enough
-// loads are in flight; the first two go out before the table is built.
-// Building the table costs each cluster about what 65536 elements cost the
-// direct kernel, so smaller tensors, and any that take the element-by-element
-// path, use the direct kernel.
+// y = bf16(GELU(h)), and so its FP8 code at a given scale, depends only on the
+// 16 bits of h.  For large tensors each CTA first gets a table over all 65536
+// inputs into shared memory; the CTAs of a thread-block cluster compute it
+// once between them, every y with gelu_pair -- the arithmetic of the kernel
+// above, so the same bits.  The CTA then streams its share of the tensor with
+// shared-memory lookups in place of the GELU arithmetic:
+//  - with y, the table holds y (128 KB) and each y is then quantized as above;
+//  - for the codes alone it holds the FP8 code of every input at this launch's
+//    scale (64 KB, each quantized once), so an element costs one byte lookup
+//    (or, for one element in eight, the arithmetic), and amax comes from the
+//    largest input (gelu_code_table_kernel).
+// One CTA per SM, looping over the vectors two at a time, with the next two
+// already loading while the current two are looked up, so that enough loads
+// are in flight; the first two go out before the table is built.  Building
+// the table costs each cluster about what 65536 elements cost the direct
+// kernel, so smaller tensors, and any that take the element-by-element path,
+// use the direct kernel.
 
-// threads per CTA: 1024 for the codes alone; 512 when y is stored too (its
-// extra registers would spill at 1024)
-template <bool WRITE_Y>
-__host__ __device__ constexpr int gelu_table_threads() { return WRITE_Y ? 512 : 1024; }
-constexpr uint32_t kGeluTableBytes = 65536u * 2u;
+// Threads per CTA: 1024 for the codes alone; 512 when y is stored too (its
+// extra registers would spill at 1024).
+constexpr int kGeluYTableThreads = 512;
+constexpr int kGeluCodeTableThreads = 1024;
+constexpr uint32_t kGeluYTableBytes = 65536u * 2u;
+constexpr uint32_t kGeluCodeTableBytes = 65536u;
 // Fewer elements take the direct kernel (measured crossovers on GB300: the
 // table wins from about 2^24 elements for the codes alone, 2^26 with y).
 #ifdef FP8Q_TEST_GELU_TABLE_MIN_ELEMS  // test-only build: small tensors take the table path too
@@ -215,11 +248,11 @@ constexpr int kGeluTableUnroll = 2;
 // CTAs of one thread-block cluster (on as many SMs) build their tables
 // together: each computes its share of the entries and stores each into the
 // shared memory of every CTA of the cluster.  Measured on GB300 (8192x16384):
-// clusters of 2 for the codes alone (1024 threads build fast; 72.1 us, 74.3
-// without clusters, 74.2 with 4), of 4 with y (512 threads; 112.7 us, 118.5
-// without, 117.4 with 2).  Clusters of 8 leave SMs idle (86.4 us codes only).
-template <bool WRITE_Y>
-__host__ __device__ constexpr int gelu_table_cluster() { return WRITE_Y ? 4 : 2; }
+// with y (512 threads), clusters of 4, 112.7 us, against 118.5 without and
+// 117.4 with 2; codes alone (1024 threads), clusters of 2, 69.7 us, against
+// 71.6 with 4.  Clusters of 8 leave SMs idle.
+constexpr int kGeluYTableCluster = 4;
+constexpr int kGeluCodeTableCluster = 2;
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
@@ -253,6 +286,44 @@ __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Fill the table of every CTA of the cluster: word p of kWords is entry(p).
+// CTA rank r computes the words of its share, [r kWords / C, (r + 1) kWords / C),
+// and stores each into the same place in every CTA of the cluster.  No CTA may
+// touch another's shared memory before that CTA is known to be running: each
+// arrives on the cluster barrier at entry and waits on it just before its
+// first remote store, with its first word computed in between.  The caller
+// then makes every table complete with cluster_sync_all.
+template <int kCtaThreads, int kCluster, int kWords, typename Entry>
+__device__ __forceinline__ void cluster_build(uint32_t* tab32, Entry entry) {
+    constexpr int kShare = kWords / kCluster;
+    static_assert(kShare % kCtaThreads == 0, "every thread computes the same number of words");
+    cluster_arrive_relaxed();
+    const uint32_t rank = cluster_ctarank();
+    uint32_t dst[kCluster];
+#pragma unroll
+    for (int r = 0; r < kCluster; ++r) dst[r] = cluster_map(smem_addr(tab32), (uint32_t)r);
+    int p = (int)rank * kShare + threadIdx.x;
+    uint32_t v = entry(p);
+    cluster_wait();
+    for (;;) {
+#pragma unroll
+        for (int r = 0; r < kCluster; ++r) st_cluster_u32(dst[r] + 4u * (uint32_t)p, v);
+        p += kCtaThreads;
+        if (p >= ((int)rank + 1) * kShare) break;
+        v = entry(p);
+    }
+}
+
+// The next vectors of 16 bf16 of a thread that visits v, v + stride, ...
+__device__ __forceinline__ void gelu_load2(const GeluArgs& a, int64_t v, int64_t stride, uint4 (&wa)[2],
+                                           uint4 (&wb)[2]) {
+#pragma unroll
+    for (int u = 0; u < kGeluTableUnroll; ++u) {
+        const int64_t vu = v + u * stride;
+        if (vu < a.nvec) ld_stream_v8(a.h + a.head + vu * GeluGeom::kVecElems, wa[u], wb[u]);
+    }
+}
+
 __device__ __forceinline__ uint32_t gelu_lookup_pair(const uint16_t* tab, uint32_t w) {
     return (uint32_t)tab[w & 0xFFFFu] | ((uint32_t)tab[w >> 16] << 16);
 }
@@ -262,64 +333,31 @@ __device__ __forceinline__ uint4 gelu_lookup4(const uint16_t* tab, const uint4& 
                       gelu_lookup_pair(tab, w.w));
 }
 
-template <int FMT, bool WRITE_Y>
-__global__ void __launch_bounds__(gelu_table_threads<WRITE_Y>(), 1)
-    gelu_table_quantize_amax_kernel(const GeluArgs a) {
-    constexpr int kGeluTableThreads = gelu_table_threads<WRITE_Y>();
-    extern __shared__ __align__(16) uint32_t tab32[];  // word p: the results for inputs 2p and 2p + 1
-    __shared__ uint32_t red[kGeluTableThreads / 32];
+template <int FMT>
+__global__ void __launch_bounds__(kGeluYTableThreads, 1) gelu_table_quantize_amax_kernel(const GeluArgs a) {
+    extern __shared__ __align__(16) uint32_t tab32[];  // word p: the y of inputs 2p and 2p + 1
+    __shared__ uint32_t red[kGeluYTableThreads / 32];
     constexpr int E = GeluGeom::kVecElems;
-    const int64_t stride = (int64_t)gridDim.x * kGeluTableThreads;
+    const int64_t stride = (int64_t)gridDim.x * kGeluYTableThreads;
     uint32_t m2 = 0, ms = 0;
-    int64_t v0 = (int64_t)blockIdx.x * kGeluTableThreads + threadIdx.x;
-    // The first vectors' loads go out before the table is built, so the build
-    // hides their latency.
+    int64_t v0 = (int64_t)blockIdx.x * kGeluYTableThreads + threadIdx.x;
     uint4 wa[kGeluTableUnroll], wb[kGeluTableUnroll];
-#pragma unroll
-    for (int u = 0; u < kGeluTableUnroll; ++u) {
-        const int64_t v = v0 + u * stride;
-        if (v < a.nvec) ld_stream_v8(a.h + a.head + v * E, wa[u], wb[u]);
-    }
-    {
-        constexpr int kGeluTableCluster = gelu_table_cluster<WRITE_Y>();
-        constexpr int kShare = 32768 / kGeluTableCluster;  // at least the CTA's thread count
-        // No CTA may touch another's shared memory before that CTA is known to
-        // be running: arrive on the cluster barrier now, and wait on it just
-        // before the first remote store, with the first pair computed meanwhile.
-        cluster_arrive_relaxed();
-        const uint32_t rank = cluster_ctarank();
-        uint32_t dst[kGeluTableCluster];
-#pragma unroll
-        for (int r = 0; r < kGeluTableCluster; ++r) dst[r] = cluster_map(smem_addr(tab32), (uint32_t)r);
-        int p = (int)rank * kShare + threadIdx.x;
-        uint32_t y = gelu_pair((uint32_t)(2 * p) | ((uint32_t)(2 * p + 1) << 16));
-        cluster_wait();
-        for (;;) {
-#pragma unroll
-            for (int r = 0; r < kGeluTableCluster; ++r) st_cluster_u32(dst[r] + 4u * (uint32_t)p, y);
-            p += kGeluTableThreads;
-            if (p >= ((int)rank + 1) * kShare) break;
-            y = gelu_pair((uint32_t)(2 * p) | ((uint32_t)(2 * p + 1) << 16));
-        }
-    }
+    gelu_load2(a, v0, stride, wa, wb);  // before the build, which hides their latency
+    cluster_build<kGeluYTableThreads, kGeluYTableCluster, 32768>(
+        tab32, [](int p) { return gelu_pair((uint32_t)(2 * p) | ((uint32_t)(2 * p + 1) << 16)); });
     const QScale c = make_qscale(a.scale);
     cluster_sync_all();  // every CTA's table is complete; no remote store comes after this
     const uint16_t* tab = reinterpret_cast<const uint16_t*>(tab32);
     for (; v0 < a.nvec; v0 += kGeluTableUnroll * stride) {
         uint4 na[kGeluTableUnroll], nb[kGeluTableUnroll];
-        const int64_t v1 = v0 + kGeluTableUnroll * stride;
-#pragma unroll
-        for (int u = 0; u < kGeluTableUnroll; ++u) {
-            const int64_t v = v1 + u * stride;
-            if (v < a.nvec) ld_stream_v8(a.h + a.head + v * E, na[u], nb[u]);
-        }
+        gelu_load2(a, v0 + kGeluTableUnroll * stride, stride, na, nb);
 #pragma unroll
         for (int u = 0; u < kGeluTableUnroll; ++u) {
             const int64_t v = v0 + u * stride;
             if (v < a.nvec) {
                 const uint4 ya = gelu_lookup4(tab, wa[u]), yb = gelu_lookup4(tab, wb[u]);
-                if (c.fast) gelu_emit<FMT, true, WRITE_Y>(a, c, v, ya, yb, m2);
-                else        gelu_emit<FMT, false, WRITE_Y>(a, c, v, ya, yb, m2);
+                if (c.fast) gelu_emit<FMT, true, true>(a, c, v, ya, yb, m2);
+                else        gelu_emit<FMT, false, true>(a, c, v, ya, yb, m2);
             }
         }
 #pragma unroll
@@ -331,10 +369,10 @@ __global__ void __launch_bounds__(gelu_table_threads<WRITE_Y>(), 1)
     if (blockIdx.x == 0) {  // scalar head and tail, each shorter than one vector
         const int64_t tail0 = a.head + a.nvec * E;
         const int64_t nscalar = a.head + (a.n - tail0);
-        for (int64_t j = threadIdx.x; j < nscalar; j += kGeluTableThreads) {
+        for (int64_t j = threadIdx.x; j < nscalar; j += kGeluYTableThreads) {
             const int64_t i = j < a.head ? j : tail0 + (j - a.head);
             const uint32_t yw = tab[a.h[i]];
-            if (WRITE_Y) a.y[i] = (uint16_t)yw;
+            a.y[i] = (uint16_t)yw;
             ms = max(ms, abs_bits_lo(yw));
             a.q[i] = (uint8_t)((c.fast ? quant_pair<FMT, true>(yw, c) : quant_pair<FMT, false>(yw, c)) & 0xFFu);
         }
@@ -346,7 +384,142 @@ __global__ void __launch_bounds__(gelu_table_threads<WRITE_Y>(), 1)
     __syncthreads();
     if (threadIdx.x == 0) {
         uint32_t b = red[0];
-        for (int w = 1; w < kGeluTableThreads / 32; ++w) b = max(b, red[w]);
+        for (int w = 1; w < kGeluYTableThreads / 32; ++w) b = max(b, red[w]);
+        atomicMax(reinterpret_cast<int*>(a.amax), (int)b);
+    }
+}
+
+// max(a, b) per bf16 lane by value (-0 and +0 either way); a NaN in either
+// gives the canonical NaN.
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// The FP8 codes of four inputs (two words) from the code table, in order.
+__device__ __forceinline__ uint32_t code_lookup4(const uint8_t* tab, uint32_t w0, uint32_t w1) {
+    return (uint32_t)tab[w0 & 0xFFFFu] | ((uint32_t)tab[w0 >> 16] << 8) | ((uint32_t)tab[w1 & 0xFFFFu] << 16) |
+           ((uint32_t)tab[w1 >> 16] << 24);
+}
+
+__device__ __forceinline__ uint32_t max8(uint32_t m, const uint4& a, const uint4& b) {
+    return bf16x2_max(m, bf16x2_max(bf16x2_max(bf16x2_max(a.x, a.y), bf16x2_max(a.z, a.w)),
+                                    bf16x2_max(bf16x2_max(b.x, b.y), bf16x2_max(b.z, b.w))));
+}
+
+// The codes of the thread's vectors v_first, v_first + stride, ... (the first
+// two already loading in wa, wb), and the largest input into hm2.  The lookups
+// keep the shared-memory pipe the busiest unit of the SM (a warp's 32 random
+// byte lookups cost about 3.3 bank wavefronts), while instruction issue has
+// room: so the first two elements of every vector are computed (gelu_pair and
+// the quantize, the same bits as their table entries) and the other 14 looked
+// up.  Measured on GB300 (8192x16384, CUDA events): 69.5 us, against 70.0-70.6
+// with every element looked up and 69.7-70.0 with four of 16 computed.
+template <int FMT, bool FAST>
+__device__ __forceinline__ void code_table_stream(const GeluArgs& a, const uint8_t* tab, const QScale& c,
+                                                  int64_t v_first, int64_t stride, uint4 (&wa)[2], uint4 (&wb)[2],
+                                                  uint32_t& hm2) {
+    constexpr int E = GeluGeom::kVecElems;
+    for (int64_t v0 = v_first; v0 < a.nvec; v0 += kGeluTableUnroll * stride) {
+        uint4 na[kGeluTableUnroll], nb[kGeluTableUnroll];
+        gelu_load2(a, v0 + kGeluTableUnroll * stride, stride, na, nb);
+#pragma unroll
+        for (int u = 0; u < kGeluTableUnroll; ++u) {
+            const int64_t v = v0 + u * stride;
+            if (v < a.nvec) {
+                hm2 = max8(hm2, wa[u], wb[u]);
+                // the first two elements computed, the other 14 looked up
+                const uint32_t o0 = quant_pair<FMT, FAST>(gelu_pair(wa[u].x), c) |
+                                    ((uint32_t)tab[wa[u].y & 0xFFFFu] << 16) | ((uint32_t)tab[wa[u].y >> 16] << 24);
+                st_v4(a.q + a.head + v * E, make_uint4(o0, code_lookup4(tab, wa[u].z, wa[u].w),
+                                                       code_lookup4(tab, wb[u].x, wb[u].y),
+                                                       code_lookup4(tab, wb[u].z, wb[u].w)));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kGeluTableUnroll; ++u) {
+            wa[u] = na[u];
+            wb[u] = nb[u];
+        }
+    }
+}
+
+// |y| of the low bf16 of w as a binary32 bit pattern, every NaN canonical.
+__device__ __forceinline__ uint32_t gelu_abs_bits(uint32_t w) { return abs_bits_lo(bf16x2_absmax(gelu_pair(w), 0u)); }
+
+// Every negative input (and -0, -inf) gives |y| below 0.1875 (bf16 0x3E40):
+// the tanh-form GELU is smallest near x = -0.75, where it is about -0.170.
+constexpr uint32_t kGeluNegativeBound = 0x3E400000u;
+
+// Codes alone through a table of the FP8 code of every input (64 KB).
+//
+// amax = max|y| over the tensor without any y: the computed y is
+// non-decreasing in h from +0 to +inf (and not below 0 there), and every
+// negative input gives |y| below 0.1875 -- both hold for every bf16 input,
+// and the tests check them.  So when the largest input hm a thread has seen
+// is a NaN, or is at least +0 with |y(hm)| at least 0.1875, the largest |y|
+// of its elements is |y(hm)|, computed once with gelu_pair.  A thread for
+// which that fails (all of its inputs below about 0.3, or none) reads its
+// elements again and takes the largest |y| of gelu_pair on each.
+template <int FMT>
+__global__ void __launch_bounds__(kGeluCodeTableThreads, 1) gelu_code_table_kernel(const GeluArgs a) {
+    extern __shared__ __align__(16) uint32_t tab32[];  // byte h: the FP8 code of y(h) / scale
+    __shared__ uint32_t red[kGeluCodeTableThreads / 32];
+    constexpr int E = GeluGeom::kVecElems;
+    const int64_t stride = (int64_t)gridDim.x * kGeluCodeTableThreads;
+    const int64_t v_first = (int64_t)blockIdx.x * kGeluCodeTableThreads + threadIdx.x;
+    uint4 wa[kGeluTableUnroll], wb[kGeluTableUnroll];
+    gelu_load2(a, v_first, stride, wa, wb);  // before the build, which hides their latency
+    const QScale c = make_qscale(a.scale);
+    // word p: the codes of inputs 4p .. 4p + 3, lowest byte first
+    if (c.fast)
+        cluster_build<kGeluCodeTableThreads, kGeluCodeTableCluster, 16384>(tab32, [&c](int p) {
+            const uint32_t h = 4u * (uint32_t)p;
+            return quant_quad_x2<FMT, true>(gelu_pair(h | ((h + 1u) << 16)), gelu_pair((h + 2u) | ((h + 3u) << 16)), c);
+        });
+    else
+        cluster_build<kGeluCodeTableThreads, kGeluCodeTableCluster, 16384>(tab32, [&c](int p) {
+            const uint32_t h = 4u * (uint32_t)p;
+            return quant_quad_x2<FMT, false>(gelu_pair(h | ((h + 1u) << 16)), gelu_pair((h + 2u) | ((h + 3u) << 16)), c);
+        });
+    cluster_sync_all();  // every CTA's table is complete; no remote store comes after this
+    const uint8_t* tab = reinterpret_cast<const uint8_t*>(tab32);
+    uint32_t hm2 = 0xFF80FF80u;  // the largest input so far, per bf16 lane (-inf: none)
+    if (c.fast) code_table_stream<FMT, true>(a, tab, c, v_first, stride, wa, wb, hm2);
+    else        code_table_stream<FMT, false>(a, tab, c, v_first, stride, wa, wb, hm2);
+    const int64_t tail0 = a.head + a.nvec * E;
+    const int64_t nscalar = blockIdx.x == 0 ? a.head + (a.n - tail0) : 0;  // head and tail: CTA 0
+    for (int64_t j = threadIdx.x; j < nscalar; j += kGeluCodeTableThreads) {
+        const int64_t i = j < a.head ? j : tail0 + (j - a.head);
+        const uint32_t hv = a.h[i];
+        a.q[i] = tab[hv];
+        hm2 = bf16x2_max(hm2, hv | (hv << 16));
+    }
+    const uint32_t hm = bf16x2_max(hm2, hm2 >> 16) & 0xFFFFu;
+    uint32_t m = gelu_abs_bits(hm);
+    if ((hm & 0x8000u) || m < kGeluNegativeBound) {  // read the thread's elements again
+        uint32_t m2 = 0;
+        for (int64_t v = v_first; v < a.nvec; v += stride) {
+            uint4 x, z;
+            ld_stream_v8(a.h + a.head + v * E, x, z);
+            m2 = bf16x2_absmax(m2, bf16x2_absmax(
+                                       bf16x2_absmax(bf16x2_absmax(gelu_pair(x.x), gelu_pair(x.y)),
+                                                     bf16x2_absmax(gelu_pair(x.z), gelu_pair(x.w))),
+                                       bf16x2_absmax(bf16x2_absmax(gelu_pair(z.x), gelu_pair(z.y)),
+                                                     bf16x2_absmax(gelu_pair(z.z), gelu_pair(z.w)))));
+        }
+        m = max(abs_bits_lo(m2), m2 & 0x7FFF0000u);
+        for (int64_t j = threadIdx.x; j < nscalar; j += kGeluCodeTableThreads)
+            m = max(m, gelu_abs_bits(a.h[j < a.head ? j : tail0 + (j - a.head)]));
+    }
+    // CTA-wide max of |y|, one atomic
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t b = red[0];
+        for (int w = 1; w < kGeluCodeTableThreads / 32; ++w) b = max(b, red[w]);
         atomicMax(reinterpret_cast<int*>(a.amax), (int)b);
     }
 }
@@ -471,27 +644,6 @@ __device__ __forceinline__ uint32_t ln_pair(uint32_t w, float nmean, float2 rstd
     return cvt_bf16x2(y.x, y.y);
 }
 
-// quant_pair's fast path, two lanes at a time: y0 = RN(x r), e = fma(y0, s, -x),
-// y = fma(-e, r, y0) is the correctly rounded quotient in each lane.
-template <int FMT>
-__device__ __forceinline__ uint32_t quant_pair_x2(uint32_t w, const QScale& c) {
-    w = bf16x2_clamp(w, c.t2);
-    const float2 x = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
-    const float2 y0 = mul2_rn(x, splat2(c.r));
-    const float2 e = fma2_rn(y0, splat2(c.s), make_float2(-x.x, -x.y));
-    const float2 y = fma2_rn(make_float2(-e.x, -e.y), splat2(c.r), y0);
-    return cvt_fp8x2<FMT>(y.x, y.y);
-}
-
-// Eight bf16 of y -> eight FP8 codes.
-template <int FMT, bool FAST>
-__device__ __forceinline__ uint2 ln_quant8(const uint4& y, const QScale& c) {
-    if (FAST)
-        return make_uint2(quant_pair_x2<FMT>(y.x, c) | (quant_pair_x2<FMT>(y.y, c) << 16),
-                          quant_pair_x2<FMT>(y.z, c) | (quant_pair_x2<FMT>(y.w, c) << 16));
-    return make_uint2(quant_quad<FMT, false>(y.x, y.y, c), quant_quad<FMT, false>(y.z, y.w, c));
-}
-
 __device__ __forceinline__ float max_nan_f32(float a, float b) {
     float d;
     asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
@@ -510,7 +662,7 @@ __device__ __forceinline__ void ln_out8(const LnArgs& a, uint4 w, const float2 (
     yv.w = ln_pair(w.w, stats.x, rstd2, g[3], b[3]);
     if (WRITE_Y) st_cs_v4(a.y + off, yv);
     m2 = bf16x2_absmax(m2, bf16x2_absmax(bf16x2_absmax(yv.x, yv.y), bf16x2_absmax(yv.z, yv.w)));
-    st_cs_v2(a.q + off, ln_quant8<FMT, FAST>(yv, c));
+    st_cs_v2(a.q + off, quant8<FMT, FAST>(yv, c));
 }
 
 __device__ __forceinline__ void load4f2(const float* p, float2 (&d)[4]) {
@@ -739,20 +891,19 @@ fp8q_status launch_layernorm(const LnArgs& a, cudaStream_t s) {
     return launch_layernorm_hpt<FMT, WRITE_Y, 8>(a, s);
 }
 
-template <int FMT, bool WRITE_Y>
-fp8q_status launch_gelu_table(const GeluArgs& a, cudaStream_t s) {
-    static ResidentCache cache;
-    constexpr int kGeluTableThreads = gelu_table_threads<WRITE_Y>();
-    constexpr int kGeluTableCluster = gelu_table_cluster<WRITE_Y>();
-    auto kern = gelu_table_quantize_amax_kernel<FMT, WRITE_Y>;
+// Launch a table kernel on the clusters that fit at once (at most one CTA per
+// vector pair of its threads, rounded up to whole clusters).
+template <typename Kern>
+fp8q_status launch_gelu_table(Kern kern, int threads, int cluster, uint32_t smem, ResidentCache& cache,
+                              const GeluArgs& a, cudaStream_t s, const char* name) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kGeluTableCluster;
+    attr[0].val.clusterDim.x = (unsigned)cluster;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(kGeluTableThreads);
-    cfg.dynamicSmemBytes = kGeluTableBytes;
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
@@ -765,26 +916,40 @@ fp8q_status launch_gelu_table(const GeluArgs& a, cudaStream_t s) {
             if (cache.e[k].dev == dev) ctas = cache.e[k].ctas;
         if (ctas == 0) {
             // resident CTAs: the clusters that fit at once, times their size
-            err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGeluTableBytes);
+            err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             int clusters = 0, sms = 0;
             if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-            cfg.gridDim = dim3((unsigned)(sms / kGeluTableCluster * kGeluTableCluster));
+            cfg.gridDim = dim3((unsigned)(sms / cluster * cluster));
             if (err == cudaSuccess) err = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
             if (err == cudaSuccess && clusters < 1) err = cudaErrorInvalidConfiguration;
             if (err == cudaSuccess) {
-                ctas = clusters * kGeluTableCluster;
+                ctas = clusters * cluster;
                 if (cache.n < 32) cache.e[cache.n++] = {dev, ctas};
             }
         }
     }
-    if (err != cudaSuccess) return cuda_fail(err, "gelu_table_quantize_amax_kernel setup");
-    const int64_t per_cta = (int64_t)kGeluTableThreads * kGeluTableUnroll;
+    if (err != cudaSuccess) return cuda_fail(err, name);
+    const int64_t per_cta = (int64_t)threads * kGeluTableUnroll;
     const int64_t need = (a.nvec + per_cta - 1) / per_cta;
     int grid = (int)(need < ctas ? (need > 0 ? need : 1) : ctas);
-    grid = (grid + kGeluTableCluster - 1) / kGeluTableCluster * kGeluTableCluster;  // whole clusters
+    grid = (grid + cluster - 1) / cluster * cluster;  // whole clusters
     cfg.gridDim = dim3((unsigned)grid);
     err = cudaLaunchKernelEx(&cfg, kern, a);
-    return err == cudaSuccess ? FP8Q_OK : cuda_fail(err, "gelu_table_quantize_amax_kernel launch");
+    return err == cudaSuccess ? FP8Q_OK : cuda_fail(err, name);
+}
+
+template <int FMT>
+fp8q_status launch_gelu_y_table(const GeluArgs& a, cudaStream_t s) {
+    static ResidentCache cache;
+    return launch_gelu_table(gelu_table_quantize_amax_kernel<FMT>, kGeluYTableThreads, kGeluYTableCluster,
+                             kGeluYTableBytes, cache, a, s, "gelu_table_quantize_amax_kernel");
+}
+
+template <int FMT>
+fp8q_status launch_gelu_code_table(const GeluArgs& a, cudaStream_t s) {
+    static ResidentCache cache;
+    return launch_gelu_table(gelu_code_table_kernel<FMT>, kGeluCodeTableThreads, kGeluCodeTableCluster,
+                             kGeluCodeTableBytes, cache, a, s, "gelu_code_table_kernel");
 }
 
 }  // namespace
@@ -824,8 +989,8 @@ fp8q_status fp8q_gelu_quantize_amax(const void* h_bf16, void* y_bf16, uint8_t* q
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (sp.mode == kModeVec && n >= (y_bf16 ? kGeluTableMinElemsWithY : kGeluTableMinElems)) {
         if (fmt == FP8Q_E4M3FN)
-            return y_bf16 ? launch_gelu_table<FP8Q_E4M3FN, true>(a, s) : launch_gelu_table<FP8Q_E4M3FN, false>(a, s);
-        return y_bf16 ? launch_gelu_table<FP8Q_E5M2, true>(a, s) : launch_gelu_table<FP8Q_E5M2, false>(a, s);
+            return y_bf16 ? launch_gelu_y_table<FP8Q_E4M3FN>(a, s) : launch_gelu_code_table<FP8Q_E4M3FN>(a, s);
+        return y_bf16 ? launch_gelu_y_table<FP8Q_E5M2>(a, s) : launch_gelu_code_table<FP8Q_E5M2>(a, s);
     }
     auto kern = fmt == FP8Q_E4M3FN ? (y_bf16 ? gelu_quantize_amax_kernel<FP8Q_E4M3FN, true>
                                              : gelu_quantize_amax_kernel<FP8Q_E4M3FN, false>)

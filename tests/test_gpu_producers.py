@@ -11,6 +11,7 @@ GELU also has a determinism check: both GELU kernels give the bits of the
 fixed binary32 sequence they are built on (tests/csrc/gelu_sequence.c).
 """
 import math
+import zlib
 
 import numpy as np
 import pytest
@@ -158,13 +159,14 @@ def test_gelu_table_path_every_bf16_pattern(dev, seq_gelu):
     want_y = seq_gelu(pb)
     assert_gelu_y(pb, want_y, "the fixed sequence")
     wy = torch.from_numpy(want_y.view(np.int16).copy()).view(torch.bfloat16).to(dev)
-    for k, (fmt, s) in enumerate([(E4M3FN, 1.0), (E5M2, 0.37), (E4M3FN, 2.0 ** 70), (E5M2, 3.0e-5),
-                                  (E4M3FN, 0.0), (E4M3FN, math.nan)]):
-        with_y = k % 2 == 0
+    for fmt, s, with_y in [(E4M3FN, 1.0, True), (E5M2, 0.37, False), (E4M3FN, 2.0 ** 70, True),
+                           (E5M2, 3.0e-5, False), (E4M3FN, 0.0, True), (E4M3FN, math.nan, False),
+                           (E4M3FN, 2.0 ** 70, False), (E5M2, 0.0, False)]:
         reps = 1024 if with_y else 256                    # 2^26 or 2^24 elements
         h = pat.repeat(reps)
         y, q, am = run_gelu(h, fmt, s, dev, want_y=with_y)
-        rq, _ = oracle.quantize_amax(want_y, fmt, np.float32(s))
+        rq, ra = oracle.quantize_amax(want_y, fmt, np.float32(s))
+        assert_f32_equal([float(am)], [ra], f"table amax, scale {s!r}")
         wq = torch.from_numpy(rq).to(dev)
         # every element against its pattern's expected value, compared on the device
         assert torch.equal(q.view(reps, 65536), wq.expand(reps, 65536)) or \
@@ -210,6 +212,53 @@ def test_gelu_table_path_unaligned_head_and_tail(dev):
     assert_f32_equal([float(am)], [ra], "table path amax")
     check_guards(qbuf, n, off)
     check_guards(ybuf, n, off, fill=0x5A5A)
+
+
+def _patterns(lo, hi):
+    """bf16 patterns lo..hi (inclusive) as a host array."""
+    return np.arange(lo, hi + 1, dtype=np.uint32).astype(np.uint16)
+
+
+def _to_dev(bits, dev):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+@pytest.mark.parametrize("case", ["negative", "small positive", "half N(0,1) half negative", "one NaN",
+                                  "one +inf", "seeded amax"])
+def test_gelu_code_table_amax(dev, seq_gelu, case):
+    """Codes alone on the table path (2^24 elements and more): the amax comes from each
+    thread's largest input, and a thread whose largest input is below about 0.3 (or
+    negative) reads its elements again.  Tensors where every thread, no thread or some
+    threads do; every code and the amax against the oracle's quantize of y."""
+    n = (1 << 24) + 5
+    rng = np.random.default_rng(zlib.crc32(case.encode()))
+    normal = np.asarray(torch.from_numpy(rng.standard_normal(n).astype(np.float32)).to(torch.bfloat16)
+                        .view(torch.int16).numpy()).view(np.uint16)
+    neg = _patterns(0x8000, 0xFF80)                          # -0 ... -inf
+    amax0 = 0.0
+    if case == "negative":
+        hb = neg[rng.integers(0, neg.size, n)]
+    elif case == "small positive":
+        hb = _patterns(0x0000, 0x3E7F)[rng.integers(0, 0x3E80, n)]   # +0 ... just under 0.25
+    elif case == "half N(0,1) half negative":
+        hb = normal.copy()
+        hb[n // 2:] = neg[rng.integers(0, neg.size, n - n // 2)]
+    elif case == "one NaN":
+        hb = normal.copy()
+        hb[n // 3] = 0x7FC1
+    elif case == "one +inf":
+        hb = normal.copy()
+        hb[n - 2] = 0x7F80                                   # in the scalar tail
+    else:
+        hb = neg[rng.integers(0, neg.size, n)]
+        amax0 = 0.5                                          # above every |y|: the seed stays
+    h = _to_dev(hb, dev)
+    for fmt, scale in ((E4M3FN, np.float32(0.0123)), (E5M2, np.float32(2.0 ** 70))):
+        _, q, am = run_gelu(h, fmt, scale, dev, want_y=False, amax0=amax0)
+        want_y = seq_gelu(hb)
+        rq, ra = par_quantize_amax(want_y, fmt, scale, amax0)
+        assert_codes_equal(q.cpu().numpy(), rq, fmt, f"{case} codes")
+        assert_f32_equal([float(am)], [ra], f"{case} amax")
 
 
 def test_gelu_table_path_more_than_2_pow_31_elements(dev, seq_gelu):
