@@ -244,7 +244,10 @@ constexpr int64_t kGeluTableMinElemsWithY = FP8Q_TEST_GELU_TABLE_MIN_ELEMS;
 constexpr int64_t kGeluTableMinElems = (int64_t)1 << 24;
 constexpr int64_t kGeluTableMinElemsWithY = (int64_t)1 << 26;
 #endif
+// Vectors in flight per thread, two beyond the two being converted (with y,
+// three or four measured 125-127 us on 8192x16384, against 113).
 constexpr int kGeluTableUnroll = 2;
+constexpr int kGeluYUnroll = 2;
 // CTAs of one thread-block cluster (on as many SMs) build their tables
 // together: each computes its share of the entries and stores each into the
 // shared memory of every CTA of the cluster.  Measured on GB300 (8192x16384):
@@ -314,11 +317,12 @@ __device__ __forceinline__ void cluster_build(uint32_t* tab32, Entry entry) {
     }
 }
 
-// The next vectors of 16 bf16 of a thread that visits v, v + stride, ...
-__device__ __forceinline__ void gelu_load2(const GeluArgs& a, int64_t v, int64_t stride, uint4 (&wa)[2],
-                                           uint4 (&wb)[2]) {
+// The next U vectors of 16 bf16 of a thread that visits v, v + stride, ...
+template <int U>
+__device__ __forceinline__ void gelu_load(const GeluArgs& a, int64_t v, int64_t stride, uint4 (&wa)[U],
+                                          uint4 (&wb)[U]) {
 #pragma unroll
-    for (int u = 0; u < kGeluTableUnroll; ++u) {
+    for (int u = 0; u < U; ++u) {
         const int64_t vu = v + u * stride;
         if (vu < a.nvec) ld_stream_v8(a.h + a.head + vu * GeluGeom::kVecElems, wa[u], wb[u]);
     }
@@ -341,18 +345,18 @@ __global__ void __launch_bounds__(kGeluYTableThreads, 1) gelu_table_quantize_ama
     const int64_t stride = (int64_t)gridDim.x * kGeluYTableThreads;
     uint32_t m2 = 0, ms = 0;
     int64_t v0 = (int64_t)blockIdx.x * kGeluYTableThreads + threadIdx.x;
-    uint4 wa[kGeluTableUnroll], wb[kGeluTableUnroll];
-    gelu_load2(a, v0, stride, wa, wb);  // before the build, which hides their latency
+    uint4 wa[kGeluYUnroll], wb[kGeluYUnroll];
+    gelu_load(a, v0, stride, wa, wb);  // before the build, which hides their latency
     cluster_build<kGeluYTableThreads, kGeluYTableCluster, 32768>(
         tab32, [](int p) { return gelu_pair((uint32_t)(2 * p) | ((uint32_t)(2 * p + 1) << 16)); });
     const QScale c = make_qscale(a.scale);
     cluster_sync_all();  // every CTA's table is complete; no remote store comes after this
     const uint16_t* tab = reinterpret_cast<const uint16_t*>(tab32);
-    for (; v0 < a.nvec; v0 += kGeluTableUnroll * stride) {
-        uint4 na[kGeluTableUnroll], nb[kGeluTableUnroll];
-        gelu_load2(a, v0 + kGeluTableUnroll * stride, stride, na, nb);
+    for (; v0 < a.nvec; v0 += kGeluYUnroll * stride) {
+        uint4 na[kGeluYUnroll], nb[kGeluYUnroll];
+        gelu_load(a, v0 + kGeluYUnroll * stride, stride, na, nb);
 #pragma unroll
-        for (int u = 0; u < kGeluTableUnroll; ++u) {
+        for (int u = 0; u < kGeluYUnroll; ++u) {
             const int64_t v = v0 + u * stride;
             if (v < a.nvec) {
                 const uint4 ya = gelu_lookup4(tab, wa[u]), yb = gelu_lookup4(tab, wb[u]);
@@ -361,7 +365,7 @@ __global__ void __launch_bounds__(kGeluYTableThreads, 1) gelu_table_quantize_ama
             }
         }
 #pragma unroll
-        for (int u = 0; u < kGeluTableUnroll; ++u) {
+        for (int u = 0; u < kGeluYUnroll; ++u) {
             wa[u] = na[u];
             wb[u] = nb[u];
         }
@@ -423,7 +427,7 @@ __device__ __forceinline__ void code_table_stream(const GeluArgs& a, const uint8
     constexpr int E = GeluGeom::kVecElems;
     for (int64_t v0 = v_first; v0 < a.nvec; v0 += kGeluTableUnroll * stride) {
         uint4 na[kGeluTableUnroll], nb[kGeluTableUnroll];
-        gelu_load2(a, v0 + kGeluTableUnroll * stride, stride, na, nb);
+        gelu_load(a, v0 + kGeluTableUnroll * stride, stride, na, nb);
 #pragma unroll
         for (int u = 0; u < kGeluTableUnroll; ++u) {
             const int64_t v = v0 + u * stride;
@@ -470,7 +474,7 @@ __global__ void __launch_bounds__(kGeluCodeTableThreads, 1) gelu_code_table_kern
     const int64_t stride = (int64_t)gridDim.x * kGeluCodeTableThreads;
     const int64_t v_first = (int64_t)blockIdx.x * kGeluCodeTableThreads + threadIdx.x;
     uint4 wa[kGeluTableUnroll], wb[kGeluTableUnroll];
-    gelu_load2(a, v_first, stride, wa, wb);  // before the build, which hides their latency
+    gelu_load(a, v_first, stride, wa, wb);  // before the build, which hides their latency
     const QScale c = make_qscale(a.scale);
     // word p: the codes of inputs 4p .. 4p + 3, lowest byte first
     if (c.fast)
@@ -894,7 +898,7 @@ fp8q_status launch_layernorm(const LnArgs& a, cudaStream_t s) {
 // Launch a table kernel on the clusters that fit at once (at most one CTA per
 // vector pair of its threads, rounded up to whole clusters).
 template <typename Kern>
-fp8q_status launch_gelu_table(Kern kern, int threads, int cluster, uint32_t smem, ResidentCache& cache,
+fp8q_status launch_gelu_table(Kern kern, int threads, int unroll, int cluster, uint32_t smem, ResidentCache& cache,
                               const GeluArgs& a, cudaStream_t s, const char* name) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -929,7 +933,7 @@ fp8q_status launch_gelu_table(Kern kern, int threads, int cluster, uint32_t smem
         }
     }
     if (err != cudaSuccess) return cuda_fail(err, name);
-    const int64_t per_cta = (int64_t)threads * kGeluTableUnroll;
+    const int64_t per_cta = (int64_t)threads * unroll;
     const int64_t need = (a.nvec + per_cta - 1) / per_cta;
     int grid = (int)(need < ctas ? (need > 0 ? need : 1) : ctas);
     grid = (grid + cluster - 1) / cluster * cluster;  // whole clusters
@@ -941,14 +945,14 @@ fp8q_status launch_gelu_table(Kern kern, int threads, int cluster, uint32_t smem
 template <int FMT>
 fp8q_status launch_gelu_y_table(const GeluArgs& a, cudaStream_t s) {
     static ResidentCache cache;
-    return launch_gelu_table(gelu_table_quantize_amax_kernel<FMT>, kGeluYTableThreads, kGeluYTableCluster,
+    return launch_gelu_table(gelu_table_quantize_amax_kernel<FMT>, kGeluYTableThreads, kGeluYUnroll, kGeluYTableCluster,
                              kGeluYTableBytes, cache, a, s, "gelu_table_quantize_amax_kernel");
 }
 
 template <int FMT>
 fp8q_status launch_gelu_code_table(const GeluArgs& a, cudaStream_t s) {
     static ResidentCache cache;
-    return launch_gelu_table(gelu_code_table_kernel<FMT>, kGeluCodeTableThreads, kGeluCodeTableCluster,
+    return launch_gelu_table(gelu_code_table_kernel<FMT>, kGeluCodeTableThreads, kGeluTableUnroll, kGeluCodeTableCluster,
                              kGeluCodeTableBytes, cache, a, s, "gelu_code_table_kernel");
 }
 
