@@ -291,6 +291,14 @@ def test_gelu_table_path_more_than_2_pow_31_elements(dev, seq_gelu):
     assert torch.equal(y.view(torch.int16)[full * m:], wy[: n - full * m]), "y, last partial period"
     assert torch.equal(q[:full * m].view(full, m), wq.expand(full, m)), "q, whole periods"
     assert torch.equal(q[full * m:], wq[: n - full * m]), "q, last partial period"
+    # the codes alone (the code table kernel) on the same input
+    q.fill_(0)
+    am2 = f32(0.0, dev)
+    fp8q.fp8q_gelu_quantize_amax(h, None, q, E4M3FN, f32(scale, dev), am2)
+    torch.cuda.synchronize()
+    assert_f32_equal([float(am2)], [ra], "amax over 2^31 + 19 elements, codes alone")
+    assert torch.equal(q[:full * m].view(full, m), wq.expand(full, m)), "q alone, whole periods"
+    assert torch.equal(q[full * m:], wq[: n - full * m]), "q alone, last partial period"
     del h, y, q
     torch.cuda.empty_cache()
 
@@ -423,6 +431,39 @@ def test_layernorm_full_size(dev):
     x = W.residual_stream(device=dev)
     gamma, beta = W.layernorm_params(x.shape[1], device=dev)
     check_layernorm(x, gamma, beta, E4M3FN, np.float32(0.031), dev, what="8192x4096")
+
+
+def test_layernorm_more_than_2_pow_31_elements(dev):
+    """Row offsets stay 64-bit: 131073 rows of 16384 (2^31 + 16384 elements).  The rows
+    around the 2^31 boundary, the first and the last are compared with the oracle (y within
+    the tolerance, codes exact against the quantize of y); the amax equals max|y| over the
+    whole output, and the codes-alone call gives the same codes and amax."""
+    rows, H = 131073, 16384
+    g = torch.Generator(device=dev)
+    g.manual_seed(23)
+    x = torch.empty((rows, H), dtype=torch.bfloat16, device=dev)
+    for r0 in range(0, rows, 8192):                  # N(mu_r, sigma_r^2) rows, in slices
+        r1 = min(rows, r0 + 8192)
+        mu = torch.randn((r1 - r0, 1), generator=g, device=dev)
+        sd = torch.rand((r1 - r0, 1), generator=g, device=dev) * 2 + 0.1
+        x[r0:r1] = (torch.randn((r1 - r0, H), generator=g, device=dev) * sd + mu).to(torch.bfloat16)
+    gamma = (1 + 0.1 * torch.randn(H, generator=g, device=dev)).float()
+    beta = (0.1 * torch.randn(H, generator=g, device=dev)).float()
+    scale = np.float32(0.027)
+    y, q, am = run_layernorm(x, gamma, beta, E4M3FN, scale, dev, True)
+    _, q2, am2 = run_layernorm(x, gamma, beta, E4M3FN, scale, dev, False)
+    assert torch.equal(q, q2), "codes with and without y"
+    yi = y.view(torch.int16)
+    amax_y = (yi.view(-1) & 0x7FFF).max().item()          # |y| bits (no NaN here)
+    assert_f32_equal([float(am), float(am2)], [np.uint32(amax_y << 16).view(np.float32)] * 2, "amax = max|y|")
+    picks = [0, 1, 2, 131070, 131071, 131072]          # row 131072 starts at element 2^31
+    xb = W.bf16_bits(x[picks])
+    yb = W.bf16_bits(y[picks])
+    assert_layernorm_y(xb, H, gamma.cpu().numpy(), beta.cpu().numpy(), 1e-6, yb, "rows around 2^31")
+    rq, _ = oracle.quantize_amax(yb.reshape(-1), E4M3FN, scale)
+    assert_codes_equal(q[picks].cpu().numpy().reshape(-1), rq, E4M3FN, "codes of rows around 2^31")
+    del x, y, q, q2
+    torch.cuda.empty_cache()
 
 
 def test_layernorm_close_to_torch_layer_norm(dev):
