@@ -571,7 +571,8 @@ __global__ void __launch_bounds__(kGeluCodeTableThreads, 1) gelu_code_table_kern
 // report failure, to exercise the path without any fault.
 
 constexpr int kLnMaxH = 16384;
-constexpr int kLnMaxHalfPerThread = 8;  // H <= 256 * 8 * 8
+constexpr int kLnMaxHalfPerThread = 8;  // the largest HPT instantiated
+static_assert(kLnMaxH <= kThreads * 8 * kLnMaxHalfPerThread, "every half-vector of a row has a thread");
 constexpr int kLnWarps = kThreads / 32;
 constexpr int kLnMaxBatch = kLnWarps;
 constexpr int kLnBufs = 2;                      // batches in the ring
