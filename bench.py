@@ -1196,7 +1196,7 @@ def run_reference(args):
 
 
 CASES = ("quantize_8192x16384", "quantize_8192x4096", "dequantize_8192x16384", "update_576x1024",
-         "gelu_8192x16384", "layernorm_8192x4096", "qdq_8192x16384")
+         "gelu_8192x16384", "gelu_y_8192x16384", "layernorm_8192x4096", "qdq_8192x16384")
 
 
 def run_case(name: str, launches: int):
@@ -1231,12 +1231,13 @@ def run_case(name: str, launches: int):
     elif name == "update_576x1024":
         hist, new, scale, scale_inv, sf = W.scale_update_inputs(dev)
         launch = lambda: f.fp8q_amax_scale_update(hist, new, scale, scale_inv, f.E4M3FN, f.ALGO_MAX, 0, sf)
-    elif name == "gelu_8192x16384":
+    elif name in ("gelu_8192x16384", "gelu_y_8192x16384"):
         g = torch.Generator(device=dev)
         g.manual_seed(7)
         h = torch.randn(N_ACT, generator=g, device=dev).to(torch.bfloat16)
         q = torch.empty(N_ACT, dtype=torch.uint8, device=dev)
-        launch = lambda: f.fp8q_gelu_quantize_amax(h, None, q, f.E4M3FN, sc, am)
+        y = torch.empty(N_ACT, dtype=torch.bfloat16, device=dev) if name == "gelu_y_8192x16384" else None
+        launch = lambda: f.fp8q_gelu_quantize_amax(h, y, q, f.E4M3FN, sc, am)
     elif name == "layernorm_8192x4096":
         x = W.residual_stream(device=dev)
         gam, bet = W.layernorm_params(x.shape[1], device=dev)
