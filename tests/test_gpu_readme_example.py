@@ -1,4 +1,4 @@
-"""The Python example in README.md runs as written (a delayed-scaling step)."""
+"""The Python example in the top-level readme runs as written (a delayed-scaling step)."""
 import os
 import re
 
@@ -11,9 +11,9 @@ from conftest import ROOT
 def test_readme_example_runs():
     text = open(os.path.join(ROOT, "README.md")).read()
     blocks = re.findall(r"```python\n(.*?)```", text, re.S)
-    assert blocks, "no python example in README.md"
+    assert blocks, "no python example in the readme"
     ns = {}
-    exec(compile(blocks[0], "README.md example", "exec"), ns)
+    exec(compile(blocks[0], "readme example", "exec"), ns)
     import torch
     torch.cuda.synchronize()
     # the update moved each slot's amax into the history and set scale = amax / 448
