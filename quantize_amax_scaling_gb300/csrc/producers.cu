@@ -235,14 +235,15 @@ constexpr int kGeluYTableThreads = 512;
 constexpr int kGeluCodeTableThreads = 1024;
 constexpr uint32_t kGeluYTableBytes = 65536u * 2u;
 constexpr uint32_t kGeluCodeTableBytes = 65536u;
-// Fewer elements take the direct kernel (measured crossovers on GB300: the
-// table wins from about 2^24 elements for the codes alone, 2^26 with y).
+// Fewer elements take the direct kernel.  Measured on GB300 from a cold L2
+// (direct / table, us): codes alone 16.8 / 16.8 at 2^23 elements, 25.2 / 21.3
+// at 2^24; with y 25.3 / 27.4 at 2^24, 41.4 / 39.4 at 2^25.
 #ifdef FP8Q_TEST_GELU_TABLE_MIN_ELEMS  // test-only build: small tensors take the table path too
 constexpr int64_t kGeluTableMinElems = FP8Q_TEST_GELU_TABLE_MIN_ELEMS;
 constexpr int64_t kGeluTableMinElemsWithY = FP8Q_TEST_GELU_TABLE_MIN_ELEMS;
 #else
-constexpr int64_t kGeluTableMinElems = (int64_t)1 << 24;
-constexpr int64_t kGeluTableMinElemsWithY = (int64_t)1 << 26;
+constexpr int64_t kGeluTableMinElems = (int64_t)1 << 23;
+constexpr int64_t kGeluTableMinElemsWithY = (int64_t)1 << 25;
 #endif
 // Vectors in flight per thread, two beyond the two being converted (with y,
 // three or four measured 125-127 us on 8192x16384, against 113).
