@@ -765,6 +765,60 @@ def test_layernorm_tolerance_holds_a_binary32_evaluation(orc, H):
     assert np.mean(lo[benign] == hi[benign]) > 0.9
 
 
+def _f32_chain_sum(a, L):
+    """Row sums in binary32: chains of L elements added left to right, then a pairwise
+    tree over the chains (longest chain L + ceil(log2(H / L)))."""
+    a = a.astype(np.float32)
+    rows, H = a.shape
+    nc = H // L
+    s = np.zeros((rows, nc), np.float32)
+    leaves = a.reshape(rows, nc, L)
+    for k in range(L):
+        s = (s + leaves[:, :, k]).astype(np.float32)
+    while s.shape[1] > 1:
+        if s.shape[1] % 2:
+            s = np.concatenate([s, np.zeros((rows, 1), np.float32)], axis=1)
+        s = (s[:, 0::2] + s[:, 1::2]).astype(np.float32)
+    return s[:, 0]
+
+
+@pytest.mark.parametrize("H", [1024, 4096, 16384])
+def test_layernorm_tolerance_holds_the_longest_allowed_chains(orc, H):
+    """The tolerance covers any binary32 evaluation whose sums have chains of additions up
+    to D = H/128 + 32 long: here chains as long as that allows, left to right, and the
+    normalisation fused (one rounding for (x - mean) * (rstd * gamma) + beta), on rows with
+    outliers, large means and small spreads."""
+    D = H // 128 + 32
+    L = 1
+    while 2 * L + int(np.ceil(np.log2(H / (2 * L)))) <= D and 2 * L <= H:
+        L *= 2
+    assert L + int(np.ceil(np.log2(H / L))) <= D
+    rng = np.random.default_rng(97 + H)
+    rows = 12
+    mu = np.array([0.0, 2.0, -2.0, 30.0, 0.5, -40.0, 1.0, 3.0, 0.0, 100.0, -0.01, 7.0])[:, None]
+    sd = np.array([1.0, 0.5, 0.5, 0.3, 4.0, 1.0, 1e-3, 2.0, 50.0, 1.0, 0.1, 1e-2])[:, None]
+    xv = rng.normal(0, 1, (rows, H)) * sd + mu
+    out = rng.random((rows, H)) < 1e-3
+    xv[out] *= 100.0
+    x = torch.from_numpy(xv.astype(np.float32)).to(torch.bfloat16)
+    g = (1 + 0.1 * rng.normal(0, 1, H)).astype(np.float32)
+    b = (0.1 * rng.normal(0, 1, H)).astype(np.float32)
+    xf = x.float().numpy().astype(np.float32)
+    S = _f32_chain_sum(xf, L)
+    Q = _f32_chain_sum((xf * xf).astype(np.float32), L)
+    mean = (S / np.float32(H)).astype(np.float32)
+    var = np.maximum((Q / np.float32(H)).astype(np.float32) - (mean * mean).astype(np.float32), np.float32(0))
+    rstd = (np.float32(1) / np.sqrt((var + np.float32(1e-6)).astype(np.float32))).astype(np.float32)
+    d = (xf - mean[:, None]).astype(np.float32)
+    m = (rstd[:, None] * g[None, :]).astype(np.float32)
+    yf = (d.astype(np.float64) * m.astype(np.float64) + b[None, :].astype(np.float64)).astype(np.float32)
+    y32 = torch.from_numpy(yf).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).reshape(-1)
+    r, mean64, rstd64 = orc.layernorm_ref(_u16(x), H, g, b, 1e-6)
+    E = orc.layernorm_tolerance(x.double().numpy(), g, b, 1e-6, mean64, rstd64, r)
+    ok = orc.bf16_within(y32, r, E.reshape(-1))
+    assert ok.all(), f"{(~ok).sum()} elements outside, rows {np.unique(np.nonzero(~ok)[0] // H)}"
+
+
 def test_gelu_tolerance_at_infinity_is_exact(orc):
     r = orc.gelu_ref_array(np.array([0x7F80, 0xFF80], np.uint16))
     E = orc.gelu_tolerance(np.array([math.inf, -math.inf]), r)
