@@ -55,3 +55,50 @@ def test_gelu_table_path_rounded_grid(hooks_lib, seq_gelu, n, off, with_y):
     if with_y:
         assert_bf16_equal(W.bf16_bits(y), want_y, f"table y n={n}")
         check_guards(ybuf, n, off, fill=0x5A5A)
+
+
+RANDOM_CASES = 16
+
+
+@pytest.mark.parametrize("k", range(RANDOM_CASES))
+def test_gelu_table_path_random_small_tensors(hooks_lib, seq_gelu, k):
+    """Seeded random sizes, offsets, formats, scales (the slow-path ones too) and input
+    kinds through the table kernels of the test-hooks build: many threads have few or no
+    elements, so the codes-alone kernel's amax often comes from its re-read."""
+    rng = np.random.default_rng(1000 + k)
+    dev = torch.device("cuda:0")
+    n = int(rng.integers(1, 200_000))
+    off = int(rng.integers(0, 16))
+    with_y = bool(k % 2)
+    fmt = fp8q.E4M3FN if k % 4 < 2 else fp8q.E5M2
+    scale = np.float32([0.0123, 1.0, 3.7e-3, 2.0 ** 70, 0.0, 2.5e-2][k % 6])
+    kind = k % 4
+    v = rng.standard_normal(n + 16) * 3.0
+    if kind == 1:
+        v = -np.abs(v)                     # every input negative
+    elif kind == 2:
+        v = np.abs(v) * 0.05               # every input below about 0.3
+    hb = torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    if kind == 3 and n > 10:
+        hb[off + int(rng.integers(0, n))] = 0x7F80 if k % 8 == 3 else 0xFFC3
+    hbuf = torch.from_numpy(hb.view(np.int16).copy()).view(torch.bfloat16).to(dev)
+    h = hbuf[off: off + n]
+    qbuf, q = guarded(n, torch.uint8, dev, off)
+    ybuf, y = guarded(n, torch.bfloat16, dev, off, fill=0x5A5A) if with_y else (None, None)
+    amax0 = float(rng.choice([0.0, 0.01]))
+    am = torch.full((1,), amax0, device=dev)
+    sc = torch.full((1,), float(scale), device=dev)
+    st = torch.cuda.current_stream().cuda_stream
+    status = hooks_lib.fp8q_gelu_quantize_amax(h.data_ptr(), y.data_ptr() if with_y else None, q.data_ptr(), n,
+                                               fmt, sc.data_ptr(), am.data_ptr(), st)
+    assert status == 0
+    torch.cuda.synchronize()
+    want_y = seq_gelu(W.bf16_bits(h))
+    rq, ra = oracle.quantize_amax(want_y, fmt, scale, amax0)
+    what = f"case {k}: n={n} off={off} y={with_y} scale={scale}"
+    assert_codes_equal(q.cpu().numpy(), rq, fmt, what + " codes")
+    assert_f32_equal([float(am)], [ra], what + " amax")
+    check_guards(qbuf, n, off)
+    if with_y:
+        assert_bf16_equal(W.bf16_bits(y), want_y, what + " y")
+        check_guards(ybuf, n, off, fill=0x5A5A)
