@@ -358,6 +358,20 @@ def test_layernorm_shapes(dev, rows, H):
         check_layernorm(x, gamma, beta, fmt, scale, dev, amax0=0.25 * k, what=f"{rows}x{H} scale {scale}")
 
 
+@pytest.mark.parametrize("k", range(12))
+def test_layernorm_random_shapes(dev, k):
+    """Seeded random row counts and lengths (H a multiple of 16 up to 16384), a scale per
+    case (slow-path ones too) and both formats, on the LayerNorm input workload's rows."""
+    rng = np.random.default_rng(500 + k)
+    H = 16 * int(rng.integers(1, 1025))
+    rows = int(rng.integers(1, max(2, min(600, (1 << 21) // H))))
+    x = W.residual_stream(seed=900 + k, device=dev, shape=(rows, H))
+    gamma, beta = W.layernorm_params(H, seed=k, device=dev)
+    fmt = E4M3FN if k % 2 else E5M2
+    scale = [0.0123, 1.0, 2.0 ** 70, 3.3e-3, 0.0, 0.07][k % 6]
+    check_layernorm(x, gamma, beta, fmt, scale, dev, amax0=0.1 * (k % 3), what=f"{rows}x{H} scale {scale}")
+
+
 @pytest.mark.parametrize("rows,H", [(20000, 48), (5000, 4096), (3000, 8192), (1000, 16384), (7001, 272)])
 def test_layernorm_many_rows(dev, rows, H):
     """More rows than the persistent grid has warps (or warp groups), so each one loops."""
