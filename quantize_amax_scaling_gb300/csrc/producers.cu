@@ -236,8 +236,8 @@ constexpr int kGeluCodeTableThreads = 1024;
 constexpr uint32_t kGeluYTableBytes = 65536u * 2u;
 constexpr uint32_t kGeluCodeTableBytes = 65536u;
 // Fewer elements take the direct kernel.  Measured on GB300 from a cold L2
-// (direct / table, us): codes alone 16.8 / 16.8 at 2^23 elements, 25.2 / 21.3
-// at 2^24; with y 25.3 / 27.4 at 2^24, 41.4 / 39.4 at 2^25.
+// (direct / table, us): codes alone 12.7 / 12.7 at 2^22 elements, 16.8 / 14.8
+// at 2^23, 25.3 / 19.2 at 2^24; with y 25.3 / 27.4 at 2^24, 41.7 / 39.7 at 2^25.
 #ifdef FP8Q_TEST_GELU_TABLE_MIN_ELEMS  // test-only build: small tensors take the table path too
 constexpr int64_t kGeluTableMinElems = FP8Q_TEST_GELU_TABLE_MIN_ELEMS;
 constexpr int64_t kGeluTableMinElemsWithY = FP8Q_TEST_GELU_TABLE_MIN_ELEMS;
@@ -251,12 +251,17 @@ constexpr int kGeluTableUnroll = 2;
 constexpr int kGeluYUnroll = 2;
 // CTAs of one thread-block cluster (on as many SMs) build their tables
 // together: each computes its share of the entries and stores each into the
-// shared memory of every CTA of the cluster.  Measured on GB300 (8192x16384):
-// with y (512 threads), clusters of 4, 112.7 us, against 118.5 without and
-// 117.4 with 2; codes alone (1024 threads), clusters of 2, 69.7 us, against
-// 71.6 with 4.  Clusters of 8 leave SMs idle.
+// shared memory of every CTA of the cluster.  Larger clusters build faster
+// but leave more SMs idle (the clusters that fit at once cover fewer SMs).
+// Measured on GB300: with y (512 threads, 8192x16384), clusters of 4, 112.7
+// us, against 118.5 without and 117.4 with 2.  Codes alone (1024 threads),
+// from a cold L2: clusters of 8 below 2^25 elements (14.8 us at 2^23 and 18.9
+// at 2^24, against 16.9 and 21.1-21.2 with 2 or 4), clusters of 2 from there
+// (8192x16384 back to back: 69.7 us, against 71.6 with 4).
 constexpr int kGeluYTableCluster = 4;
+constexpr int kGeluCodeTableClusterSmall = 8;
 constexpr int kGeluCodeTableCluster = 2;
+constexpr int64_t kGeluCodeTableSmallBelow = (int64_t)1 << 25;
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
@@ -467,7 +472,7 @@ constexpr uint32_t kGeluNegativeBound = 0x3E400000u;
 // of its elements is |y(hm)|, computed once with gelu_pair.  A thread for
 // which that fails (all of its inputs below about 0.3, or none) reads its
 // elements again and takes the largest |y| of gelu_pair on each.
-template <int FMT>
+template <int FMT, int CLUSTER>
 __global__ void __launch_bounds__(kGeluCodeTableThreads, 1) gelu_code_table_kernel(const GeluArgs a) {
     extern __shared__ __align__(16) uint32_t tab32[];  // byte h: the FP8 code of y(h) / scale
     __shared__ uint32_t red[kGeluCodeTableThreads / 32];
@@ -479,12 +484,12 @@ __global__ void __launch_bounds__(kGeluCodeTableThreads, 1) gelu_code_table_kern
     const QScale c = make_qscale(a.scale);
     // word p: the codes of inputs 4p .. 4p + 3, lowest byte first
     if (c.fast)
-        cluster_build<kGeluCodeTableThreads, kGeluCodeTableCluster, 16384>(tab32, [&c](int p) {
+        cluster_build<kGeluCodeTableThreads, CLUSTER, 16384>(tab32, [&c](int p) {
             const uint32_t h = 4u * (uint32_t)p;
             return quant_quad_x2<FMT, true>(gelu_pair(h | ((h + 1u) << 16)), gelu_pair((h + 2u) | ((h + 3u) << 16)), c);
         });
     else
-        cluster_build<kGeluCodeTableThreads, kGeluCodeTableCluster, 16384>(tab32, [&c](int p) {
+        cluster_build<kGeluCodeTableThreads, CLUSTER, 16384>(tab32, [&c](int p) {
             const uint32_t h = 4u * (uint32_t)p;
             return quant_quad_x2<FMT, false>(gelu_pair(h | ((h + 1u) << 16)), gelu_pair((h + 2u) | ((h + 3u) << 16)), c);
         });
@@ -953,9 +958,14 @@ fp8q_status launch_gelu_y_table(const GeluArgs& a, cudaStream_t s) {
 
 template <int FMT>
 fp8q_status launch_gelu_code_table(const GeluArgs& a, cudaStream_t s) {
-    static ResidentCache cache;
-    return launch_gelu_table(gelu_code_table_kernel<FMT>, kGeluCodeTableThreads, kGeluTableUnroll, kGeluCodeTableCluster,
-                             kGeluCodeTableBytes, cache, a, s, "gelu_code_table_kernel");
+    static ResidentCache cache, cache_small;
+    if (a.n < kGeluCodeTableSmallBelow)
+        return launch_gelu_table(gelu_code_table_kernel<FMT, kGeluCodeTableClusterSmall>, kGeluCodeTableThreads,
+                                 kGeluTableUnroll, kGeluCodeTableClusterSmall, kGeluCodeTableBytes, cache_small, a, s,
+                                 "gelu_code_table_kernel");
+    return launch_gelu_table(gelu_code_table_kernel<FMT, kGeluCodeTableCluster>, kGeluCodeTableThreads,
+                             kGeluTableUnroll, kGeluCodeTableCluster, kGeluCodeTableBytes, cache, a, s,
+                             "gelu_code_table_kernel");
 }
 
 }  // namespace

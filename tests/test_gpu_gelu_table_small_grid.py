@@ -1,10 +1,10 @@
-"""The GELU table kernel on small tensors, through the test-hooks build in which
+"""The GELU table kernels on small tensors, through the test-hooks build in which
 every vector-path tensor takes the table path (FP8Q_TEST_GELU_TABLE_MIN_ELEMS=1).
 
-The table kernel's grid is the CTAs the tensor needs, rounded up to whole
-thread-block clusters (2 CTAs for the codes alone, 4 with y), so here some CTAs
-have no vectors to convert but still take part in the cluster's table build;
-CTA 0 also converts the scalar head and tail.  Every output is compared: y with
+A table kernel's grid is the CTAs the tensor needs, rounded up to whole
+thread-block clusters (8 CTAs for the codes alone below 2^25 elements, 4 with
+y), so here some CTAs have no vectors to convert but still take part in the
+cluster's table build; CTA 0 also converts the scalar head and tail.  Every output is compared: y with
 the fixed binary32 sequence (which the GPU GELU tests hold to the float64
 tolerance), the codes and the amax with the oracle's quantize of that y.
 """
@@ -21,9 +21,9 @@ pytestmark = pytest.mark.gpu
 
 # vectors of 16 elements per CTA: 1024 threads x 2 (codes only), 512 x 2 (with y)
 CASES = [  # (elements, offset, with y)
-    (16 * 2048 + 7, 0, False),            # 1 CTA needed, grid 2 (one whole cluster)
-    (16 * (2048 * 2 + 5) + 3, 3, False),  # 3 CTAs needed, grid rounded up to 4
-    (16 * 100 + 9, 5, False),             # 1 CTA needed, grid 2
+    (16 * 2048 + 7, 0, False),            # 1 CTA needed, grid 8 (one whole cluster)
+    (16 * (2048 * 8 + 5) + 3, 3, False),  # 9 CTAs needed, grid rounded up to 16
+    (16 * 100 + 9, 5, False),             # 1 CTA needed, grid 8
     (16 * 1024 + 1, 1, True),             # 1 CTA needed, grid rounded up to 4
     (16 * (1024 * 5 - 7) + 11, 2, True),  # 5 CTAs needed, grid 8
 ]
