@@ -253,12 +253,15 @@ constexpr int kGeluYUnroll = 2;
 // together: each computes its share of the entries and stores each into the
 // shared memory of every CTA of the cluster.  Larger clusters build faster
 // but leave more SMs idle (the clusters that fit at once cover fewer SMs).
-// Measured on GB300: with y (512 threads, 8192x16384), clusters of 4, 112.7
-// us, against 118.5 without and 117.4 with 2.  Codes alone (1024 threads),
-// from a cold L2: clusters of 8 below 2^25 elements (14.8 us at 2^23 and 18.9
-// at 2^24, against 16.9 and 21.1-21.2 with 2 or 4), clusters of 2 from there
-// (8192x16384 back to back: 69.7 us, against 71.6 with 4).
+// Measured on GB300: with y (512 threads), clusters of 8 below 2^26 elements
+// (cold L2, 2^25: 37.7 us, against 39.7 with 2 or 4), clusters of 4 from there
+// (8192x16384: 112.7 us, against 118.5 without and 117.4 with 2).  Codes alone
+// (1024 threads), from a cold L2: clusters of 8 below 2^25 elements (14.8 us
+// at 2^23 and 18.9 at 2^24, against 16.9 and 21.1-21.2 with 2 or 4), clusters
+// of 2 from there (8192x16384 back to back: 69.7 us, against 71.6 with 4).
+constexpr int kGeluYTableClusterSmall = 8;
 constexpr int kGeluYTableCluster = 4;
+constexpr int64_t kGeluYTableSmallBelow = (int64_t)1 << 26;
 constexpr int kGeluCodeTableClusterSmall = 8;
 constexpr int kGeluCodeTableCluster = 2;
 constexpr int64_t kGeluCodeTableSmallBelow = (int64_t)1 << 25;
@@ -343,7 +346,7 @@ __device__ __forceinline__ uint4 gelu_lookup4(const uint16_t* tab, const uint4& 
                       gelu_lookup_pair(tab, w.w));
 }
 
-template <int FMT>
+template <int FMT, int CLUSTER>
 __global__ void __launch_bounds__(kGeluYTableThreads, 1) gelu_table_quantize_amax_kernel(const GeluArgs a) {
     extern __shared__ __align__(16) uint32_t tab32[];  // word p: the y of inputs 2p and 2p + 1
     __shared__ uint32_t red[kGeluYTableThreads / 32];
@@ -353,7 +356,7 @@ __global__ void __launch_bounds__(kGeluYTableThreads, 1) gelu_table_quantize_ama
     int64_t v0 = (int64_t)blockIdx.x * kGeluYTableThreads + threadIdx.x;
     uint4 wa[kGeluYUnroll], wb[kGeluYUnroll];
     gelu_load(a, v0, stride, wa, wb);  // before the build, which hides their latency
-    cluster_build<kGeluYTableThreads, kGeluYTableCluster, 32768>(
+    cluster_build<kGeluYTableThreads, CLUSTER, 32768>(
         tab32, [](int p) { return gelu_pair((uint32_t)(2 * p) | ((uint32_t)(2 * p + 1) << 16)); });
     const QScale c = make_qscale(a.scale);
     cluster_sync_all();  // every CTA's table is complete; no remote store comes after this
@@ -951,9 +954,14 @@ fp8q_status launch_gelu_table(Kern kern, int threads, int unroll, int cluster, u
 
 template <int FMT>
 fp8q_status launch_gelu_y_table(const GeluArgs& a, cudaStream_t s) {
-    static ResidentCache cache;
-    return launch_gelu_table(gelu_table_quantize_amax_kernel<FMT>, kGeluYTableThreads, kGeluYUnroll, kGeluYTableCluster,
-                             kGeluYTableBytes, cache, a, s, "gelu_table_quantize_amax_kernel");
+    static ResidentCache cache, cache_small;
+    if (a.n < kGeluYTableSmallBelow)
+        return launch_gelu_table(gelu_table_quantize_amax_kernel<FMT, kGeluYTableClusterSmall>, kGeluYTableThreads,
+                                 kGeluYUnroll, kGeluYTableClusterSmall, kGeluYTableBytes, cache_small, a, s,
+                                 "gelu_table_quantize_amax_kernel");
+    return launch_gelu_table(gelu_table_quantize_amax_kernel<FMT, kGeluYTableCluster>, kGeluYTableThreads,
+                             kGeluYUnroll, kGeluYTableCluster, kGeluYTableBytes, cache, a, s,
+                             "gelu_table_quantize_amax_kernel");
 }
 
 template <int FMT>

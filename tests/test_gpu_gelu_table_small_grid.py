@@ -2,11 +2,12 @@
 every vector-path tensor takes the table path (FP8Q_TEST_GELU_TABLE_MIN_ELEMS=1).
 
 A table kernel's grid is the CTAs the tensor needs, rounded up to whole
-thread-block clusters (8 CTAs for the codes alone below 2^25 elements, 4 with
-y), so here some CTAs have no vectors to convert but still take part in the
-cluster's table build; CTA 0 also converts the scalar head and tail.  Every output is compared: y with
-the fixed binary32 sequence (which the GPU GELU tests hold to the float64
-tolerance), the codes and the amax with the oracle's quantize of that y.
+thread-block clusters (8 CTAs below 2^25 elements for the codes alone and below
+2^26 with y), so here some CTAs have no vectors to convert but still take part
+in the cluster's table build; CTA 0 also converts the scalar head and tail.
+Every output is compared: y with the fixed binary32 sequence (which the GPU
+GELU tests hold to the float64 tolerance), the codes and the amax with the
+oracle's quantize of that y.
 """
 import numpy as np
 import pytest
@@ -24,7 +25,7 @@ CASES = [  # (elements, offset, with y)
     (16 * 2048 + 7, 0, False),            # 1 CTA needed, grid 8 (one whole cluster)
     (16 * (2048 * 8 + 5) + 3, 3, False),  # 9 CTAs needed, grid rounded up to 16
     (16 * 100 + 9, 5, False),             # 1 CTA needed, grid 8
-    (16 * 1024 + 1, 1, True),             # 1 CTA needed, grid rounded up to 4
+    (16 * 1024 + 1, 1, True),             # 1 CTA needed, grid rounded up to 8
     (16 * (1024 * 5 - 7) + 11, 2, True),  # 5 CTAs needed, grid 8
 ]
 
