@@ -59,6 +59,25 @@ __device__ __forceinline__ void fold(int (&key)[4], bool (&nan)[4], float4 v) {
     }
 }
 
+// Column j's selected amax -- the new entry and, for max, the warps' maxima of
+// the rows that survive the roll -- and its scale.
+__device__ __forceinline__ void finish_slot(const UpdArgs& a, int c0, int j, float newest, int slot_fmt,
+                                            bool want_max, const int (&s_key)[kUpdThreads / 32][kUpdCols],
+                                            const int (&s_nan)[kUpdThreads / 32][kUpdCols]) {
+    float amax = newest;
+    if (want_max) {
+        int kb = INT_MIN;
+        bool nb = isnan(newest);
+        for (int w = 0; w < kUpdThreads / 32; ++w) {
+            kb = max(kb, s_key[w][j]);
+            nb |= (s_nan[w][j] != 0);
+        }
+        if (a.H > 1) amax = fmaxf(amax, key_float(kb));
+        if (nb) amax = __int_as_float(0x7FC00000);
+    }
+    slot_scale(amax, slot_fmt, a.margin, a.scale + c0 + j, a.scale_inv + c0 + j);
+}
+
 template <bool VEC4>
 __global__ void __launch_bounds__(kUpdThreads) amax_scale_update_kernel(const UpdArgs a) {
     __shared__ int s_key[kUpdThreads / 32][kUpdCols];
@@ -78,6 +97,46 @@ __global__ void __launch_bounds__(kUpdThreads) amax_scale_update_kernel(const Up
     if (threadIdx.x < ncols) {
         newest = a.amax_new[c0 + threadIdx.x];
         if (a.slot_format) slot_fmt = a.slot_format[c0 + threadIdx.x];
+    }
+
+    if (H <= kUpdChunk) {
+        // One chunk, in blocks: thread t holds rows kUpdRows t ... kUpdRows t + kUpdRows - 1.
+        // The roll moves each of them one row older.  All but the last land in rows of the
+        // same block, which only this thread reads, so they are stored as soon as they
+        // are loaded; the last lands in the first row of the next thread's block and
+        // waits for the barrier below, by which time every row has been read.
+        float4 v[kUpdRows];
+        const int64_t r0 = (int64_t)threadIdx.x * kUpdRows;
+#pragma unroll
+        for (int k = 0; k < kUpdRows; ++k)
+            if (r0 + k < H) v[k] = load_row<VEC4>(a, r0 + k, c0, ncols);
+        if (want_max) {
+            // old rows 0..H-2 survive the roll; row H-1 drops out of the window
+#pragma unroll
+            for (int k = 0; k < kUpdRows; ++k)
+                if (r0 + k + 1 < H) fold(key, nan, v[k]);
+        }
+#pragma unroll
+        for (int k = 0; k + 1 < kUpdRows; ++k)
+            if (r0 + k + 1 < H) store_row<VEC4>(a, r0 + k + 1, c0, ncols, v[k]);
+        if (want_max) {
+            const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int kw = __reduce_max_sync(0xFFFFFFFFu, key[j]);
+                const bool nw = __any_sync(0xFFFFFFFFu, nan[j]);
+                if (lane == 0) {
+                    s_key[warp][j] = kw;
+                    s_nan[warp][j] = nw;
+                }
+            }
+        }
+        __syncthreads();  // every row has been read; the warps' maxima are in shared memory
+        if (r0 + kUpdRows < H) store_row<VEC4>(a, r0 + kUpdRows, c0, ncols, v[kUpdRows - 1]);
+        // row 0 (read above by thread 0) receives the new amax
+        if (threadIdx.x < ncols) a.hist[c0 + threadIdx.x] = newest;
+        if (threadIdx.x < ncols) finish_slot(a, c0, threadIdx.x, newest, slot_fmt, want_max, s_key, s_nan);
+        return;
     }
 
     float4 cur[kUpdRows], nxt[kUpdRows];
@@ -130,22 +189,7 @@ __global__ void __launch_bounds__(kUpdThreads) amax_scale_update_kernel(const Up
         }
         __syncthreads();
     }
-    if (threadIdx.x < ncols) {
-        const int j = threadIdx.x;
-        const int s = c0 + j;
-        float amax = newest;
-        if (want_max) {
-            int kb = INT_MIN;
-            bool nb = isnan(newest);
-            for (int w = 0; w < kUpdThreads / 32; ++w) {
-                kb = max(kb, s_key[w][j]);
-                nb |= (s_nan[w][j] != 0);
-            }
-            if (H > 1) amax = fmaxf(amax, key_float(kb));
-            if (nb) amax = __int_as_float(0x7FC00000);
-        }
-        slot_scale(amax, slot_fmt, a.margin, a.scale + s, a.scale_inv + s);
-    }
+    if (threadIdx.x < ncols) finish_slot(a, c0, threadIdx.x, newest, slot_fmt, want_max, s_key, s_nan);
 }
 
 // Ring-buffer form of the update: the window stays where it is and only each
