@@ -449,7 +449,10 @@ def measure_graph(args, step, stream, dev):
     f = step.fp8q
     st = stream.cuda_stream
 
-    def timed(fn, reps):
+    def timed(fn, reps, replays=1):
+        """us per repetition: the median over `replays` timed replays of one graph of
+        `reps` repetitions (several replays of a long graph keep the event timer's
+        granularity, a few us on this GPU, well below the figure's last digit)."""
         with torch.cuda.stream(stream):
             fn()
             stream.synchronize()
@@ -459,13 +462,14 @@ def measure_graph(args, step, stream, dev):
                     fn()
             for _ in range(2):
                 g.replay()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            g.replay()
-            e1.record(stream)
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(replays)]
+            for e0, e1 in ev:
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
         torch.cuda.synchronize(dev)
-        return e0.elapsed_time(e1) * 1e3 / reps  # us per repetition
+        return statistics.median(e0.elapsed_time(e1) * 1e3 / reps for e0, e1 in ev)
 
     reps = max(4, min(args.steps, 50))
     step_us = timed(lambda: step.run(stream), reps)
@@ -477,9 +481,9 @@ def measure_graph(args, step, stream, dev):
     sc, si = step.scale.clone(), step.scale_inv.clone()
     ring = lambda: f.fp8q_amax_scale_update_ring(ring_hist, head, step.amax_new, sc, si, f.E4M3FN,
                                                  f.ALGO_MAX, 0, step.slot_format, st)
-    deq_us = timed(deq, 20)
-    pair_us = timed(lambda: (deq(), upd()), 20)
-    ring_pair_us = timed(lambda: (deq(), ring()), 20)
+    deq_us = timed(deq, 100, 5)
+    pair_us = timed(lambda: (deq(), upd()), 100, 5)
+    ring_pair_us = timed(lambda: (deq(), ring()), 100, 5)
     return {"ms_per_step": round(step_us / 1e3, 4), "replays_of_step": reps,
             "GB/s": round(STEP_BYTES / (step_us * 1e-6) / 1e9, 1),
             "scale_update_us_after_dequantize": round(pair_us - deq_us, 3),
@@ -727,7 +731,7 @@ def measure_next_rows(args, step, stream, dev, peak):
                                                step.act, qf, slot, amf[1:2], f.E4M3FN, f.ALGO_MAX, 0,
                                                step.slot_format, stream.cuda_stream)
 
-    def graph_us(fn, reps=10):
+    def graph_us(fn, reps=10, replays=3):
         with torch.cuda.stream(stream):
             fn()
             stream.synchronize()
@@ -736,13 +740,14 @@ def measure_next_rows(args, step, stream, dev, peak):
                 for _ in range(reps):
                     fn()
             gr.replay()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            gr.replay()
-            e1.record(stream)
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(replays)]
+            for e0, e1 in ev:
+                e0.record(stream)
+                gr.replay()
+                e1.record(stream)
         torch.cuda.synchronize(dev)
-        return e0.elapsed_time(e1) * 1e3 / reps
+        return statistics.median(e0.elapsed_time(e1) * 1e3 / reps for e0, e1 in ev)
 
     # The same pair on a small tensor (1024x1024), launched eagerly: the regime in
     # which one launch instead of two matters (the update's cost is launch overhead).
@@ -764,8 +769,8 @@ def measure_next_rows(args, step, stream, dev, peak):
                     "eagerly back to back (per call: device time between events over the loop)",
         "fused_us": round(timed_loop(fused_small), 3),
         "two_launches_us": round(timed_loop(two_small), 3),
-        "fused_us_graph": round(graph_us(fused_small), 3),
-        "two_launches_us_graph": round(graph_us(two_small), 3)}
+        "fused_us_graph": round(graph_us(fused_small, 100), 3),
+        "two_launches_us_graph": round(graph_us(two_small, 100), 3)}
 
     out["amax_scale_update_ring_quantize"] = {
         "workload": "ring update of 576 slots x history 1024 + quantize of the bf16 8192x16384 activation "
