@@ -493,8 +493,8 @@ def measure_graph(args, step, stream, dev):
                    "minus dequantize alone, both as graphs"}
 
 
-def measure_other_configs(step, stream, dev, peak, warm=20, reps=20):
-    """Two more quantize workloads, each launch timed on its own (median of `reps`).
+def measure_other_configs(step, stream, dev, peak, warm=20, reps=50):
+    """Two more quantize workloads, each launch timed on its own (mean of `reps`).
 
     - The MLP input activation, bf16 8192x4096 N(0,1) with 0.1% outliers x100,
       e4m3fn with the scale of the previous step's amax: its 100.7 MB of
@@ -514,7 +514,11 @@ def measure_other_configs(step, stream, dev, peak, warm=20, reps=20):
     st = stream.cuda_stream
     out = {}
 
-    def median_us(launch, before=None):
+    def mean_us(launch, before=None):
+        """Mean and median device time of single launches, each between its own
+        events.  The event timer ticks every 2 us or so on this GPU, so a single
+        launch's time is quantised; the mean over many launches (whose start is
+        not tied to the tick) is not, the median is."""
         times = []
         with torch.cuda.stream(stream):
             for _ in range(warm):
@@ -531,7 +535,8 @@ def measure_other_configs(step, stream, dev, peak, warm=20, reps=20):
                 e1.record(stream)
                 times.append((e0, e1))
         torch.cuda.synchronize(dev)
-        return statistics.median(a.elapsed_time(b) * 1e3 for a, b in times)
+        us = [a.elapsed_time(b) * 1e3 for a, b in times]
+        return statistics.fmean(us), statistics.median(us)
 
     prev = W.mlp_activation(W.SEED_MLP + 1, dev)
     sc = (prev.float().abs().max() / 448.0).reshape(1)
@@ -545,11 +550,11 @@ def measure_other_configs(step, stream, dev, peak, warm=20, reps=20):
     for key, before, how in (("mlp_activation", lambda: flush.sum(), "cold, clean: 256 MB read before every launch"),
                              ("mlp_activation_after_writes", flush.zero_,
                               "cold, dirty: 256 MB written before every launch")):
-        us = median_us(launch, before=before)
+        us, us_med = mean_us(launch, before=before)
         gbs = nbytes / (us * 1e-6) / 1e9
         out[key] = {"workload": "bf16 8192x4096 N(0,1), 0.1% outliers x100 -> e4m3fn + amax",
-                    "l2": how, "launches_timed": reps, "us_median": round(us, 3), "GB/s": round(gbs, 1),
-                    "frac_of_peak": round(gbs / peak, 4), "bytes_per_launch": nbytes}
+                    "l2": how, "launches_timed": reps, "us": round(us, 3), "us_median": round(us_med, 3),
+                    "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4), "bytes_per_launch": nbytes}
     del x, q, flush
 
     xs = [t.reshape(-1) for t in W.ragged_tensors(dev)]
@@ -557,13 +562,13 @@ def measure_other_configs(step, stream, dev, peak, warm=20, reps=20):
     ams = torch.zeros(len(xs), device=dev)
     scales = [step.scale[i:i + 1] for i in range(len(xs))]
     amaxes = [ams[i:i + 1] for i in range(len(xs))]
-    us = median_us(lambda: f.fp8q_multi_quantize_amax(xs, qs, f.E4M3FN, scales, amaxes, st))
+    us, us_med = mean_us(lambda: f.fp8q_multi_quantize_amax(xs, qs, f.E4M3FN, scales, amaxes, st))
     nbytes = 3 * sum(t.numel() for t in xs)
     gbs = nbytes / (us * 1e-6) / 1e9
     out["ragged_twelve_tensors"] = {"workload": "12 bf16 N(0,1) tensors 2048x12288 .. 12288x4096 "
                                                 "(465.6 M elements) -> e4m3fn + 12 amaxes, one launch",
                                     "l2": "inputs larger than L2", "launches_timed": reps,
-                                    "us_median": round(us, 3), "GB/s": round(gbs, 1),
+                                    "us": round(us, 3), "us_median": round(us_med, 3), "GB/s": round(gbs, 1),
                                     "frac_of_peak": round(gbs / peak, 4), "bytes_per_launch": nbytes}
     del xs, qs
     torch.cuda.empty_cache()
