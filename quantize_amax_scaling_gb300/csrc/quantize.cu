@@ -37,14 +37,17 @@ __global__ void __launch_bounds__(kThreads) quantize_amax_kernel(const __grid_co
 }
 
 // ----------------------------------------------------------------------------
-// Quantize + amax of one tensor by a persistent grid of balanced, contiguous
-// ranges: CTA b converts vectors [b * per, (b + 1) * per) of the tensor, its
-// threads taking every 256th vector, and each thread keeps its next two
-// vectors loading while it converts the current two.  With one CTA per tile,
-// a tensor of a few waves of tiles ends on a partial wave that leaves most
-// SMs idle (2048 tiles over 608 resident CTAs is 3.4 waves); here every CTA
-// streams the same amount.  The launcher picks it for vector-path tensors of
-// at most kStreamMaxTiles tiles (2560: 41.9 M elements).
+// Quantize + amax of one tensor by a persistent grid: the tensor's 16-element
+// vectors in chunks of kStreamUnroll * kThreads, CTA b taking chunks b, b + G,
+// b + 2G, ... (G CTAs), each thread keeping its next two vectors loading while
+// it converts the current two.  With one CTA per tile, a tensor of a few waves
+// of tiles ends on a partial wave that leaves most SMs idle (2048 tiles over
+// 608 resident CTAs is 3.4 waves); here every CTA streams within one chunk of
+// the same amount, and at any moment the CTAs work on one window of the tensor
+// (measured on 8192x4096 from a cold L2: as fast as contiguous balanced ranges
+// per CTA from a clean L2, 4% faster after dirty writes).  The launcher picks
+// it for vector-path tensors of at most kStreamMaxTiles tiles (2560: 41.9 M
+// elements).
 
 constexpr int kStreamCtasPerSm = 4;
 constexpr int kStreamUnroll = 2;
@@ -53,11 +56,12 @@ template <int FMT, bool FAST>
 __device__ __forceinline__ void stream_range(const QCursor& k, int64_t v0, int64_t end, uint4 (&a)[kStreamUnroll],
                                              uint4 (&b)[kStreamUnroll], uint32_t& m2) {
     const uint16_t* xb = k.x + k.head;
-    for (; v0 < end; v0 += kStreamUnroll * kThreads) {
+    const int64_t cstride = (int64_t)gridDim.x * kStreamUnroll * kThreads;
+    for (; v0 < end; v0 += cstride) {
         uint4 na[kStreamUnroll], nb[kStreamUnroll];
 #pragma unroll
         for (int u = 0; u < kStreamUnroll; ++u) {
-            const int64_t v = v0 + (kStreamUnroll + u) * kThreads;
+            const int64_t v = v0 + cstride + u * kThreads;
             if (v < end) ld_stream_v8(xb + v * QuantGeom::kVecElems, na[u], nb[u]);
         }
 #pragma unroll
@@ -74,11 +78,11 @@ __device__ __forceinline__ void stream_range(const QCursor& k, int64_t v0, int64
 }
 
 template <int FMT>
-__global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) quantize_amax_stream_kernel(const QTensor t, int64_t per) {
+__global__ void __launch_bounds__(kThreads, kStreamCtasPerSm) quantize_amax_stream_kernel(const QTensor t) {
     __shared__ uint32_t red[kThreads / 32];
     const Split sp = split_tensor<QuantGeom>((uintptr_t)t.x, (uintptr_t)t.q, t.n);  // the vector path
-    const int64_t beg = (int64_t)blockIdx.x * per;
-    const int64_t end = min(beg + per, sp.nvec);
+    const int64_t beg = (int64_t)blockIdx.x * (kStreamUnroll * kThreads);  // this CTA's first chunk
+    const int64_t end = sp.nvec;
     uint4 a[kStreamUnroll], b[kStreamUnroll];
     const int64_t v0 = beg + threadIdx.x;
 #pragma unroll
@@ -222,8 +226,8 @@ fp8q_status launch_quantize_one(const fp8q_tensor& t, cudaStream_t stream) {
     const cudaError_t err = sm_count(&sms);
     if (err != cudaSuccess) return cuda_fail(err, "quantize_amax_stream_kernel setup");
     const int64_t ctas = (int64_t)sms * kStreamCtasPerSm;
-    const int64_t per = (sp.nvec + ctas - 1) / ctas;  // >= 1: at least two tiles of vectors
-    const int64_t grid = (sp.nvec + per - 1) / per;
+    const int64_t chunks = (sp.nvec + kStreamUnroll * kThreads - 1) / (kStreamUnroll * kThreads);
+    const int64_t grid = chunks < ctas ? chunks : ctas;
     QTensor d;
     d.x = static_cast<const uint16_t*>(t.x_bf16);
     d.q = t.q;
@@ -232,7 +236,7 @@ fp8q_status launch_quantize_one(const fp8q_tensor& t, cudaStream_t stream) {
     d.n = t.n;
     d.tile_end = 0;
     return launch_kernel(quantize_amax_stream_kernel<FMT>, dim3((unsigned)grid), dim3(kThreads), 0, stream,
-                         "quantize_amax_stream_kernel", d, per);
+                         "quantize_amax_stream_kernel", d);
 }
 
 template <int FMT>
