@@ -191,11 +191,11 @@ fp8q_status launch_quantize(const fp8q_tensor* list, int32_t count, cudaStream_t
 }
 
 // Most tiles (16384 elements each) of a tensor that takes the persistent
-// grid; larger tensors run one CTA per tile.  Measured on GB300 (median of
-// 20 launches): at 2048 tiles the persistent grid takes 16.4-17.4 us from a
-// cold, clean L2 against 18.5 us, and 14.3 us back to back against 16.3 us;
-// from 3072 tiles up both forms tie from a clean L2, while after 256 MB of
-// dirty writes one CTA per tile is 9-11% faster (29.1 against 32.8 us at 3072).
+// grid; larger tensors run one CTA per tile.  Measured on GB300 (means of 40
+// launches): at 2048 tiles the persistent grid takes 16.5 us from a cold,
+// clean L2 against 18.5 us (a median), and 14.3 us back to back against 16.3;
+// from 3072 tiles up it is faster from a clean L2 (22.5 against 24.7 us at
+// 3072) but slower after 256 MB of dirty writes (30.9 against 29.5 us).
 constexpr int64_t kStreamMaxTiles = 2560;
 
 // Resident CTAs of the persistent grid per device (multiprocessors x
