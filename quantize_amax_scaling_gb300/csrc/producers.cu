@@ -255,15 +255,16 @@ constexpr int kGeluYUnroll = 2;
 // but leave more SMs idle (the clusters that fit at once cover fewer SMs).
 // Measured on GB300: with y (512 threads), clusters of 8 below 2^26 elements
 // (cold L2, 2^25: 37.7 us, against 39.7 with 2 or 4), clusters of 4 from there
-// (8192x16384: 112.7 us, against 118.5 without and 117.4 with 2).  Codes alone
-// (1024 threads), from a cold L2: clusters of 8 below 2^25 elements (14.8 us
-// at 2^23 and 18.9 at 2^24, against 16.9 and 21.1-21.2 with 2 or 4), clusters
-// of 2 from there (8192x16384 back to back: 69.7 us, against 71.6 with 4).
+// (8192x16384 back to back: 112.0 us, against 114.6 with 2 and 113.3 with 8).
+// Codes alone (1024 threads): clusters of 8 below 2^25 elements (cold L2: 14.8
+// us at 2^23 and 18.9 at 2^24, against 16.9 and 21.1-21.2 with 2 or 4),
+// clusters of 4 from there (back to back: 22.7, 38.7 and 65.6 us at 2^25,
+// 2^26 and 2^27, against 24.7, 37.4 and 67.0 with 2).
 constexpr int kGeluYTableClusterSmall = 8;
 constexpr int kGeluYTableCluster = 4;
 constexpr int64_t kGeluYTableSmallBelow = (int64_t)1 << 26;
 constexpr int kGeluCodeTableClusterSmall = 8;
-constexpr int kGeluCodeTableCluster = 2;
+constexpr int kGeluCodeTableCluster = 4;
 constexpr int64_t kGeluCodeTableSmallBelow = (int64_t)1 << 25;
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
