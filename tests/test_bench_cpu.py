@@ -102,10 +102,11 @@ def test_compact_rows_and_detail_file(tmp_path):
     nxt = {"qdq_amax": {"frac_of_peak": 0.99}, "gelu_quantize_amax": {"codes_only": {"frac_of_peak": 0.82}},
            "layernorm_quantize_amax": {"codes_only": {"frac_of_peak": 0.6}},
            "amax_scale_update_ring": {"us": 7.6}}
-    rows = bench.compact_rows(kernels, nxt, other)
+    rows = bench.compact_rows(kernels, nxt, other, {"ring_update_us_after_dequantize": 2.9})
     assert rows == {"multi_quantize_frac": 0.95, "dequantize_frac": 0.94, "mlp_activation_8192x4096_frac": 0.9,
                     "ragged_12_frac": 1.04, "qdq_frac": 0.99, "gelu_codes_frac": 0.82,
-                    "layernorm_codes_frac": 0.6, "ring_update_us": 7.6}
+                    "layernorm_codes_frac": 0.6, "ring_update_us": 2.9, "ring_update_us_eager": 7.6}
+    assert "ring_update_us" not in bench.compact_rows(kernels, nxt, other)
     assert bench.compact_rows(kernels, None, None) == {"multi_quantize_frac": 0.95, "dequantize_frac": 0.94}
     p = tmp_path / "sub" / "detail.json"
     where = bench.write_detail({"a": 1}, str(p))
