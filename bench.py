@@ -32,9 +32,9 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "quantize+amax HBM GB/s (% of GB300 peak); scale-update µs per 576-slot call"
-WORKLOAD = ("fp8 delayed-scaling step, FFN config: quantize+amax act 8192x16384 (e4m3fn) + "
-            "multi-tensor quantize W1 4096x16384, W2 16384x4096 (e4m3fn, 1 launch) + dequantize "
-            "grad 8192x16384 (e5m2) + amax_scale_update 576 slots x history 1024")
+WORKLOAD = ("FP8 delayed-scaling step, FFN config: quantize+amax act 8192x16384 e4m3fn; W1 4096x16384 + "
+            "W2 16384x4096 e4m3fn in one multi-tensor launch; dequantize grad 8192x16384 e5m2; "
+            "update 576 slots x 1024")
 
 ACT = (8192, 16384)
 W1 = (4096, 16384)
@@ -127,7 +127,7 @@ class ClockSampler:
         reasons = [name for b, name in self.REASONS.items() if bits & b and name != "gpu_idle"]
         return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": self.max_mhz, "reasons": reasons,
                 "samples": len(self.samples), "power_w_max": max(s[2] for s in self.samples),
-                "source": "nvml, sampled on the host while the timed steps ran"}
+                "source": "nvml on the host, during the timed steps"}
 
 
 # --------------------------------------------------------------------------- multi-rank helpers
@@ -377,7 +377,7 @@ def run_gpu(args, ws, rank, local):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f32",
-        "data": "synthetic (seeded; shapes of the FFN/MLP and 96-layer workloads)",
+        "data": "synthetic (seeded; FFN/MLP and 96-layer shapes)",
         "config": {"workload": WORKLOAD, "step_bytes": STEP_BYTES,
                    "l2": "inputs larger than L2 (a step streams 1.21 GB)",
                    "parallelism": f"replicas x{ws} (no collective)"},
@@ -402,7 +402,8 @@ def run_gpu(args, ws, rank, local):
         cba = cpu_baseline_all_cores(args.cpu_sample_frac)
         pc = cpu_per_config(args.cpu_config_seconds)
         detail["cpu_baseline"], detail["cpu_baseline_all_cores"], detail["cpu_per_config"] = cb, cba, pc
-        out["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        out["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind")}
+        out["cpu_baseline"]["sample"] = cb["sample_short"]
         out["cpu_baseline"]["all_cores"] = {"value": cba["value"], "cores": cba["cores"]}
         out["cpu_baseline"]["per_config"] = pc["compact"]
     out["detail"] = write_detail(detail, args.detail)
@@ -1051,8 +1052,8 @@ def cpu_baseline(frac: float):
     _oracle_step(inp)
     dt = time.perf_counter() - t0
     return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": desc, "seconds": round(dt, 3),
-            "host": f"{os.uname().machine}, {os.cpu_count()} cores present"}
+            "sample": desc, "sample_short": f"first {frac:g} of each step tensor + one 576x1024 update",
+            "seconds": round(dt, 3), "host": f"{os.uname().machine}, {os.cpu_count()} cores present"}
 
 
 def cpu_baseline_all_cores(frac: float):
