@@ -360,8 +360,12 @@ def test_scale_update_576_slots_full(dev, algo, margin, per_slot):
                  slot_format=sf.numpy() if per_slot else None, steps=3)
 
 
-SHAPES = [(1, 1), (1, 5), (2, 3), (16, 2), (17, 7), (1023, 577), (1024, 575), (1025, 576),
-          (1024, 4), (2053, 12), (3000, 8), (4096, 4)]
+# H up to 1024 takes the one-chunk path, where each thread holds 4 consecutive rows and the
+# last one crosses into the next thread's block (and, every 128 rows, the next warp's);
+# longer histories stream in chunks.
+SHAPES = [(1, 1), (1, 5), (2, 3), (3, 9), (4, 4), (5, 6), (16, 2), (17, 7), (127, 5), (129, 8),
+          (257, 3), (513, 16), (1023, 577), (1024, 575), (1025, 576), (1024, 4), (2053, 12), (3000, 8),
+          (4096, 4)]
 
 
 @pytest.mark.parametrize("H,S", SHAPES)
