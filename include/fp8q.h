@@ -227,6 +227,11 @@ fp8q_status fp8q_amax_scale_update_ring(float* amax_history, int32_t* head, int3
  * the y returned.
  * h_bf16: n bf16 (device).  y_bf16: n bf16 (device, written) or NULL when only
  * the FP8 codes are wanted.  q, scale, amax: as for fp8q_quantize_amax.
+ * Large tensors go through a table of every bf16 input built by thread-block
+ * clusters; on a device where no such cluster can be resident (a partitioned
+ * or shared GPU) the call takes the element-by-element kernel, with the same
+ * results.  The first large call on a device queries how many clusters fit
+ * (host-side calls, allowed during graph capture).
  * Errors: as for fp8q_quantize_amax, plus an odd y_bf16.
  */
 fp8q_status fp8q_gelu_quantize_amax(const void* h_bf16, void* y_bf16, uint8_t* q, int64_t n,

@@ -908,9 +908,20 @@ fp8q_status launch_layernorm(const LnArgs& a, cudaStream_t s) {
 
 // Launch a table kernel on the clusters that fit at once (at most one CTA per
 // vector pair of its threads, rounded up to whole clusters).
+#ifdef FP8Q_TEST_HOOKS  // test-only build: clusters larger than this count as not fitting (0: no limit)
+int g_test_gelu_max_cluster = 0;
+#endif
+
+// A table kernel needs its thread-block clusters resident at once.  Where no
+// cluster of its size fits (a partitioned or shared GPU), this returns
+// FP8Q_ERR_UNSUPPORTED without recording a CUDA error, and the caller takes a
+// smaller cluster or the direct kernel.
 template <typename Kern>
 fp8q_status launch_gelu_table(Kern kern, int threads, int unroll, int cluster, uint32_t smem, ResidentCache& cache,
                               const GeluArgs& a, cudaStream_t s, const char* name) {
+#ifdef FP8Q_TEST_HOOKS
+    if (g_test_gelu_max_cluster > 0 && cluster > g_test_gelu_max_cluster) return FP8Q_ERR_UNSUPPORTED;
+#endif
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -936,14 +947,14 @@ fp8q_status launch_gelu_table(Kern kern, int threads, int unroll, int cluster, u
             if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
             cfg.gridDim = dim3((unsigned)(sms / cluster * cluster));
             if (err == cudaSuccess) err = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
-            if (err == cudaSuccess && clusters < 1) err = cudaErrorInvalidConfiguration;
             if (err == cudaSuccess) {
-                ctas = clusters * cluster;
+                ctas = clusters > 0 ? clusters * cluster : -1;  // -1: no cluster of this size fits
                 if (cache.n < 32) cache.e[cache.n++] = {dev, ctas};
             }
         }
     }
     if (err != cudaSuccess) return cuda_fail(err, name);
+    if (ctas < 0) return FP8Q_ERR_UNSUPPORTED;
     const int64_t per_cta = (int64_t)threads * unroll;
     const int64_t need = (a.nvec + per_cta - 1) / per_cta;
     int grid = (int)(need < ctas ? (need > 0 ? need : 1) : ctas);
@@ -953,25 +964,33 @@ fp8q_status launch_gelu_table(Kern kern, int threads, int unroll, int cluster, u
     return err == cudaSuccess ? FP8Q_OK : cuda_fail(err, name);
 }
 
+// The table kernel with y, its cluster size chosen by the tensor's size; a
+// smaller cluster where the first does not fit; FP8Q_ERR_UNSUPPORTED where
+// neither does (the caller then takes the direct kernel).
 template <int FMT>
 fp8q_status launch_gelu_y_table(const GeluArgs& a, cudaStream_t s) {
     static ResidentCache cache, cache_small;
-    if (a.n < kGeluYTableSmallBelow)
-        return launch_gelu_table(gelu_table_quantize_amax_kernel<FMT, kGeluYTableClusterSmall>, kGeluYTableThreads,
-                                 kGeluYUnroll, kGeluYTableClusterSmall, kGeluYTableBytes, cache_small, a, s,
-                                 "gelu_table_quantize_amax_kernel");
+    if (a.n < kGeluYTableSmallBelow) {
+        const fp8q_status st = launch_gelu_table(gelu_table_quantize_amax_kernel<FMT, kGeluYTableClusterSmall>,
+                                                 kGeluYTableThreads, kGeluYUnroll, kGeluYTableClusterSmall,
+                                                 kGeluYTableBytes, cache_small, a, s, "gelu_table_quantize_amax_kernel");
+        if (st != FP8Q_ERR_UNSUPPORTED) return st;
+    }
     return launch_gelu_table(gelu_table_quantize_amax_kernel<FMT, kGeluYTableCluster>, kGeluYTableThreads,
                              kGeluYUnroll, kGeluYTableCluster, kGeluYTableBytes, cache, a, s,
                              "gelu_table_quantize_amax_kernel");
 }
 
+// The code table kernel, likewise.
 template <int FMT>
 fp8q_status launch_gelu_code_table(const GeluArgs& a, cudaStream_t s) {
     static ResidentCache cache, cache_small;
-    if (a.n < kGeluCodeTableSmallBelow)
-        return launch_gelu_table(gelu_code_table_kernel<FMT, kGeluCodeTableClusterSmall>, kGeluCodeTableThreads,
-                                 kGeluTableUnroll, kGeluCodeTableClusterSmall, kGeluCodeTableBytes, cache_small, a, s,
-                                 "gelu_code_table_kernel");
+    if (a.n < kGeluCodeTableSmallBelow) {
+        const fp8q_status st = launch_gelu_table(gelu_code_table_kernel<FMT, kGeluCodeTableClusterSmall>,
+                                                 kGeluCodeTableThreads, kGeluTableUnroll, kGeluCodeTableClusterSmall,
+                                                 kGeluCodeTableBytes, cache_small, a, s, "gelu_code_table_kernel");
+        if (st != FP8Q_ERR_UNSUPPORTED) return st;
+    }
     return launch_gelu_table(gelu_code_table_kernel<FMT, kGeluCodeTableCluster>, kGeluCodeTableThreads,
                              kGeluTableUnroll, kGeluCodeTableCluster, kGeluCodeTableBytes, cache, a, s,
                              "gelu_code_table_kernel");
@@ -983,6 +1002,12 @@ fp8q_status launch_gelu_code_table(const GeluArgs& a, cudaStream_t s) {
 // C ABI
 
 extern "C" {
+
+#ifdef FP8Q_TEST_HOOKS
+// Test-only build: GELU table kernels with clusters larger than `max_cluster`
+// behave as if their clusters did not fit (0 lifts the limit).
+void fp8q_test_set_gelu_max_cluster(int max_cluster) { g_test_gelu_max_cluster = max_cluster; }
+#endif
 
 fp8q_status fp8q_gelu_quantize_amax(const void* h_bf16, void* y_bf16, uint8_t* q, int64_t n,
                                     fp8q_format fmt, const float* scale, float* amax, void* stream) {
@@ -1013,9 +1038,13 @@ fp8q_status fp8q_gelu_quantize_amax(const void* h_bf16, void* y_bf16, uint8_t* q
     const int grid = (int)(sp.tiles < 0x7FFFFFFF ? sp.tiles : 0x7FFFFFFF);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (sp.mode == kModeVec && n >= (y_bf16 ? kGeluTableMinElemsWithY : kGeluTableMinElems)) {
+        fp8q_status st;
         if (fmt == FP8Q_E4M3FN)
-            return y_bf16 ? launch_gelu_y_table<FP8Q_E4M3FN>(a, s) : launch_gelu_code_table<FP8Q_E4M3FN>(a, s);
-        return y_bf16 ? launch_gelu_y_table<FP8Q_E5M2>(a, s) : launch_gelu_code_table<FP8Q_E5M2>(a, s);
+            st = y_bf16 ? launch_gelu_y_table<FP8Q_E4M3FN>(a, s) : launch_gelu_code_table<FP8Q_E4M3FN>(a, s);
+        else
+            st = y_bf16 ? launch_gelu_y_table<FP8Q_E5M2>(a, s) : launch_gelu_code_table<FP8Q_E5M2>(a, s);
+        if (st != FP8Q_ERR_UNSUPPORTED) return st;
+        // no table kernel's cluster fits on this device: the direct kernel below
     }
     auto kern = fmt == FP8Q_E4M3FN ? (y_bf16 ? gelu_quantize_amax_kernel<FP8Q_E4M3FN, true>
                                              : gelu_quantize_amax_kernel<FP8Q_E4M3FN, false>)

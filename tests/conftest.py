@@ -66,14 +66,16 @@ def hooks_lib(tmp_path_factory):
     """libfp8q built once more with its test hooks (never the product build):
     FP8Q_TEST_LN_GIVE_UP_AT=1 makes each LayerNorm warp's wait for its second row
     report failure; FP8Q_TEST_GELU_TABLE_MIN_ELEMS=1 sends every vector-path GELU
-    tensor through the table kernel, however small.  Loaded with ctypes; only the
-    entry points the hook tests call are declared."""
+    tensor through the table kernel, however small; FP8Q_TEST_HOOKS exports
+    fp8q_test_set_gelu_max_cluster, which makes larger thread-block clusters count as
+    not fitting.  Loaded with ctypes; only the entry points the hook tests call are
+    declared."""
     import ctypes
 
     from quantize_amax_scaling_gb300 import build
 
     path = str(tmp_path_factory.mktemp("hooks") / "libfp8q_test_hooks.so")
-    build.build_variant(path, ["FP8Q_TEST_LN_GIVE_UP_AT=1", "FP8Q_TEST_GELU_TABLE_MIN_ELEMS=1"])
+    build.build_variant(path, ["FP8Q_TEST_LN_GIVE_UP_AT=1", "FP8Q_TEST_GELU_TABLE_MIN_ELEMS=1", "FP8Q_TEST_HOOKS"])
     L = ctypes.CDLL(path)
     vp = ctypes.c_void_p
     L.fp8q_layernorm_quantize_amax.argtypes = [vp, vp, vp, ctypes.c_int64, ctypes.c_int32, vp, vp, ctypes.c_float,
@@ -81,4 +83,6 @@ def hooks_lib(tmp_path_factory):
     L.fp8q_layernorm_quantize_amax.restype = ctypes.c_int
     L.fp8q_gelu_quantize_amax.argtypes = [vp, vp, vp, ctypes.c_int64, ctypes.c_int, vp, vp, vp]
     L.fp8q_gelu_quantize_amax.restype = ctypes.c_int
+    L.fp8q_test_set_gelu_max_cluster.argtypes = [ctypes.c_int]
+    L.fp8q_test_set_gelu_max_cluster.restype = None
     return L

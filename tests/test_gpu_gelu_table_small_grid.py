@@ -103,3 +103,38 @@ def test_gelu_table_path_random_small_tensors(hooks_lib, seq_gelu, k):
     if with_y:
         assert_bf16_equal(W.bf16_bits(y), want_y, what + " y")
         check_guards(ybuf, n, off, fill=0x5A5A)
+
+
+@pytest.mark.parametrize("max_cluster,with_y", [(4, False), (2, False), (4, True), (2, True)])
+def test_gelu_table_falls_back_where_clusters_do_not_fit(hooks_lib, seq_gelu, max_cluster, with_y):
+    """Where no cluster of a table kernel's size fits, the call takes a smaller cluster
+    (clusters of 4 instead of 8) or else the direct kernel, with the same results: here the
+    test build makes clusters above `max_cluster` count as not fitting."""
+    dev = torch.device("cuda:0")
+    n, off = 16 * 5000 + 9, 3
+    g = torch.Generator(device=dev)
+    g.manual_seed(max_cluster * 10 + with_y)
+    hbuf = (torch.randn(n + 16, generator=g, device=dev) * 3.0).to(torch.bfloat16)
+    h = hbuf[off: off + n]
+    qbuf, q = guarded(n, torch.uint8, dev, off)
+    ybuf, y = guarded(n, torch.bfloat16, dev, off, fill=0x5A5A) if with_y else (None, None)  # aligned like h
+    am = torch.zeros(1, device=dev)
+    scale = np.float32(0.0123)
+    sc = torch.full((1,), float(scale), device=dev)
+    st = torch.cuda.current_stream().cuda_stream
+    hooks_lib.fp8q_test_set_gelu_max_cluster(max_cluster)
+    try:
+        status = hooks_lib.fp8q_gelu_quantize_amax(h.data_ptr(), y.data_ptr() if with_y else None, q.data_ptr(),
+                                                   n, fp8q.E4M3FN, sc.data_ptr(), am.data_ptr(), st)
+        torch.cuda.synchronize()
+    finally:
+        hooks_lib.fp8q_test_set_gelu_max_cluster(0)
+    assert status == 0
+    want_y = seq_gelu(W.bf16_bits(h))
+    rq, ra = oracle.quantize_amax(want_y, fp8q.E4M3FN, scale)
+    assert_codes_equal(q.cpu().numpy(), rq, fp8q.E4M3FN, "fallback codes")
+    assert_f32_equal([float(am)], [ra], "fallback amax")
+    check_guards(qbuf, n, off)
+    if with_y:
+        assert_bf16_equal(W.bf16_bits(y), want_y, "fallback y")
+        check_guards(ybuf, n, off, fill=0x5A5A)
