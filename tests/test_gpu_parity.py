@@ -405,7 +405,8 @@ def test_scale_update_specials(dev):
 # --------------------------------------------------------------------------- limits and capture
 
 def test_more_than_2_pow_31_elements(dev):
-    """Tile and index arithmetic stays 64-bit: quantize and dequantize 2^31 + 4099 elements."""
+    """Tile and index arithmetic stays 64-bit: quantize, dequantize, the fused quantize ->
+    dequantize and the ragged quantize over 2^31 + 4099 elements."""
     n = (1 << 31) + 4099
     g = torch.Generator(device=dev)
     g.manual_seed(31)
@@ -429,7 +430,21 @@ def test_more_than_2_pow_31_elements(dev):
         rq, _ = par_quantize_amax(W.bf16_bits(x[i:i + m]), E4M3FN, scale)
         assert_codes_equal(q[i:i + m].cpu().numpy(), rq, E4M3FN, f"n > 2^31, chunk at {i}")
         assert_bf16_equal(W.bf16_bits(y[i:i + m]), par_dequantize(rq, E4M3FN, scale), f"dequant chunk at {i}")
-    del x, q, y
+    # the fused quantize -> dequantize equals the two calls, and the ragged path over a list of
+    # a small tensor and this one equals the single calls
+    y2 = torch.empty(n, dtype=torch.bfloat16, device=dev)
+    am2 = f32(0.0, dev)
+    fp8q.fp8q_qdq_amax(x, y2, E4M3FN, f32(scale, dev), am2)
+    small = x[: 3 * 16384 + 5].clone()
+    qs, q2 = torch.empty_like(small, dtype=torch.uint8), torch.empty_like(q)
+    ams = torch.zeros(2, device=dev)
+    fp8q.fp8q_multi_quantize_amax([small, x], [qs, q2], E4M3FN, [f32(scale, dev), f32(scale, dev)],
+                                  [ams[0:1], ams[1:2]])
+    torch.cuda.synchronize()
+    assert torch.equal(y2.view(torch.int16), y.view(torch.int16)) and float(am2) == 1000.0
+    assert torch.equal(q2, q) and float(ams[1]) == 1000.0
+    assert torch.equal(qs, q[: small.numel()])
+    del x, q, y, y2, q2
     torch.cuda.empty_cache()
 
 
