@@ -266,13 +266,14 @@ fp8q_status fp8q_gelu_quantize_amax(const void* h_bf16, void* y_bf16, uint8_t* q
  * or NULL when only the FP8 codes are wanted.  q: rows * hidden bytes
  * (device).  gamma, beta: hidden floats each (device).  These five must be
  * 16-byte aligned.  scale, amax: as for fp8q_quantize_amax.  hidden: a
- * multiple of 16 from 16 to 16384.
+ * multiple of 16 from 16 to 32768 (rows longer than 16384 take 4 * hidden
+ * bytes of shared memory per CTA, one CTA per SM).
  * The first call on a device also sets the kernel's shared-memory limit
  * (cudaFuncSetAttribute) and reads its occupancy.  Those are host-side calls,
  * not stream work, so that first call may itself be captured in a CUDA graph.
  * Errors: FP8Q_ERR_INVALID_ARG for a bad fmt, rows < 0, hidden < 16 or not a
  * multiple of 16, a NULL pointer (other than y_bf16) with rows > 0, or a
- * misaligned scale/amax; FP8Q_ERR_UNSUPPORTED for hidden > 16384 or a
+ * misaligned scale/amax; FP8Q_ERR_UNSUPPORTED for hidden > 32768 or a
  * misaligned x_bf16, y_bf16, q, gamma or beta; FP8Q_ERR_CUDA if the launch
  * or its first-call set-up fails.  rows == 0 launches nothing.
  */

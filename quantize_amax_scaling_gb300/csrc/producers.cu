@@ -542,7 +542,7 @@ __global__ void __launch_bounds__(kGeluCodeTableThreads, 1) gelu_code_table_kern
 // LayerNorm producer fused with quantize + amax
 //
 // Flax's default LayerNorm in binary32, row by row (H elements, a multiple of
-// 16, at most 16384): mean = S / H, var = max(0, Q / H - mean^2) (a NaN kept),
+// 16, at most 32768): mean = S / H, var = max(0, Q / H - mean^2) (a NaN kept),
 // rstd = 1 / sqrt(var + eps), y = (x - mean) * (rstd * gamma) + beta rounded
 // to bf16, then the quantize path on y: FP8 codes of y / scale and
 // amax = max |y|.
@@ -580,13 +580,17 @@ __global__ void __launch_bounds__(kGeluCodeTableThreads, 1) gelu_code_table_kern
 // (FP8Q_TEST_LN_GIVE_UP_AT) makes the wait of a CTA's batch of that index
 // report failure, to exercise the path without any fault.
 
-constexpr int kLnMaxH = 16384;
-constexpr int kLnMaxHalfPerThread = 8;  // the largest HPT instantiated
+constexpr int kLnMaxH = 32768;
+constexpr int kLnMaxHalfPerThread = 16;  // the largest HPT instantiated
 static_assert(kLnMaxH <= kThreads * 8 * kLnMaxHalfPerThread, "every half-vector of a row has a thread");
 constexpr int kLnWarps = kThreads / 32;
 constexpr int kLnMaxBatch = kLnWarps;
 constexpr int kLnBufs = 2;                      // batches in the ring
-constexpr uint32_t kLnRingBytes = 64u * 1024u;  // ring per CTA (both batches)
+constexpr uint32_t kLnRingBytes = 64u * 1024u;  // ring per CTA (both batches), rows up to 16384
+// Longer rows (batches of one row) take a ring of two rows: 4 H bytes, 128 KB at most.
+__host__ __device__ constexpr uint32_t ln_ring_bytes(int H) {
+    return kLnBufs * 2u * (uint32_t)H > kLnRingBytes ? kLnBufs * 2u * (uint32_t)H : kLnRingBytes;
+}
 constexpr int kLnTimeoutBits = 0x7FFFFFFF;
 
 struct LnArgs {
@@ -868,10 +872,12 @@ fp8q_status launch_layernorm_hpt(LnArgs a, cudaStream_t s) {
     static ResidentCache cache;
     auto kern = layernorm_quantize_amax_kernel<FMT, WRITE_Y, HPT>;
     const uint32_t row_bytes = 2u * (uint32_t)a.H;
-    uint32_t batch = kLnRingBytes / (kLnBufs * row_bytes);
+    uint32_t batch = ln_ring_bytes(a.H) / (kLnBufs * row_bytes);
     batch = batch >= 8 ? 8 : batch >= 4 ? 4 : batch >= 2 ? 2 : 1;  // a power of two: 8 / batch warps a row
     a.batch = (int32_t)batch;
     const uint32_t smem = kLnBufs * batch * row_bytes;
+    // the most any H of this instance takes: the resident count holds for all of them
+    const uint32_t smem_max = ln_ring_bytes(HPT * kThreads * 8 < kLnMaxH ? HPT * kThreads * 8 : kLnMaxH);
     int dev = 0, ctas = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err == cudaSuccess) {
@@ -880,9 +886,9 @@ fp8q_status launch_layernorm_hpt(LnArgs a, cudaStream_t s) {
             if (cache.e[k].dev == dev) ctas = cache.e[k].ctas;
         if (ctas == 0) {
             int per_sm = 0, sms = 0;
-            err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLnRingBytes);
+            err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_max);
             if (err == cudaSuccess)
-                err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, kLnRingBytes);
+                err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem_max);
             if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
             if (err == cudaSuccess && per_sm < 1) err = cudaErrorInvalidConfiguration;
             if (err == cudaSuccess) {
@@ -903,7 +909,8 @@ fp8q_status launch_layernorm(const LnArgs& a, cudaStream_t s) {
     if (hpt <= 1) return launch_layernorm_hpt<FMT, WRITE_Y, 1>(a, s);
     if (hpt <= 2) return launch_layernorm_hpt<FMT, WRITE_Y, 2>(a, s);
     if (hpt <= 4) return launch_layernorm_hpt<FMT, WRITE_Y, 4>(a, s);
-    return launch_layernorm_hpt<FMT, WRITE_Y, 8>(a, s);
+    if (hpt <= 8) return launch_layernorm_hpt<FMT, WRITE_Y, 8>(a, s);
+    return launch_layernorm_hpt<FMT, WRITE_Y, 16>(a, s);
 }
 
 // Launch a table kernel on the clusters that fit at once (at most one CTA per

@@ -108,7 +108,7 @@ def test_layernorm_quantize_argument_errors(L):
     assert call(3, -1) == INVALID
     for h in (0, 8, 24, -16):                        # hidden >= 16 and a multiple of 16
         assert call(4, h) == INVALID
-    assert call(4, 16384 + 16) == UNSUPPORTED        # longest row one CTA holds is 16384
+    assert call(4, 32768 + 16) == UNSUPPORTED        # longest row one CTA holds is 32768
     assert call(8, 2) == INVALID
     for i in (0, 2, 5, 6, 9, 10):
         assert call(i, None) == INVALID

@@ -346,12 +346,13 @@ def check_layernorm(x, gamma, beta, fmt, scale, dev, eps=1e-6, amax0=0.0, what="
 
 
 LN_SHAPES = [(1, 16), (3, 272), (2, 4096), (2, 16384), (7, 4112), (300, 48), (5, 4080), (4, 8208),
-             (33, 1024), (2, 12288), (9, 2064), (17, 6160)]
+             (33, 1024), (2, 12288), (9, 2064), (17, 6160),
+             (3, 16400), (5, 18432), (2, 24576), (4, 32768)]   # rows longer than 16384: one row a batch
 
 
 @pytest.mark.parametrize("rows,H", LN_SHAPES)
 def test_layernorm_shapes(dev, rows, H):
-    """Row lengths from 16 to 16384 (one to four warps a row, ragged last vectors)."""
+    """Row lengths from 16 to 32768 (one to eight warps a row in the statistics, ragged last vectors)."""
     x = W.residual_stream(seed=rows * 7919 + H, device=dev, shape=(rows, H))
     gamma, beta = W.layernorm_params(H, seed=H, device=dev)
     for k, (fmt, scale) in enumerate([(E4M3FN, 0.0123), (E5M2, 1.0), (E4M3FN, 2.0 ** 70), (E5M2, 3.3e-3)]):
@@ -360,10 +361,10 @@ def test_layernorm_shapes(dev, rows, H):
 
 @pytest.mark.parametrize("k", range(12))
 def test_layernorm_random_shapes(dev, k):
-    """Seeded random row counts and lengths (H a multiple of 16 up to 16384), a scale per
+    """Seeded random row counts and lengths (H a multiple of 16 up to 32768), a scale per
     case (slow-path ones too) and both formats, on the LayerNorm input workload's rows."""
     rng = np.random.default_rng(500 + k)
-    H = 16 * int(rng.integers(1, 1025))
+    H = 16 * int(rng.integers(1, 2049))
     rows = int(rng.integers(1, max(2, min(600, (1 << 21) // H))))
     x = W.residual_stream(seed=900 + k, device=dev, shape=(rows, H))
     gamma, beta = W.layernorm_params(H, seed=k, device=dev)
@@ -372,7 +373,8 @@ def test_layernorm_random_shapes(dev, k):
     check_layernorm(x, gamma, beta, fmt, scale, dev, amax0=0.1 * (k % 3), what=f"{rows}x{H} scale {scale}")
 
 
-@pytest.mark.parametrize("rows,H", [(20000, 48), (5000, 4096), (3000, 8192), (1000, 16384), (7001, 272)])
+@pytest.mark.parametrize("rows,H", [(20000, 48), (5000, 4096), (3000, 8192), (1000, 16384), (7001, 272),
+                                    (600, 32768)])
 def test_layernorm_many_rows(dev, rows, H):
     """More rows than the persistent grid has warps (or warp groups), so each one loops."""
     x = W.residual_stream(seed=rows + H, device=dev, shape=(rows, H))
