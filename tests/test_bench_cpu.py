@@ -107,6 +107,8 @@ def test_compact_rows_and_detail_file(tmp_path):
                     "ragged_12_frac": 1.04, "qdq_frac": 0.99, "gelu_codes_frac": 0.82,
                     "layernorm_codes_frac": 0.6, "ring_update_us": 2.9, "ring_update_us_eager": 7.6}
     assert "ring_update_us" not in bench.compact_rows(kernels, nxt, other)
+    other["mlp_activation"]["same_bytes_library"] = {"device_copy": {"frac_of_peak": 0.88}}
+    assert bench.compact_rows(kernels, nxt, other)["mlp_same_bytes_copy_frac"] == 0.88
     assert bench.compact_rows(kernels, None, None) == {"multi_quantize_frac": 0.95, "dequantize_frac": 0.94}
     p = tmp_path / "sub" / "detail.json"
     where = bench.write_detail({"a": 1}, str(p))
