@@ -388,6 +388,8 @@ def run_gpu(args, ws, rank, local):
         "scale_update_us": upd_graph if upd_graph is not None else round(avg["amax_scale_update"], 3),
         "scale_update_us_eager": round(avg["amax_scale_update"], 3),
         "scale_update_launches": 1,
+        # what a one-element torch fill costs in the update's place in the same graphs
+        "graph_node_floor_us": graph["one_element_fill_us_after_dequantize"] if graph else None,
         "roofline": {"kernel": "quantize_amax_kernel 8192x16384", "bound": "hbm", "achieved": round(q_gbs, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(q_gbs / peak, 4), "traffic": traffic,
                      "peak_source": "measured" if peak_src == "measured" else "fallback"},
@@ -489,13 +491,17 @@ def measure_graph(args, step, stream, dev):
     sc, si = step.scale.clone(), step.scale_inv.clone()
     ring = lambda: f.fp8q_amax_scale_update_ring(ring_hist, head, step.amax_new, sc, si, f.E4M3FN,
                                                  f.ALGO_MAX, 0, step.slot_format, st)
+    tiny = torch.zeros(1, device=dev)
     deq_us = timed(deq, 100, 5)
     pair_us = timed(lambda: (deq(), upd()), 100, 5)
     ring_pair_us = timed(lambda: (deq(), ring()), 100, 5)
+    # the same difference for a one-element torch fill: what any kernel node costs there
+    floor_us = timed(lambda: (deq(), tiny.zero_()), 100, 5)
     return {"ms_per_step": round(step_us / 1e3, 4), "replays_of_step": reps,
             "GB/s": round(STEP_BYTES / (step_us * 1e-6) / 1e9, 1),
             "scale_update_us_after_dequantize": round(pair_us - deq_us, 3),
             "ring_update_us_after_dequantize": round(ring_pair_us - deq_us, 3),
+            "one_element_fill_us_after_dequantize": round(floor_us - deq_us, 3),
             "how": "one step captured as a CUDA graph, its kernels in launch order (no branches), "
                    "CUDA events around the replay; the update's time is (dequantize+update) pairs "
                    "minus dequantize alone, both as graphs"}

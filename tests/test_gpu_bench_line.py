@@ -33,6 +33,8 @@ def test_bench_prints_one_line_with_the_metric_and_its_evidence(tmp_path):
     # a streaming kernel cannot beat the copy peak by much, nor should it fall far below it
     assert 0.5 < r["frac"] < 1.2 and 0.5 < d["quantize_amax_frac"] < 1.2
     assert 0 < d["scale_update_us"] < 20
+    if d.get("graph_node_floor_us") is not None:   # a one-element fill in the update's place
+        assert 0 < d["graph_node_floor_us"] < d["scale_update_us"]
     for k, v in d["rows"].items():
         assert v > 0, k
     assert 0.5 < d["value"] / r["peak"] < 1.3      # the whole step, GB/s against the same peak
