@@ -108,7 +108,7 @@ def test_quantize_ragged_sizes_offsets_with_canaries(dev, n):
                                      (2560 * 16384, 0, 0), (2560 * 16384 + 16, 0, 0), (2560 * 16384 + 16, 5, 5),
                                      (2560 * 16384 - 1, 7, 7)])
 def test_quantize_both_grids_around_the_threshold(dev, n, xo, qo):
-    """Single tensors of up to 2560 tiles take the persistent grid of balanced ranges,
+    """Single tensors of up to 2560 tiles take the persistent grid-stride grid,
     larger ones one CTA per tile: both sides of the switch, with heads and tails."""
     g = torch.Generator(device=dev)
     g.manual_seed(n % 100003)
