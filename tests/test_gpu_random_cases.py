@@ -1,4 +1,5 @@
-"""Seeded random cases for the streaming calls, every element against the oracle.
+"""Seeded random cases for the streaming calls and the scale updates, every element
+against the oracle.
 
 Each case draws its size log-uniformly from 1 element (or from 2^15) to 2^26.5 (so that
 every grid form and vector/scalar split comes up: one CTA per tile, the persistent
@@ -7,7 +8,9 @@ grid-stride grid, heads and tails), element offsets of input and output from 0 t
 (a third from the special and slow-path scales, the rest 2^U(-40, 40)), an amax seed,
 and data of a random magnitude with random special values sprinkled in (signed zeros,
 infinities, NaN, bf16 subnormals, the largest finite bf16).  Outputs sit between canary
-guards.  The case parameters come from fixed seeds, so every run draws the same cases.
+guards.  The scale updates draw the history's length and slot count, the options, the
+amax distribution with specials, the scales and (ring) the heads, corrupt ones included.
+The case parameters come from fixed seeds, so every run draws the same cases.
 """
 import math
 
@@ -19,6 +22,7 @@ from gpu_helpers import (SCALES_ALL, assert_bf16_equal, assert_f32_equal, bf16_b
                          check_quantize_full, combine_amax, f32, guarded, par_dequantize, par_qdq_amax,
                          par_quantize_amax, assert_codes_equal)
 from quantize_amax_scaling_gb300 import fp8q
+from test_gpu_parity import _ring_case, _update_case
 
 pytestmark = pytest.mark.gpu
 
@@ -173,3 +177,63 @@ def test_random_multi_tensor_list(dev, c):
         want.setdefault(owner[i], []).append(ra)
     for o, vals in want.items():
         assert_f32_equal([got_am[o]], [combine_amax(vals)], f"amax {o}")
+
+
+# --------------------------------------------------------------------------- scale update
+
+def draw_update(seed):
+    """A random history (1 to ~4700 rows, 1 to ~1200 slots), its specials, the options."""
+    rng = np.random.default_rng(seed)
+    H = max(1, int(2.0 ** rng.uniform(0, 12.2)))
+    S = max(1, int(2.0 ** rng.uniform(0, 10.2)))
+    return dict(H=H, S=S, algo=int(rng.integers(2)), fmt=E4M3FN if rng.random() < 0.5 else E5M2,
+                margin=int(rng.choice([-64, -3, -1, 0, 0, 1, 2, 7, 64])), per_slot=rng.random() < 0.5,
+                steps=int(rng.integers(1, 4)), offset=int(rng.random() < 0.2), data_seed=seed * 7 + 5)
+
+
+def update_inputs(c):
+    """lognormal history and new amaxes with 5% zeros and a few specials (NaN, inf, negative,
+    subnormal, near the float32 top), scales from 2^U(-10, 10), slot formats with a few
+    unknown codes (whose slots keep their scales)."""
+    rng = np.random.default_rng(c["data_seed"])
+    H, S = c["H"], c["S"]
+    sigma = rng.uniform(0.5, 4.0)
+    hist = np.exp(rng.normal(0, sigma, (H, S))).astype(np.float32)
+    new = np.exp(rng.normal(0, sigma, S)).astype(np.float32)
+    hist[rng.random((H, S)) < 0.05] = 0.0
+    new[rng.random(S) < 0.05] = 0.0
+    specials = np.array([np.nan, np.inf, -1.5, 1e-45, 3e38, 0.0], np.float32)
+    for arr in (hist.reshape(-1), new):
+        k = int(rng.integers(0, 4))
+        arr[rng.integers(0, arr.size, k)] = specials[rng.integers(0, specials.size, k)]
+    scale0 = (2.0 ** rng.uniform(-10, 10, S)).astype(np.float32)
+    sf = None
+    if c["per_slot"]:
+        sf = rng.integers(0, 2, S).astype(np.uint8)
+        sf[rng.random(S) < 0.05] = 7
+    return hist, new, scale0, sf
+
+
+UPDATE_CASES = [draw_update(5000 + i) for i in range(24)]
+
+
+def update_id(c):
+    return f"{c['H']}x{c['S']}-a{c['algo']}-f{c['fmt']}-m{c['margin']}-p{int(c['per_slot'])}-o{c['offset']}"
+
+
+@pytest.mark.parametrize("c", UPDATE_CASES, ids=update_id)
+def test_random_scale_update(dev, c):
+    hist, new, scale0, sf = update_inputs(c)
+    _update_case(dev, hist, new, fmt=c["fmt"], algo=c["algo"], margin=c["margin"], slot_format=sf,
+                 steps=c["steps"], scale0=scale0, hist_offset=c["offset"])
+
+
+@pytest.mark.parametrize("c", UPDATE_CASES, ids=update_id)
+def test_random_ring_update(dev, c):
+    hist, new, scale0, sf = update_inputs(c)
+    rng = np.random.default_rng(c["data_seed"] + 1)
+    head = rng.integers(0, c["H"], c["S"]).astype(np.int32)
+    bad = rng.random(c["S"]) < 0.05          # corrupt heads: those slots stay untouched
+    head[bad] = rng.choice(np.array([-1, c["H"], 1 << 30], np.int32), int(bad.sum()))
+    _ring_case(dev, hist, head, new, algo=c["algo"], margin=c["margin"], slot_format=sf,
+               steps=c["steps"], scale0=scale0, hist_offset=c["offset"])
