@@ -9,7 +9,8 @@ grid-stride grid, heads and tails), element offsets of input and output from 0 t
 and data of a random magnitude with random special values sprinkled in (signed zeros,
 infinities, NaN, bf16 subnormals, the largest finite bf16).  Outputs sit between canary
 guards.  The scale updates draw the history's length and slot count, the options, the
-amax distribution with specials, the scales and (ring) the heads, corrupt ones included.
+amax distribution with specials, the scales and (ring) the heads, corrupt ones included;
+the ring update fused with the next quantize draws those, the slot and the tensor's size.
 The case parameters come from fixed seeds, so every run draws the same cases.
 """
 import math
@@ -22,7 +23,7 @@ from gpu_helpers import (SCALES_ALL, assert_bf16_equal, assert_f32_equal, bf16_b
                          check_quantize_full, combine_amax, f32, guarded, par_dequantize, par_qdq_amax,
                          par_quantize_amax, assert_codes_equal)
 from quantize_amax_scaling_gb300 import fp8q
-from test_gpu_parity import _ring_case, _update_case
+from test_gpu_parity import _fused_case, _ring_case, _update_case
 
 pytestmark = pytest.mark.gpu
 
@@ -237,3 +238,24 @@ def test_random_ring_update(dev, c):
     head[bad] = rng.choice(np.array([-1, c["H"], 1 << 30], np.int32), int(bad.sum()))
     _ring_case(dev, hist, head, new, algo=c["algo"], margin=c["margin"], slot_format=sf,
                steps=c["steps"], scale0=scale0, hist_offset=c["offset"])
+
+
+def draw_fused(seed):
+    rng = np.random.default_rng(seed)
+    H = max(1, int(2.0 ** rng.uniform(0, 11)))
+    S = max(1, int(2.0 ** rng.uniform(0, 10.2)))
+    n = 0 if rng.random() < 0.1 else draw_size(rng, 23)
+    return dict(H=H, S=S, slot=int(rng.integers(S)), n=n, algo=int(rng.integers(2)),
+                margin=int(rng.choice([-3, 0, 0, 1, 5])), per_slot=rng.random() < 0.5,
+                steps=int(rng.integers(1, 4)), seed=seed)
+
+
+FUSED_CASES = [draw_fused(6000 + i) for i in range(16)]
+
+
+@pytest.mark.parametrize("c", FUSED_CASES, ids=lambda c: f"{c['H']}x{c['S']}-slot{c['slot']}-n{c['n']}")
+def test_random_ring_update_quantize(dev, c):
+    """The ring update of every slot fused with the quantize of x by one slot's new scale,
+    chained over 1 to 3 steps, against the oracle's update followed by its quantize."""
+    _fused_case(dev, c["H"], c["S"], c["slot"], c["n"], c["algo"], c["margin"], c["per_slot"],
+                steps=c["steps"], seed=c["seed"])
