@@ -1232,7 +1232,8 @@ def run_reference(args):
 
 
 CASES = ("quantize_8192x16384", "quantize_8192x4096", "dequantize_8192x16384", "update_576x1024",
-         "gelu_8192x16384", "gelu_y_8192x16384", "layernorm_8192x4096", "qdq_8192x16384")
+         "gelu_8192x16384", "gelu_y_8192x16384", "layernorm_8192x4096", "layernorm_4096x8192",
+         "qdq_8192x16384")
 
 
 def run_case(name: str, launches: int):
@@ -1274,8 +1275,8 @@ def run_case(name: str, launches: int):
         q = torch.empty(N_ACT, dtype=torch.uint8, device=dev)
         y = torch.empty(N_ACT, dtype=torch.bfloat16, device=dev) if name == "gelu_y_8192x16384" else None
         launch = lambda: f.fp8q_gelu_quantize_amax(h, y, q, f.E4M3FN, sc, am)
-    elif name == "layernorm_8192x4096":
-        x = W.residual_stream(device=dev)
+    elif name in ("layernorm_8192x4096", "layernorm_4096x8192"):
+        x = W.residual_stream(device=dev, shape=(8192, 4096) if name == "layernorm_8192x4096" else (4096, 8192))
         gam, bet = W.layernorm_params(x.shape[1], device=dev)
         q = torch.empty(x.shape, dtype=torch.uint8, device=dev)
         launch = lambda: f.fp8q_layernorm_quantize_amax(x, None, q, gam, bet, f.E4M3FN, sc, am)

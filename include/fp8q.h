@@ -250,8 +250,8 @@ fp8q_status fp8q_gelu_quantize_amax(const void* h_bf16, void* y_bf16, uint8_t* q
  * with S = sum x and Q = sum x^2.  Precision: y is the bf16 rounding of a
  * value within a stated bound of the exact (float64) LayerNorm; the bound
  * follows binary32 error analysis with row sums whose longest chain of
- * additions is at most 32 (rows are summed in a fixed order, so a call is
- * reproducible bit for bit), and y is that exact value rounded once to bf16
+ * additions is at most hidden / 128 + 32 (rows are summed in a fixed order, so
+ * a call is reproducible bit for bit), and y is that exact value rounded once to bf16
  * unless it lies close to a bf16 rounding boundary.  The codes and the amax
  * are always exactly those of quantizing the y returned.  A NaN or infinite
  * x makes its row's y NaN.
@@ -266,8 +266,12 @@ fp8q_status fp8q_gelu_quantize_amax(const void* h_bf16, void* y_bf16, uint8_t* q
  * or NULL when only the FP8 codes are wanted.  q: rows * hidden bytes
  * (device).  gamma, beta: hidden floats each (device).  These five must be
  * 16-byte aligned.  scale, amax: as for fp8q_quantize_amax.  hidden: a
- * multiple of 16 from 16 to 32768 (rows longer than 16384 take 4 * hidden
- * bytes of shared memory per CTA, one CTA per SM).
+ * multiple of 16 from 16 to 32768.  Rows longer than 4096 run on
+ * thread-block clusters of ceil(hidden / 4096) CTAs, each CTA a column slice
+ * (up to 96 KB of shared memory); where no cluster of that size fits on the
+ * device, one CTA takes each batch of rows instead (rows longer than 16384
+ * then take 4 * hidden bytes of shared memory, one CTA per SM).  Both give y
+ * within the same bound, not always the same bits.
  * The first call on a device also sets the kernel's shared-memory limit
  * (cudaFuncSetAttribute) and reads its occupancy.  Those are host-side calls,
  * not stream work, so that first call may itself be captured in a CUDA graph.

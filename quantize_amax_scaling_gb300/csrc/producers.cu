@@ -605,6 +605,7 @@ struct LnArgs {
     int32_t H;
     int32_t batch;  // rows per batch: 1, 2, 4 or 8
     float eps;
+    int32_t slice_half;  // cluster kernel: half-vectors of 8 per CTA's column slice
 };
 
 // Streaming stores whose target this kernel never reads back: no memory
@@ -693,20 +694,20 @@ __device__ __forceinline__ void load4f2(const float* p, float2 (&d)[4]) {
     d[3] = make_float2(v.z, v.w);
 }
 
-// Phase 2 over one batch: rows two at a time.
+// Phase 2 over one batch: rows two at a time.  The staged rows are
+// `row_bytes` apart in shared memory and hold the `nh` half-vectors that
+// start at column col0 of the row (the whole row, or a cluster CTA's slice).
 template <int FMT, bool WRITE_Y, int HPT, bool FAST>
 __device__ __forceinline__ void ln_emit_batch(const LnArgs& a, const uint8_t* base, const float2* stats, int nr,
                                               int64_t r0, const float2 (&gr)[HPT <= 2 ? HPT : 1][4],
                                               const float2 (&br)[HPT <= 2 ? HPT : 1][4], const QScale& c,
-                                              uint32_t& m2) {
+                                              uint32_t& m2, uint32_t row_bytes, int nh, int col0) {
     constexpr bool kGammaInRegs = (HPT <= 2);
-    const int nh = a.H / 8;
-    const uint32_t row_bytes = 2u * (uint32_t)a.H;
     for (int r = 0; r < nr; r += 2) {
         const bool pair = r + 1 < nr;
         const float2 s0 = stats[r], s1 = stats[pair ? r + 1 : r];
         const uint8_t* srow = base + (size_t)r * row_bytes;
-        const int64_t row_off = (r0 + r) * a.H;
+        const int64_t row_off = (r0 + r) * a.H + col0;
 #pragma unroll
         for (int i = 0; i < HPT; ++i) {
             const int u = threadIdx.x + i * kThreads;
@@ -722,8 +723,8 @@ __device__ __forceinline__ void ln_emit_batch(const LnArgs& a, const uint8_t* ba
                         b[e] = br[kGammaInRegs ? i : 0][e];
                     }
                 } else {
-                    load4f2(a.gamma + 8 * u, g);
-                    load4f2(a.beta + 8 * u, b);
+                    load4f2(a.gamma + col0 + 8 * u, g);
+                    load4f2(a.beta + col0 + 8 * u, b);
                 }
                 const int64_t off = row_off + 8 * u;
                 ln_out8<FMT, WRITE_Y, FAST>(a, w0, g, b, s0, c, off, m2);
@@ -731,6 +732,61 @@ __device__ __forceinline__ void ln_emit_batch(const LnArgs& a, const uint8_t* ba
             }
         }
     }
+}
+
+// Phase 1 for one staged row of nv8 half-vectors: the sums S = sum x and
+// Q = sum x^2 of the row's warps (group prow, wpr warps, this one ppart),
+// each warp in four chains per lane, folded, then over the lanes (xor
+// butterfly: every lane gets the same bits) and, for wpr > 1, the group's
+// warp totals added in warp order after a named barrier.  The group's first
+// warp returns the row's totals; a warp whose copy did not arrive reads nothing.
+// With kGroupOk, group_ok (for the group's first warp) also says whether every
+// warp of the group saw its copy arrive.
+template <bool kGroupOk = false>
+__device__ __forceinline__ void ln_row_sums(const uint8_t* xr, int nv8, bool warp_arrived, int lane, int warp,
+                                            int prow, int ppart, int wpr, float2* part, float& S, float& Q,
+                                            uint32_t* warp_ok = nullptr, bool* group_ok = nullptr) {
+    float s[4] = {0.0f, 0.0f, 0.0f, 0.0f}, q[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    for (int j = lane + 32 * ppart; warp_arrived && j < nv8; j += 32 * wpr) {
+        const uint4 w = *reinterpret_cast<const uint4*>(xr + 16 * j);
+        acc_bf16<true>(w.x, s[0], q[0]);
+        acc_bf16<true>(w.y, s[1], q[1]);
+        acc_bf16<true>(w.z, s[2], q[2]);
+        acc_bf16<true>(w.w, s[3], q[3]);
+        acc_bf16<false>(w.x, s[0], q[0]);
+        acc_bf16<false>(w.y, s[1], q[1]);
+        acc_bf16<false>(w.z, s[2], q[2]);
+        acc_bf16<false>(w.w, s[3], q[3]);
+    }
+    S = __fadd_rn(__fadd_rn(s[0], s[1]), __fadd_rn(s[2], s[3]));
+    Q = __fadd_rn(__fadd_rn(q[0], q[1]), __fadd_rn(q[2], q[3]));
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        S = __fadd_rn(S, __shfl_xor_sync(0xFFFFFFFFu, S, o));
+        Q = __fadd_rn(Q, __shfl_xor_sync(0xFFFFFFFFu, Q, o));
+    }
+    if (kGroupOk) *group_ok = warp_arrived;
+    if (wpr > 1) {
+        if (lane == 0) {
+            part[warp] = make_float2(S, Q);
+            if (kGroupOk) warp_ok[warp] = warp_arrived ? 1u : 0u;
+        }
+        named_sync(1 + prow, 32 * wpr);
+        if (ppart == 0) {  // the row's warp totals, in warp order
+            for (int p = 1; p < wpr; ++p) {
+                S = __fadd_rn(S, part[warp + p].x);
+                Q = __fadd_rn(Q, part[warp + p].y);
+                if (kGroupOk) *group_ok = *group_ok && warp_ok[warp + p] != 0;
+            }
+        }
+    }
+}
+
+// (-mean, rstd) of a row of H elements from its sums.
+__device__ __forceinline__ float2 ln_row_stats(float S, float Q, float Hf, float eps) {
+    const float mean = __fdiv_rn(S, Hf);
+    const float var = max_nan_f32(__fsub_rn(__fdiv_rn(Q, Hf), __fmul_rn(mean, mean)), 0.0f);
+    return make_float2(-mean, __frsqrt_rn(__fadd_rn(var, eps)));
 }
 
 // HPT: most 8-element half-vectors a thread owns per row (ceil(H / 2048)).
@@ -795,46 +851,14 @@ __global__ void __launch_bounds__(kThreads, 2) layernorm_quantize_amax_kernel(co
         // CTA then agrees on the outcome at its barrier below.
         const bool warp_arrived = __all_sync(0xFFFFFFFFu, arrived);
         if (prow < nr) {
-            const uint8_t* xr = base + (size_t)prow * row_bytes;
-            float s[4] = {0.0f, 0.0f, 0.0f, 0.0f}, q[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            for (int j = lane + 32 * ppart; warp_arrived && j < nv8; j += 32 * wpr) {
-                const uint4 w = *reinterpret_cast<const uint4*>(xr + 16 * j);
-                acc_bf16<true>(w.x, s[0], q[0]);
-                acc_bf16<true>(w.y, s[1], q[1]);
-                acc_bf16<true>(w.z, s[2], q[2]);
-                acc_bf16<true>(w.w, s[3], q[3]);
-                acc_bf16<false>(w.x, s[0], q[0]);
-                acc_bf16<false>(w.y, s[1], q[1]);
-                acc_bf16<false>(w.z, s[2], q[2]);
-                acc_bf16<false>(w.w, s[3], q[3]);
-            }
-            float S = __fadd_rn(__fadd_rn(s[0], s[1]), __fadd_rn(s[2], s[3]));
-            float Q = __fadd_rn(__fadd_rn(q[0], q[1]), __fadd_rn(q[2], q[3]));
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) {
-                S = __fadd_rn(S, __shfl_xor_sync(0xFFFFFFFFu, S, o));
-                Q = __fadd_rn(Q, __shfl_xor_sync(0xFFFFFFFFu, Q, o));
-            }
-            if (wpr > 1) {
-                if (lane == 0) part[warp] = make_float2(S, Q);
-                named_sync(1 + prow, 32 * wpr);
-                if (ppart == 0) {  // the row's warp totals, in warp order
-                    for (int p = 1; p < wpr; ++p) {
-                        S = __fadd_rn(S, part[warp + p].x);
-                        Q = __fadd_rn(Q, part[warp + p].y);
-                    }
-                }
-            }
-            if (ppart == 0 && lane == 0) {
-                const float mean = __fdiv_rn(S, Hf);
-                const float var = max_nan_f32(__fsub_rn(__fdiv_rn(Q, Hf), __fmul_rn(mean, mean)), 0.0f);
-                stats[prow] = make_float2(-mean, __frsqrt_rn(__fadd_rn(var, a.eps)));
-            }
+            float S, Q;
+            ln_row_sums(base + (size_t)prow * row_bytes, nv8, warp_arrived, lane, warp, prow, ppart, wpr, part, S, Q);
+            if (ppart == 0 && lane == 0) stats[prow] = ln_row_stats(S, Q, Hf, a.eps);
         }
         ok = __syncthreads_and(arrived) != 0;
         if (!ok) break;  // uniform
-        if (c.fast) ln_emit_batch<FMT, WRITE_Y, HPT, true>(a, base, stats, nr, r0, gr, br, c, m2);
-        else        ln_emit_batch<FMT, WRITE_Y, HPT, false>(a, base, stats, nr, r0, gr, br, c, m2);
+        if (c.fast) ln_emit_batch<FMT, WRITE_Y, HPT, true>(a, base, stats, nr, r0, gr, br, c, m2, row_bytes, nh, 0);
+        else        ln_emit_batch<FMT, WRITE_Y, HPT, false>(a, base, stats, nr, r0, gr, br, c, m2, row_bytes, nh, 0);
         __syncthreads();  // every thread is done with this slot and with stats[] and part[]
         if (threadIdx.x == 0 && k + kLnBufs < n_mine) {  // refill the slot, kLnBufs batches ahead
             const int64_t next_r0 = (blockIdx.x + (k + kLnBufs) * G) * R;
@@ -854,6 +878,190 @@ __global__ void __launch_bounds__(kThreads, 2) layernorm_quantize_amax_kernel(co
         return;
     }
     flush_amax(m2, 0u, a.amax, red);
+}
+
+// ----------------------------------------------------------------------------
+// LayerNorm rows longer than 4096, split over a thread-block cluster
+//
+// With H > 4096 a CTA of 256 threads cannot keep the gamma and beta of a whole
+// row in registers, and reading them again for every row costs more than the
+// rest of the work.  A cluster of C = ceil(H / 4096) CTAs takes each batch of
+// rows together: CTA c owns the column slice of half-vectors [c hs, (c+1) hs)
+// (hs = ceil(H / 8C), the last slice shorter), stages that slice of each of the
+// batch's rows (one bulk copy per row, all completing on the slot's mbarrier)
+// and keeps its slice's gamma and beta in registers for the whole launch.
+// Phase 1 sums its slice of each row as the single-CTA kernel does.  The
+// row's first lane then sends (S, Q, "every warp of the group saw its copy")
+// to every CTA of the cluster, itself included, with st.async: a 16-byte store
+// into the other CTA's shared memory that completes on that CTA's exchange
+// mbarrier of the batch's parity, which expects C x 16 bytes per row.  The
+// writer needs no fence, and no cluster barrier runs per batch.  Each CTA
+// waits (bounded) for its exchange barrier; the row's first lane adds the C
+// partials in rank order, so every CTA derives the same (mean, rstd) bits, and
+// checks the C flags; one CTA barrier then agrees on the outcome and
+// publishes the statistics.  Phase 2 is the single-CTA kernel's on the slice.
+// A CTA writes a peer's slot of parity p for batch j only after its own
+// exchange for batch j - 1 completed, which needed that peer's sums of batch
+// j - 1, sent after the peer had read its slot for batch j - 2: one slot per
+// parity is enough.  The longest chain of additions is the slice's plus C - 1,
+// within H / 128 + 32.  Remote stores start after a split cluster barrier that
+// every CTA enters once its mbarriers are initialised, and every CTA passes a
+// last cluster barrier before it exits, so no CTA writes into one that has
+// left.  A copy that never arrives clears its group's flag; every CTA then
+// stops at the same batch, marks amax and drains its copies.
+
+constexpr int kLnClusterMax = 8;
+constexpr int kLnSliceHalf = kThreads * 2;  // half-vectors a CTA's slice may hold (4096 columns)
+constexpr uint32_t kLnClusterRingBytes = 96u * 1024u;  // both slots at most (two CTAs an SM): batches of 8 rows up to 3072 columns
+
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
+// A 16-byte store into another CTA's shared memory that completes on an
+// mbarrier there (its expected transaction bytes): no fence on the writing side.
+__device__ __forceinline__ void st_async_v4(uint32_t addr, uint4 v, uint32_t remote_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     addr),
+                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(remote_bar)
+                 : "memory");
+}
+
+// The copies of one batch: the slice of each of its nr rows, completing on bar.
+__device__ __forceinline__ void ln_slice_batch_load(const LnArgs& a, uint8_t* dst, int64_t r0, int nr, int h0,
+                                                    uint32_t slice_bytes, uint32_t row_stride, uint64_t* bar) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"((uint32_t)nr * slice_bytes)
+                 : "memory");
+    for (int r = 0; r < nr; ++r)
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                smem_addr(dst + (size_t)r * row_stride)),
+            "l"(a.x + (r0 + r) * a.H + 8 * h0), "r"(slice_bytes), "r"(smem_addr(bar))
+            : "memory");
+}
+
+template <int FMT, bool WRITE_Y>
+__global__ void __launch_bounds__(kThreads, 2) layernorm_cluster_quantize_amax_kernel(const LnArgs a) {
+    extern __shared__ __align__(128) uint8_t ring[];  // kLnBufs batches of a.batch slices of 16 slice_half bytes
+    __shared__ uint64_t bar[kLnBufs];                        // the ring's copies
+    __shared__ uint64_t xbar[2];                             // the partial sums' arrival, by batch parity
+    __shared__ float2 part[kLnWarps];
+    __shared__ uint32_t warp_ok[kLnWarps];
+    __shared__ float2 stats[kLnMaxBatch];
+    __shared__ uint4 xpart[2][kLnClusterMax][kLnMaxBatch];  // (S, Q, group arrived, 0) of every CTA, by batch parity
+    __shared__ uint32_t red[kLnWarps];
+    const int C = (int)cluster_nctarank(), crank = (int)cluster_ctarank();
+    const int h0 = crank * a.slice_half;                        // the slice's first half-vector
+    const int nhc = min(a.slice_half, a.H / 8 - h0);           // > 0: the launch keeps every slice non-empty
+    const int R = a.batch;
+    const int wpr = kLnWarps / R;
+    const uint32_t row_stride = 16u * (uint32_t)a.slice_half;  // bytes between staged rows
+    const uint32_t slice_bytes = 16u * (uint32_t)nhc;
+    const uint32_t buf_bytes = (uint32_t)R * row_stride;
+    const int64_t nb = (a.rows + R - 1) / R;
+    const int64_t cid = blockIdx.x / C, G = gridDim.x / C;     // clusters take batches cid, cid + G, ...
+    const int64_t n_mine = (nb - 1 - cid) / G + 1;             // the launch keeps G <= nb
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int prow = warp / wpr, ppart = warp % wpr;
+
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < kLnBufs; ++b) mbar_init(&bar[b]);
+        for (int b = 0; b < 2; ++b) mbar_init(&xbar[b]);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        for (int64_t k = 0; k < kLnBufs && k < n_mine; ++k) {
+            const int64_t r0 = (cid + k * G) * R;
+            const int nr = a.rows - r0 < R ? (int)(a.rows - r0) : R;
+            ln_slice_batch_load(a, ring + (size_t)k * buf_bytes, r0, nr, h0, slice_bytes, row_stride, &bar[k]);
+        }
+    }
+    cluster_arrive_relaxed();  // after the barriers' initialisation; waited on before the first remote store
+    const QScale c = make_qscale(a.scale);
+    const float Hf = (float)a.H;
+    float2 gr[2][4], br[2][4];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int u = threadIdx.x + i * kThreads;
+        if (u < nhc) {
+            load4f2(a.gamma + 8 * (h0 + u), gr[i]);
+            load4f2(a.beta + 8 * (h0 + u), br[i]);
+        }
+    }
+    __syncthreads();  // barriers initialised before anyone waits on them
+
+    uint32_t m2 = 0;
+    bool ok = true;
+    int64_t k = 0;
+    for (; k < n_mine; ++k) {
+        const int buf = (int)(k % kLnBufs);
+        const int xp = (int)(k & 1);
+        const int64_t r0 = (cid + k * G) * R;
+        const int nr = a.rows - r0 < R ? (int)(a.rows - r0) : R;
+        const uint8_t* base = ring + (size_t)buf * buf_bytes;
+        if (threadIdx.x == 0)  // the batch's partial sums from every CTA of the cluster
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(&xbar[xp])),
+                         "r"((uint32_t)C * 16u * (uint32_t)nr)
+                         : "memory");
+        bool arrived = mbar_wait(&bar[buf], (uint32_t)((k / kLnBufs) & 1));
+#ifdef FP8Q_TEST_LN_GIVE_UP_AT
+        if (k == FP8Q_TEST_LN_GIVE_UP_AT) arrived = false;
+#endif
+        const bool warp_arrived = __all_sync(0xFFFFFFFFu, arrived);
+        const bool first = prow < nr && ppart == 0 && lane == 0;  // the lane that speaks for its row
+        if (k == 0) cluster_wait();  // every CTA of the cluster is running, its barriers initialised
+        if (prow < nr) {
+            float S, Q;
+            bool group_ok;
+            ln_row_sums<true>(base + (size_t)prow * row_stride, nhc, warp_arrived, lane, warp, prow, ppart, wpr, part,
+                              S, Q, warp_ok, &group_ok);
+            if (first) {
+                const uint32_t at = smem_addr(&xpart[xp][crank][prow]), xb = smem_addr(&xbar[xp]);
+                const uint4 v = make_uint4(__float_as_uint(S), __float_as_uint(Q), group_ok ? 1u : 0u, 0u);
+                for (int r = 0; r < C; ++r) st_async_v4(cluster_map(at, (uint32_t)r), v, cluster_map(xb, (uint32_t)r));
+            }
+        }
+        // Every CTA gets the same C x nr partials; the row's first lane adds them in
+        // rank order, and every CTA stops at the same batch if any group's copy failed.
+        bool mine_ok = mbar_wait(&xbar[xp], (uint32_t)((k >> 1) & 1));
+        if (first && mine_ok) {
+            uint4 v = xpart[xp][0][prow];
+            float Sx = __uint_as_float(v.x), Qx = __uint_as_float(v.y);
+            mine_ok = v.z != 0;
+            for (int r = 1; r < C; ++r) {
+                v = xpart[xp][r][prow];
+                Sx = __fadd_rn(Sx, __uint_as_float(v.x));
+                Qx = __fadd_rn(Qx, __uint_as_float(v.y));
+                mine_ok = mine_ok && v.z != 0;
+            }
+            stats[prow] = ln_row_stats(Sx, Qx, Hf, a.eps);
+        }
+        ok = __syncthreads_and(mine_ok) != 0;  // also publishes stats[]
+        if (!ok) break;  // uniform over the cluster (a lost exchange only after a second)
+        if (c.fast) ln_emit_batch<FMT, WRITE_Y, 2, true>(a, base, stats, nr, r0, gr, br, c, m2, row_stride, nhc, 8 * h0);
+        else        ln_emit_batch<FMT, WRITE_Y, 2, false>(a, base, stats, nr, r0, gr, br, c, m2, row_stride, nhc, 8 * h0);
+        __syncthreads();  // every thread is done with this slot and with stats[] and part[]
+        if (threadIdx.x == 0 && k + kLnBufs < n_mine) {
+            const int64_t next_r0 = (cid + (k + kLnBufs) * G) * R;
+            const int next_nr = a.rows - next_r0 < R ? (int)(a.rows - next_r0) : R;
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            ln_slice_batch_load(a, ring + (size_t)buf * buf_bytes, next_r0, next_nr, h0, slice_bytes, row_stride,
+                                &bar[buf]);
+        }
+    }
+    if (!ok) {
+        if (threadIdx.x == 0) {
+            atomicMax(reinterpret_cast<int*>(a.amax), kLnTimeoutBits);
+            for (int64_t j = k; j < n_mine && j < k + kLnBufs; ++j)
+                mbar_wait(&bar[j % kLnBufs], (uint32_t)((j / kLnBufs) & 1));
+        }
+    } else {
+        flush_amax(m2, 0u, a.amax, red);
+    }
+    // No CTA leaves while another of its cluster may still write into its shared memory.
+    cluster_arrive_relaxed();
+    cluster_wait();
 }
 
 // Resident CTAs of one kernel per device, taken on the first launch there
@@ -903,11 +1111,77 @@ fp8q_status launch_layernorm_hpt(LnArgs a, cudaStream_t s) {
     return launch_kernel(kern, dim3((unsigned)grid), dim3(kThreads), smem, s, "layernorm_quantize_amax_kernel", a);
 }
 
+#ifdef FP8Q_TEST_HOOKS  // test-only build: LayerNorm clusters larger than this count as not fitting (0: no limit)
+int g_test_ln_max_cluster = 0;
+#endif
+
+// Rows longer than 4096 on clusters of ceil(H / 4096) CTAs, each cluster taking
+// batches of rows in turn over the clusters that fit at once.  Where no cluster
+// of that size fits (a partitioned or shared GPU), this returns
+// FP8Q_ERR_UNSUPPORTED without recording a CUDA error, and the caller takes the
+// single-CTA kernel.
+template <int FMT, bool WRITE_Y>
+fp8q_status launch_layernorm_cluster(LnArgs a, cudaStream_t s) {
+    static ResidentCache cache[kLnClusterMax + 1];  // resident clusters x C, by cluster size C
+    const int nh = a.H / 8;
+    const int C = (nh + kLnSliceHalf - 1) / kLnSliceHalf;  // 2 .. 8 for 4096 < H <= 32768
+    const int hs = (nh + C - 1) / C;                       // every slice non-empty: nh > 512 (C - 1) >= C (C - 1)
+#ifdef FP8Q_TEST_HOOKS
+    if (g_test_ln_max_cluster > 0 && C > g_test_ln_max_cluster) return FP8Q_ERR_UNSUPPORTED;
+#endif
+    uint32_t batch = kLnClusterRingBytes / (kLnBufs * 16u * (uint32_t)hs);
+    batch = batch >= 8 ? 8 : batch >= 4 ? 4 : batch >= 2 ? 2 : 1;
+    a.batch = (int32_t)batch;
+    a.slice_half = hs;
+    auto kern = layernorm_cluster_quantize_amax_kernel<FMT, WRITE_Y>;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kLnClusterRingBytes;  // the most any slice takes: the resident count holds for all
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int dev = 0, ctas = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err == cudaSuccess) {
+        ResidentCache& rc = cache[C];
+        std::lock_guard<std::mutex> lock(rc.mu);
+        for (int k = 0; k < rc.n; ++k)
+            if (rc.e[k].dev == dev) ctas = rc.e[k].ctas;
+        if (ctas == 0) {
+            int clusters = 0, sms = 0;
+            err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLnClusterRingBytes);
+            if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            cfg.gridDim = dim3((unsigned)(sms / C * C));
+            if (err == cudaSuccess) err = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+            if (err == cudaSuccess) {
+                ctas = clusters > 0 ? clusters * C : -1;  // -1: no cluster of this size fits
+                if (rc.n < 32) rc.e[rc.n++] = {dev, ctas};
+            }
+        }
+    }
+    if (err != cudaSuccess) return cuda_fail(err, "layernorm_cluster_quantize_amax_kernel setup");
+    if (ctas < 0) return FP8Q_ERR_UNSUPPORTED;
+    const int64_t batches = (a.rows + batch - 1) / batch;
+    const int64_t clusters = batches < (int64_t)(ctas / C) ? batches : (int64_t)(ctas / C);
+    cfg.gridDim = dim3((unsigned)(clusters * C));
+    cfg.dynamicSmemBytes = kLnBufs * batch * 16u * (uint32_t)hs;
+    err = cudaLaunchKernelEx(&cfg, kern, a);
+    return err == cudaSuccess ? FP8Q_OK : cuda_fail(err, "layernorm_cluster_quantize_amax_kernel");
+}
+
 template <int FMT, bool WRITE_Y>
 fp8q_status launch_layernorm(const LnArgs& a, cudaStream_t s) {
     const int hpt = (a.H / 8 + kThreads - 1) / kThreads;  // half-vectors per thread
     if (hpt <= 1) return launch_layernorm_hpt<FMT, WRITE_Y, 1>(a, s);
     if (hpt <= 2) return launch_layernorm_hpt<FMT, WRITE_Y, 2>(a, s);
+    const fp8q_status st = launch_layernorm_cluster<FMT, WRITE_Y>(a, s);
+    if (st != FP8Q_ERR_UNSUPPORTED) return st;
+    // no cluster of that size fits on this device: one CTA per batch of rows
     if (hpt <= 4) return launch_layernorm_hpt<FMT, WRITE_Y, 4>(a, s);
     if (hpt <= 8) return launch_layernorm_hpt<FMT, WRITE_Y, 8>(a, s);
     return launch_layernorm_hpt<FMT, WRITE_Y, 16>(a, s);
@@ -1014,6 +1288,9 @@ extern "C" {
 // Test-only build: GELU table kernels with clusters larger than `max_cluster`
 // behave as if their clusters did not fit (0 lifts the limit).
 void fp8q_test_set_gelu_max_cluster(int max_cluster) { g_test_gelu_max_cluster = max_cluster; }
+// Test-only build: LayerNorm clusters larger than `max_cluster` behave as if
+// they did not fit (0 lifts the limit).
+void fp8q_test_set_ln_max_cluster(int max_cluster) { g_test_ln_max_cluster = max_cluster; }
 #endif
 
 fp8q_status fp8q_gelu_quantize_amax(const void* h_bf16, void* y_bf16, uint8_t* q, int64_t n,
@@ -1083,6 +1360,7 @@ fp8q_status fp8q_layernorm_quantize_amax(const void* x_bf16, void* y_bf16, uint8
     a.H = hidden;
     a.batch = 0;
     a.eps = eps;
+    a.slice_half = 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (fmt == FP8Q_E4M3FN)
         return y_bf16 ? launch_layernorm<FP8Q_E4M3FN, true>(a, s) : launch_layernorm<FP8Q_E4M3FN, false>(a, s);

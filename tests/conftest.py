@@ -67,8 +67,9 @@ def hooks_lib(tmp_path_factory):
     FP8Q_TEST_LN_GIVE_UP_AT=1 makes each LayerNorm warp's wait for its second row
     report failure; FP8Q_TEST_GELU_TABLE_MIN_ELEMS=1 sends every vector-path GELU
     tensor through the table kernel, however small; FP8Q_TEST_HOOKS exports
-    fp8q_test_set_gelu_max_cluster, which makes larger thread-block clusters count as
-    not fitting.  Loaded with ctypes; only the entry points the hook tests call are
+    fp8q_test_set_gelu_max_cluster and fp8q_test_set_ln_max_cluster, which make larger
+    thread-block clusters of the GELU table and the LayerNorm kernels count as not
+    fitting.  Loaded with ctypes; only the entry points the hook tests call are
     declared."""
     import ctypes
 
@@ -85,4 +86,6 @@ def hooks_lib(tmp_path_factory):
     L.fp8q_gelu_quantize_amax.restype = ctypes.c_int
     L.fp8q_test_set_gelu_max_cluster.argtypes = [ctypes.c_int]
     L.fp8q_test_set_gelu_max_cluster.restype = None
+    L.fp8q_test_set_ln_max_cluster.argtypes = [ctypes.c_int]
+    L.fp8q_test_set_ln_max_cluster.restype = None
     return L

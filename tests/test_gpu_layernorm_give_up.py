@@ -7,7 +7,9 @@ returns.  In correct operation every copy arrives, so this test uses the
 library built once more with the test hook FP8Q_TEST_LN_GIVE_UP_AT=1: the wait
 for each CTA's second batch then reports failure although its copy did arrive.
 The call must return, leave the marker in amax, have finished each CTA's first
-batch exactly as the normal library does, and leave the device usable.
+batch exactly as the normal library does, and leave the device usable.  Rows longer
+than 4096 run on thread-block clusters, whose CTAs agree at the cluster barrier: the
+whole cluster stops after its first batch.
 """
 import numpy as np
 import pytest
@@ -19,10 +21,10 @@ from quantize_amax_scaling_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 
 
-def test_layernorm_give_up_marks_amax_and_returns(hooks_lib):
+@pytest.mark.parametrize("rows,H", [(4096, 4096), (4096, 12288)])   # one CTA a batch; a cluster of 3 a batch
+def test_layernorm_give_up_marks_amax_and_returns(hooks_lib, rows, H):
     hooked = hooks_lib
     dev = torch.device("cuda:0")
-    rows, H = 4096, 4096
     x = W.residual_stream(seed=13, device=dev, shape=(rows, H))
     gamma, beta = W.layernorm_params(H, device=dev)
     scale = torch.full((1,), 0.03, device=dev)
