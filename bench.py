@@ -428,6 +428,8 @@ def compact_rows(kernels, next_rows, other_configs, graph=None):
         r["qdq_frac"] = next_rows["qdq_amax"]["frac_of_peak"]
         r["gelu_codes_frac"] = next_rows["gelu_quantize_amax"]["codes_only"]["frac_of_peak"]
         r["layernorm_codes_frac"] = next_rows["layernorm_quantize_amax"]["codes_only"]["frac_of_peak"]
+        if "layernorm_quantize_amax_wide" in next_rows:
+            r["layernorm_12288_codes_frac"] = next_rows["layernorm_quantize_amax_wide"]["codes_only"]["frac_of_peak"]
         if graph:
             r["ring_update_us"] = graph["ring_update_us_after_dequantize"]
         r["ring_update_us_eager"] = next_rows["amax_scale_update_ring"]["us"]
@@ -706,6 +708,26 @@ def measure_next_rows(args, step, stream, dev, peak):
                         "frac_of_peak": round(5 * n_ln / (us_lyq * 1e-6) / 1e9 / peak, 4),
                         "bytes_per_launch": 5 * n_ln},
         "unfused_torch_layer_norm_then_quantize_us": round(us_lu, 3)}
+    del xs, qs, ys
+
+    # The same producer on rows of 12288 (GPT-175B's width; thread-block clusters of 3)
+    rows_w, hid_w = 2730, 12288
+    xs = [W.residual_stream(seed=W.SEED_MLP + 20 + i, device=dev, shape=(rows_w, hid_w)) for i in range(4)]
+    gam_w, bet_w = W.layernorm_params(hid_w, device=dev)
+    qs = [torch.empty((rows_w, hid_w), dtype=torch.uint8, device=dev) for _ in range(4)]
+    ys = [torch.empty((rows_w, hid_w), dtype=torch.bfloat16, device=dev) for _ in range(4)]
+
+    def ln_w(with_y):
+        i = it[0] = (it[0] + 1) % 4
+        f.fp8q_layernorm_quantize_amax(xs[i], ys[i] if with_y else None, qs[i], gam_w, bet_w, f.E4M3FN, sc0, am,
+                                       stream=stream.cuda_stream)
+    n_w = rows_w * hid_w
+    us_w, us_wy = timed_loop(lambda: ln_w(False)), timed_loop(lambda: ln_w(True))
+    out["layernorm_quantize_amax_wide"] = {
+        "workload": "bf16 2730x12288 (the LayerNorm input's rows) -> LayerNorm -> e4m3fn + amax, clusters of 3 "
+                    "CTAs a row; 4 buffer sets in rotation",
+        "codes_only": {"us": round(us_w, 3), "frac_of_peak": round(3 * n_w / (us_w * 1e-6) / 1e9 / peak, 4)},
+        "with_bf16_y": {"us": round(us_wy, 3), "frac_of_peak": round(5 * n_w / (us_wy * 1e-6) / 1e9 / peak, 4)}}
     del xs, qs, ys
 
     # Ring-buffer update against the rolled one, each timed right after a
