@@ -567,7 +567,8 @@ __global__ void __launch_bounds__(kGeluCodeTableThreads, 1) gelu_code_table_kern
 // bf16, store y (optional) and quantize, two rows at a time.  Thread t owns
 // the 8-element half-vectors t, t + 256, ... of every row; with H <= 4096
 // those are at most two, and their gamma and beta stay in registers for the
-// whole launch.  Shared-memory reads are 16 bytes per lane at consecutive
+// whole launch (longer rows take the cluster kernel below, or this one reading
+// gamma and beta per row where no cluster fits).  Shared-memory reads are 16 bytes per lane at consecutive
 // addresses (no bank conflicts).  The normalisation takes the bf16 operand
 // straight from its word (add.f32.bf16), then rstd * gamma and the fused
 // multiply-add with beta two lanes at a time.
