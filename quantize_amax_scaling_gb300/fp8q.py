@@ -114,11 +114,12 @@ def _dev(t, kind, name):
     dtype), "f32" or "i32".
     """
     global _FP8_DTYPES
+    if _FP8_DTYPES is None:
+        import torch
+        _FP8_DTYPES = (torch.uint8, torch.float8_e4m3fn, torch.float8_e5m2)
     if t is None:
         return
     import torch
-    if _FP8_DTYPES is None:
-        _FP8_DTYPES = (torch.uint8, torch.float8_e4m3fn, torch.float8_e5m2)
     ok = {"bf16": (torch.bfloat16,), "u8": _FP8_DTYPES, "f32": (torch.float32,),
           "i32": (torch.int32,)}[kind]
     if not t.is_cuda:
@@ -195,30 +196,68 @@ def fp8q_layernorm_quantize_amax(x, y, q, gamma, beta, fmt, scale, amax, eps=1e-
                                               _stream(stream)), "fp8q_layernorm_quantize_amax")
 
 
-def fp8q_multi_quantize_amax(xs, qs, fmt, scales, amaxes, stream=None):
+class TensorList:
+    """A ragged list checked and marshalled once into the ``fp8q_tensor`` array that
+    ``fp8q_multi_quantize_amax`` takes.
+
+    ``scales`` and ``amaxes`` are sequences of one-element float32 tensors (or views
+    into one vector) aligned with ``xs``.  Passing a TensorList instead of the four
+    sequences skips the per-tensor checks on every call, which for hundreds of small
+    tensors take longer than the launch itself.  The list keeps the tensors alive; it
+    reads their storage when called, so tensors resized or replaced since it was built
+    need a new list.
+    """
+
+    def __init__(self, xs, qs, scales, amaxes):
+        count = len(xs)
+        if not (len(qs) == len(scales) == len(amaxes) == count):
+            raise ValueError("xs, qs, scales and amaxes must have the same length")
+        import torch
+        _dev(None, "bf16", "")
+        cur = None
+        kinds = ((torch.bfloat16,), _FP8_DTYPES, (torch.float32,), (torch.float32,))
+        arr = (Tensor * max(1, count))()
+        for i in range(count):
+            ts = (xs[i], qs[i], scales[i], amaxes[i])
+            for t, ok, k, nm in zip(ts, kinds, ("bf16", "u8", "f32", "f32"), ("x", "q", "scale", "amax")):
+                if t is None:
+                    raise ValueError(f"{nm}[{i}] is None")
+                # the common case in one expression; anything else gets _dev's message
+                if t.dtype not in ok or not t.is_cuda or not t.is_contiguous():
+                    _dev(t, k, f"{nm}[{i}]")
+                if cur is None:
+                    cur = torch.cuda.current_device()
+                if t.get_device() != cur:
+                    _dev(t, k, f"{nm}[{i}]")
+            n = ts[0].numel()
+            if ts[1].numel() != n:
+                raise ValueError(f"tensor {i}: q must have as many elements as x")
+            arr[i].x_bf16 = ts[0].data_ptr()
+            arr[i].q = ts[1].data_ptr()
+            arr[i].n = n
+            arr[i].scale = ts[2].data_ptr()
+            arr[i].amax = ts[3].data_ptr()
+        self.count = count
+        self.array = arr
+        self.address = ctypes.cast(arr, ctypes.c_void_p)
+        self._keep = (list(xs), list(qs), list(scales), list(amaxes))
+
+
+def fp8q_multi_quantize_amax(xs, qs=None, fmt=E4M3FN, scales=None, amaxes=None, stream=None):
     """fp8q_quantize_amax over a ragged list of tensors, one launch.
 
-    ``scales`` and ``amaxes`` are sequences of one-element float32 tensors (or
-    views into one vector) aligned with ``xs``.
+    Either the four aligned sequences (xs, qs, scales, amaxes: see TensorList),
+    checked on every call, or a TensorList built once as ``xs`` (leave qs, scales
+    and amaxes out).
     """
-    count = len(xs)
-    if not (len(qs) == len(scales) == len(amaxes) == count):
-        raise ValueError("xs, qs, scales and amaxes must have the same length")
-    arr = (Tensor * max(1, count))()
-    for i in range(count):
-        n = _numel(xs[i])
-        if _numel(qs[i]) != n:
-            raise ValueError(f"tensor {i}: q must have as many elements as x")
-        for t, k, nm in ((xs[i], "bf16", "x"), (qs[i], "u8", "q"), (scales[i], "f32", "scale"),
-                         (amaxes[i], "f32", "amax")):
-            _dev(t, k, f"{nm}[{i}]")
-        arr[i].x_bf16 = _ptr(xs[i])
-        arr[i].q = _ptr(qs[i])
-        arr[i].n = n
-        arr[i].scale = _ptr(scales[i])
-        arr[i].amax = _ptr(amaxes[i])
-    _check(lib().fp8q_multi_quantize_amax(ctypes.cast(arr, ctypes.c_void_p), count, fmt,
-                                          _stream(stream)), "fp8q_multi_quantize_amax")
+    if isinstance(xs, TensorList):
+        if qs is not None or scales is not None or amaxes is not None:
+            raise ValueError("pass either a TensorList or xs, qs, scales and amaxes")
+        tl = xs
+    else:
+        tl = TensorList(xs, qs, scales, amaxes)
+    _check(lib().fp8q_multi_quantize_amax(tl.address, tl.count, fmt, _stream(stream)),
+           "fp8q_multi_quantize_amax")
 
 
 def fp8q_dequantize(q, y, fmt, scale, stream=None):

@@ -235,6 +235,37 @@ def test_binding_refuses_tensors_on_another_device(monkeypatch):
                                 fake(torch.float32, 1), fake(torch.float32, 0))
 
 
+def test_tensor_list_refuses_host_tensors_and_other_devices(monkeypatch):
+    """The multi-tensor list's one-pass checks refuse what the per-tensor checks refuse."""
+    import types
+    import torch
+    from quantize_amax_scaling_gb300 import fp8q
+    x = torch.zeros(8, dtype=torch.bfloat16)
+    q = torch.zeros(8, dtype=torch.uint8)
+    s = torch.ones(1)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        fp8q.TensorList([x], [q], [s], [s.clone()])
+
+    def fake(dtype, index, n=8):
+        return types.SimpleNamespace(is_cuda=True, dtype=dtype, is_contiguous=lambda: True,
+                                     device=torch.device("cuda", index), get_device=lambda: index,
+                                     numel=lambda: n, data_ptr=lambda: 0x10000)
+
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 0)
+    ok = fp8q.TensorList([fake(torch.bfloat16, 0)], [fake(torch.float8_e4m3fn, 0)], [fake(torch.float32, 0)],
+                         [fake(torch.float32, 0)])
+    assert ok.count == 1 and ok.array[0].n == 8
+    with pytest.raises(ValueError, match="current CUDA device"):
+        fp8q.TensorList([fake(torch.bfloat16, 0)], [fake(torch.uint8, 0)], [fake(torch.float32, 1)],
+                        [fake(torch.float32, 0)])
+    with pytest.raises(ValueError, match="dtype"):
+        fp8q.TensorList([fake(torch.float16, 0)], [fake(torch.uint8, 0)], [fake(torch.float32, 0)],
+                        [fake(torch.float32, 0)])
+    with pytest.raises(ValueError, match="as many elements"):
+        fp8q.TensorList([fake(torch.bfloat16, 0)], [fake(torch.uint8, 0, 9)], [fake(torch.float32, 0)],
+                        [fake(torch.float32, 0)])
+
+
 def test_product_code_never_touches_the_oracle():
     """The package (kernels, binding, build) neither imports, includes nor links the oracle."""
     pkg = os.path.join(ROOT, "quantize_amax_scaling_gb300")

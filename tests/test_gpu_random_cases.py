@@ -259,3 +259,25 @@ def test_random_ring_update_quantize(dev, c):
     chained over 1 to 3 steps, against the oracle's update followed by its quantize."""
     _fused_case(dev, c["H"], c["S"], c["slot"], c["n"], c["algo"], c["margin"], c["per_slot"],
                 steps=c["steps"], seed=c["seed"])
+
+
+def test_tensor_list_built_once_gives_the_same_as_the_sequences(dev):
+    """A TensorList reused over calls: the same codes and amaxes as passing the sequences."""
+    rng = np.random.default_rng(77)
+    sizes = [int(v) for v in rng.integers(1, 70000, 300)]
+    xs = [to_device(data_bits(rng, n), dev, 0) for n in sizes]
+    qa = [torch.empty(n, dtype=torch.uint8, device=dev) for n in sizes]
+    qb = [torch.empty(n, dtype=torch.uint8, device=dev) for n in sizes]
+    sc = torch.tensor([draw_scale(rng) for _ in sizes], dtype=torch.float32, device=dev)
+    am_a, am_b = torch.zeros(len(sizes), device=dev), torch.zeros(len(sizes), device=dev)
+    sl = [sc[i:i + 1] for i in range(len(sizes))]
+    fp8q.fp8q_multi_quantize_amax(xs, qa, E5M2, sl, [am_a[i:i + 1] for i in range(len(sizes))])
+    tl = fp8q.TensorList(xs, qb, sl, [am_b[i:i + 1] for i in range(len(sizes))])
+    for _ in range(3):                       # reused: amax max-accumulates to the same values
+        fp8q.fp8q_multi_quantize_amax(tl, fmt=E5M2)
+    torch.cuda.synchronize()
+    for a, b in zip(qa, qb):
+        assert torch.equal(a, b)
+    assert torch.equal(am_a.view(torch.int32), am_b.view(torch.int32))
+    with pytest.raises(ValueError):
+        fp8q.fp8q_multi_quantize_amax(tl, qa, E5M2)
