@@ -548,21 +548,22 @@ __global__ void __launch_bounds__(kGeluCodeTableThreads, 1) gelu_code_table_kern
 // amax = max |y|.
 //
 // Persistent grid (as many CTAs as fit at once, at most one per batch).  A
-// batch is R consecutive rows (R a power of two up to 8, chosen so that two
+// batch is R consecutive rows (R a power of two up to 32, chosen so that two
 // batches fit the 64 KB shared-memory ring); CTA b takes batches b, b + G, ...
 // A batch arrives by one cp.async.bulk copy completing on the mbarrier of its
 // ring slot, and the slot is refilled with the batch two ahead once the CTA is
 // done with it, so one batch is always in flight while the CTA computes the
 // other.
 //
-// Phase 1, statistics: all 8 warps work, 8 / R on each row.  Warp part p of a
+// Phase 1, statistics: all 8 warps work, 8 / R on each row (R / 8 rows each,
+// one after the other, when R > 8).  Warp part p of a
 // row sums the row's 8-element vectors p, p + 8/R, ... of its lanes in four
 // chains per lane (S = sum x and Q = sum x^2, the product exact inside each
 // fma), folds them and the lanes (an xor butterfly, whose two lanes per
 // exchange add the same two values, so every lane gets the same bits), and
 // the row's warps add their totals in warp order after a named barrier.  The
-// longest chain of additions is 2 ceil(H / (256 (8 / R))) + 6 + 8 / R, at most
-// H / 128 + 32.  The row's first warp stores (-mean, rstd).
+// longest chain of additions is 2 ceil(H / (256 w)) + 6 + w with w = max(1, 8 / R)
+// warps a row, at most H / 128 + 32.  The row's first warp stores (-mean, rstd).
 // Phase 2, output: after one CTA barrier, all 256 threads normalise, round to
 // bf16, store y (optional) and quantize, two rows at a time.  Thread t owns
 // the 8-element half-vectors t, t + 256, ... of every row; with H <= 4096
@@ -585,7 +586,8 @@ constexpr int kLnMaxH = 32768;
 constexpr int kLnMaxHalfPerThread = 16;  // the largest HPT instantiated
 static_assert(kLnMaxH <= kThreads * 8 * kLnMaxHalfPerThread, "every half-vector of a row has a thread");
 constexpr int kLnWarps = kThreads / 32;
-constexpr int kLnMaxBatch = kLnWarps;
+constexpr int kLnMaxBatch = 4 * kLnWarps;  // single-CTA kernel: short rows, several rows a warp
+constexpr int kLnClusterBatch = kLnWarps;  // cluster kernel: at most one row a warp
 constexpr int kLnBufs = 2;                      // batches in the ring
 constexpr uint32_t kLnRingBytes = 64u * 1024u;  // ring per CTA (both batches), rows up to 16384
 // Longer rows (batches of one row) take a ring of two rows: 4 H bytes, 128 KB at most.
@@ -604,7 +606,7 @@ struct LnArgs {
     float* amax;
     int64_t rows;
     int32_t H;
-    int32_t batch;  // rows per batch: 1, 2, 4 or 8
+    int32_t batch;  // rows per batch: a power of two up to 32 (cluster kernel: up to 8)
     float eps;
     int32_t slice_half;  // cluster kernel: half-vectors of 8 per CTA's column slice
 };
@@ -704,6 +706,19 @@ __device__ __forceinline__ void ln_emit_batch(const LnArgs& a, const uint8_t* ba
                                               const float2 (&br)[HPT <= 2 ? HPT : 1][4], const QScale& c,
                                               uint32_t& m2, uint32_t row_bytes, int nh, int col0) {
     constexpr bool kGammaInRegs = (HPT <= 2);
+    if (HPT == 1 && 2 * nh <= kThreads) {
+        // Short rows (up to 1024 columns): thread t takes half-vector t % nh of rows
+        // t / nh, t / nh + P, ... (P = 256 / nh >= 2 rows a pass), so that all threads
+        // work (its gamma and beta were loaded for that column).  256 columns: 40 us
+        // for 2^25 elements, against 63 us with one thread a column and rows two at a
+        // time; 512: 31 against 40 us; with one row a pass (1536 columns) it was 7% slower.
+        const int P = kThreads / nh, u = threadIdx.x % nh;
+        for (int r = threadIdx.x / nh; r < nr && threadIdx.x < P * nh; r += P) {
+            const uint4 w = *reinterpret_cast<const uint4*>(base + (size_t)r * row_bytes + 16 * u);
+            ln_out8<FMT, WRITE_Y, FAST>(a, w, gr[0], br[0], stats[r], c, (r0 + r) * a.H + col0 + 8 * u, m2);
+        }
+        return;
+    }
     for (int r = 0; r < nr; r += 2) {
         const bool pair = r + 1 < nr;
         const float2 s0 = stats[r], s1 = stats[pair ? r + 1 : r];
@@ -801,7 +816,7 @@ __global__ void __launch_bounds__(kThreads, 2) layernorm_quantize_amax_kernel(co
     constexpr bool kGammaInRegs = (HPT <= 2);
     const int nv8 = a.H / 8, nh = a.H / 8;
     const int R = a.batch;
-    const int wpr = kLnWarps / R;  // warps per row in phase 1
+    const int wpr = R < kLnWarps ? kLnWarps / R : 1;  // warps per row in phase 1
     const uint32_t row_bytes = 2u * (uint32_t)a.H;
     const uint32_t buf_bytes = (uint32_t)R * row_bytes;
     const int64_t nb = (a.rows + R - 1) / R;
@@ -825,7 +840,8 @@ __global__ void __launch_bounds__(kThreads, 2) layernorm_quantize_amax_kernel(co
     if (kGammaInRegs) {
 #pragma unroll
         for (int i = 0; i < (kGammaInRegs ? HPT : 0); ++i) {
-            const int u = threadIdx.x + i * kThreads;
+            // short rows (up to 1024 columns): column threadIdx.x % nh, see ln_emit_batch
+            const int u = (HPT == 1 && 2 * nh <= kThreads) ? (int)threadIdx.x % nh : threadIdx.x + i * kThreads;
             if (u < nh) {
                 load4f2(a.gamma + 8 * u, gr[i]);
                 load4f2(a.beta + 8 * u, br[i]);
@@ -851,10 +867,11 @@ __global__ void __launch_bounds__(kThreads, 2) layernorm_quantize_amax_kernel(co
         // its own wait saw (a warp whose copy is missing reads nothing); the
         // CTA then agrees on the outcome at its barrier below.
         const bool warp_arrived = __all_sync(0xFFFFFFFFu, arrived);
-        if (prow < nr) {
+        // row prow, and with more rows than warps also prow + 8, prow + 16, ...
+        for (int row = prow; row < nr; row += kLnWarps) {
             float S, Q;
-            ln_row_sums(base + (size_t)prow * row_bytes, nv8, warp_arrived, lane, warp, prow, ppart, wpr, part, S, Q);
-            if (ppart == 0 && lane == 0) stats[prow] = ln_row_stats(S, Q, Hf, a.eps);
+            ln_row_sums(base + (size_t)row * row_bytes, nv8, warp_arrived, lane, warp, prow, ppart, wpr, part, S, Q);
+            if (ppart == 0 && lane == 0) stats[row] = ln_row_stats(S, Q, Hf, a.eps);
         }
         ok = __syncthreads_and(arrived) != 0;
         if (!ok) break;  // uniform
@@ -951,8 +968,8 @@ __global__ void __launch_bounds__(kThreads, 2) layernorm_cluster_quantize_amax_k
     __shared__ uint64_t xbar[2];                             // the partial sums' arrival, by batch parity
     __shared__ float2 part[kLnWarps];
     __shared__ uint32_t warp_ok[kLnWarps];
-    __shared__ float2 stats[kLnMaxBatch];
-    __shared__ uint4 xpart[2][kLnClusterMax][kLnMaxBatch];  // (S, Q, group arrived, 0) of every CTA, by batch parity
+    __shared__ float2 stats[kLnClusterBatch];
+    __shared__ uint4 xpart[2][kLnClusterMax][kLnClusterBatch];  // (S, Q, group arrived, 0) of every CTA, by batch parity
     __shared__ uint32_t red[kLnWarps];
     const int C = (int)cluster_nctarank(), crank = (int)cluster_ctarank();
     const int h0 = crank * a.slice_half;                        // the slice's first half-vector
@@ -1082,7 +1099,8 @@ fp8q_status launch_layernorm_hpt(LnArgs a, cudaStream_t s) {
     auto kern = layernorm_quantize_amax_kernel<FMT, WRITE_Y, HPT>;
     const uint32_t row_bytes = 2u * (uint32_t)a.H;
     uint32_t batch = ln_ring_bytes(a.H) / (kLnBufs * row_bytes);
-    batch = batch >= 8 ? 8 : batch >= 4 ? 4 : batch >= 2 ? 2 : 1;  // a power of two: 8 / batch warps a row
+    // a power of two: 8 / batch warps a row, or batch / 8 rows a warp
+    batch = batch >= 32 ? 32 : batch >= 16 ? 16 : batch >= 8 ? 8 : batch >= 4 ? 4 : batch >= 2 ? 2 : 1;
     a.batch = (int32_t)batch;
     const uint32_t smem = kLnBufs * batch * row_bytes;
     // the most any H of this instance takes: the resident count holds for all of them

@@ -1,8 +1,8 @@
 """The LayerNorm launch choices, restated on the host, against the tolerance's bound on
 the row sums' longest chain of additions (H // 128 + 32) and the ring's shared memory.
 
-The single-CTA kernel takes batches of R rows (a power of two up to 8 filling two ring
-slots of 64 KB, or one row a slot in a ring of 4H bytes), 8 / R warps a row; a warp's
+The single-CTA kernel takes batches of R rows (a power of two up to 32 filling two ring
+slots of 64 KB, or one row a slot in a ring of 4H bytes), max(1, 8 / R) warps a row; a warp's
 lane sums its half-vectors of 8 in four chains of two elements each, folds them (2),
 the lanes (5) and the row's warps (8 / R - 1).  The cluster kernel does the same on a
 column slice of hs = ceil(H / 8C) half-vectors (C = ceil(H / 4096)), R filling two ring
@@ -14,15 +14,18 @@ RING = 64 * 1024
 CLUSTER_RING = 96 * 1024
 
 
-def pow2_batch(b):
-    return 8 if b >= 8 else 4 if b >= 4 else 2 if b >= 2 else 1
+def pow2_batch(b, top=8):
+    r = 1
+    while r * 2 <= min(b, top):
+        r *= 2
+    return r
 
 
 def single_cta_chain(H):
     nh = H // 8
     ring = max(RING, 2 * 2 * H)
-    R = pow2_batch(ring // (2 * 2 * H))
-    wpr = 8 // R
+    R = pow2_batch(ring // (2 * 2 * H), 32)
+    wpr = max(1, 8 // R)
     return 2 * -(-nh // (32 * wpr)) + 2 + 5 + (wpr - 1), 2 * R * 2 * H
 
 
