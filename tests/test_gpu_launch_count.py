@@ -126,3 +126,45 @@ print("OK")
     env = dict(os.environ, PYTHONPATH=ROOT + os.pathsep + os.environ.get("PYTHONPATH", ""))
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300, env=env)
     assert r.returncode == 0 and r.stdout.strip().endswith("OK"), r.stdout + r.stderr
+
+
+def test_cluster_kernels_first_call_inside_graph_capture():
+    """The same for the calls that launch thread-block clusters and query how many fit
+    (cudaOccupancyMaxActiveClusters) on their first use: the LayerNorm on rows of 12288
+    and the two GELU table kernels."""
+    import subprocess
+    import sys
+    code = r'''
+import torch
+from quantize_amax_scaling_gb300 import fp8q, workloads as W
+dev = torch.device("cuda:0")
+x = W.residual_stream(seed=2, device=dev, shape=(40, 12288))
+g, b = W.layernorm_params(12288, device=dev)
+sc = torch.full((1,), 0.02, device=dev)
+q, am = torch.empty(x.shape, dtype=torch.uint8, device=dev), torch.zeros(1, device=dev)
+gen = torch.Generator(device=dev); gen.manual_seed(3)
+h = torch.randn(1 << 25, generator=gen, device=dev).to(torch.bfloat16)
+gy, gq, gam = torch.empty_like(h), torch.empty(h.numel(), dtype=torch.uint8, device=dev), torch.zeros(1, device=dev)
+hq, hqam = torch.empty(1 << 23, dtype=torch.uint8, device=dev), torch.zeros(1, device=dev)
+gr = torch.cuda.CUDAGraph()
+with torch.cuda.graph(gr, stream=torch.cuda.Stream()):
+    fp8q.fp8q_layernorm_quantize_amax(x, None, q, g, b, fp8q.E4M3FN, sc, am)
+    fp8q.fp8q_gelu_quantize_amax(h, gy, gq, fp8q.E4M3FN, sc, gam)
+    fp8q.fp8q_gelu_quantize_amax(h[: 1 << 23], None, hq, fp8q.E4M3FN, sc, hqam)
+gr.replay()
+torch.cuda.synchronize()
+q2, am2 = torch.empty_like(q), torch.zeros(1, device=dev)
+fp8q.fp8q_layernorm_quantize_amax(x, None, q2, g, b, fp8q.E4M3FN, sc, am2)
+gy2, gq2, gam2 = torch.empty_like(gy), torch.empty_like(gq), torch.zeros(1, device=dev)
+fp8q.fp8q_gelu_quantize_amax(h, gy2, gq2, fp8q.E4M3FN, sc, gam2)
+hq2, hqam2 = torch.empty_like(hq), torch.zeros(1, device=dev)
+fp8q.fp8q_gelu_quantize_amax(h[: 1 << 23], None, hq2, fp8q.E4M3FN, sc, hqam2)
+torch.cuda.synchronize()
+assert torch.equal(q, q2) and float(am) == float(am2)
+assert torch.equal(gy.view(torch.int16), gy2.view(torch.int16)) and torch.equal(gq, gq2) and float(gam) == float(gam2)
+assert torch.equal(hq, hq2) and float(hqam) == float(hqam2)
+print("OK")
+'''
+    env = dict(os.environ, PYTHONPATH=ROOT + os.pathsep + os.environ.get("PYTHONPATH", ""))
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300, env=env)
+    assert r.returncode == 0 and r.stdout.strip().endswith("OK"), r.stdout + r.stderr
