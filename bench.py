@@ -253,6 +253,7 @@ def run_gpu(args, ws, rank, local):
     step = Step(dev)
     stream = torch.cuda.Stream(dev)
     peak, peak_src = measured_peaks()
+    torch.cuda.synchronize(dev)  # the step's inputs, made on the default stream, are complete
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -465,6 +466,7 @@ def measure_graph(args, step, stream, dev):
         """us per repetition: the median over `replays` timed replays of one graph of
         `reps` repetitions (several replays of a long graph keep the event timer's
         granularity, a few us on this GPU, well below the figure's last digit)."""
+        torch.cuda.synchronize(dev)  # inputs made on the default stream are complete
         with torch.cuda.stream(stream):
             fn()
             stream.synchronize()
@@ -536,6 +538,7 @@ def measure_other_configs(step, stream, dev, peak, warm=20, reps=50):
         launch's time is quantised; the mean over many launches (whose start is
         not tied to the tick) is not, the median is."""
         times = []
+        torch.cuda.synchronize(dev)  # inputs made on the default stream are complete
         with torch.cuda.stream(stream):
             for _ in range(warm):
                 if before:
@@ -622,6 +625,7 @@ def measure_next_rows(args, step, stream, dev, peak):
     it = [0]
 
     def timed_loop(fn):
+        torch.cuda.synchronize(dev)  # inputs made on the default stream are complete
         with torch.cuda.stream(stream):
             for _ in range(3):
                 fn()
@@ -751,6 +755,7 @@ def measure_next_rows(args, step, stream, dev, peak):
     roll_hist = step.hist.clone()
     sc, si = step.scale.clone(), step.scale_inv.clone()
     times = {"ring": [], "roll": []}
+    torch.cuda.synchronize(dev)
     with torch.cuda.stream(stream):
         for i in range(n_iter + 3):
             for kind in ("ring", "roll"):
@@ -799,6 +804,7 @@ def measure_next_rows(args, step, stream, dev, peak):
                                                step.slot_format, stream.cuda_stream)
 
     def graph_us(fn, reps=10, replays=3):
+        torch.cuda.synchronize(dev)
         with torch.cuda.stream(stream):
             fn()
             stream.synchronize()
