@@ -392,18 +392,18 @@ def test_layernorm_every_scale_and_flax_defaults(dev):
             check_layernorm(x, ones, zeros, fmt, s, dev, what=f"scale {s!r}")
 
 
-def test_layernorm_degenerate_rows(dev):
+@pytest.mark.parametrize("H", [512, 8192, 20480])   # one CTA a batch; clusters of 2 and 5
+def test_layernorm_degenerate_rows(dev, H):
     """Constant rows (var = 0: y = beta exactly), rows with inf or NaN (y NaN), and rows
     outside binary32's range for the statistics (Q overflows; eps = 0 on constant or
     subnormal rows), where no tolerance applies but the codes and amax must still be
     exactly those of y."""
-    H = 512
     rows = []
     rows.append(np.full(H, 0x3F80, np.uint16))                        # all 1.0
     rows.append(np.zeros(H, np.uint16))                               # all +0
     r = np.full(H, 0x4000, np.uint16); r[17] = 0x7F80; rows.append(r)   # +inf
     r = np.full(H, 0x4000, np.uint16); r[300] = 0x7FC1; rows.append(r)  # NaN
-    r = np.full(H, 0x4000, np.uint16); r[5] = 0xFF80; r[6] = 0x7F80; rows.append(r)  # +inf and -inf
+    r = np.full(H, 0x4000, np.uint16); r[5] = 0xFF80; r[H - 6] = 0x7F80; rows.append(r)  # +inf and -inf
     rows.append(np.where(np.arange(H) % 2 == 0, 0x7F00, 0xFF00).astype(np.uint16))  # +-1.7e38: Q overflows
     rows.append(np.where(np.arange(H) % 3 == 0, 0x0001, 0x8002).astype(np.uint16))  # bf16 subnormals
     rows.append((np.arange(H) % 7 + 0x3F80).astype(np.uint16))        # values near 1 (cancellation)
