@@ -109,6 +109,8 @@ def test_compact_rows_and_detail_file(tmp_path):
     assert "ring_update_us" not in bench.compact_rows(kernels, nxt, other)
     other["mlp_activation"]["same_bytes_library"] = {"device_copy": {"frac_of_peak": 0.88}}
     assert bench.compact_rows(kernels, nxt, other)["mlp_same_bytes_copy_frac"] == 0.88
+    nxt["layernorm_quantize_amax_wide"] = {"codes_only": {"frac_of_peak": 0.51}}
+    assert bench.compact_rows(kernels, nxt, other)["layernorm_12288_codes_frac"] == 0.51
     assert bench.compact_rows(kernels, None, None) == {"multi_quantize_frac": 0.95, "dequantize_frac": 0.94}
     p = tmp_path / "sub" / "detail.json"
     where = bench.write_detail({"a": 1}, str(p))
