@@ -798,6 +798,34 @@ __device__ __forceinline__ void ln_row_sums(const uint8_t* xr, int nv8, bool war
     }
 }
 
+// The same sums over 8 lanes (lane sl of its group of 8), for short rows: each
+// lane sums its half-vectors sl, sl + 8, ... in four chains, folds them, and the
+// group adds its lanes by an xor butterfly over 4, 2, 1 (every lane of the group
+// gets the same bits).  All 32 lanes of the warp call it together; a group whose
+// row does not exist or whose copy is missing reads nothing.
+constexpr int kLnShortHalf = 128;  // half-vectors a row (1024 columns) up to which phase 1 uses 8 lanes a row
+__device__ __forceinline__ void ln_row_sums8(const uint8_t* xr, int nv8, bool read, int sl, float& S, float& Q) {
+    float s[4] = {0.0f, 0.0f, 0.0f, 0.0f}, q[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    for (int j = sl; read && j < nv8; j += 8) {
+        const uint4 w = *reinterpret_cast<const uint4*>(xr + 16 * j);
+        acc_bf16<true>(w.x, s[0], q[0]);
+        acc_bf16<true>(w.y, s[1], q[1]);
+        acc_bf16<true>(w.z, s[2], q[2]);
+        acc_bf16<true>(w.w, s[3], q[3]);
+        acc_bf16<false>(w.x, s[0], q[0]);
+        acc_bf16<false>(w.y, s[1], q[1]);
+        acc_bf16<false>(w.z, s[2], q[2]);
+        acc_bf16<false>(w.w, s[3], q[3]);
+    }
+    S = __fadd_rn(__fadd_rn(s[0], s[1]), __fadd_rn(s[2], s[3]));
+    Q = __fadd_rn(__fadd_rn(q[0], q[1]), __fadd_rn(q[2], q[3]));
+#pragma unroll
+    for (int o = 4; o >= 1; o >>= 1) {
+        S = __fadd_rn(S, __shfl_xor_sync(0xFFFFFFFFu, S, o));
+        Q = __fadd_rn(Q, __shfl_xor_sync(0xFFFFFFFFu, Q, o));
+    }
+}
+
 // (-mean, rstd) of a row of H elements from its sums.
 __device__ __forceinline__ float2 ln_row_stats(float S, float Q, float Hf, float eps) {
     const float mean = __fdiv_rn(S, Hf);
@@ -867,11 +895,23 @@ __global__ void __launch_bounds__(kThreads, 2) layernorm_quantize_amax_kernel(co
         // its own wait saw (a warp whose copy is missing reads nothing); the
         // CTA then agrees on the outcome at its barrier below.
         const bool warp_arrived = __all_sync(0xFFFFFFFFu, arrived);
-        // row prow, and with more rows than warps also prow + 8, prow + 16, ...
-        for (int row = prow; row < nr; row += kLnWarps) {
-            float S, Q;
-            ln_row_sums(base + (size_t)row * row_bytes, nv8, warp_arrived, lane, warp, prow, ppart, wpr, part, S, Q);
-            if (ppart == 0 && lane == 0) stats[row] = ln_row_stats(S, Q, Hf, a.eps);
+        if (HPT == 1 && nv8 <= kLnShortHalf) {
+            // Short rows (up to 1024 columns, R >= 16): 8 lanes a row, 4 rows a warp at once.
+            const int sub = lane >> 3, sl = lane & 7;
+            for (int base_row = 0; base_row < nr; base_row += 4 * kLnWarps) {
+                const int row = base_row + 4 * warp + sub;
+                float S, Q;
+                ln_row_sums8(base + (size_t)row * row_bytes, nv8, warp_arrived && row < nr, sl, S, Q);
+                if (sl == 0 && row < nr) stats[row] = ln_row_stats(S, Q, Hf, a.eps);
+            }
+        } else {
+            // row prow, and with more rows than warps also prow + 8, prow + 16, ...
+            for (int row = prow; row < nr; row += kLnWarps) {
+                float S, Q;
+                ln_row_sums(base + (size_t)row * row_bytes, nv8, warp_arrived, lane, warp, prow, ppart, wpr, part, S,
+                            Q);
+                if (ppart == 0 && lane == 0) stats[row] = ln_row_stats(S, Q, Hf, a.eps);
+            }
         }
         ok = __syncthreads_and(arrived) != 0;
         if (!ok) break;  // uniform
