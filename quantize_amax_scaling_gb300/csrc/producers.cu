@@ -556,7 +556,8 @@ __global__ void __launch_bounds__(kGeluCodeTableThreads, 1) gelu_code_table_kern
 // other.
 //
 // Phase 1, statistics: all 8 warps work, 8 / R on each row (R / 8 rows each,
-// one after the other, when R > 8).  Warp part p of a
+// one after the other, when R > 8; up to 1024 columns 8 lanes take a row, see
+// ln_row_sums8).  Warp part p of a
 // row sums the row's 8-element vectors p, p + 8/R, ... of its lanes in four
 // chains per lane (S = sum x and Q = sum x^2, the product exact inside each
 // fma), folds them and the lanes (an xor butterfly, whose two lanes per
